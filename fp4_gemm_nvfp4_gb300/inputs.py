@@ -1,0 +1,160 @@
+"""Seeded synthetic inputs for the NVFP4 linear-layer pipeline.
+
+This module holds no quantization or GEMM arithmetic: it draws numbers.  It is
+the one module that both the CUDA path's callers and the CPU oracle's callers
+use, so that both sides see the same bytes.
+
+Shapes and distributions follow the pages' 3B model: hidden 3072, FFN 9216,
+24 query heads and 12 KV heads of head_dim 128, 2048-token sequences
+("Full-Stack FP4" summary page, Results and Analysis).  Values are drawn in
+float32 with numpy's PCG64 ``default_rng(seed)`` and rounded to bfloat16
+(nearest, ties to even).
+"""
+from dataclasses import dataclass, field
+from typing import Dict, List, Tuple
+
+import numpy as np
+
+HIDDEN = 3072
+FFN = 9216
+N_HEADS = 24
+N_KV_HEADS = 12
+HEAD_DIM = 128
+SEQ = 2048
+
+
+def to_bf16_bits(x) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), nearest with ties to even."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounding = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    return ((u + rounding) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def normal(rows: int, cols: int, seed: int, std: float = 1.0, outlier_channels: int = 0,
+           outlier_scale: float = 50.0) -> np.ndarray:
+    """N(0, std^2) bf16 bits; ``outlier_channels`` columns scaled by ``outlier_scale``."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((rows, cols), dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    if outlier_channels:
+        ch = rng.choice(cols, outlier_channels, replace=False)
+        x[:, ch] *= np.float32(outlier_scale)
+    return to_bf16_bits(x)
+
+
+def student_t(rows: int, cols: int, seed: int, df: float = 3.0, scale: float = 1e-3) -> np.ndarray:
+    """Student-t(df) * scale bf16 bits (heavy-tailed gradients)."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_t(df, size=(rows, cols)).astype(np.float32)
+    x *= np.float32(scale)
+    return to_bf16_bits(x)
+
+
+def rht_sign_mask(seed: int) -> int:
+    """The 16 random signs of D for one backward pass, as a bit mask."""
+    rng = np.random.default_rng([seed, 0xD])
+    return int(rng.integers(0, 1 << 16))
+
+
+def outlier_count(cols: int, fraction: float = 0.001) -> int:
+    """0.1% of the channels, at least one."""
+    return max(1, int(round(cols * fraction)))
+
+
+@dataclass
+class Operand:
+    """One bf16 input tensor of a workload and how it is quantized."""
+    name: str
+    rows: int
+    cols: int
+    kind: str            # "normal", "weight", "grad"
+    seed: int
+    outliers: int = 0
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    operands: List[Operand] = field(default_factory=list)
+    # (name, A operand, A orientation, B operand, B orientation)
+    gemms: List[Tuple[str, str, str, str, str]] = field(default_factory=list)
+
+    def make(self, name: str) -> np.ndarray:
+        op = next(o for o in self.operands if o.name == name)
+        if op.kind == "normal":
+            return normal(op.rows, op.cols, op.seed, 1.0, op.outliers)
+        if op.kind == "weight":
+            return normal(op.rows, op.cols, op.seed, 0.02)
+        if op.kind == "grad":
+            return student_t(op.rows, op.cols, op.seed)
+        raise ValueError(op.kind)
+
+
+def c1_single_linear() -> Workload:
+    """M=128 tokens, K=1024, N=1024; 4 of 1024 X channels x50; seed 0."""
+    return Workload("c1_linear_fwd_128x1024x1024", 0, [
+        Operand("X", 128, 1024, "normal", 0, outliers=4),
+        Operand("W", 1024, 1024, "weight", 1),
+    ], [("fprop", "X", "row", "W", "row")])
+
+
+def c2_attention_projections(tokens: int = 4 * SEQ) -> Workload:
+    qkv = (N_HEADS + 2 * N_KV_HEADS) * HEAD_DIM          # 6144
+    return Workload(f"c2_attn_proj_{tokens}tok", 2, [
+        Operand("X", tokens, HIDDEN, "normal", 20, outliers=outlier_count(HIDDEN)),
+        Operand("W_qkv", qkv, HIDDEN, "weight", 21),
+        Operand("W_o", HIDDEN, HIDDEN, "weight", 22),
+        Operand("dY_qkv", tokens, qkv, "grad", 23),
+        Operand("dY_o", tokens, HIDDEN, "grad", 24),
+    ], [("fprop_qkv", "X", "row", "W_qkv", "row2d"),
+        ("fprop_o", "X", "row", "W_o", "row2d"),
+        ("dgrad_qkv", "dY_qkv", "row", "W_qkv", "col2d"),
+        ("dgrad_o", "dY_o", "row", "W_o", "col2d")])
+
+
+def c3_ffn_wgrad(tokens: int = 4 * SEQ) -> Workload:
+    return Workload(f"c3_ffn_wgrad_{tokens}tok", 3, [
+        Operand("dY", tokens, FFN, "grad", 30),
+        Operand("X", tokens, HIDDEN, "normal", 31),
+    ], [("wgrad", "dY", "col_rht_sr", "X", "col_rht")])
+
+
+def c4_ffn_layer_step(tokens: int = 8 * SEQ) -> Workload:
+    return Workload(f"c4_ffn_layer_step_{tokens}tok", 4, [
+        Operand("X", tokens, HIDDEN, "normal", 40, outliers=outlier_count(HIDDEN)),
+        Operand("W_up", FFN, HIDDEN, "weight", 41),
+        Operand("H", tokens, FFN, "normal", 42, outliers=outlier_count(FFN)),
+        Operand("W_down", HIDDEN, FFN, "weight", 43),
+        Operand("dY_down", tokens, HIDDEN, "grad", 44),
+        Operand("dY_up", tokens, FFN, "grad", 45),
+    ], [("fprop_up", "X", "row", "W_up", "row2d"),
+        ("fprop_down", "H", "row", "W_down", "row2d"),
+        ("dgrad_down", "dY_down", "row_sr", "W_down", "col2d"),
+        ("dgrad_up", "dY_up", "row_sr", "W_up", "col2d"),
+        ("wgrad_down", "dY_down", "col_rht_sr", "H", "col_rht"),
+        ("wgrad_up", "dY_up", "col_rht_sr", "X", "col_rht")])
+
+
+def c5_sweep_sizes() -> List[Tuple[int, int]]:
+    """(rows, row_length) of the quantizer sweep: 2^20..2^29 elements."""
+    out = []
+    for n in (1 << 20, 1 << 22, 1 << 24, 1 << 26, 1 << 28, 1 << 29):
+        for L in (3072, 9216, 8192):
+            rows = (n // L) // 16 * 16
+            out.append((rows, L))
+    return out
+
+
+WORKLOADS: Dict[str, callable] = {
+    "c1": c1_single_linear,
+    "c2": c2_attention_projections,
+    "c3": c3_ffn_wgrad,
+    "c4": c4_ffn_layer_step,
+}

@@ -1,0 +1,596 @@
+"""Pins for the CPU oracle: facts the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: a value the
+pages print (tests/golden), a library routine run independently (torch's
+float8/bfloat16 casts, cuRAND's host Philox generator), a closed form, an
+invariant, or exact brute force.  No expected value here comes from the CUDA
+library.
+"""
+import ctypes
+import ctypes.util
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_gemm_nvfp4_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _grid():
+    rows = []
+    with open(os.path.join(GOLDEN, "e2m1_grid.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                code, e, m, val = line.split()
+                rows.append((int(code), int(e), int(m), float(val)))
+    return rows
+
+
+def _bins():
+    bins, ties = [], []
+    with open(os.path.join(GOLDEN, "e2m1_bins.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            parts = line.split()
+            if parts[0] == "tie":
+                ties.append((float(parts[1]), float(parts[2])))
+            else:
+                lo, hi, val, step = parts
+                bins.append((float(lo), float(hi), float(val), None if step == "-" else float(step)))
+    return bins, ties
+
+
+GRID = np.array([g[3] for g in _grid()])
+
+
+def _unpack(codes):
+    lo = codes & 0xF
+    hi = codes >> 4
+    return np.stack([lo, hi], axis=-1).reshape(codes.shape[0], -1)
+
+
+def _e2m1_values(codes4):
+    mag = GRID[codes4 & 7]
+    return np.where(codes4 & 8, -mag, mag)
+
+
+def _torch_e4m3_values(codes):
+    t = torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+# ---------------------------------------------------------------- E2M1 ----
+def test_e2m1_grid_matches_page_enumeration():
+    for code, e, m, val in _grid():
+        # the page's definition: bias 1, exponent 0 is subnormal (0.m * 2^0)
+        by_bits = m * 0.5 if e == 0 else 2.0 ** (e - 1) * (1 + m / 2)
+        assert by_bits == val
+        assert oracle.e2m1_value(code) == val
+        assert oracle.e2m1_value(code | 8) == -val
+
+
+def test_e2m1_rne_bins_and_ties():
+    bins, ties = _bins()
+    eps = 1e-6
+    for lo, hi, val, _ in bins:
+        inside = [lo + eps, (lo + min(hi, 8.0)) / 2, min(hi, 100.0) - eps]
+        for v in inside:
+            q = oracle.e2m1_value(oracle.e2m1_rne(v))
+            assert q == val, (v, q, val)
+            assert oracle.e2m1_value(oracle.e2m1_rne(-v)) == -val
+    for tie, expect in ties:
+        assert oracle.e2m1_value(oracle.e2m1_rne(tie)) == expect, tie
+        assert oracle.e2m1_value(oracle.e2m1_rne(-tie)) == -expect, tie
+    for big in (6.0, 7.0, 1e9, 3.4e38):
+        assert oracle.e2m1_rne(big) == 7 and oracle.e2m1_rne(-big) == 15
+
+
+def test_e2m1_rne_error_within_half_step():
+    """Appendix 7 of "Full-Stack FP4": RTN error |delta| <= step_k / 2."""
+    rng = np.random.default_rng(1)
+    v = np.concatenate([np.arange(0, 6.0, 1 / 4096, dtype=np.float32),
+                        rng.uniform(0, 6, 200000).astype(np.float32)])
+    q = _e2m1_values(oracle.e2m1_rne_array(v))
+    bins, _ = _bins()
+    for lo_grid, hi_grid in zip(GRID[:-1], GRID[1:]):
+        sel = (v >= lo_grid) & (v < hi_grid)
+        step = hi_grid - lo_grid
+        assert np.all(np.abs(q[sel] - v[sel]) <= step / 2)
+        assert np.all((q[sel] == lo_grid) | (q[sel] == hi_grid))
+    # and the result is the nearest grid point
+    nearest = np.min(np.abs(v[:, None] - GRID[None, :]), axis=1)
+    assert np.array_equal(np.abs(q - v), nearest)
+
+
+def test_e2m1_sign_bit_follows_input():
+    assert oracle.e2m1_rne(-0.1) == 8       # negative value rounding to zero keeps its sign
+    assert oracle.e2m1_rne(-0.0) == 8
+    assert oracle.e2m1_rne(0.0) == 0
+    assert oracle.e2m1_sr(-0.0, 0) == 8
+    assert oracle.e2m1_sr(-0.2, 0xFFFFFFFF) == 8
+
+
+def test_e2m1_sr_grid_points_never_move():
+    words = [0, 1, 0xFF, 0x100, 0x7FFFFFFF, 0xFFFFFFFF]
+    for code in range(8):
+        for w in words:
+            assert oracle.e2m1_sr(float(GRID[code]), w) == code
+            assert oracle.e2m1_sr(-float(GRID[code]), w) == code | 8
+
+
+def test_e2m1_sr_probability_threshold():
+    """P(up) = d / step realised with 24-bit words: up iff u < ceil(frac * 2^24)."""
+    for v in (0.1, 0.3, 0.74, 1.2, 1.6, 1.9, 2.2, 2.9, 3.3, 4.5, 5.9, 1e-7):
+        k = int(np.searchsorted(GRID, v, side="right") - 1)
+        frac = Fraction(float(np.float32(v))) - Fraction(float(GRID[k]))
+        frac /= Fraction(float(GRID[k + 1] - GRID[k]))
+        thr = math.ceil(frac * 2 ** 24)
+        assert oracle.e2m1_sr(v, (thr - 1) << 8) == k + 1
+        assert oracle.e2m1_sr(v, ((thr - 1) << 8) | 0xFF) == k + 1
+        assert oracle.e2m1_sr(v, thr << 8) == k
+
+
+@pytest.mark.parametrize("v", [0.1, 0.3, 0.74, 1.2, 1.9, 2.2, 2.9, 3.3, 4.5, 5.9])
+def test_e2m1_sr_unbiased_with_page_variance(v):
+    """Appendix 7: SR is unbiased with variance d (step - d); 10^6 draws, 4 sigma."""
+    n = 1_000_000
+    rng = np.random.default_rng(int(v * 1000))
+    words = rng.integers(0, 2 ** 32, n, dtype=np.uint64).astype(np.uint32)
+    q = _e2m1_values(oracle.e2m1_sr_array(np.full(n, v, np.float32), words))
+    k = int(np.searchsorted(GRID, v, side="right") - 1)
+    step = GRID[k + 1] - GRID[k]
+    d = float(np.float32(v)) - GRID[k]
+    var = d * (step - d)
+    err = q - float(np.float32(v))
+    assert abs(err.mean()) <= 4 * math.sqrt(var / n)
+    assert abs(err.var() / var - 1) < 0.01
+
+
+def test_rtn_mse_uniform_in_bin():
+    """Appendix 7: input-averaged RTN MSE is step^2 / 12 inside a bin."""
+    rng = np.random.default_rng(7)
+    for lo, hi in zip(GRID[:-1], GRID[1:]):
+        v = rng.uniform(lo, hi, 200000).astype(np.float32)
+        q = _e2m1_values(oracle.e2m1_rne_array(v))
+        mse = np.mean((q - v.astype(np.float64)) ** 2)
+        assert abs(mse / ((hi - lo) ** 2 / 12) - 1) < 0.02
+
+
+# ---------------------------------------------------------------- E4M3 ----
+def test_e4m3_decode_matches_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = _torch_e4m3_values(codes)
+    ours = np.array([oracle.e4m3_value(c) for c in codes])
+    assert np.array_equal(np.isnan(ref), np.isnan(ours))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], ours[ok])
+    assert oracle.e4m3_value(0x7E) == 448.0
+
+
+def test_e4m3_encode_matches_torch_rne():
+    vals = _torch_e4m3_values(np.arange(0x7F, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2
+    rng = np.random.default_rng(3)
+    rand = np.concatenate([rng.uniform(0, 464, 100000),
+                           np.exp(rng.uniform(np.log(1e-6), np.log(463.9), 100000))])
+    x = np.concatenate([vals, mids, rand]).astype(np.float32)
+    x = x[x < 464]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ours = oracle.e4m3_rne_satfinite_array(x)
+    assert np.array_equal(ours, ref)
+    # satfinite: beyond the largest finite value everything lands on 448
+    big = np.array([448.0, 449.0, 464.0, 500.0, 1e6, 3.4e38], np.float32)
+    assert np.all(oracle.e4m3_rne_satfinite_array(big) == 0x7E)
+
+
+# -------------------------------------------------------------- Philox ----
+def _curand():
+    for name in ("libcurand.so", "libcurand.so.10"):
+        for d in ("/usr/local/cuda/lib64", ""):
+            path = os.path.join(d, name) if d else name
+            try:
+                return ctypes.CDLL(path)
+            except OSError:
+                continue
+    found = ctypes.util.find_library("curand")
+    return ctypes.CDLL(found) if found else None
+
+
+def _curand_philox_host(seed, n):
+    lib = _curand()
+    if lib is None:
+        pytest.skip("cuRAND host library not available")
+    gen = ctypes.c_void_p()
+    CURAND_RNG_PSEUDO_PHILOX4_32_10 = 161
+    assert lib.curandCreateGeneratorHost(ctypes.byref(gen), CURAND_RNG_PSEUDO_PHILOX4_32_10) == 0
+    try:
+        assert lib.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+        out = np.zeros(n, np.uint32)
+        assert lib.curandGenerate(gen, out.ctypes.data_as(ctypes.c_void_p), ctypes.c_size_t(n)) == 0
+    finally:
+        lib.curandDestroyGenerator(gen)
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 0x123456789ABCDEF0, 0xFFFFFFFFFFFFFFFF, 2 ** 32 + 7])
+def test_philox_matches_curand_host_generator(seed):
+    """cuRAND's host Philox4x32-10 emits block i from counter (0, 0, i, 0) under
+    key (seed lo, seed hi); the oracle's round function must reproduce it."""
+    n_blocks = 512
+    ref = _curand_philox_host(seed, 4 * n_blocks).reshape(n_blocks, 4)
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for i in list(range(16)) + [100, 255, 511]:
+        ours = oracle.philox4x32_10([0, 0, i, 0], key)
+        assert np.array_equal(ours, ref[i]), i
+    # the SR word of element idx < 4 in stream s is word idx of block s
+    for s in (0, 3, 77):
+        for idx in range(4):
+            assert oracle.sr_word(seed, s, idx) == ref[s][idx]
+
+
+def test_sr_word_counter_layout():
+    """g = idx >> 2 goes to counter words 0-1, the stream to words 2-3."""
+    seed, stream = 0xDEADBEEF12345678, 0x0000000A00000005
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for idx in (0, 5, 1 << 33, (1 << 40) + 3):
+        g = idx >> 2
+        block = oracle.philox4x32_10([g & 0xFFFFFFFF, g >> 32, stream & 0xFFFFFFFF, stream >> 32], key)
+        assert oracle.sr_word(seed, stream, idx) == block[idx & 3]
+
+
+# ----------------------------------------------------------------- RHT ----
+def _sylvester(n):
+    """The recursion on the "OptiTrain-FP4" page: H_1 = [1], H_2k = [[H, H], [H, -H]]."""
+    h = np.array([[1]], dtype=np.int64)
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def _rht_matrix(mask):
+    """4*U column by column from the oracle's butterfly applied to unit vectors."""
+    cols = []
+    for j in range(16):
+        e = np.zeros(16, np.float32)
+        e[j] = 1.0
+        cols.append(oracle.rht16(e, mask) * 4)
+    return np.stack(cols, axis=1).astype(np.float64)
+
+
+@pytest.mark.parametrize("mask", [0, 0xFFFF, 0x5A3C, 0x0001, 0x8000])
+def test_rht_matches_sylvester_times_signs(mask):
+    H = _sylvester(16)
+    D = np.diag([-1 if (mask >> i) & 1 else 1 for i in range(16)])
+    assert np.array_equal(_rht_matrix(mask), (H @ D).astype(np.float64))
+
+
+def test_rht_orthogonality():
+    """H16 H16^T = 16 I exactly; U^T U = I ("Pretraining LLMs with NVFP4", B.4)."""
+    M = _rht_matrix(0).astype(np.int64)
+    assert set(np.unique(M)) == {-1, 1}
+    assert np.array_equal(M @ M.T, 16 * np.eye(16, dtype=np.int64))
+    U = _rht_matrix(0xB7E1) / 4
+    assert np.array_equal(U.T @ U, np.eye(16))
+
+
+def test_rht_spreads_a_spike():
+    for j in range(16):
+        e = np.zeros(16, np.float32)
+        e[j] = 1.0
+        assert np.all(np.abs(oracle.rht16(e, 0x1234)) == 0.25)
+
+
+def test_rht_preserves_inner_products():
+    """(UA)^T (UB) = A^T B: exact for small integers (the butterfly is exact)."""
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        a = rng.integers(-8, 9, 16).astype(np.float32)
+        b = rng.integers(-8, 9, 16).astype(np.float32)
+        mask = int(rng.integers(0, 1 << 16))
+        ua = oracle.rht16(a, mask).astype(np.float64)
+        ub = oracle.rht16(b, mask).astype(np.float64)
+        assert ua @ ub == a.astype(np.float64) @ b.astype(np.float64)
+    for _ in range(200):
+        a = rng.standard_normal(16).astype(np.float32)
+        b = rng.standard_normal(16).astype(np.float32)
+        mask = int(rng.integers(0, 1 << 16))
+        lhs = oracle.rht16(a, mask).astype(np.float64) @ oracle.rht16(b, mask).astype(np.float64)
+        rhs = a.astype(np.float64) @ b.astype(np.float64)
+        assert abs(lhs - rhs) <= 1e-6 * (np.abs(a) @ np.abs(b)) + 1e-12
+
+
+# ------------------------------------------------------------ quantize ----
+def _rand_bits(rows, cols, seed, scale=1.0, outliers=0):
+    return inputs.normal(rows, cols, seed, scale, outliers)
+
+
+def test_tensor_scale_puts_the_amax_block_on_448():
+    """The tensor scale keeps every block scale inside E4M3 and the block that
+    holds the tensor amax gets the largest scale, 448."""
+    for seed in range(4):
+        x = _rand_bits(64, 256, seed, outliers=3)
+        q = oracle.quantize(x)
+        xf = inputs.bf16_bits_to_f32(x)
+        assert q["amax"] == np.abs(xf).max()
+        r, c = np.unravel_index(np.argmax(np.abs(xf)), xf.shape)
+        assert q["scales"][r, c // 16] == 0x7E
+        assert q["scales"].max() <= 0x7E
+        assert abs(float(q["s_enc"]) * float(q["s_g"]) - 1.0) < 1e-6
+
+
+def test_zero_tensor():
+    x = np.zeros((32, 64), np.uint16)
+    q = oracle.quantize(x)
+    assert q["amax"] == 0 and q["s_enc"] == 1 and q["s_g"] == 1
+    assert not q["codes"].any() and not q["scales"].any()
+
+
+def test_block_amax_lands_on_six_with_near_fp8_precision():
+    """Block amax -> FP4 max 6 and the amax element kept to E4M3 precision
+    ("Pretraining LLMs with NVFP4", Sec. 2: at least 1 of 16 at near-FP8)."""
+    x = _rand_bits(128, 512, 11, outliers=4)
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    q = oracle.quantize(x)
+    codes = _unpack(q["codes"])
+    deq = oracle.dequantize(q["codes"], q["scales"], q["s_g"])
+    blocks = np.abs(xf).reshape(128, 32, 16)
+    arg = blocks.argmax(axis=2)
+    checked = 0
+    for r in range(128):
+        for b in range(32):
+            if q["scales"][r, b] < 0x08:        # subnormal scale: invariant not claimed
+                continue
+            j = 16 * b + arg[r, b]
+            amax_b = blocks[r, b].max()
+            assert codes[r, j] & 7 == 7
+            assert abs(abs(deq[r, j]) - amax_b) <= (2 ** -4 + 2 ** -20) * amax_b
+            checked += 1
+    assert checked > 3000
+
+
+def test_rne_dequantized_error_within_half_step():
+    x = inputs.student_t(64, 1024, 12)
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    q = oracle.quantize(x)
+    deq = oracle.dequantize(q["codes"], q["scales"], q["s_g"])
+    unit = np.repeat(_torch_e4m3_values(q["scales"]), 16, axis=1) * float(q["s_g"])
+    # position of |x| on the grid of this block, in grid units
+    a = np.abs(xf) / np.where(unit == 0, 1, unit)
+    k = np.clip(np.searchsorted(GRID, a, side="right") - 1, 0, 6)
+    half_step = np.where(a >= 6, np.inf, (GRID[k + 1] - GRID[k]) / 2)
+    bound = half_step * unit * (1 + 2 ** -20) + 1e-30
+    sat = a >= 6
+    assert np.all(np.abs(deq - xf)[~sat] <= bound[~sat])
+    assert np.all(np.abs(deq)[sat] == 6 * unit[sat])
+
+
+@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("use_rht", [False, True])
+def test_colwise_equals_rowwise_of_transpose(rounding, use_rht):
+    x = _rand_bits(48, 80, 21, outliers=2)
+    kw = dict(scaling=0, rounding=rounding, use_rht=use_rht, sign_mask=0x3C5A, seed=99, stream_id=4)
+    col = oracle.quantize(x, oracle.COLWISE, **kw)
+    row_t = oracle.quantize(np.ascontiguousarray(x.T), oracle.ROWWISE, **kw)
+    assert col["amax"] == row_t["amax"]
+    assert np.array_equal(col["codes"], row_t["codes"])
+    assert np.array_equal(col["scales"], row_t["scales"])
+
+
+@pytest.mark.parametrize("rounding", [0, 1])
+def test_2d_colwise_is_exact_transpose(rounding):
+    """16x16 scaling gives the same quantized tensor in both orientations
+    ("Pretraining LLMs with NVFP4", Sec. 4 Two-dimensional scaling)."""
+    x = _rand_bits(64, 96, 31, scale=0.02)
+    kw = dict(scaling=1, rounding=rounding, seed=5, stream_id=1)
+    row = oracle.quantize(x, oracle.ROWWISE, **kw)
+    col = oracle.quantize(x, oracle.COLWISE, **kw)
+    assert np.array_equal(_unpack(row["codes"]), _unpack(col["codes"]).T)
+    # one scale per 16x16 tile, repeated along the tile's 16 rows
+    tiles_r = row["scales"].reshape(4, 16, 6)
+    assert np.all(tiles_r == tiles_r[:, :1, :])
+    assert np.array_equal(tiles_r[:, 0, :], col["scales"].reshape(6, 16, 4)[:, 0, :].T)
+    # the tile scale comes from the tile amax
+    xf = np.abs(inputs.bf16_bits_to_f32(x)).reshape(4, 16, 6, 16).max(axis=(1, 3))
+    r, c = np.unravel_index(np.argmax(xf), xf.shape)
+    assert tiles_r[r, 0, c] == 0x7E
+
+
+def test_rht_quantize_equals_quantize_of_rotated_input():
+    """With the RHT on, the oracle quantizes U x blockwise ("Full-Stack FP4"
+    Eq. (2)); for small-integer inputs U x is exact, so rotating by the
+    Sylvester matrix first and quantizing without RHT must agree bit for bit."""
+    rng = np.random.default_rng(8)
+    xf = rng.integers(-8, 9, (32, 64)).astype(np.float32)
+    mask = 0x9E37
+    U = (_sylvester(16) @ np.diag([-1 if (mask >> i) & 1 else 1 for i in range(16)])) / 4.0
+    rot = (xf.reshape(32, 4, 16).astype(np.float64) @ U.T).reshape(32, 64).astype(np.float32)
+    x = inputs.to_bf16_bits(xf)
+    x_rot = inputs.to_bf16_bits(rot)
+    assert np.array_equal(inputs.bf16_bits_to_f32(x_rot), rot)     # exact in bf16
+    for rounding in (0, 1):
+        a = oracle.quantize(x, use_rht=True, sign_mask=mask, rounding=rounding, seed=3)
+        b = oracle.quantize(x_rot, use_rht=False, rounding=rounding, seed=3)
+        assert a["amax"] == b["amax"]
+        assert np.array_equal(a["codes"], b["codes"]) and np.array_equal(a["scales"], b["scales"])
+
+
+def test_sr_quantize_is_seeded_and_stream_separated():
+    x = inputs.student_t(16, 256, 4)
+    a = oracle.quantize(x, rounding=1, seed=10, stream_id=1)
+    b = oracle.quantize(x, rounding=1, seed=10, stream_id=1)
+    c = oracle.quantize(x, rounding=1, seed=10, stream_id=2)
+    d = oracle.quantize(x, rounding=1, seed=11, stream_id=1)
+    assert np.array_equal(a["codes"], b["codes"])
+    assert not np.array_equal(a["codes"], c["codes"])
+    assert not np.array_equal(a["codes"], d["codes"])
+    assert np.array_equal(a["scales"], c["scales"])
+
+
+def test_quantize_row_subset_matches_full():
+    x = _rand_bits(64, 128, 2, outliers=1)
+    full = oracle.quantize(x, rounding=1, seed=1)
+    part = oracle.quantize(x, rounding=1, seed=1, rows_subset=(17, 40))
+    assert np.array_equal(full["codes"][17:40], part["codes"])
+    assert np.array_equal(full["scales"][17:40], part["scales"])
+
+
+def test_quantize_rejects_bad_shapes():
+    with pytest.raises(ValueError):
+        oracle.quantize(np.zeros((16, 24), np.uint16))
+    with pytest.raises(ValueError):
+        oracle.quantize(np.zeros((16, 32), np.uint16), scaling=1, use_rht=True)
+    with pytest.raises(ValueError):
+        oracle.quantize(np.zeros((24, 32), np.uint16), scaling=1)
+
+
+# ---------------------------------------------------------- dequantize ----
+def test_dequantize_grid_values():
+    codes4 = np.arange(16, dtype=np.uint8)
+    packed = (codes4[0::2] | (codes4[1::2] << 4)).reshape(1, 8)
+    ones = np.full((1, 1), 0x38, np.uint8)                # E4M3 1.0
+    deq = oracle.dequantize(packed, ones, 1.0)[0]
+    assert np.array_equal(deq[:8], GRID) and np.array_equal(deq[8:], -GRID)
+    # x^ = x_E2M1 * s * s_g ("Full-Stack FP4", Sec. 2) with dyadic s and s_g
+    sc = np.full((1, 1), 0x48, np.uint8)                 # E4M3 4.0 (exponent 9)
+    deq = oracle.dequantize(packed, sc, 0.125)[0]
+    assert np.array_equal(deq[:8], GRID * 4 * 0.125)
+
+
+def test_round_bf16_single_rounding():
+    rng = np.random.default_rng(9)
+    x = np.concatenate([rng.standard_normal(5000), rng.standard_normal(5000) * 1e-30,
+                        rng.standard_normal(5000) * 1e30]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    ours = np.array([oracle.round_bf16(float(v)) for v in x], np.uint16)
+    assert np.array_equal(ours, ref)
+    # above a bf16 tie by less than a float32 ulp: must round up, not to even
+    assert oracle.round_bf16(1.0 + 2 ** -8 + 2 ** -30) == 0x3F81
+    assert oracle.round_bf16(1.0 + 2 ** -8) == 0x3F80
+    assert oracle.round_bf16(-(1.0 + 3 * 2 ** -8)) == 0xBF82
+
+
+# ---------------------------------------------------------------- GEMM ----
+def _random_operand(rng, rows, K, scale_max=0x7E):
+    codes = rng.integers(0, 256, (rows, K // 2), dtype=np.uint8)
+    scales = rng.integers(0, scale_max + 1, (rows, K // 16), dtype=np.uint8)
+    s_g = np.float32(rng.uniform(0.01, 3.0))
+    return dict(codes=codes, scales=scales, s_g=s_g)
+
+
+def _exact_gemm(a, b):
+    """Exact rational y = s_gA s_gB sum_k (e2m1 * s)(e2m1 * s), decoded with the
+    page grid and torch's E4M3 table."""
+    ea = _e2m1_values(_unpack(a["codes"]))
+    eb = _e2m1_values(_unpack(b["codes"]))
+    sa = np.repeat(_torch_e4m3_values(a["scales"]), 16, axis=1)
+    sb = np.repeat(_torch_e4m3_values(b["scales"]), 16, axis=1)
+    M, K = ea.shape
+    N = eb.shape[0]
+    sg = Fraction(float(a["s_g"])) * Fraction(float(b["s_g"]))
+    y = np.empty((M, N), object)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                acc += Fraction(ea[m, k]) * Fraction(sa[m, k]) * Fraction(eb[n, k]) * Fraction(sb[n, k])
+            y[m, n] = acc * sg
+    return y
+
+
+def test_gemm_matches_exact_rational_brute_force():
+    rng = np.random.default_rng(13)
+    for _ in range(3):
+        a = _random_operand(rng, 4, 32)
+        b = _random_operand(rng, 4, 32)
+        y, ab = oracle.gemm_f64(a, b)
+        exact = _exact_gemm(a, b)
+        for m in range(4):
+            for n in range(4):
+                assert y[m, n] == float(exact[m, n])
+
+
+def test_gemm_integer_special_case():
+    """All scales 1 and s_g = 1: an integer-valued dot product of E2M1 values."""
+    rng = np.random.default_rng(14)
+    a = _random_operand(rng, 8, 64)
+    b = _random_operand(rng, 6, 64)
+    a["scales"][:] = 0x38
+    b["scales"][:] = 0x38
+    a["s_g"] = b["s_g"] = np.float32(1.0)
+    y, _ = oracle.gemm_f64(a, b)
+    ia = (2 * _e2m1_values(_unpack(a["codes"]))).astype(np.int64)
+    ib = (2 * _e2m1_values(_unpack(b["codes"]))).astype(np.int64)
+    assert np.array_equal(y * 4, (ia @ ib.T).astype(np.float64))
+
+
+def test_gemm_gram_matrix_is_symmetric_psd_diagonal():
+    x = _rand_bits(24, 128, 15)
+    q = oracle.quantize(x)
+    y, ab = oracle.gemm_f64(q, q)
+    assert np.array_equal(y, y.T)
+    assert np.all(np.diag(y) >= 0) and np.array_equal(np.diag(y), np.diag(ab))
+
+
+def test_gemm_row_subset():
+    rng = np.random.default_rng(16)
+    a = _random_operand(rng, 10, 64)
+    b = _random_operand(rng, 7, 64)
+    full, _ = oracle.gemm_f64(a, b)
+    sub, _ = oracle.gemm_f64(a, b, row_ids=[9, 0, 4])
+    assert np.array_equal(sub, full[[9, 0, 4]])
+
+
+def test_sr_gemm_error_variance_matches_eq5():
+    """Appendix 7, Eq. (5): with SR the output error is unbiased with variance
+    sum_i (x_i^2 s_w,i^2 + w_i^2 s_x,i^2 + s_x,i^2 s_w,i^2)."""
+    rng = np.random.default_rng(17)
+    K = 256
+    x = inputs.to_bf16_bits(rng.uniform(-1, 1, (3, K)).astype(np.float32))
+    w = inputs.to_bf16_bits(rng.uniform(-1, 1, (4, K)).astype(np.float32))
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    wf = inputs.bf16_bits_to_f32(w).astype(np.float64)
+    y_true = xf @ wf.T
+
+    def sr_var(bits, q):
+        vals = inputs.bf16_bits_to_f32(bits).astype(np.float64)
+        unit = np.repeat(_torch_e4m3_values(q["scales"]), 16, axis=1) * float(q["s_g"])
+        a = np.abs(vals) / unit
+        k = np.clip(np.searchsorted(GRID, a, side="right") - 1, 0, 6)
+        d = a - GRID[k]
+        return d * (GRID[k + 1] - GRID[k] - d) * unit ** 2
+
+    S = 400
+    errs = []
+    for s in range(S):
+        qx = oracle.quantize(x, rounding=1, seed=1000 + s, stream_id=1)
+        qw = oracle.quantize(w, rounding=1, seed=5000 + s, stream_id=2)
+        y, _ = oracle.gemm_f64(qx, qw, with_abs=False)
+        errs.append(y - y_true)
+    errs = np.array(errs)
+    var_x = sr_var(x, qx)
+    var_w = sr_var(w, qw)
+    pred = (xf ** 2) @ var_w.T + var_x @ (wf ** 2).T + var_x @ var_w.T
+    emp = errs.var(axis=0)
+    assert abs(emp.mean() / pred.mean() - 1) < 0.1
+    assert np.all(np.abs(errs.mean(axis=0)) <= 5 * np.sqrt(pred / S))
+
+
+# -------------------------------------------------------------- inputs ----
+def test_input_generators_are_seeded_and_shaped():
+    a = inputs.normal(32, 64, 1, outlier_channels=2)
+    b = inputs.normal(32, 64, 1, outlier_channels=2)
+    assert np.array_equal(a, b) and a.dtype == np.uint16
+    assert inputs.rht_sign_mask(3) == inputs.rht_sign_mask(3)
+    for rows, L in inputs.c5_sweep_sizes():
+        assert rows % 16 == 0 and rows * L <= 1 << 29
+    with open(os.path.join(GOLDEN, "model_3b_shapes.txt")) as f:
+        shapes = dict(line.split() for line in f if line.strip() and not line.startswith("#"))
+    assert int(shapes["hidden"]) == inputs.HIDDEN and int(shapes["ffn"]) == inputs.FFN
+    assert int(shapes["heads"]) == inputs.N_HEADS and int(shapes["kv_heads"]) == inputs.N_KV_HEADS
