@@ -1,0 +1,452 @@
+"""Benchmark: the full NVFP4 linear-layer step of the 3B model's FFN at 16384
+tokens on one GB300 (quantize every operand, then Fprop / Dgrad / Wgrad of the
+up 3072->9216 and down 9216->3072 projections).
+
+Prints one JSON line.  `value` is the step's GEMM work (6 GEMMs x 2*M*N*K)
+divided by the device time of the whole step (all quantize and GEMM kernels),
+inputs resident in HBM.  `e2e` is the same metric with the bf16 inputs copied
+from pinned host memory and the six outputs copied back inside the timed
+region.  `roofline` reports the kernel that takes most of the step's time
+against its measured peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 (torchrun) each rank runs an independent replica of the step: the
+path has no exchange step, so there is no collective on the data path.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 GEMM TFLOPS & quantize GB/s at 3B shapes, % of FP4/HBM roofline (1 GB300)"
+WORKLOAD = "c4_ffn_layer_step_16384tok"
+TOKENS, HIDDEN, FFN = 16384, 3072, 9216
+# FP4 dense peak = measured bf16 peak x nominal fp4/bf16 ratio (13.5 / 2.25)
+FP4_OVER_BF16 = 13.5 / 2.25
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ setup --
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# The step: (name, input, kwargs for ops.quantize) and the six GEMMs.
+QUANTS = [
+    ("X.row", "X", dict(rowwise=True)),
+    ("X.col_rht", "X", dict(rowwise=False, colwise=True, rht_mask="mask")),
+    ("W_up.2d", "W_up", dict(rowwise=True, colwise=True, two_d=True)),
+    ("H.row", "H", dict(rowwise=True)),
+    ("H.col_rht", "H", dict(rowwise=False, colwise=True, rht_mask="mask")),
+    ("W_down.2d", "W_down", dict(rowwise=True, colwise=True, two_d=True)),
+    ("dY_down.row_sr", "dY_down", dict(rowwise=True, sr=True, stream_id=1)),
+    ("dY_down.col_rht_sr", "dY_down", dict(rowwise=False, colwise=True, sr=True, rht_mask="mask",
+                                           stream_id=2)),
+    ("dY_up.row_sr", "dY_up", dict(rowwise=True, sr=True, stream_id=3)),
+    ("dY_up.col_rht_sr", "dY_up", dict(rowwise=False, colwise=True, sr=True, rht_mask="mask",
+                                       stream_id=4)),
+]
+GEMMS = [
+    # name, A (quant name, orientation), B (quant name, orientation)
+    ("fprop_up", ("X.row", "row"), ("W_up.2d", "row")),
+    ("fprop_down", ("H.row", "row"), ("W_down.2d", "row")),
+    ("dgrad_down", ("dY_down.row_sr", "row"), ("W_down.2d", "col")),
+    ("dgrad_up", ("dY_up.row_sr", "row"), ("W_up.2d", "col")),
+    ("wgrad_down", ("dY_down.col_rht_sr", "col"), ("H.col_rht", "col")),
+    ("wgrad_up", ("dY_up.col_rht_sr", "col"), ("X.col_rht", "col")),
+]
+SHAPES = {"X": (TOKENS, HIDDEN), "W_up": (FFN, HIDDEN), "H": (TOKENS, FFN), "W_down": (HIDDEN, FFN),
+          "dY_down": (TOKENS, HIDDEN), "dY_up": (TOKENS, FFN)}
+
+
+def host_inputs(seed_base=4):
+    from fp4_gemm_nvfp4_gb300 import inputs
+    wl = inputs.c4_ffn_layer_step(TOKENS)
+    return {name: wl.make(name) for name in SHAPES}, inputs.rht_sign_mask(seed_base)
+
+
+def quant_launches(kw):
+    """Kernels one quantize call launches: an amax pass and an encode pass per
+    RHT orientation, else one amax pass plus one encode pass."""
+    if kw.get("rht_mask") is not None:
+        return 2 * (int(kw.get("rowwise", True)) + int(kw.get("colwise", False)))
+    if kw.get("two_d"):
+        return 2
+    return 1 + int(kw.get("rowwise", True)) + int(kw.get("colwise", False))
+
+
+def quant_bytes(rows, cols, kw):
+    """Algorithmic HBM bytes of one quantize call: each amax pass reads the
+    input once, each encode pass reads it again and writes 0.5 B of codes and
+    1/16 B of scales per element per emitted orientation."""
+    n = rows * cols
+    outs = int(kw.get("rowwise", True)) + int(kw.get("colwise", False))
+    if kw.get("rht_mask") is not None:      # one amax and one encode pass per orientation
+        amax_passes, encode_reads = outs, outs
+    elif kw.get("two_d"):                   # one encode pass emits both orientations
+        amax_passes, encode_reads = 1, 1
+    else:
+        amax_passes, encode_reads = 1, outs
+    return n * 2 * (amax_passes + encode_reads) + n * outs * (0.5 + 1 / 16)
+
+
+class Step:
+    """Device buffers and the launch sequence of one layer step."""
+
+    def __init__(self, dev_inputs, mask, seed):
+        import torch
+        from fp4_gemm_nvfp4_gb300 import ops
+        self.torch, self.ops = torch, ops
+        self.x = dev_inputs
+        self.mask = mask
+        self.seed = seed
+        self.q = {}
+        self.kw = {}
+        for name, src, kw in QUANTS:
+            kw = dict(kw)
+            if kw.get("rht_mask") == "mask":
+                kw["rht_mask"] = mask
+            rows, cols = SHAPES[src]
+            row = ops.alloc_operand(rows, cols) if kw.get("rowwise", True) else None
+            col = ops.alloc_operand(cols, rows) if kw.get("colwise", False) else None
+            self.q[name] = (row, col)
+            self.kw[name] = kw
+        self.out = {}
+        for gname, (an, ao), (bn, bo) in GEMMS:
+            a = self.operand(an, ao)
+            b = self.operand(bn, bo)
+            self.out[gname] = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device="cuda")
+        self.ws = ops.Workspace()
+
+    def operand(self, name, orient):
+        row, col = self.q[name]
+        return row if orient == "row" else col
+
+    def flops(self):
+        total = 0
+        for gname, (an, ao), (bn, bo) in GEMMS:
+            a, b = self.operand(an, ao), self.operand(bn, bo)
+            total += 2 * a.rows * b.rows * a.cols
+        return total
+
+    def launches(self):
+        return sum(quant_launches(self.kw[n]) for n, _, _ in QUANTS) + len(GEMMS)
+
+    def run(self, events=None):
+        """Enqueue one step; with `events`, record a (start, end) pair around
+        every quantize call and every GEMM on the current stream."""
+        ops, torch = self.ops, self.torch
+        seed = self.seed
+        for name, src, _ in QUANTS:
+            kw = self.kw[name]
+            row, col = self.q[name]
+            if events is not None:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+            ops.quantize(self.x[src], out_row=row, out_col=col, seed=seed, workspace=self.ws, **kw)
+            if events is not None:
+                e1 = torch.cuda.Event(enable_timing=True)
+                e1.record()
+                events.append(("q:" + name, e0, e1))
+        for gname, (an, ao), (bn, bo) in GEMMS:
+            if events is not None:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+            ops.gemm(self.operand(an, ao), self.operand(bn, bo), out=self.out[gname])
+            if events is not None:
+                e1 = torch.cuda.Event(enable_timing=True)
+                e1.record()
+                events.append(("g:" + gname, e0, e1))
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ CPU oracle --
+def _oracle_kw(kw, mask, seed):
+    return dict(scaling=1 if kw.get("two_d") else 0, rounding=1 if kw.get("sr") else 0,
+                use_rht=kw.get("rht_mask") is not None,
+                sign_mask=mask if kw.get("rht_mask") is not None else 0,
+                seed=seed, stream_id=kw.get("stream_id", 0))
+
+
+def cpu_baseline(host, mask, seed, rows_a=8, rows_b=1024):
+    """The oracle, as it stands, on a bounded sample of the step.  Each GEMM
+    computes a rows_a x rows_b block of its output; the quantize calls encode
+    exactly the operand rows that block needs (each after the oracle's own
+    full-tensor amax pass).  Returns (GEMM FLOP of the sample / total seconds
+    in TFLOP/s, seconds, description, threads)."""
+    import oracle
+    src_of = {n: s for n, s, _ in QUANTS}
+    kw_of = {n: k for n, _, k in QUANTS}
+    t0 = time.perf_counter()
+    flops = 0
+    for gname, (an, ao), (bn, bo) in GEMMS:
+        ops_ = []
+        for qn, orient, nrows in ((an, ao, rows_a), (bn, bo, rows_b)):
+            o = oracle.ROWWISE if orient == "row" else oracle.COLWISE
+            ops_.append(oracle.quantize(host[src_of[qn]], o, rows_subset=(0, nrows),
+                                        **_oracle_kw(kw_of[qn], mask, seed)))
+        a, b = ops_
+        oracle.gemm_f64(a, b, with_abs=False)
+        flops += 2 * rows_a * rows_b * a["codes"].shape[1] * 2
+    dt = time.perf_counter() - t0
+    desc = (f"oracle on the host cores: each of the 6 GEMMs on a {rows_a} x {rows_b} block of its "
+            f"output, its operand rows quantized by the oracle (full-tensor amax pass included)")
+    return flops / dt / 1e12, dt, desc, oracle.num_threads()
+
+
+# --------------------------------------------------------------- measure --
+def measure(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    from fp4_gemm_nvfp4_gb300 import capi, ops
+
+    host, mask = host_inputs()
+    seed = 4 + 1000 * rank
+    dev = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in host.items()}
+    step = Step(dev, mask, seed)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+            torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step.run()
+    barrier()
+    status = ops.device_error()
+    if status != capi.NVFP4_OK:
+        raise RuntimeError(f"device status after warm-up: {capi.status_string(status)}")
+
+    # ---- device-resident timing: events around the step and every launch
+    per_step_events = []
+    with ClockSampler(local) as clocks:
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            ev = []
+            step.run(ev)
+            per_step_events.append(ev)
+        t_end.record(stream)
+        barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = t.item()
+    ms_per_step = total_ms / args.steps
+    launch_ms = {}
+    for ev in per_step_events:
+        for name, e0, e1 in ev:
+            launch_ms.setdefault(name, []).append(e0.elapsed_time(e1))
+    avg = {k: sum(v) / len(v) for k, v in launch_ms.items()}
+    flops = step.flops()
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs in, outputs out, every step
+    pinned_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+                 for k, v in host.items()}
+    pinned_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in step.out.items()}
+    h2d = sum(t.numel() * 2 for t in pinned_in.values())
+    d2h = sum(t.numel() * 2 for t in pinned_out.values())
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 5))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for k, t in pinned_in.items():
+            dev[k].copy_(t, non_blocking=True)
+        step.run()
+        for k, t in pinned_out.items():
+            t.copy_(step.out[k], non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = t.item()
+    status = ops.device_error()
+    if status != capi.NVFP4_OK:
+        raise RuntimeError(f"device status after timing: {capi.status_string(status)}")
+
+    # ---- roofline of the dominant kernel class
+    peaks, peak_src = load_peaks()
+    gemm_ms = sum(v for k, v in avg.items() if k.startswith("g:"))
+    quant_ms = sum(v for k, v in avg.items() if k.startswith("q:"))
+    gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
+    qbytes = 0.0
+    for name, src, kw in QUANTS:
+        qbytes += quant_bytes(*SHAPES[src], step.kw[name])
+    quant_gbs = qbytes / (quant_ms * 1e-3) / 1e9
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    if gemm_ms >= quant_ms:
+        roof = {"kernel": "gemm_nvf4_kernel (6 GEMMs of the step)", "bound": "tensor",
+                "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                "frac": round(gemm_tflops / fp4_peak, 4), "traffic": None,
+                "peak_source": f"{peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal fp4/bf16)"}
+    else:
+        roof = {"kernel": "quantize (amax + encode passes of the step)", "bound": "hbm",
+                "achieved": round(quant_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                "peak_source": f"{peak_src} hbm_gbs"}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
+                   "gemm_gflop_per_step": round(flops / 1e9, 1), "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (one step touches about 2 GB)"},
+        "roofline": roof,
+        "gemm_tflops": round(gemm_tflops, 1),
+        "gemm_frac_of_fp4_peak": round(gemm_tflops / fp4_peak, 4),
+        "quantize_gbs": round(quant_gbs, 1),
+        "quantize_frac_of_hbm": round(quant_gbs / peaks["hbm_gbs"], 4),
+        "per_launch_ms": {k: round(v, 4) for k, v in sorted(avg.items())},
+        "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": step.launches() * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, dt, desc, cores = cpu_baseline(host, mask, seed)
+        result["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                  "sample": desc, "seconds": round(dt, 2)}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return result, rank
+
+
+def reference_arm(args):
+    """The oracle as the reference implementation, on the host cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    host, mask = host_inputs()
+    seed = 4
+    kw = dict(rows_a=2, rows_b=256)
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(host, mask, seed, **kw)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, dt, desc, cores = cpu_baseline(host, mask, seed, **kw)
+        vals.append(v)
+    total = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN,
+                                            "ffn": FFN},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+    if args.impl == "reference":
+        r = reference_arm(args)
+        if r is not None:
+            print(json.dumps(r))
+        return
+    result, rank = measure(args)
+    if rank == 0:
+        print(json.dumps(result))
+
+
+if __name__ == "__main__":
+    main()

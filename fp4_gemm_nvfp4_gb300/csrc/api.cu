@@ -1,0 +1,181 @@
+// api.cu -- the C ABI of include/nvfp4.h: argument validation and dispatch.
+//
+// Every check runs on the host before anything is enqueued, so an error
+// status means no kernel was launched (except NVFP4_ERR_CUDA from a launch).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/nvfp4.h"
+#include "kernels.h"
+
+namespace {
+
+using nvfp4::QuantTarget;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Validate one emitted orientation (logical [lrows][lcols]).
+nvfp4_status check_target(const nvfp4_tensor* t, int64_t lrows, int64_t lcols) {
+    if (!t) return NVFP4_ERR_INVALID_ARG;
+    if (t->rows != lrows || t->cols != lcols) return NVFP4_ERR_INVALID_ARG;
+    if (!t->global_scale) return NVFP4_ERR_INVALID_ARG;
+    if (lrows > 0 && lcols > 0) {
+        if (!t->codes || !t->scales) return NVFP4_ERR_INVALID_ARG;
+        if (t->ld_codes < lcols / 2) return NVFP4_ERR_SHAPE;
+        if (t->ld_codes % 16 != 0 || !aligned16(t->codes) || !aligned16(t->scales)) return NVFP4_ERR_ALIGNMENT;
+    }
+    return NVFP4_OK;
+}
+
+QuantTarget to_target(const nvfp4_tensor* t) {
+    return QuantTarget{t->codes, t->ld_codes, t->scales, t->amax, t->global_scale, t->rows, t->cols};
+}
+
+nvfp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld_x, nvfp4_scaling scaling,
+                           nvfp4_rounding rounding, uint64_t seed, uint64_t stream_id, int orientations,
+                           const nvfp4_tensor* out_row, const nvfp4_tensor* out_col, bool rht, uint16_t mask,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (scaling != NVFP4_SCALE_1X16 && scaling != NVFP4_SCALE_16X16) return NVFP4_ERR_INVALID_ARG;
+    if (rounding != NVFP4_ROUND_RNE && rounding != NVFP4_ROUND_SR) return NVFP4_ERR_INVALID_ARG;
+    if (orientations < 1 || orientations > 3) return NVFP4_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+    const bool want_row = (orientations & NVFP4_ROWWISE) != 0;
+    const bool want_col = (orientations & NVFP4_COLWISE) != 0;
+    const bool two_d = scaling == NVFP4_SCALE_16X16;
+    if (rht && two_d) return NVFP4_ERR_UNSUPPORTED;
+    if (cols % 16 != 0) return NVFP4_ERR_SHAPE;
+    if ((two_d || want_col) && rows % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (rows > 0 && cols > 0) {
+        if (!x) return NVFP4_ERR_INVALID_ARG;
+        if (ld_x < cols) return NVFP4_ERR_SHAPE;
+        if (ld_x % 8 != 0 || !aligned16(x)) return NVFP4_ERR_ALIGNMENT;
+    }
+    if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return NVFP4_ERR_UNSUPPORTED;
+    if (rows * (cols / 16) >= (int64_t(1) << 32) - 1) return NVFP4_ERR_UNSUPPORTED;
+    nvfp4_status s;
+    if (want_row && (s = check_target(out_row, rows, cols)) != NVFP4_OK) return s;
+    if (want_col && (s = check_target(out_col, cols, rows)) != NVFP4_OK) return s;
+    if (!workspace || workspace_bytes < nvfp4::kQuantizeWorkspaceBytes || !aligned16(workspace))
+        return NVFP4_ERR_WORKSPACE;
+
+    QuantTarget tr{}, tc{};
+    if (want_row) tr = to_target(out_row);
+    if (want_col) tc = to_target(out_col);
+    const cudaError_t e = nvfp4::launch_quantize(
+        static_cast<const uint16_t*>(x), rows, cols, ld_x, two_d, rounding == NVFP4_ROUND_SR, rht, mask, seed,
+        stream_id, want_row ? &tr : nullptr, want_col ? &tc : nullptr, static_cast<float*>(workspace), stream);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status check_operand(const nvfp4_tensor* t) {
+    if (!t || !t->codes || !t->scales || !t->global_scale) return NVFP4_ERR_INVALID_ARG;
+    if (t->rows < 0 || t->cols < 0) return NVFP4_ERR_SHAPE;
+    if (t->cols % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (t->ld_codes < t->cols / 2) return NVFP4_ERR_SHAPE;
+    if (t->ld_codes % 16 != 0 || !aligned16(t->codes) || !aligned16(t->scales)) return NVFP4_ERR_ALIGNMENT;
+    if (t->rows >= (int64_t(1) << 31) || t->cols >= (int64_t(1) << 31)) return NVFP4_ERR_UNSUPPORTED;
+    return NVFP4_OK;
+}
+
+nvfp4::GemmOperand to_operand(const nvfp4_tensor* t) {
+    return nvfp4::GemmOperand{t->codes, t->ld_codes, t->scales, t->global_scale, t->rows, t->cols};
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nvfp4_scale_bytes(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return (size_t)(ceil_div(rows, 128) * ceil_div(cols, 64) * 512);
+}
+
+size_t nvfp4_quantize_workspace_size(int64_t rows, int64_t cols, int orientations) {
+    (void)rows;
+    (void)cols;
+    (void)orientations;
+    return nvfp4::kQuantizeWorkspaceBytes;
+}
+
+nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, nvfp4_scaling scaling,
+                            nvfp4_rounding rounding, uint64_t seed, uint64_t stream_id, int orientations,
+                            const nvfp4_tensor* out_row, const nvfp4_tensor* out_col, void* workspace,
+                            size_t workspace_bytes, nvfp4_stream_t stream) {
+    return quantize_impl(x, rows, cols, ld_x, scaling, rounding, seed, stream_id, orientations, out_row, out_col,
+                         false, 0, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, nvfp4_scaling scaling,
+                                nvfp4_rounding rounding, uint64_t seed, uint64_t stream_id, int orientations,
+                                const nvfp4_tensor* out_row, const nvfp4_tensor* out_col, uint16_t rht_sign_mask,
+                                void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    return quantize_impl(x, rows, cols, ld_x, scaling, rounding, seed, stream_id, orientations, out_row, out_col,
+                         true, rht_sign_mask, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, int64_t ldd,
+                        nvfp4_dtype out_dtype, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status s;
+    if ((s = check_operand(A)) != NVFP4_OK) return s;
+    if ((s = check_operand(B)) != NVFP4_OK) return s;
+    if (A->cols != B->cols) return NVFP4_ERR_SHAPE;
+    if (!D) return NVFP4_ERR_INVALID_ARG;
+    const int64_t M = A->rows, N = B->rows, K = A->cols;
+    const int64_t esz = out_dtype == NVFP4_OUT_FP32 ? 4 : 2;
+    if (ldd < N) return NVFP4_ERR_SHAPE;
+    if (!aligned16(D) || (ldd * esz) % 16 != 0) return NVFP4_ERR_ALIGNMENT;
+    if (ceil_div(M, 128) * ceil_div(N, 256) >= (int64_t(1) << 32)) return NVFP4_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (M == 0 || N == 0) return NVFP4_OK;
+    if (K == 0)   // empty reduction: D = 0
+        return cudaMemset2DAsync(D, (size_t)(ldd * esz), 0, (size_t)(N * esz), (size_t)M, st) == cudaSuccess
+                   ? NVFP4_OK
+                   : NVFP4_ERR_CUDA;
+    const cudaError_t e = nvfp4::launch_gemm(to_operand(A), to_operand(B), D, ldd, out_dtype == NVFP4_OUT_FP32, st);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, void* y, int64_t ldy, nvfp4_dtype out_dtype,
+                              nvfp4_stream_t stream) {
+    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status s;
+    if ((s = check_operand(q)) != NVFP4_OK) return s;
+    if (!y) return NVFP4_ERR_INVALID_ARG;
+    const int64_t esz = out_dtype == NVFP4_OUT_FP32 ? 4 : 2;
+    if (ldy < q->cols) return NVFP4_ERR_SHAPE;
+    if (!aligned16(y) || (ldy * esz) % 16 != 0) return NVFP4_ERR_ALIGNMENT;
+    if (q->rows * (q->cols / 16) >= (int64_t(1) << 32) - 1) return NVFP4_ERR_UNSUPPORTED;
+    const cudaError_t e = nvfp4::launch_dequantize(q->codes, q->ld_codes, q->scales, q->global_scale, q->rows,
+                                                   q->cols, y, ldy, out_dtype == NVFP4_OUT_FP32,
+                                                   reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+const char* nvfp4_status_string(nvfp4_status status) {
+    switch (status) {
+        case NVFP4_OK: return "NVFP4_OK";
+        case NVFP4_ERR_INVALID_ARG: return "NVFP4_ERR_INVALID_ARG";
+        case NVFP4_ERR_SHAPE: return "NVFP4_ERR_SHAPE";
+        case NVFP4_ERR_ALIGNMENT: return "NVFP4_ERR_ALIGNMENT";
+        case NVFP4_ERR_UNSUPPORTED: return "NVFP4_ERR_UNSUPPORTED";
+        case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
+        case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT";
+        case NVFP4_ERR_WORKSPACE: return "NVFP4_ERR_WORKSPACE";
+    }
+    return "NVFP4_ERR_UNKNOWN";
+}
+
+nvfp4_status nvfp4_device_error(nvfp4_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return NVFP4_ERR_CUDA;
+    unsigned int status = 0;
+    if (nvfp4::gemm_read_and_clear_status(&status) != cudaSuccess) return NVFP4_ERR_CUDA;
+    return (status & nvfp4::kStatusTimeoutBit) ? NVFP4_ERR_TIMEOUT : NVFP4_OK;
+}
+
+}  // extern "C"

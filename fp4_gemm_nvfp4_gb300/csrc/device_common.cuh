@@ -1,0 +1,393 @@
+// device_common.cuh -- device helpers shared by the NVFP4 kernels (sm_103a).
+//
+// Inline-PTX wrappers for mbarrier, TMA (cp.async.bulk*) and tcgen05, plus the
+// bit-level helpers of the NVFP4 format (E2M1 codes, E4M3 block scales, the
+// tile layout of the scale buffer).  Format facts: "Full-Stack FP4", Sec. 2
+// (x^ = x_E2M1 * s * s_g, 16-element blocks, E4M3 s, FP32 s_g); the byte and
+// bit layouts are the ones documented in include/nvfp4.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace nvfp4 {
+
+// ---------------------------------------------------------------- scales ---
+// Offset of block scale (r, j) in the tile layout: 128-row x 4-scale tiles of
+// 512 bytes, rows interleaved as (r % 32) * 16 + ((r / 32) % 4) * 4.
+__host__ __device__ __forceinline__ uint64_t scale_offset(uint32_t r, uint32_t j, uint32_t s4) {
+    return ((uint64_t)(r >> 7) * s4 + (j >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u +
+           (j & 3u);
+}
+
+// ------------------------------------------------------------ conversions ---
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// E4M3 (FN) encode of a finite non-negative value: nearest, ties to even,
+// saturating at 448.
+__device__ __forceinline__ uint32_t e4m3_encode_satfinite(float x) {
+    uint16_t pair;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.0f), "f"(x));
+    return pair & 0xFFu;
+}
+
+// E4M3 decode of a non-negative code (exact).
+__device__ __forceinline__ float e4m3_decode(uint32_t c) {
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    if (e == 0) return __uint2float_rn(m) * 0.001953125f;       // m * 2^-9
+    return __uint_as_float(((e + 120u) << 23) | (m << 20));     // 2^(e-7) * (1 + m/8)
+}
+
+// Eight values -> eight E2M1 codes (RNE, saturating), element 0 in the low
+// nibble.  The code's sign bit is forced to the value's sign bit so that
+// negative values rounding to zero encode as 0x8.
+__device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
+    uint32_t out;
+    asm("{\n\t"
+        ".reg .b8 q0, q1, q2, q3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+        "mov.b32 %0, {q0, q1, q2, q3};\n\t"
+        "}"
+        : "=r"(out)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    uint32_t signs = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) signs |= (__float_as_uint(v[i]) >> 31) << (4 * i + 3);
+    return out | signs;
+}
+
+// Stochastic rounding of one value to an E2M1 code with a 32-bit random word
+// ("Full-Stack FP4", Appendix 7: round up with probability d / step).  The
+// step is a power of two on every bin, so frac * 2^24 is exact.
+__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t word) {
+    const uint32_t sign = __float_as_uint(v) >> 31;
+    const float a = fabsf(v);
+    uint32_t code;
+    if (a >= 6.0f) {
+        code = 7u;
+    } else {
+        float lo, scale;
+        if (a < 2.0f) {          // grid 0, .5, 1, 1.5 (step 0.5)
+            code = (uint32_t)__fmul_rn(a, 2.0f);
+            lo = __fmul_rn((float)code, 0.5f);
+            scale = 33554432.0f;  // 2^24 / 0.5
+        } else if (a < 4.0f) {   // grid 2, 3 (step 1)
+            lo = floorf(a);
+            code = 2u + (uint32_t)lo;
+            scale = 16777216.0f;
+        } else {                 // grid 4 (step 2)
+            lo = 4.0f;
+            code = 6u;
+            scale = 8388608.0f;
+        }
+        const float frac24 = __fmul_rn(__fsub_rn(a, lo), scale);
+        code += (__uint2float_rn(word >> 8) < frac24) ? 1u : 0u;
+    }
+    return code | (sign << 3);
+}
+
+// --------------------------------------------------------------- Philox ----
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+// The four SR words of elements 4g .. 4g+3.
+__device__ __forceinline__ uint4 sr_words4(uint64_t seed, uint64_t stream_id, uint64_t g) {
+    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), (uint32_t)stream_id,
+                                    (uint32_t)(stream_id >> 32)),
+                         (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// ------------------------------------------------------------------ RHT ----
+// t <- H16 * D * t / 4: negate per mask, butterfly stages 0..3, times 0.25.
+__device__ __forceinline__ void rht16(float* t, uint32_t sign_mask) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = __uint_as_float(__float_as_uint(t[i]) ^ (((sign_mask >> i) & 1u) << 31));
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (i & (1 << s)) continue;
+            const float a = t[i], b = t[i | (1 << s)];
+            t[i] = __fadd_rn(a, b);
+            t[i | (1 << s)] = __fsub_rn(a, b);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = __fmul_rn(t[i], 0.25f);
+}
+
+// ------------------------------------------------------------ tensor scale -
+struct TensorScale {
+    float s_enc, s_g;
+};
+
+// S_enc = 2688 / amax (1 if amax == 0, FLT_MAX on overflow), s_g = 1 / S_enc.
+__device__ __forceinline__ TensorScale tensor_scale(float amax) {
+    float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(2688.0f, amax);
+    if (isinf(s)) s = 3.402823466e38f;
+    return {s, __fdiv_rn(1.0f, s)};
+}
+
+// Block scale code and encode multiplier r_b from the block amax.
+__device__ __forceinline__ uint32_t block_scale(float amax_b, float s_enc, float* r_b) {
+    const float sb32 = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
+    const uint32_t code = e4m3_encode_satfinite(sb32);
+    const float sb = e4m3_decode(code);
+    *r_b = (sb == 0.0f) ? 0.0f : __fdiv_rn(s_enc, sb);
+    return code;
+}
+
+// Encode the 16 values t of one block with multiplier r_b: codes in a uint2
+// (element 0 in the low nibble of byte 0).  idx_base is the SR index of
+// element 0 (a multiple of 16 for 1x16 blocks).
+template <bool kSR>
+__device__ __forceinline__ uint2 encode16(const float* t, float r_b, uint64_t seed, uint64_t stream_id,
+                                          uint64_t idx_base) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(t[i], r_b);
+    if constexpr (!kSR) {
+        return make_uint2(e2m1_rne_x8(v), e2m1_rne_x8(v + 8));
+    } else {
+        uint32_t w[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 r = sr_words4(seed, stream_id, (idx_base >> 2) + q);
+            w[4 * q + 0] = r.x; w[4 * q + 1] = r.y; w[4 * q + 2] = r.z; w[4 * q + 3] = r.w;
+        }
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            lo |= e2m1_sr(v[i], w[i]) << (4 * i);
+            hi |= e2m1_sr(v[8 + i], w[8 + i]) << (4 * i);
+        }
+        return make_uint2(lo, hi);
+    }
+}
+
+// ------------------------------------------------------------ reductions ---
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Max over `n` partial maxima, computed by the whole block; every thread gets
+// the result.  `red` is __shared__ float[32].
+__device__ __forceinline__ float block_max_of(const float* __restrict__ partials, int n, float* red) {
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, partials[i]);
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0.0f;
+        v = warp_max(v);
+        if (threadIdx.x == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float r = red[0];
+    __syncthreads();
+    return r;
+}
+
+// Block-wide max written to partials[blockIdx.x] by thread 0.
+__device__ __forceinline__ void block_max_store(float m, float* __restrict__ partials, float* red) {
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0.0f;
+        v = warp_max(v);
+        if (threadIdx.x == 0) partials[blockIdx.x] = v;
+    }
+}
+
+// --------------------------------------------------------------- memory ----
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
+    uint32_t r;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------------------- mbarrier ----
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete, giving up after timeout_ns.
+// Returns false on timeout; the caller records it.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try_wait(a, parity)) return true;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+// ------------------------------------------------------------------ TMA ----
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// Plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// --------------------------------------------------------------- tcgen05 ---
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has
+// completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// and stride byte offsets (>> 4), version 1 at bit 46, swizzle mode at 61.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swizzle << 61);
+}
+
+// D(tmem) (+)= A(smem) * B(smem)^T with E2M1 operands and per-16 E4M3 scales
+// taken from tensor memory (kind::mxf4nvf4, 4 scales per row per K = 64).
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+        "}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// Copy 32 rows x 16 bytes from shared memory into tensor-memory lanes 0-31
+// (4 columns), replicated into all four 32-lane groups.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns -> 32 registers per thread.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+}  // namespace nvfp4

@@ -1,0 +1,54 @@
+// kernels.h -- host-side launchers of the NVFP4 kernels (internal to the
+// library; the public interface is include/nvfp4.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+// Bit the kernels set in their device status word when a bounded wait runs out.
+constexpr unsigned int kStatusTimeoutBit = 1u;
+
+// One emitted orientation of a quantize call: logical [lrows][lcols].
+struct QuantTarget {
+    uint8_t* codes;
+    int64_t ld_codes;
+    uint8_t* scales;
+    float* amax;      // may be null
+    float* sg;
+    int64_t lrows, lcols;
+};
+
+// Device workspace floats the amax passes of one quantize call use.
+constexpr int kMaxAmaxPartials = 4096;
+constexpr size_t kQuantizeWorkspaceBytes = 2 * kMaxAmaxPartials * sizeof(float);
+
+cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool scale_2d,
+                            bool sr, bool rht, uint32_t sign_mask, uint64_t seed, uint64_t stream_id,
+                            const QuantTarget* row, const QuantTarget* col, float* workspace,
+                            cudaStream_t stream);
+
+struct GemmOperand {
+    const uint8_t* codes;
+    int64_t ld_codes;
+    const uint8_t* scales;
+    const float* sg;
+    int64_t rows, cols;
+};
+
+cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int64_t ldd, bool out_fp32,
+                        cudaStream_t stream);
+
+// Read and clear the GEMM kernels' device status word (synchronous).
+cudaError_t gemm_read_and_clear_status(unsigned int* status);
+
+cudaError_t launch_dequantize(const uint8_t* codes, int64_t ld_codes, const uint8_t* scales, const float* sg,
+                              int64_t rows, int64_t cols, void* y, int64_t ldy, bool out_fp32,
+                              cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace nvfp4

@@ -10,6 +10,7 @@ Shapes and distributions follow the pages' 3B model: hidden 3072, FFN 9216,
 float32 with numpy's PCG64 ``default_rng(seed)`` and rounded to bfloat16
 (nearest, ties to even).
 """
+import os
 from dataclasses import dataclass, field
 from typing import Dict, List, Tuple
 
@@ -35,25 +36,64 @@ def bf16_bits_to_f32(bits) -> np.ndarray:
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+_CHUNK_ROWS = 512          # fixed chunking: results do not depend on the thread count
+
+
+def _chunked(rows: int, cols: int, seed: int, draw) -> np.ndarray:
+    """Fill a float32 [rows, cols] array chunk by chunk of _CHUNK_ROWS rows;
+    chunk c draws from default_rng(SeedSequence([seed, c])).  Chunks run on a
+    thread pool (numpy's bulk samplers release the GIL)."""
+    out = np.empty((rows, cols), np.float32)
+    n_chunks = (rows + _CHUNK_ROWS - 1) // _CHUNK_ROWS
+
+    def work(c):
+        r0, r1 = c * _CHUNK_ROWS, min(rows, (c + 1) * _CHUNK_ROWS)
+        rng = np.random.default_rng(np.random.SeedSequence([seed, c]))
+        draw(rng, out[r0:r1])
+
+    if n_chunks <= 1:
+        for c in range(n_chunks):
+            work(c)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=min(n_chunks, os.cpu_count() or 1)) as ex:
+            list(ex.map(work, range(n_chunks)))
+    return out
+
+
 def normal(rows: int, cols: int, seed: int, std: float = 1.0, outlier_channels: int = 0,
            outlier_scale: float = 50.0) -> np.ndarray:
-    """N(0, std^2) bf16 bits; ``outlier_channels`` columns scaled by ``outlier_scale``."""
-    rng = np.random.default_rng(seed)
-    x = rng.standard_normal((rows, cols), dtype=np.float32)
-    if std != 1.0:
-        x *= np.float32(std)
+    """N(0, std^2) bf16 bits; ``outlier_channels`` columns (chosen by
+    default_rng(seed)) scaled by ``outlier_scale``."""
+    def draw(rng, block):
+        rng.standard_normal(block.shape, dtype=np.float32, out=block)
+        if std != 1.0:
+            block *= np.float32(std)
+
+    x = _chunked(rows, cols, seed, draw)
     if outlier_channels:
-        ch = rng.choice(cols, outlier_channels, replace=False)
+        ch = np.random.default_rng(seed).choice(cols, outlier_channels, replace=False)
         x[:, ch] *= np.float32(outlier_scale)
     return to_bf16_bits(x)
 
 
-def student_t(rows: int, cols: int, seed: int, df: float = 3.0, scale: float = 1e-3) -> np.ndarray:
-    """Student-t(df) * scale bf16 bits (heavy-tailed gradients)."""
-    rng = np.random.default_rng(seed)
-    x = rng.standard_t(df, size=(rows, cols)).astype(np.float32)
-    x *= np.float32(scale)
-    return to_bf16_bits(x)
+def student_t(rows: int, cols: int, seed: int, df: int = 3, scale: float = 1e-3) -> np.ndarray:
+    """Student-t(df) * scale bf16 bits (heavy-tailed gradients), drawn as
+    Z / sqrt(chi2_df / df) with chi2_df a sum of df squared standard normals."""
+    def draw(rng, block):
+        rng.standard_normal(block.shape, dtype=np.float32, out=block)
+        chi2 = np.zeros(block.shape, np.float32)
+        g = np.empty(block.shape, np.float32)
+        for _ in range(int(df)):
+            rng.standard_normal(block.shape, dtype=np.float32, out=g)
+            g *= g
+            chi2 += g
+        chi2 *= np.float32(1.0 / df)
+        np.sqrt(chi2, out=chi2)
+        block /= chi2
+        block *= np.float32(scale)
+
+    return to_bf16_bits(_chunked(rows, cols, seed, draw))
 
 
 def rht_sign_mask(seed: int) -> int:

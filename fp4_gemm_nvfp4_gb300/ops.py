@@ -1,0 +1,136 @@
+"""torch-facing helpers over the C ABI.
+
+PyTorch provides the device memory and the stream; every step of the
+quantize / GEMM / dequantize path runs in the library's CUDA kernels.  These
+helpers only allocate the caller-owned buffers the ABI expects and marshal
+pointers.
+"""
+from dataclasses import dataclass
+from typing import Optional, Tuple
+
+import torch
+
+from . import capi
+
+
+@dataclass
+class NVFP4Operand:
+    """Device buffers of one encoded operand (see nvfp4_tensor)."""
+    codes: torch.Tensor      # uint8 [rows, ld_codes]
+    scales: torch.Tensor     # uint8 [nvfp4_scale_bytes(rows, cols)]
+    amax: torch.Tensor       # float32 [1]
+    global_scale: torch.Tensor  # float32 [1]
+    rows: int
+    cols: int
+
+    @property
+    def ld_codes(self) -> int:
+        return self.codes.shape[1]
+
+    def struct(self) -> capi.nvfp4_tensor:
+        return capi.nvfp4_tensor(self.codes.data_ptr(), self.scales.data_ptr(),
+                                 self.amax.data_ptr(), self.global_scale.data_ptr(),
+                                 self.rows, self.cols, self.ld_codes)
+
+    def nbytes(self) -> int:
+        return self.codes.numel() + self.scales.numel() + 8
+
+
+def _round_up(v: int, m: int) -> int:
+    return (v + m - 1) // m * m
+
+
+def alloc_operand(rows: int, cols: int, device="cuda") -> NVFP4Operand:
+    ld = max(16, _round_up(cols // 2, 16))
+    nscale = max(16, capi.nvfp4_scale_bytes(rows, cols))
+    return NVFP4Operand(
+        codes=torch.empty((rows, ld), dtype=torch.uint8, device=device),
+        scales=torch.empty(nscale, dtype=torch.uint8, device=device),
+        amax=torch.empty(1, dtype=torch.float32, device=device),
+        global_scale=torch.empty(1, dtype=torch.float32, device=device),
+        rows=rows, cols=cols)
+
+
+def stream_handle(stream: Optional[torch.cuda.Stream] = None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class Workspace:
+    """Caller-owned scratch for the quantizer (one per stream)."""
+
+    def __init__(self, device="cuda"):
+        n = capi.nvfp4_quantize_workspace_size(0, 0, 3)
+        self.buf = torch.empty(n, dtype=torch.uint8, device=device)
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    @property
+    def nbytes(self) -> int:
+        return self.buf.numel()
+
+
+_workspaces = {}
+
+
+def _workspace(device) -> Workspace:
+    key = torch.device(device)
+    if key not in _workspaces:
+        _workspaces[key] = Workspace(key)
+    return _workspaces[key]
+
+
+def quantize(x: torch.Tensor, *, two_d: bool = False, sr: bool = False, rht_mask: Optional[int] = None,
+             seed: int = 0, stream_id: int = 0, rowwise: bool = True, colwise: bool = False,
+             out_row: Optional[NVFP4Operand] = None, out_col: Optional[NVFP4Operand] = None,
+             workspace: Optional[Workspace] = None, stream=None
+             ) -> Tuple[Optional[NVFP4Operand], Optional[NVFP4Operand]]:
+    """Quantize a bf16 CUDA matrix (nvfp4_quantize / nvfp4_rht_quantize)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    if rowwise and out_row is None:
+        out_row = alloc_operand(rows, cols, x.device)
+    if colwise and out_col is None:
+        out_col = alloc_operand(cols, rows, x.device)
+    ws = workspace or _workspace(x.device)
+    orient = (capi.NVFP4_ROWWISE if rowwise else 0) | (capi.NVFP4_COLWISE if colwise else 0)
+    sr_ = capi.NVFP4_ROUND_SR if sr else capi.NVFP4_ROUND_RNE
+    sc = capi.NVFP4_SCALE_16X16 if two_d else capi.NVFP4_SCALE_1X16
+    trow = out_row.struct() if rowwise else None
+    tcol = out_col.struct() if colwise else None
+    st = stream_handle(stream)
+    if rht_mask is None:
+        status = capi.nvfp4_quantize(x.data_ptr(), rows, cols, x.stride(0), sc, sr_, seed, stream_id,
+                                     orient, trow, tcol, ws.ptr, ws.nbytes, st)
+    else:
+        status = capi.nvfp4_rht_quantize(x.data_ptr(), rows, cols, x.stride(0), sc, sr_, seed,
+                                         stream_id, orient, trow, tcol, rht_mask, ws.ptr, ws.nbytes, st)
+    capi.check(status, "nvfp4_quantize")
+    return (out_row if rowwise else None), (out_col if colwise else None)
+
+
+def gemm(a: NVFP4Operand, b: NVFP4Operand, out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None,
+         stream=None) -> torch.Tensor:
+    """D = A * B^T (nvfp4_gemm)."""
+    if out is None:
+        out = torch.empty((a.rows, b.rows), dtype=out_dtype, device=a.codes.device)
+    dt = capi.NVFP4_OUT_FP32 if out.dtype == torch.float32 else capi.NVFP4_OUT_BF16
+    status = capi.nvfp4_gemm(a.struct(), b.struct(), out.data_ptr(), out.stride(0), dt, None, 0,
+                             stream_handle(stream))
+    capi.check(status, "nvfp4_gemm")
+    return out
+
+
+def dequantize(q: NVFP4Operand, out_dtype=torch.float32, stream=None) -> torch.Tensor:
+    """x^ = e2m1 * s_b * s_g (nvfp4_dequantize)."""
+    y = torch.empty((q.rows, q.cols), dtype=out_dtype, device=q.codes.device)
+    dt = capi.NVFP4_OUT_FP32 if out_dtype == torch.float32 else capi.NVFP4_OUT_BF16
+    capi.check(capi.nvfp4_dequantize(q.struct(), y.data_ptr(), y.stride(0), dt, stream_handle(stream)),
+               "nvfp4_dequantize")
+    return y
+
+
+def device_error(stream=None) -> int:
+    return capi.nvfp4_device_error(stream_handle(stream))

@@ -1,0 +1,219 @@
+/*
+ * nvfp4.h -- C ABI of the NVFP4 linear-layer library for one GB300 (sm_103a).
+ *
+ * The library quantizes bf16 tensors to NVFP4 and multiplies NVFP4 operands
+ * on the tcgen05 tensor cores.  Sources (page title, section):
+ *  [FS]  "Full-Stack FP4" (academ.us 2607.04422): Sec. 2 Preliminaries (NVFP4
+ *        format x^ = x_E2M1 * s * s_g, blocks of 1x16 or 16x16, the three
+ *        linear GEMMs); Sec. 3.2 Eq. (1)-(2) (Q_1x16, Q_16x1, Q_16x16 operands
+ *        of Fprop/Dgrad/Wgrad, H16^r random Hadamard on the Wgrad inputs);
+ *        Appendix 7 (E2M1 bins, RTN and SR).
+ *  [NV]  "Pretraining Large Language Models with NVFP4" (paperlayer
+ *        2509.25149v2): Sec. 2 NVFP4 Format (block amax -> FP4 max, E4M3
+ *        block scale, FP32 tensor scale); Sec. 4 Training Methodology (RNE for
+ *        weights and activations, SR on gradients, RHT on Wgrad inputs, 2D
+ *        weight scaling, FP4 GEMMs with BF16/FP32 outputs); B.4 (RHT scale
+ *        computed in the rotated space, H H^T = I).
+ *  [OT]  "OptiTrain-FP4" README (github mirror): E2M1 code table, Sylvester
+ *        Hadamard recursion, 1/sqrt(N) normalisation.
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE memory owned by the caller.  The library
+ *    allocates no memory and keeps no state between calls except one device
+ *    status word (see nvfp4_device_error).  It is safe to call from several
+ *    host threads.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  Arguments are validated on the host before any
+ *    launch; an error return means nothing was enqueued, except
+ *    NVFP4_ERR_CUDA, which reports a failed launch.  No C++ exception crosses
+ *    the ABI.
+ *  - bf16 inputs are row-major with a leading dimension in elements.  Inputs
+ *    must be finite; NaN or Inf inputs give unspecified codes.
+ *  - Numbers are bit-exact with the documented arithmetic (below); the
+ *    repository's CPU oracle implements the same arithmetic independently.
+ *
+ * Encoded operand (nvfp4_tensor)
+ *  A logical matrix [rows][cols] whose cols run along the GEMM reduction
+ *  dimension, stored as:
+ *   codes  : [rows][ld_codes] bytes; element (r, c) is the 4-bit E2M1 code in
+ *            byte codes[r*ld_codes + c/2], low nibble for even c.  Code bits:
+ *            sign (bit 3), exponent (bits 2:1, bias 1), mantissa (bit 0);
+ *            magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 for codes 0..7 [OT].
+ *   scales : one E4M3 (bias 7, max 448) block scale per 16 consecutive
+ *            elements of a row, in the tensor-core tile layout.  With
+ *            j = c / 16 and S4 = ceil(cols / 64):
+ *              offset(r, j) = ((r / 128) * S4 + j / 4) * 512
+ *                             + (r % 32) * 16 + ((r / 32) % 4) * 4 + j % 4
+ *            in a buffer of nvfp4_scale_bytes(rows, cols) bytes.  Padding
+ *            bytes (rows >= `rows` or j >= cols/16) are written as 0 by the
+ *            quantizer.  With 16x16 scaling the tile scale is repeated on each
+ *            of the tile's 16 rows.
+ *   amax   : 1 float, the tensor amax the scale was derived from (may be NULL).
+ *   global_scale : 1 float, the decode scale s_g; never leaves the device.
+ *  Decoding: x^(r, c) = e2m1(code) * e4m3(scale) * s_g [FS Sec. 2].
+ *
+ * Quantizer arithmetic (binary32, round-to-nearest-even, no fused ops)
+ *  1. amax_t = max |t| over the tensor, t = x, or t = U x per 16-block along
+ *     the emitted orientation's reduction dimension when the RHT is on
+ *     [NV B.4: the scale is computed in the rotated space].
+ *  2. S_enc = 2688 / amax_t (448 * 6: the tensor amax maps onto the largest
+ *     E4M3 scale times the largest E2M1 value) [NV Sec. 2]; S_enc = 1 when
+ *     amax_t = 0, FLT_MAX on overflow; s_g = 1 / S_enc.
+ *  3. per block: s_b = E4M3_rne_satfinite((amax_b / 6) * S_enc) [NV Sec. 2:
+ *     the block amax maps onto the FP4 maximum 6]; amax_b is over the 1x16
+ *     block or the 16x16 tile of x.
+ *  4. r_b = S_enc / s_b (0 if s_b = 0); v = t * r_b.
+ *  5. RNE: nearest E2M1 value, ties to the even mantissa, |v| > 6 -> 6 [NV
+ *     Sec. 4].  SR [FS App. 7]: round |v| up from grid point c_k to c_k+1 iff
+ *     (float)(w >> 8) < ((|v| - c_k) / step_k) * 2^24, w a 32-bit Philox4x32-10
+ *     word; |v| >= 6 -> 6.  The code's sign bit is the sign bit of v.
+ *  6. Philox4x32-10 (Salmon et al., SC'11) word for element idx:
+ *     key = (seed lo32, seed hi32), counter = (g lo32, g hi32, stream_id lo32,
+ *     stream_id hi32), g = idx / 4, word idx % 4; idx = r * cols + c in the
+ *     emitted logical matrix (for 16x16 scaling: the row-wise index of x, so
+ *     that both orientations share one draw per element).
+ *  7. RHT [FS Eq. (2), NV Sec. 4, OT]: U = H16 * D / 4, D = diag(-1 where bit
+ *     i of rht_sign_mask is set); computed as: negate per D, butterfly stages
+ *     s = 0, 1, 2, 3 mapping (t[i], t[i ^ 2^s]) (i without bit s) to
+ *     (t[i] + t[i ^ 2^s], t[i] - t[i ^ 2^s]), then multiply by 0.25.
+ *
+ * Orientations
+ *  ROWWISE emits the logical matrix x [rows][cols]; COLWISE emits x^T
+ *  [cols][rows], i.e. 1x16 blocks run down 16 consecutive rows of x (Q_16x1
+ *  of [FS Eq. (2)]).  For the three GEMMs of a linear layer Y = X W^T:
+ *   Fprop  Y  = X  W^T   : A = X rowwise,  B = W rowwise
+ *   Dgrad  dX = dY W     : A = dY rowwise, B = W colwise (16x16: same codes)
+ *   Wgrad  dW = dY^T X   : A = dY colwise, B = X colwise (RHT on both, same D)
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NVFP4_API __attribute__((visibility("default")))
+#else
+#define NVFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *nvfp4_stream_t;   /* a cudaStream_t */
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,   /* NULL pointer, bad enum, inconsistent tensor */
+    NVFP4_ERR_SHAPE = 2,         /* a dimension breaks the format (cols % 16 ...) */
+    NVFP4_ERR_ALIGNMENT = 3,     /* a pointer or leading dimension is misaligned */
+    NVFP4_ERR_UNSUPPORTED = 4,   /* valid but not implemented (e.g. 2D + RHT) */
+    NVFP4_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    NVFP4_ERR_TIMEOUT = 6,       /* a kernel gave up on a bounded wait */
+    NVFP4_ERR_WORKSPACE = 7      /* workspace missing or too small */
+} nvfp4_status;
+
+typedef enum { NVFP4_SCALE_1X16 = 0, NVFP4_SCALE_16X16 = 1 } nvfp4_scaling;
+typedef enum { NVFP4_ROUND_RNE = 0, NVFP4_ROUND_SR = 1 } nvfp4_rounding;
+typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_FP32 = 1 } nvfp4_dtype;
+enum { NVFP4_ROWWISE = 1, NVFP4_COLWISE = 2 };   /* bit mask of orientations to emit */
+
+typedef struct {
+    uint8_t *codes;          /* device, [rows][ld_codes] bytes */
+    uint8_t *scales;         /* device, nvfp4_scale_bytes(rows, cols) bytes, tile layout */
+    float   *amax;           /* device, 1 float, or NULL */
+    float   *global_scale;   /* device, 1 float: s_g */
+    int64_t  rows;           /* logical rows */
+    int64_t  cols;           /* logical columns = reduction dimension */
+    int64_t  ld_codes;       /* bytes between rows of codes */
+} nvfp4_tensor;
+
+/* Bytes of the scale buffer of a [rows][cols] operand (tile layout above). */
+NVFP4_API size_t nvfp4_scale_bytes(int64_t rows, int64_t cols);
+
+/* Bytes of device workspace nvfp4_quantize / nvfp4_rht_quantize need. */
+NVFP4_API size_t nvfp4_quantize_workspace_size(int64_t rows, int64_t cols, int orientations);
+
+/*
+ * nvfp4_quantize -- quantize x (bf16, [rows][ld_x], row-major) to NVFP4
+ * without the Hadamard transform [FS Sec. 2; NV Sec. 2, Sec. 4].
+ *  scaling      1x16 blocks (activations, gradients) or 16x16 tiles (weights).
+ *  rounding     RNE (weights, activations) or SR (gradients).
+ *  seed, stream_id  select the Philox stream of SR (ignored for RNE); use a
+ *               different stream_id for each quantization of one tensor.
+ *  orientations NVFP4_ROWWISE and/or NVFP4_COLWISE.
+ *  out_row      ROWWISE output: rows = rows, cols = cols (NULL if not emitted).
+ *  out_col      COLWISE output: rows = cols, cols = rows (NULL if not emitted).
+ *  workspace    device scratch of nvfp4_quantize_workspace_size() bytes,
+ *               16-byte aligned; used only during this call's kernels.
+ * Requirements (else the status in brackets):
+ *  cols % 16 == 0 [SHAPE]; COLWISE or 16x16: rows % 16 == 0 [SHAPE];
+ *  x 16-byte aligned, ld_x % 8 == 0, ld_x >= cols [ALIGNMENT / SHAPE];
+ *  codes 16-byte aligned, ld_codes % 16 == 0, ld_codes >= cols/2 of the
+ *  emitted orientation [ALIGNMENT / SHAPE]; scales 16-byte aligned; at most
+ *  2^32 - 1 blocks of 16 per orientation [UNSUPPORTED].
+ * Both orientations of one call share the tensor amax (no RHT) and write it
+ * to both tensors.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize(const void *x, int64_t rows, int64_t cols, int64_t ld_x,
+                            nvfp4_scaling scaling, nvfp4_rounding rounding,
+                            uint64_t seed, uint64_t stream_id, int orientations,
+                            const nvfp4_tensor *out_row, const nvfp4_tensor *out_col,
+                            void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_rht_quantize -- as nvfp4_quantize, with the 16-point random Hadamard
+ * transform U = H16 * D / 4 applied along the reduction dimension of each
+ * emitted orientation before scaling [FS Eq. (2); NV Sec. 4, B.4].  Each
+ * orientation gets its own amax and s_g, both taken in the rotated space.
+ * Pass the same rht_sign_mask for the two operands of one Wgrad GEMM: U^T U = I
+ * cancels in the product.  16x16 scaling with the RHT is NVFP4_ERR_UNSUPPORTED
+ * (the pages apply the RHT to the 1x16-scaled Wgrad inputs only).
+ */
+NVFP4_API nvfp4_status nvfp4_rht_quantize(const void *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                nvfp4_scaling scaling, nvfp4_rounding rounding,
+                                uint64_t seed, uint64_t stream_id, int orientations,
+                                const nvfp4_tensor *out_row, const nvfp4_tensor *out_col,
+                                uint16_t rht_sign_mask,
+                                void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm -- D = A * B^T with NVFP4 operands and FP32 accumulation
+ * [FS Sec. 2; NV Sec. 4: FP4 inputs, BF16 or FP32 outputs]:
+ *   D[m][n] = s_gA * s_gB * sum_k e2m1(a_mk) s_A(m, k/16) e2m1(b_nk) s_B(n, k/16)
+ *  A            [M][K] operand (A->rows = M, A->cols = K).
+ *  B            [N][K] operand (B->rows = N, B->cols = K).
+ *  D            device, row-major [M][ldd] of out_dtype (bf16 or fp32).
+ *  workspace    unused by the current kernels; may be NULL.
+ * Requirements: K % 16 == 0 [SHAPE]; M, N >= 1; codes/scales/D 16-byte
+ * aligned, ld_codes % 16 == 0, ldd * sizeof(out) % 16 == 0 [ALIGNMENT].
+ * The kernel's pipeline waits are bounded; a wait that runs out records a
+ * timeout which nvfp4_device_error() reports.
+ */
+NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_tensor *A, const nvfp4_tensor *B, void *D, int64_t ldd,
+                        nvfp4_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                        nvfp4_stream_t stream);
+
+/*
+ * nvfp4_dequantize -- y = e2m1(code) * s_b * s_g for every element of q
+ * [FS Sec. 2], rounded once (nearest even) to out_dtype; y is row-major
+ * [q->rows][ldy].  Requirements: y 16-byte aligned, ldy * sizeof(out) % 16 == 0.
+ */
+NVFP4_API nvfp4_status nvfp4_dequantize(const nvfp4_tensor *q, void *y, int64_t ldy,
+                              nvfp4_dtype out_dtype, nvfp4_stream_t stream);
+
+/* Human-readable name of a status. */
+NVFP4_API const char *nvfp4_status_string(nvfp4_status status);
+
+/*
+ * Synchronize `stream`, then read and clear the device status word that
+ * kernels set when a bounded wait runs out.  Returns NVFP4_OK,
+ * NVFP4_ERR_TIMEOUT, or NVFP4_ERR_CUDA if the synchronization failed.
+ */
+NVFP4_API nvfp4_status nvfp4_device_error(nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_H */

@@ -1,0 +1,157 @@
+"""CPU-side checks of the C ABI: the library loads, exports every entry point
+include/nvfp4.h declares, and its host-side validation rejects bad arguments
+before any CUDA call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from fp4_gemm_nvfp4_gb300 import build as libbuild
+from fp4_gemm_nvfp4_gb300 import capi
+from tests import helpers
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return capi.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"NVFP4_API\s+[\w\s\*]+?\b(nvfp4_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("nvfp4_quantize", "nvfp4_rht_quantize", "nvfp4_gemm", "nvfp4_dequantize"):
+        assert required in names
+    assert set(names) == set(capi.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert capi.nvfp4_status_string(code).startswith("NVFP4_")
+    assert capi.nvfp4_status_string(0) == "NVFP4_OK"
+    assert capi.nvfp4_status_string(99) == "NVFP4_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (128, 64), (129, 64), (128, 65 * 16), (8192, 3072),
+                                       (16384, 9216), (0, 64), (7, 0)])
+def test_scale_bytes_match_documented_layout(lib, rows, cols):
+    assert capi.nvfp4_scale_bytes(rows, cols) == helpers.scale_bytes(rows, cols)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (200, 48), (384, 1024), (130, 80)])
+def test_scale_layout_is_a_bijection_into_the_buffer(rows, cols):
+    m = helpers.scale_index_map(rows, cols)
+    assert m.min() >= 0 and m.max() < helpers.scale_bytes(rows, cols)
+    assert np.unique(m).size == m.size
+
+
+# ---- host-side validation (returns before any CUDA call) -------------------
+A16 = 1 << 20      # fake, 16-byte aligned "device" addresses: never dereferenced
+
+
+def tensor(rows, cols, ld=None, codes=A16, scales=A16 * 2, sg=A16 * 3):
+    return capi.nvfp4_tensor(codes, scales, 0, sg, rows, cols,
+                             ld if ld is not None else max(16, (cols // 2 + 15) // 16 * 16))
+
+
+def quantize(**kw):
+    args = dict(x=A16 * 4, rows=64, cols=64, ld_x=64, scaling=0, rounding=0, seed=0, stream_id=0,
+                orientations=1, out_row=tensor(64, 64), out_col=tensor(64, 64),
+                workspace=A16 * 5, workspace_bytes=capi.nvfp4_quantize_workspace_size(64, 64, 3),
+                stream=None)
+    args.update(kw)
+    return capi.nvfp4_quantize(*args.values())
+
+
+def test_quantize_validation(lib):
+    E = capi
+    assert quantize(cols=40, out_row=tensor(64, 40)) == E.NVFP4_ERR_SHAPE           # cols % 16
+    assert quantize(orientations=2, rows=24, out_col=tensor(64, 24)) == E.NVFP4_ERR_SHAPE
+    assert quantize(scaling=1, rows=24, out_row=tensor(24, 64)) == E.NVFP4_ERR_SHAPE
+    assert quantize(x=A16 + 8) == E.NVFP4_ERR_ALIGNMENT
+    assert quantize(ld_x=68) == E.NVFP4_ERR_ALIGNMENT
+    assert quantize(ld_x=48) == E.NVFP4_ERR_SHAPE
+    assert quantize(x=None) == E.NVFP4_ERR_INVALID_ARG
+    assert quantize(orientations=0) == E.NVFP4_ERR_INVALID_ARG
+    assert quantize(orientations=4) == E.NVFP4_ERR_INVALID_ARG
+    assert quantize(scaling=2) == E.NVFP4_ERR_INVALID_ARG
+    assert quantize(rounding=5) == E.NVFP4_ERR_INVALID_ARG
+    assert quantize(out_row=None) == E.NVFP4_ERR_INVALID_ARG
+    assert quantize(out_row=tensor(64, 32)) == E.NVFP4_ERR_INVALID_ARG               # wrong shape
+    assert quantize(orientations=2, out_col=tensor(32, 64)) == E.NVFP4_ERR_INVALID_ARG
+    assert quantize(out_row=tensor(64, 64, sg=0)) == E.NVFP4_ERR_INVALID_ARG
+    assert quantize(out_row=tensor(64, 64, ld=24)) == E.NVFP4_ERR_SHAPE               # ld < cols/2
+    assert quantize(out_row=tensor(64, 64, ld=40)) == E.NVFP4_ERR_ALIGNMENT
+    assert quantize(out_row=tensor(64, 64, codes=A16 + 4)) == E.NVFP4_ERR_ALIGNMENT
+    assert quantize(out_row=tensor(64, 64, scales=A16 + 1)) == E.NVFP4_ERR_ALIGNMENT
+    assert quantize(workspace=None) == E.NVFP4_ERR_WORKSPACE
+    assert quantize(workspace_bytes=16) == E.NVFP4_ERR_WORKSPACE
+    assert quantize(rows=-1) == E.NVFP4_ERR_SHAPE
+
+
+def test_rht_quantize_rejects_2d(lib):
+    ws = capi.nvfp4_quantize_workspace_size(64, 64, 3)
+    st = capi.nvfp4_rht_quantize(A16 * 4, 64, 64, 64, capi.NVFP4_SCALE_16X16, 0, 0, 0, 1,
+                                 tensor(64, 64), None, 0x1234, A16 * 5, ws, None)
+    assert st == capi.NVFP4_ERR_UNSUPPORTED
+
+
+def test_gemm_validation(lib):
+    E = capi
+
+    def gemm(A=None, B=None, D=A16 * 6, ldd=128, dt=0):
+        A = A if A is not None else tensor(128, 256)
+        B = B if B is not None else tensor(128, 256)
+        return capi.nvfp4_gemm(A, B, D, ldd, dt, None, 0, None)
+
+    assert gemm(B=tensor(128, 128)) == E.NVFP4_ERR_SHAPE            # K mismatch
+    assert gemm(A=tensor(128, 40, ld=32), B=tensor(128, 40, ld=32)) == E.NVFP4_ERR_SHAPE
+    assert gemm(D=None) == E.NVFP4_ERR_INVALID_ARG
+    assert gemm(D=A16 + 2) == E.NVFP4_ERR_ALIGNMENT
+    assert gemm(ldd=100) == E.NVFP4_ERR_SHAPE                       # ldd < N
+    assert gemm(ldd=132) == E.NVFP4_ERR_ALIGNMENT                   # 264 bytes
+    assert gemm(dt=7) == E.NVFP4_ERR_INVALID_ARG
+    assert gemm(A=tensor(128, 256, codes=0)) == E.NVFP4_ERR_INVALID_ARG
+    assert gemm(A=tensor(128, 256, ld=120)) == E.NVFP4_ERR_SHAPE
+    assert gemm(A=tensor(128, 256, ld=136)) == E.NVFP4_ERR_ALIGNMENT
+    # empty outputs are a no-op and touch nothing
+    assert gemm(A=tensor(0, 256)) == E.NVFP4_OK
+
+
+def test_dequantize_validation(lib):
+    E = capi
+    q = tensor(64, 64)
+    assert capi.nvfp4_dequantize(q, None, 64, 0, None) == E.NVFP4_ERR_INVALID_ARG
+    assert capi.nvfp4_dequantize(q, A16 + 2, 64, 0, None) == E.NVFP4_ERR_ALIGNMENT
+    assert capi.nvfp4_dequantize(q, A16, 32, 0, None) == E.NVFP4_ERR_SHAPE
+    assert capi.nvfp4_dequantize(q, A16, 68, 0, None) == E.NVFP4_ERR_ALIGNMENT
+    assert capi.nvfp4_dequantize(q, A16, 64, 3, None) == E.NVFP4_ERR_INVALID_ARG
+
+
+def test_product_path_fails_loudly_without_the_library(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        _fresh_load(str(tmp_path / "missing.so"))
+
+
+def _fresh_load(path):
+    saved = capi._lib
+    capi._lib = None
+    try:
+        return capi.load(path)
+    finally:
+        capi._lib = saved

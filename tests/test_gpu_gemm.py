@@ -1,0 +1,177 @@
+"""GPU parity of the NVFP4 GEMM against the oracle's FP64 GEMM, through the C
+ABI.  Tolerance: |y - y_ref| <= 1e-4 * sum_k |a_k b_k| + 1e-6 per element,
+plus half a bfloat16 ulp of y_ref for BF16 output (the rounding of the output
+itself)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_gemm_nvfp4_gb300 import build as libbuild
+from fp4_gemm_nvfp4_gb300 import capi, inputs, ops
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    libbuild.build()
+    capi.load()
+
+
+def _random_operand_host(rng, rows, K):
+    codes = rng.integers(0, 256, (rows, K // 2), dtype=np.uint8)
+    scales = rng.integers(0, 0x7F, (rows, K // 16), dtype=np.uint8)   # finite E4M3 >= 0
+    s_g = np.float32(rng.uniform(0.05, 2.0))
+    return dict(codes=codes, scales=scales, s_g=s_g)
+
+
+def _upload(host, rows, K):
+    op = ops.alloc_operand(rows, K)
+    codes = np.zeros((rows, op.ld_codes), np.uint8)
+    codes[:, : K // 2] = host["codes"]
+    tiled = np.zeros(op.scales.numel(), np.uint8)
+    if rows and K:
+        tiled[helpers.scale_index_map(rows, K)] = host["scales"]
+    op.codes.copy_(torch.from_numpy(codes))
+    op.scales.copy_(torch.from_numpy(tiled))
+    op.global_scale.fill_(float(host["s_g"]))
+    op.amax.fill_(0.0)
+    return op
+
+
+def _check(y, y_ref, abs_sum, bf16):
+    bound = helpers.gemm_bound(abs_sum, y_ref, bf16)
+    err = np.abs(y.astype(np.float64) - y_ref)
+    worst = np.unravel_index(np.argmax(err / bound), err.shape)
+    assert np.all(err <= bound), (f"{int((err > bound).sum())} of {err.size} outside the bound; "
+                                  f"worst at {worst}: y={y[worst]} ref={y_ref[worst]} "
+                                  f"bound={bound[worst]}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (1, 1, 16), (200, 300, 320), (130, 260, 80),
+                                   (384, 512, 1024), (257, 129, 4096), (64, 1000, 192)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_random_operands(M, N, K, out_dtype):
+    rng = np.random.default_rng(M * 1_000_003 + N * 1009 + K)
+    a_h = _random_operand_host(rng, M, K)
+    b_h = _random_operand_host(rng, N, K)
+    a, b = _upload(a_h, M, K), _upload(b_h, N, K)
+    y = ops.gemm(a, b, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    y_ref, abs_sum = oracle.gemm_f64(a_h, b_h)
+    _check(y.float().cpu().numpy(), y_ref, abs_sum, out_dtype == torch.bfloat16)
+
+
+def test_gemm_output_leading_dimension_and_no_overwrite():
+    rng = np.random.default_rng(3)
+    M, N, K = 136, 264, 128
+    a_h, b_h = _random_operand_host(rng, M, K), _random_operand_host(rng, N, K)
+    a, b = _upload(a_h, M, K), _upload(b_h, N, K)
+    big = torch.full((M + 3, 320), 7.0, dtype=torch.float32, device="cuda")
+    ops.gemm(a, b, out=big[:M, :N])
+    torch.cuda.synchronize()
+    y_ref, abs_sum = oracle.gemm_f64(a_h, b_h)
+    host = big.cpu().numpy()
+    _check(host[:M, :N], y_ref, abs_sum, False)
+    assert np.all(host[:M, N:] == 7.0) and np.all(host[M:] == 7.0)
+
+
+def test_gemm_zero_k_gives_zero():
+    a = ops.alloc_operand(64, 0)
+    b = ops.alloc_operand(32, 0)
+    a.global_scale.fill_(1.0)
+    b.global_scale.fill_(1.0)
+    y = torch.full((64, 32), 5.0, dtype=torch.float32, device="cuda")
+    ops.gemm(a, b, out=y)
+    assert torch.count_nonzero(y).item() == 0
+
+
+def _quantized_pair(x_bits, w_bits, a_kw, b_kw):
+    """GPU and oracle quantizations of the same seeded inputs."""
+    xa = helpers.to_device_bf16(x_bits)
+    xb = helpers.to_device_bf16(w_bits)
+
+    def gpu(x, orientation, scaling=0, rounding=0, use_rht=False, sign_mask=0, seed=0, stream_id=0):
+        row, col = ops.quantize(x, two_d=scaling == 1, sr=rounding == 1,
+                                rht_mask=sign_mask if use_rht else None, seed=seed, stream_id=stream_id,
+                                rowwise=orientation == oracle.ROWWISE,
+                                colwise=orientation == oracle.COLWISE)
+        return row if orientation == oracle.ROWWISE else col
+
+    return gpu(xa, **a_kw), gpu(xb, **b_kw)
+
+
+def test_gemm_c1_single_linear_forward():
+    """128 tokens x 1024 -> 1024, outlier channels, 1x16 RNE on both operands."""
+    wl = inputs.c1_single_linear()
+    x_bits, w_bits = wl.make("X"), wl.make("W")
+    ga, gb = _quantized_pair(x_bits, w_bits, dict(orientation=oracle.ROWWISE),
+                             dict(orientation=oracle.ROWWISE))
+    qa = oracle.quantize(x_bits)
+    qb = oracle.quantize(w_bits)
+    y_ref, abs_sum = oracle.gemm_f64(qa, qb)
+    for dt in (torch.float32, torch.bfloat16):
+        y = ops.gemm(ga, gb, out_dtype=dt)
+        torch.cuda.synchronize()
+        _check(y.float().cpu().numpy(), y_ref, abs_sum, dt == torch.bfloat16)
+
+
+FULL = {
+    # name: (A rows, A cols, A kind, A quantizer kw, B rows, B cols, B kind, B quantizer kw)
+    "c2_fprop_qkv": (8192, 3072, "normal", dict(orientation=oracle.ROWWISE),
+                     6144, 3072, "weight", dict(orientation=oracle.ROWWISE, scaling=1)),
+    "c2_dgrad_o": (8192, 3072, "grad", dict(orientation=oracle.ROWWISE),
+                   3072, 3072, "weight", dict(orientation=oracle.COLWISE, scaling=1)),
+    "c3_wgrad": (8192, 9216, "grad", dict(orientation=oracle.COLWISE, rounding=1, use_rht=True,
+                                          sign_mask=0x6B2D, seed=3, stream_id=2),
+                 8192, 3072, "normal", dict(orientation=oracle.COLWISE, use_rht=True, sign_mask=0x6B2D)),
+}
+
+
+def _make(kind, rows, cols, seed):
+    if kind == "normal":
+        return inputs.normal(rows, cols, seed, outlier_channels=inputs.outlier_count(cols))
+    if kind == "weight":
+        return inputs.normal(rows, cols, seed, std=0.02)
+    return inputs.student_t(rows, cols, seed)
+
+
+@pytest.mark.parametrize("name", sorted(FULL))
+def test_gemm_full_size_sampled_rows(name):
+    ar, ac, ak, akw, br, bc, bk, bkw = FULL[name]
+    a_bits, b_bits = _make(ak, ar, ac, 11), _make(bk, br, bc, 12)
+    ga, gb = _quantized_pair(a_bits, b_bits, akw, bkw)
+    y = ops.gemm(ga, gb, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    M, N = ga.rows, gb.rows
+    rng = np.random.default_rng(7)
+    rows = np.sort(rng.choice(M, 24, replace=False))
+    rows[0], rows[-1] = 0, M - 1
+    qa = oracle.quantize(a_bits, **akw)
+    qb = oracle.quantize(b_bits, **bkw)
+    y_ref, abs_sum = oracle.gemm_f64(qa, qb, row_ids=rows)
+    _check(y[torch.from_numpy(rows).cuda()].float().cpu().numpy(), y_ref, abs_sum, True)
+
+
+def test_wgrad_rht_cancels_in_the_product():
+    """(U A)^T (U B) = A^T B: the Wgrad GEMM of RHT-quantized operands tracks the
+    un-rotated product within the quantization noise (Full-Stack FP4 Eq. (2))."""
+    T, N, K = 2048, 256, 256
+    dy = inputs.student_t(T, N, 21)
+    x = inputs.normal(T, K, 22)
+    ga, gb = _quantized_pair(dy, x, dict(orientation=oracle.COLWISE, rounding=1, use_rht=True,
+                                         sign_mask=0x1357, seed=5),
+                             dict(orientation=oracle.COLWISE, use_rht=True, sign_mask=0x1357))
+    y = ops.gemm(ga, gb, out_dtype=torch.float32).cpu().numpy().astype(np.float64)
+    exact = inputs.bf16_bits_to_f32(dy).astype(np.float64).T @ inputs.bf16_bits_to_f32(x).astype(np.float64)
+    rel = np.linalg.norm(y - exact) / np.linalg.norm(exact)
+    assert rel < 0.3          # quantization noise only (about 0.17 here)
+    # with different sign diagonals the rotations do not cancel
+    ga2, gb2 = _quantized_pair(dy, x, dict(orientation=oracle.COLWISE, use_rht=True, sign_mask=0x1357),
+                               dict(orientation=oracle.COLWISE, use_rht=True, sign_mask=0xECA8))
+    y2 = ops.gemm(ga2, gb2, out_dtype=torch.float32).cpu().numpy().astype(np.float64)
+    assert np.linalg.norm(y2 - exact) / np.linalg.norm(exact) > 0.8

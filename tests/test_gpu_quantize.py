@@ -1,0 +1,157 @@
+"""GPU parity of the quantizer against the CPU oracle (bit-exact codes, block
+scales, amax and s_g), through the C ABI."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_gemm_nvfp4_gb300 import build as libbuild
+from fp4_gemm_nvfp4_gb300 import capi, inputs, ops
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    libbuild.build()
+    capi.load()
+
+
+def gpu_quantize(bits, orientation, scaling=0, rounding=0, use_rht=False, sign_mask=0, seed=0,
+                 stream_id=0):
+    x = helpers.to_device_bf16(bits)
+    row, col = ops.quantize(x, two_d=scaling == 1, sr=rounding == 1,
+                            rht_mask=sign_mask if use_rht else None, seed=seed, stream_id=stream_id,
+                            rowwise=orientation == oracle.ROWWISE, colwise=orientation == oracle.COLWISE)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    return row if orientation == oracle.ROWWISE else col
+
+
+def assert_parity(bits, orientation, rows_subset=None, **kw):
+    g = gpu_quantize(bits, orientation, **kw)
+    codes, scales, amax, sg, tiled = helpers.operand_to_host(g)
+    ref = oracle.quantize(bits, orientation, rows_subset=rows_subset, **kw)
+    assert amax == ref["amax"], (amax, ref["amax"])
+    assert sg == ref["s_g"]
+    lr0, lr1 = ref["rows"]
+    bad = np.argwhere(codes[lr0:lr1] != ref["codes"])
+    assert bad.size == 0, f"{len(bad)} code bytes differ, first at {bad[:4].tolist()}"
+    bad = np.argwhere(scales[lr0:lr1] != ref["scales"])
+    assert bad.size == 0, f"{len(bad)} scales differ, first at {bad[:4].tolist()}"
+    if rows_subset is None and g.rows and g.cols:
+        assert not tiled[helpers.padding_mask(g.rows, g.cols)].any(), "scale padding not zero"
+    return g
+
+
+MODES = [
+    # (scaling, rounding, rht)
+    (0, 0, False), (0, 1, False), (0, 0, True), (0, 1, True), (1, 0, False), (1, 1, False),
+]
+
+
+@pytest.mark.parametrize("scaling,rounding,rht", MODES)
+@pytest.mark.parametrize("orientation", [oracle.ROWWISE, oracle.COLWISE])
+@pytest.mark.parametrize("shape", [(16, 16), (272, 336), (128, 1024), (400, 192)])
+def test_quantize_parity_small(shape, orientation, scaling, rounding, rht):
+    rows, cols = shape
+    bits = inputs.normal(rows, cols, seed=rows * 7 + cols, outlier_channels=2)
+    assert_parity(bits, orientation, scaling=scaling, rounding=rounding, use_rht=rht,
+                  sign_mask=0xA55A, seed=123456789, stream_id=5)
+
+
+@pytest.mark.parametrize("rounding", [0, 1])
+def test_quantize_rowwise_ragged_rows(rounding):
+    # rows need not be a multiple of 16 for row-wise 1x16 blocks
+    bits = inputs.student_t(1000, 64, seed=3)
+    assert_parity(bits, oracle.ROWWISE, rounding=rounding, seed=9)
+
+
+def test_quantize_zero_tensor():
+    bits = np.zeros((64, 128), np.uint16)
+    for orientation in (oracle.ROWWISE, oracle.COLWISE):
+        g = assert_parity(bits, orientation)
+        codes, scales, amax, sg, _ = helpers.operand_to_host(g)
+        assert amax == 0 and sg == 1 and not codes.any() and not scales.any()
+
+
+def test_quantize_ties_and_negative_zero():
+    """With amax = 2688 the tensor scale is exactly 1 and a block with amax 6
+    gets scale 1, so its values hit the E2M1 ties unchanged."""
+    row = np.array([6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -1.25, -1.75, -2.5,
+                    -3.5, -5.0, -0.1], np.float32)
+    x = np.tile(row, (32, 4))
+    x[0, 0] = 2688.0
+    bits = inputs.to_bf16_bits(x)
+    g = assert_parity(bits, oracle.ROWWISE)
+    codes, _, _, _, _ = helpers.operand_to_host(g)
+    nib = np.stack([codes & 0xF, codes >> 4], -1).reshape(32, -1)
+    assert list(nib[1, :16]) == [7, 0, 2, 2, 4, 4, 6, 6, 8, 10, 10, 12, 12, 14, 14, 8]
+    assert_parity(bits, oracle.ROWWISE, rounding=1, seed=1)
+
+
+def test_quantize_both_orientations_in_one_call():
+    bits = inputs.normal(256, 320, seed=44, outlier_channels=3)
+    x = helpers.to_device_bf16(bits)
+    for kw in (dict(), dict(sr=True, seed=4), dict(rht_mask=0x0F0F), dict(two_d=True)):
+        row, col = ops.quantize(x, rowwise=True, colwise=True, stream_id=2, **kw)
+        torch.cuda.synchronize()
+        common = dict(scaling=1 if kw.get("two_d") else 0, rounding=1 if kw.get("sr") else 0,
+                      use_rht="rht_mask" in kw, sign_mask=kw.get("rht_mask", 0),
+                      seed=kw.get("seed", 0), stream_id=2)
+        for op, orient in ((row, oracle.ROWWISE), (col, oracle.COLWISE)):
+            codes, scales, amax, sg, _ = helpers.operand_to_host(op)
+            ref = oracle.quantize(bits, orient, **common)
+            assert amax == ref["amax"] and sg == ref["s_g"]
+            assert np.array_equal(codes, ref["codes"]) and np.array_equal(scales, ref["scales"])
+
+
+def test_quantize_respects_leading_dimension():
+    bits = inputs.normal(96, 256, seed=5)
+    x_wide = torch.zeros((96, 320), dtype=torch.bfloat16, device="cuda")
+    x_wide[:, :256] = helpers.to_device_bf16(bits)
+    row, col = ops.quantize(x_wide[:, :256], rowwise=True, colwise=True, sr=True, seed=3)
+    torch.cuda.synchronize()
+    for op, orient in ((row, oracle.ROWWISE), (col, oracle.COLWISE)):
+        codes, scales, amax, sg, _ = helpers.operand_to_host(op)
+        ref = oracle.quantize(bits, orient, rounding=1, seed=3)
+        assert np.array_equal(codes, ref["codes"]) and np.array_equal(scales, ref["scales"])
+
+
+# ---- full-size workloads (sampled logical rows; the oracle takes the amax
+# over the whole tensor itself) -------------------------------------------
+def _ranges(n, k=48):
+    mid = (n // 2) // 16 * 16
+    return [(0, k), (mid, mid + k), (n - k, n)]
+
+
+@pytest.mark.parametrize("name,rows,cols,kind,orientation,scaling,rounding,rht", [
+    ("c2_X", 8192, 3072, "normal", oracle.ROWWISE, 0, 0, False),
+    ("c2_Wqkv_row", 6144, 3072, "weight", oracle.ROWWISE, 1, 0, False),
+    ("c2_Wqkv_col", 6144, 3072, "weight", oracle.COLWISE, 1, 0, False),
+    ("c3_dY_col", 8192, 9216, "grad", oracle.COLWISE, 0, 1, True),
+    ("c3_X_col", 8192, 3072, "normal", oracle.COLWISE, 0, 0, True),
+    ("c4_dY_row", 16384, 3072, "grad", oracle.ROWWISE, 0, 1, False),
+])
+def test_quantize_parity_full_size(name, rows, cols, kind, orientation, scaling, rounding, rht):
+    seed = zlib.crc32(name.encode()) % 1000
+    if kind == "normal":
+        bits = inputs.normal(rows, cols, seed, outlier_channels=inputs.outlier_count(cols))
+    elif kind == "weight":
+        bits = inputs.normal(rows, cols, seed, std=0.02)
+    else:
+        bits = inputs.student_t(rows, cols, seed)
+    g = gpu_quantize(bits, orientation, scaling=scaling, rounding=rounding, use_rht=rht,
+                     sign_mask=inputs.rht_sign_mask(seed), seed=seed, stream_id=1)
+    codes, scales, amax, sg, _ = helpers.operand_to_host(g)
+    lrows = rows if orientation == oracle.ROWWISE else cols
+    for lr0, lr1 in _ranges(lrows):
+        ref = oracle.quantize(bits, orientation, scaling=scaling, rounding=rounding, use_rht=rht,
+                              sign_mask=inputs.rht_sign_mask(seed), seed=seed, stream_id=1,
+                              rows_subset=(lr0, lr1))
+        assert amax == ref["amax"] and sg == ref["s_g"]
+        assert np.array_equal(codes[lr0:lr1], ref["codes"])
+        assert np.array_equal(scales[lr0:lr1], ref["scales"])
