@@ -28,8 +28,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 GEMM TFLOPS & quantize GB/s at 3B shapes, % of FP4/HBM roofline (1 GB300)"
-WORKLOAD = "c4_ffn_layer_step_16384tok"
-TOKENS, HIDDEN, FFN = 16384, 3072, 9216
+HIDDEN, FFN = 3072, 9216
+TOKENS = 16384          # the full layer step; --tokens scales it down for profiling
 # FP4 dense peak = measured bf16 peak x nominal fp4/bf16 ratio (13.5 / 2.25)
 FP4_OVER_BF16 = 13.5 / 2.25
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -75,8 +75,21 @@ GEMMS = [
     ("wgrad_down", ("dY_down.col_rht_sr", "col"), ("H.col_rht", "col")),
     ("wgrad_up", ("dY_up.col_rht_sr", "col"), ("X.col_rht", "col")),
 ]
-SHAPES = {"X": (TOKENS, HIDDEN), "W_up": (FFN, HIDDEN), "H": (TOKENS, FFN), "W_down": (HIDDEN, FFN),
-          "dY_down": (TOKENS, HIDDEN), "dY_up": (TOKENS, FFN)}
+SHAPES = {}
+
+
+def set_tokens(tokens):
+    global TOKENS
+    TOKENS = tokens
+    SHAPES.update({"X": (tokens, HIDDEN), "W_up": (FFN, HIDDEN), "H": (tokens, FFN),
+                   "W_down": (HIDDEN, FFN), "dY_down": (tokens, HIDDEN), "dY_up": (tokens, FFN)})
+
+
+set_tokens(TOKENS)
+
+
+def workload_name():
+    return f"c4_ffn_layer_step_{TOKENS}tok"
 
 
 def host_inputs(seed_base=4):
@@ -378,7 +391,7 @@ def measure(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
+        "config": {"workload": workload_name(), "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
                    "gemm_gflop_per_step": round(flops / 1e9, 1), "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (one step touches about 2 GB)"},
         "roofline": roof,
@@ -421,7 +434,7 @@ def reference_arm(args):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN,
+            "data": "synthetic", "config": {"workload": workload_name(), "tokens": TOKENS, "hidden": HIDDEN,
                                             "ffn": FFN},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": desc},
@@ -435,7 +448,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=TOKENS,
+                    help="tokens of the layer step (16384 is the benchmarked workload)")
     args = ap.parse_args()
+    set_tokens(args.tokens)
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
     if args.impl == "reference":

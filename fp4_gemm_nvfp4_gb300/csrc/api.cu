@@ -129,7 +129,7 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, i
     const int64_t M = A->rows, N = B->rows, K = A->cols;
     const int64_t esz = out_dtype == NVFP4_OUT_FP32 ? 4 : 2;
     if (ldd < N) return NVFP4_ERR_SHAPE;
-    if (!aligned16(D) || (ldd * esz) % 16 != 0) return NVFP4_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(D) % (uintptr_t)esz) != 0) return NVFP4_ERR_ALIGNMENT;
     if (ceil_div(M, 128) * ceil_div(N, 256) >= (int64_t(1) << 32)) return NVFP4_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (M == 0 || N == 0) return NVFP4_OK;

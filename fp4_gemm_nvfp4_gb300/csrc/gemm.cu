@@ -69,6 +69,7 @@ struct Params {
     void* d;
     int64_t ldd;
     int out_fp32;
+    int vec_store;             // every output row starts on a 16-byte boundary
 };
 
 // Instruction descriptor for kind::mxf4nvf4: A and B E2M1 (format 1) at bits
@@ -120,8 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------ producer
-        int32_t armed_round[kStages];
-        for (int s = 0; s < kStages; ++s) armed_round[s] = -1;
+        uint32_t armed = 0, armed_parity = 0;   // per stage: copies issued, parity of their phase
         uint32_t stage = 0, phase = 0;
         for (uint32_t tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
             const uint32_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t bytes = kABytes + kBBytes + nk * 512u * (b_hi ? 3u : 2u);
                 uint8_t* st = smem + stage * kStageBytes;
                 mbar_arrive_expect_tx(&full[stage], bytes);
-                armed_round[stage] = (int32_t)phase;   // parity of the phase these copies complete
+                armed |= 1u << stage;
+                armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                 tma_load_2d(st, &tma_a, &full[stage], (int32_t)(ks * kBKBytes), (int32_t)(mt * kBM));
                 tma_load_2d(st + kABytes, &tma_b, &full[stage], (int32_t)(ks * kBKBytes), (int32_t)(nt * kBN));
                 bulk_load(st + kABytes + kBBytes, p.sfa + ((size_t)mt * p.ksteps + k0) * 512u, nk * 512u,
@@ -154,8 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // every copy this thread issued must land before the CTA exits
+#pragma unroll
         for (int s = 0; s < kStages; ++s)
-            if (armed_round[s] >= 0) (void)mbar_wait(&full[s], (uint32_t)armed_round[s], kTimeoutNs);
+            if ((armed >> s) & 1u) (void)mbar_wait(&full[s], (armed_parity >> s) & 1u, kTimeoutNs);
     } else if (warp == 1 && lane == 0) {
         // ---------------------------------------------------- MMA issuer
         uint32_t stage = 0, phase = 0, tiles_done = 0;
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(tmem + ((q * 32u) << 16) + kAccCol + c * 32, v);
                 tmem_ld_wait();
                 if (!row_ok) continue;
-                const bool full_chunk = n0 + 32 <= p.N;
+                const bool full_chunk = p.vec_store && n0 + 32 <= p.N;
                 if (p.out_fp32) {
                     float* dst = reinterpret_cast<float*>(p.d) + (int64_t)row * p.ldd + n0;
                     if (full_chunk) {
@@ -237,8 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<float4*>(dst + i) = o;
                         }
                     } else {
-                        for (uint32_t i = 0; i < 32 && n0 + i < p.N; ++i)
-                            dst[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
+#pragma unroll
+                        for (uint32_t i = 0; i < 32; ++i)
+                            if (n0 + i < p.N) dst[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
                     }
                 } else {
                     uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + (int64_t)row * p.ldd + n0;
@@ -255,8 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint4*>(dst + 2 * i) =
                                 make_uint4(packed[i], packed[i + 1], packed[i + 2], packed[i + 3]);
                     } else {
-                        for (uint32_t i = 0; i < 32 && n0 + i < p.N; ++i)
-                            dst[i] = (uint16_t)((packed[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
+#pragma unroll
+                        for (uint32_t i = 0; i < 32; ++i)
+                            if (n0 + i < p.N) dst[i] = (uint16_t)((packed[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
                     }
                 }
             }
@@ -347,6 +351,8 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     p.d = d;
     p.ldd = ldd;
     p.out_fp32 = out_fp32 ? 1 : 0;
+    const int64_t esz = out_fp32 ? 4 : 2;
+    p.vec_store = ((reinterpret_cast<uintptr_t>(d) & 15u) == 0 && (ldd * esz) % 16 == 0) ? 1 : 0;
     const uint32_t tiles = p.m_tiles * p.n_tiles;
     const uint32_t sms = (uint32_t)device_sm_count();
     const int grid = (int)(tiles < sms ? tiles : sms);

@@ -186,8 +186,10 @@ NVFP4_API nvfp4_status nvfp4_rht_quantize(const void *x, int64_t rows, int64_t c
  *  B            [N][K] operand (B->rows = N, B->cols = K).
  *  D            device, row-major [M][ldd] of out_dtype (bf16 or fp32).
  *  workspace    unused by the current kernels; may be NULL.
- * Requirements: K % 16 == 0 [SHAPE]; M, N >= 1; codes/scales/D 16-byte
- * aligned, ld_codes % 16 == 0, ldd * sizeof(out) % 16 == 0 [ALIGNMENT].
+ * Requirements: K % 16 == 0 [SHAPE]; ldd >= N [SHAPE]; codes and scales
+ * 16-byte aligned, ld_codes % 16 == 0, D aligned to its element size
+ * [ALIGNMENT].  Rows of D that start on a 16-byte boundary are written with
+ * vector stores.  M = 0 or N = 0 enqueues nothing; K = 0 writes D = 0.
  * The kernel's pipeline waits are bounded; a wait that runs out records a
  * timeout which nvfp4_device_error() reports.
  */

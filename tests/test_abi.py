@@ -122,9 +122,9 @@ def test_gemm_validation(lib):
     assert gemm(B=tensor(128, 128)) == E.NVFP4_ERR_SHAPE            # K mismatch
     assert gemm(A=tensor(128, 40, ld=32), B=tensor(128, 40, ld=32)) == E.NVFP4_ERR_SHAPE
     assert gemm(D=None) == E.NVFP4_ERR_INVALID_ARG
-    assert gemm(D=A16 + 2) == E.NVFP4_ERR_ALIGNMENT
+    assert gemm(D=A16 + 1) == E.NVFP4_ERR_ALIGNMENT                 # bf16 needs 2-byte alignment
+    assert gemm(D=A16 + 2, dt=1) == E.NVFP4_ERR_ALIGNMENT           # fp32 needs 4-byte alignment
     assert gemm(ldd=100) == E.NVFP4_ERR_SHAPE                       # ldd < N
-    assert gemm(ldd=132) == E.NVFP4_ERR_ALIGNMENT                   # 264 bytes
     assert gemm(dt=7) == E.NVFP4_ERR_INVALID_ARG
     assert gemm(A=tensor(128, 256, codes=0)) == E.NVFP4_ERR_INVALID_ARG
     assert gemm(A=tensor(128, 256, ld=120)) == E.NVFP4_ERR_SHAPE
