@@ -6,19 +6,30 @@
 // Eq. (1)-(2); "Pretraining LLMs with NVFP4", Sec. 4 Mixed precision: FP4
 // inputs, BF16/FP32 outputs).
 //
-// Design (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      TMA producer: per stage one 128x256-fp4 A box and one
-//               256x256-fp4 B box (128-byte swizzle) plus the stage's block
-//               scales (contiguous 512-byte groups of the tile layout) by
-//               plain bulk copies, all completing on the stage's mbarrier;
-//   warp 1      TMEM owner and MMA issuer: copies the stage's scales into
-//               tensor memory (tcgen05.cp) and issues four
-//               tcgen05.mma.kind::mxf4nvf4.block_scale (K = 64 each), then
-//               commits the stage back to the producer;
-//   warps 2-5   epilogue: drain the 128 x 256 FP32 accumulator from TMEM,
-//               scale by s_gA * s_gB, convert and store.
+// Design: CTA pairs (clusters of 2, one CTA per SM), persistent over 256 x 256
+// output tiles.  The pair's tile is computed by tcgen05.mma.cta_group::2: each
+// CTA holds 128 rows of A and 128 of the 256 B rows in its shared memory and
+// 128 accumulator rows in its tensor memory, so each SM streams half of B.
+// Per CTA:
+//   warp 0      TMA producer: per stage (256 fp4 of K) a 128-row A box and a
+//               128-row B box (128-byte swizzle, completing on the leader
+//               CTA's mbarrier) and the stage's block scales (512-byte groups
+//               of the tile layout: this CTA's 128 A rows and all 256 B rows)
+//               by bulk copies completing on a local mbarrier;
+//   warp 1      TMEM allocation for the pair; in the leader CTA, the MMA
+//               issuer: four block-scaled MMAs (K = 64 each) per stage, then a
+//               commit that releases the stage in both CTAs;
+//   warps 2-5   scale warps, one per TMEM lane quadrant: move the stage's
+//               scales from shared memory into the stage's TMEM columns with
+//               tcgen05.st (off the MMA pipe) and arrive on the leader's
+//               barrier;
+//   warps 6-13  epilogue, two per lane quadrant (one per 128-column half):
+//               drain the FP32 accumulator, scale by s_gA * s_gB, release the
+//               accumulator to the leader, stage BF16 results in 128-byte-
+//               swizzled shared memory and write them with TMA stores (FP32
+//               and unaligned outputs: direct stores).
 // Every mbarrier wait is bounded (2 s); a wait that runs out sets the status
-// word read by nvfp4_device_error and the CTA drains and exits.
+// word read by nvfp4_device_error and both CTAs drain and exit.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -34,34 +45,42 @@ static __device__ unsigned int g_gemm_status = 0;
 
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
-constexpr int kBKBytes = 128;                    // 256 fp4 per row per stage
+constexpr int kPairM = 256;                      // output rows per CTA pair
+constexpr int kCtaM = 128;                       // rows of A (and accumulator lanes) per CTA
+constexpr int kBN = 256;                         // output columns per tile
+constexpr int kCtaN = 128;                       // rows of B per CTA
+constexpr int kBKBytes = 128;                    // 256 fp4 of K per row per stage
 constexpr int kStages = 4;
 constexpr int kKStepsPerStage = 4;               // K = 64 per MMA
-constexpr uint32_t kABytes = kBM * kBKBytes;     // 16 KiB
-constexpr uint32_t kBBytes = kBN * kBKBytes;     // 32 KiB
+constexpr uint32_t kABytes = kCtaM * kBKBytes;   // 16 KiB
+constexpr uint32_t kBBytes = kCtaN * kBKBytes;   // 16 KiB
 constexpr uint32_t kSFABytes = kKStepsPerStage * 512;
 constexpr uint32_t kSFBBytes = 2 * kKStepsPerStage * 512;
 constexpr uint32_t kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
-constexpr int kNumEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kNumEpiWarps;
+constexpr uint32_t kStagingBytes = kCtaM * kBN * 2;   // this CTA's BF16 rows of a tile
+constexpr int kFirstSfWarp = 2;
+constexpr int kNumSfWarps = 4;
+constexpr int kFirstEpiWarp = kFirstSfWarp + kNumSfWarps;
+constexpr int kNumEpiWarps = 8;
+constexpr int kThreads = 32 * (kFirstEpiWarp + kNumEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;                   // 256 FP32 accumulator columns
 constexpr uint32_t kSfCol0 = 256;                 // then the per-stage scale columns
 constexpr uint32_t kSfColsPerStage = 4 * kKStepsPerStage + 8 * kKStepsPerStage;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kStagingBytes + 1024 /*align*/ + 256 /*barriers*/;
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
     uint32_t M, N;
-    uint32_t m_tiles, n_tiles;
-    uint32_t ksteps;           // ceil(K / 64): MMAs per tile, also 4-scale groups per row
-    uint32_t kstages;          // ceil(ksteps / 4)
-    uint32_t sfb_row_tiles;    // ceil(N / 128)
+    uint32_t m_tiles, n_tiles;   // 256-row and 256-column tiles
+    uint32_t ksteps;             // ceil(K / 64): MMAs per tile, also 4-scale groups per row
+    uint32_t kstages;            // ceil(ksteps / 4)
+    uint32_t sfa_row_tiles;      // ceil(M / 128)
+    uint32_t sfb_row_tiles;      // ceil(N / 128)
     const uint8_t* sfa;
     const uint8_t* sfb;
     const float* sga;
@@ -69,212 +88,348 @@ struct Params {
     void* d;
     int64_t ldd;
     int out_fp32;
-    int vec_store;             // every output row starts on a 16-byte boundary
+    int vec_store;               // every output row starts on a 16-byte boundary
+    int tma_store;               // BF16 output written through the D tensor map
 };
 
 // Instruction descriptor for kind::mxf4nvf4: A and B E2M1 (format 1) at bits
 // 7 and 10, both K-major, N >> 3 at bit 17, UE4M3 scales (bit 23 = 0), M >> 7
-// at bit 27, scale-factor ids 0.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 7) << 27);
+// at bit 27 (M = 256 for the pair), scale-factor ids 0.
+constexpr uint32_t kIdesc =
+    (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kPairM >> 7) << 27);
 
 __device__ __forceinline__ void record_timeout(volatile uint32_t* abort_flag) {
     *abort_flag = 1u;
     atomicOr(&g_gemm_status, kStatusTimeoutBit);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Lane 0 waits and the warp shares the outcome, so a timeout never splits a
+// warp at a .sync.aligned instruction.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
+    uint32_t ok = 1;
+    if ((threadIdx.x & 31u) == 0) {
+        ok = mbar_wait_cluster(bar, parity, kTimeoutNs) ? 1u : 0u;
+        if (!ok) record_timeout(abort_flag);
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                     const Params p) {
+                     const __grid_constant__ CUtensorMap tma_d, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    uint64_t* empty = full + kStages;
-    uint64_t* acc_full = empty + kStages;
-    uint64_t* acc_empty = acc_full + 1;
-    uint64_t* drain = acc_empty + 1;
+    uint8_t* staging = smem + kStages * kStageBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStagingBytes);   // leader: both CTAs' A/B bytes
+    uint64_t* sf_full = full + kStages;          // local: this CTA's scale bytes
+    uint64_t* empty = sf_full + kStages;         // local: released by the leader's commit
+    uint64_t* sf_ready = empty + kStages;        // leader: both CTAs' scale warps
+    uint64_t* acc_full = sf_ready + kStages;     // local: released by the leader's commit
+    uint64_t* acc_empty = acc_full + 1;          // leader: 2 x kNumEpiWarps arrivals
+    uint64_t* drain = acc_empty + 1;             // leader
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
+            mbar_init(&sf_full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], 2 * kNumSfWarps);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, kNumEpiWarps);
+        mbar_init(acc_empty, 2 * kNumEpiWarps);
         mbar_init(drain, 1);
         *abort_flag = 0u;
         fence_barrier_init();
         prefetch_tmap(&tma_a);
         prefetch_tmap(&tma_b);
+        if (p.tma_store) prefetch_tmap(&tma_d);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
     }
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t num_tiles = p.m_tiles * p.n_tiles;
+    const uint32_t first_tile = cluster_id_x(), tile_stride = num_clusters_x();
 
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------------ producer
-        uint32_t armed = 0, armed_parity = 0;   // per stage: copies issued, parity of their phase
-        uint32_t stage = 0, phase = 0;
-        for (uint32_t tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
-            const uint32_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
-            const bool b_hi = (2 * nt + 1) < p.sfb_row_tiles;
-            for (uint32_t ks = 0; ks < p.kstages; ++ks) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, kTimeoutNs)) {
-                    record_timeout(abort_flag);
-                    break;
+    if (warp == 0) {
+        if (lane == 0) {
+            // -------------------------------------------------- producer
+            uint32_t armed = 0, armed_parity = 0;   // per stage: copies issued, parity of their phase
+            uint32_t stage = 0, phase = 0;
+            for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
+                const uint32_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+                const bool a_sf = (2 * mt + rank) < p.sfa_row_tiles;
+                const bool b_hi = (2 * nt + 1) < p.sfb_row_tiles;
+                for (uint32_t ks = 0; ks < p.kstages; ++ks) {
+                    if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, kTimeoutNs)) {
+                        record_timeout(abort_flag);
+                        break;
+                    }
+                    if (*abort_flag) break;
+                    const uint32_t k0 = ks * kKStepsPerStage;
+                    const uint32_t nk = min((uint32_t)kKStepsPerStage, p.ksteps - k0);
+                    uint8_t* st = smem + stage * kStageBytes;
+                    uint8_t* sfa_s = st + kABytes + kBBytes;
+                    uint8_t* sfb_s = sfa_s + kSFABytes;
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (kABytes + kBBytes));
+                    mbar_arrive_expect_tx(&sf_full[stage], nk * 512u * ((a_sf ? 1u : 0u) + (b_hi ? 2u : 1u)));
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    const uint32_t leader_full = map_to_cta(smem_u32(&full[stage]), 0);
+                    tma_load_2d_pair(st, &tma_a, leader_full, (int32_t)(ks * kBKBytes),
+                                     (int32_t)(mt * kPairM + rank * kCtaM));
+                    tma_load_2d_pair(st + kABytes, &tma_b, leader_full, (int32_t)(ks * kBKBytes),
+                                     (int32_t)(nt * kBN + rank * kCtaN));
+                    if (a_sf)
+                        bulk_load(sfa_s, p.sfa + ((size_t)(2 * mt + rank) * p.ksteps + k0) * 512u, nk * 512u,
+                                  &sf_full[stage]);
+                    bulk_load(sfb_s, p.sfb + ((size_t)(2 * nt) * p.ksteps + k0) * 512u, nk * 512u, &sf_full[stage]);
+                    if (b_hi)
+                        bulk_load(sfb_s + kKStepsPerStage * 512u, p.sfb + ((size_t)(2 * nt + 1) * p.ksteps + k0) * 512u,
+                                  nk * 512u, &sf_full[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-                if (*abort_flag) break;
-                const uint32_t k0 = ks * kKStepsPerStage;
-                const uint32_t nk = min((uint32_t)kKStepsPerStage, p.ksteps - k0);
-                const uint32_t bytes = kABytes + kBBytes + nk * 512u * (b_hi ? 3u : 2u);
-                uint8_t* st = smem + stage * kStageBytes;
-                mbar_arrive_expect_tx(&full[stage], bytes);
-                armed |= 1u << stage;
-                armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                tma_load_2d(st, &tma_a, &full[stage], (int32_t)(ks * kBKBytes), (int32_t)(mt * kBM));
-                tma_load_2d(st + kABytes, &tma_b, &full[stage], (int32_t)(ks * kBKBytes), (int32_t)(nt * kBN));
-                bulk_load(st + kABytes + kBBytes, p.sfa + ((size_t)mt * p.ksteps + k0) * 512u, nk * 512u,
-                          &full[stage]);
-                bulk_load(st + kABytes + kBBytes + kSFABytes, p.sfb + ((size_t)(2 * nt) * p.ksteps + k0) * 512u,
-                          nk * 512u, &full[stage]);
-                if (b_hi)
-                    bulk_load(st + kABytes + kBBytes + kSFABytes + kKStepsPerStage * 512u,
-                              p.sfb + ((size_t)(2 * nt + 1) * p.ksteps + k0) * 512u, nk * 512u, &full[stage]);
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+            }
+            // every copy must land before the pair exits: the leader's full
+            // barriers count both CTAs' tile bytes, sf_full this CTA's scales
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) {
+                if (!((armed >> s) & 1u)) continue;
+                const uint32_t par = (armed_parity >> s) & 1u;
+                if (leader) (void)mbar_wait_cluster(&full[s], par, kTimeoutNs);
+                (void)mbar_wait(&sf_full[s], par, kTimeoutNs);
             }
         }
-        // every copy this thread issued must land before the CTA exits
-#pragma unroll
-        for (int s = 0; s < kStages; ++s)
-            if ((armed >> s) & 1u) (void)mbar_wait(&full[s], (armed_parity >> s) & 1u, kTimeoutNs);
-    } else if (warp == 1 && lane == 0) {
-        // ---------------------------------------------------- MMA issuer
-        uint32_t stage = 0, phase = 0, tiles_done = 0;
-        for (uint32_t tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
-            if (!mbar_wait(acc_empty, (tiles_done & 1u) ^ 1u, kTimeoutNs)) {
-                record_timeout(abort_flag);
-                break;
-            }
-            tc_fence_after();
-            bool ok = true;
-            for (uint32_t ks = 0; ks < p.kstages; ++ks) {
-                if (!mbar_wait(&full[stage], phase, kTimeoutNs)) {
+    } else if (warp == 1) {
+        if (leader && lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            uint32_t stage = 0, phase = 0, tiles_done = 0;
+            for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
+                if (!mbar_wait_cluster(acc_empty, (tiles_done & 1u) ^ 1u, kTimeoutNs)) {
                     record_timeout(abort_flag);
-                    ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t nk = min((uint32_t)kKStepsPerStage, p.ksteps - ks * kKStepsPerStage);
-                const uint32_t st = smem_u32(smem + stage * kStageBytes);
-                const uint32_t sfa = st + kABytes + kBBytes, sfb = sfa + kSFABytes;
-                const uint32_t sf_col = tmem + kSfCol0 + stage * kSfColsPerStage;
-                for (uint32_t j = 0; j < nk; ++j) {
-                    tmem_cp_32x128b_x4(sf_col + 4 * j, smem_desc(sfa + 512 * j, 0, 128, 0));
-                    tmem_cp_32x128b_x4(sf_col + 16 + 8 * j, smem_desc(sfb + 512 * j, 0, 128, 0));
-                    tmem_cp_32x128b_x4(sf_col + 16 + 8 * j + 4,
-                                       smem_desc(sfb + kKStepsPerStage * 512 + 512 * j, 0, 128, 0));
+                bool ok = true;
+                for (uint32_t ks = 0; ks < p.kstages; ++ks) {
+                    if (!mbar_wait_cluster(&full[stage], phase, kTimeoutNs) ||
+                        !mbar_wait_cluster(&sf_ready[stage], phase, kTimeoutNs)) {
+                        record_timeout(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t nk = min((uint32_t)kKStepsPerStage, p.ksteps - ks * kKStepsPerStage);
+                    const uint32_t st = smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sf_col = tmem + kSfCol0 + stage * kSfColsPerStage;
+                    const uint64_t adesc = smem_desc(st, 16, 1024, 2);
+                    const uint64_t bdesc = smem_desc(st + kABytes, 16, 1024, 2);
+                    if (nk == (uint32_t)kKStepsPerStage) {
+                        mma_nvf4_pair_x4(tmem + kAccCol, adesc, bdesc, kIdesc, sf_col, sf_col + 16, ks != 0 ? 1u : 0u);
+                    } else {
+                        for (uint32_t j = 0; j < nk; ++j)
+                            mma_nvf4_pair(tmem + kAccCol, adesc + 2 * j, bdesc + 2 * j, kIdesc, sf_col + 4 * j,
+                                          sf_col + 16 + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair_multicast(&empty[stage], 0x3);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-                for (uint32_t j = 0; j < nk; ++j) {
-                    const uint64_t adesc = smem_desc(st + 32 * j, 16, 1024, 2);
-                    const uint64_t bdesc = smem_desc(st + kABytes + 32 * j, 16, 1024, 2);
-                    mma_nvf4(tmem + kAccCol, adesc, bdesc, kIdesc, sf_col + 4 * j, sf_col + 16 + 8 * j,
-                             (ks | j) != 0 ? 1u : 0u);
+                if (!ok) break;
+                tc_commit_pair_multicast(acc_full, 0x3);
+                ++tiles_done;
+            }
+            // all MMAs complete before either CTA frees its tensor memory
+            tc_commit_pair_multicast(drain, 0x1);
+            (void)mbar_wait(drain, 0, kTimeoutNs);
+        }
+    } else if (warp < kFirstEpiWarp) {
+        // ------------------------------------------------------ scale warps
+        // Lane i of quadrant q holds, per K = 64 step j, 4 columns of A scales
+        // (bytes 16i.. of the step's 512-byte group: rows i, i+32, i+64, i+96)
+        // and 8 columns of B scales (both 128-row halves of the N tile).
+        const uint32_t q = warp & 3u;
+        uint32_t stage = 0, phase = 0;
+        for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
+            bool ok = true;
+            for (uint32_t ks = 0; ks < p.kstages; ++ks) {
+                if (!warp_wait(&sf_full[stage], phase, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                tc_commit(&empty[stage]);
+                const uint8_t* sfa = smem + stage * kStageBytes + kABytes + kBBytes;
+                const uint8_t* sfb = sfa + kSFABytes;
+                uint32_t ra[16], rb[32];
+#pragma unroll
+                for (int j = 0; j < kKStepsPerStage; ++j) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(sfa + 512 * j + 16 * lane);
+                    ra[4 * j + 0] = w.x;
+                    ra[4 * j + 1] = w.y;
+                    ra[4 * j + 2] = w.z;
+                    ra[4 * j + 3] = w.w;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 u =
+                            *reinterpret_cast<const uint4*>(sfb + kKStepsPerStage * 512 * h + 512 * j + 16 * lane);
+                        rb[8 * j + 4 * h + 0] = u.x;
+                        rb[8 * j + 4 * h + 1] = u.y;
+                        rb[8 * j + 4 * h + 2] = u.z;
+                        rb[8 * j + 4 * h + 3] = u.w;
+                    }
+                }
+                const uint32_t col = tmem + ((q * 32u) << 16) + kSfCol0 + stage * kSfColsPerStage;
+                tmem_st_32x32b_x16(col, ra);
+                tmem_st_32x32b_x32(col + 16, rb);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&sf_ready[stage]), 0));
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            tc_commit(acc_full);
-            ++tiles_done;
         }
-        // all MMAs this thread issued complete before tensor memory is freed
-        tc_commit(drain);
-        (void)mbar_wait(drain, 0, kTimeoutNs);
-    } else if (warp >= 2) {
-        // ------------------------------------------------------- epilogue
-        const uint32_t q = warp & 3u;   // TMEM lane quadrant this warp may access
+    } else {
+        // --------------------------------------------------------- epilogue
+        const uint32_t q = warp & 3u;                          // TMEM lane quadrant
+        const uint32_t half = (warp - kFirstEpiWarp) >> 2;     // 128-column half of the tile
         const float alpha = __fmul_rn(*p.sga, *p.sgb);
+        const uint32_t leader_acc_empty = map_to_cta(smem_u32(acc_empty), 0);
+        const uint32_t row_local = q * 32 + lane;
         uint32_t tiles_done = 0;
-        for (uint32_t tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
+        for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
             const uint32_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
-            if (!mbar_wait(acc_full, tiles_done & 1u, kTimeoutNs)) {
-                record_timeout(abort_flag);
-                break;
-            }
+            if (!warp_wait(acc_full, tiles_done & 1u, abort_flag)) break;
             tc_fence_after();
-            const uint32_t row = mt * kBM + q * 32 + lane;
-            const bool row_ok = row < p.M;
-            for (uint32_t c = 0; c < kBN / 32; ++c) {
-                const uint32_t n0 = nt * kBN + c * 32;
-                if (n0 >= p.N) break;   // warp-uniform
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + ((q * 32u) << 16) + kAccCol + c * 32, v);
-                tmem_ld_wait();
-                if (!row_ok) continue;
-                const bool full_chunk = p.vec_store && n0 + 32 <= p.N;
-                if (p.out_fp32) {
-                    float* dst = reinterpret_cast<float*>(p.d) + (int64_t)row * p.ldd + n0;
-                    if (full_chunk) {
+            const uint32_t row0 = mt * kPairM + rank * kCtaM;   // first row of this CTA's half
+            const uint32_t row = row0 + row_local;
+            const uint32_t nbase = nt * kBN + half * 128;
+            const uint32_t taddr = tmem + ((q * 32u) << 16) + kAccCol + half * 128;
+            if (p.tma_store) {
+                // the previous tile's stores must have read the staging buffer
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            float4 o;
-                            o.x = __fmul_rn(__uint_as_float(v[i + 0]), alpha);
-                            o.y = __fmul_rn(__uint_as_float(v[i + 1]), alpha);
-                            o.z = __fmul_rn(__uint_as_float(v[i + 2]), alpha);
-                            o.w = __fmul_rn(__uint_as_float(v[i + 3]), alpha);
-                            *reinterpret_cast<float4*>(dst + i) = o;
-                        }
-                    } else {
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + c * 32, v);
+                    tmem_ld_wait();
+                    // 32 columns = four 16-byte pieces of one 128-byte swizzled row
+                    uint8_t* blk = staging + (2 * half + (c >> 1)) * (kCtaM * 128) + row_local * 128;
 #pragma unroll
-                        for (uint32_t i = 0; i < 32; ++i)
-                            if (n0 + i < p.N) dst[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
-                    }
-                } else {
-                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + (int64_t)row * p.ldd + n0;
-                    uint32_t packed[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
-                                                                      __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
-                        packed[i] = *reinterpret_cast<const uint32_t*>(&h);
-                    }
-                    if (full_chunk) {
-#pragma unroll
-                        for (int i = 0; i < 16; i += 4)
-                            *reinterpret_cast<uint4*>(dst + 2 * i) =
-                                make_uint4(packed[i], packed[i + 1], packed[i + 2], packed[i + 3]);
-                    } else {
-#pragma unroll
-                        for (uint32_t i = 0; i < 32; ++i)
-                            if (n0 + i < p.N) dst[i] = (uint16_t)((packed[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t piece = (uint32_t)((c & 1) * 4 + i) ^ (row_local & 7u);
+                        const uint4 w = make_uint4(
+                            pack_bf16x2(__fmul_rn(__uint_as_float(v[8 * i + 0]), alpha),
+                                        __fmul_rn(__uint_as_float(v[8 * i + 1]), alpha)),
+                            pack_bf16x2(__fmul_rn(__uint_as_float(v[8 * i + 2]), alpha),
+                                        __fmul_rn(__uint_as_float(v[8 * i + 3]), alpha)),
+                            pack_bf16x2(__fmul_rn(__uint_as_float(v[8 * i + 4]), alpha),
+                                        __fmul_rn(__uint_as_float(v[8 * i + 5]), alpha)),
+                            pack_bf16x2(__fmul_rn(__uint_as_float(v[8 * i + 6]), alpha),
+                                        __fmul_rn(__uint_as_float(v[8 * i + 7]), alpha)));
+                        *reinterpret_cast<uint4*>(blk + piece * 16) = w;
                     }
                 }
+                tc_fence_before();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_cluster(leader_acc_empty);
+                    const uint32_t y = row0 + q * 32;
+                    if (y < p.M) {
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const uint32_t x = nt * kBN + (2 * half + b) * 64;
+                            if (x < p.N)
+                                tma_store_2d(&tma_d, staging + (2 * half + b) * (kCtaM * 128) + q * 32 * 128,
+                                             (int32_t)x, (int32_t)y);
+                        }
+                    }
+                    bulk_commit_group();
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t n0 = nbase + 32 * c;
+                    if (n0 >= p.N) break;   // warp-uniform
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + c * 32, v);
+                    tmem_ld_wait();
+                    if (row >= p.M) continue;
+                    if (p.out_fp32) {
+                        float* dst = reinterpret_cast<float*>(p.d) + (int64_t)row * p.ldd + n0;
+                        if (p.vec_store && n0 + 32 <= p.N) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<float4*>(dst + i) =
+                                    make_float4(__fmul_rn(__uint_as_float(v[i]), alpha),
+                                                __fmul_rn(__uint_as_float(v[i + 1]), alpha),
+                                                __fmul_rn(__uint_as_float(v[i + 2]), alpha),
+                                                __fmul_rn(__uint_as_float(v[i + 3]), alpha));
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (n0 + i < p.N) dst[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
+                        }
+                    } else {
+                        uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + (int64_t)row * p.ldd + n0;
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            packed[i] = pack_bf16x2(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
+                                                    __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+                        if (p.vec_store && n0 + 32 <= p.N) {
+#pragma unroll
+                            for (int i = 0; i < 16; i += 4)
+                                *reinterpret_cast<uint4*>(dst + 2 * i) =
+                                    make_uint4(packed[i], packed[i + 1], packed[i + 2], packed[i + 3]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (n0 + i < p.N) dst[i] = (uint16_t)((packed[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
             ++tiles_done;
         }
+        if (p.tma_store && lane == 0) bulk_wait_all();
     }
 
+    // neither CTA frees tensor memory or exits while its peer may still use it
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host ---
@@ -309,6 +464,44 @@ bool make_codes_map(CUtensorMap* map, const GemmOperand& op, uint32_t box_rows) 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// BF16 output map: 64-column x 32-row boxes, 128-byte swizzle.
+bool make_output_map(CUtensorMap* map, void* d, int64_t M, int64_t N, int64_t ldd) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ldd * 2)};
+    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t elem[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Number of CTA pairs that can be resident at once (cached per device).
+int max_active_pairs() {
+    static int pairs[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (pairs[dev] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (unsigned)(device_sm_count() / 2), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvf4_kernel, &cfg) != cudaSuccess || n < 1)
+            n = device_sm_count() / 2;
+        pairs[dev] = n > 0 ? n : 1;
+    }
+    return pairs[dev];
+}
+
 }  // namespace
 
 int device_sm_count() {
@@ -325,8 +518,6 @@ int device_sm_count() {
 
 cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int64_t ldd, bool out_fp32,
                         cudaStream_t stream) {
-    CUtensorMap ma, mb;
-    if (!make_codes_map(&ma, a, kBM) || !make_codes_map(&mb, b, kBN)) return cudaErrorInvalidValue;
     static bool attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
@@ -336,13 +527,16 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
+    CUtensorMap ma, mb, md;
+    if (!make_codes_map(&ma, a, kCtaM) || !make_codes_map(&mb, b, kCtaN)) return cudaErrorInvalidValue;
     Params p{};
     p.M = (uint32_t)a.rows;
     p.N = (uint32_t)b.rows;
-    p.m_tiles = (uint32_t)((a.rows + kBM - 1) / kBM);
+    p.m_tiles = (uint32_t)((a.rows + kPairM - 1) / kPairM);
     p.n_tiles = (uint32_t)((b.rows + kBN - 1) / kBN);
     p.ksteps = (uint32_t)((a.cols + 63) / 64);
     p.kstages = (p.ksteps + kKStepsPerStage - 1) / kKStepsPerStage;
+    p.sfa_row_tiles = (uint32_t)((a.rows + 127) / 128);
     p.sfb_row_tiles = (uint32_t)((b.rows + 127) / 128);
     p.sfa = a.scales;
     p.sfb = b.scales;
@@ -353,10 +547,12 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     p.out_fp32 = out_fp32 ? 1 : 0;
     const int64_t esz = out_fp32 ? 4 : 2;
     p.vec_store = ((reinterpret_cast<uintptr_t>(d) & 15u) == 0 && (ldd * esz) % 16 == 0) ? 1 : 0;
+    p.tma_store = (!out_fp32 && p.vec_store && make_output_map(&md, d, a.rows, b.rows, ldd)) ? 1 : 0;
+    if (!p.tma_store) md = ma;   // unused by the kernel; any valid map
     const uint32_t tiles = p.m_tiles * p.n_tiles;
-    const uint32_t sms = (uint32_t)device_sm_count();
-    const int grid = (int)(tiles < sms ? tiles : sms);
-    gemm_nvf4_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
+    const uint32_t pairs = (uint32_t)max_active_pairs();
+    const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
+    gemm_nvf4_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, md, p);
     return cudaGetLastError();
 }
 
