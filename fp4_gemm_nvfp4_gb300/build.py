@@ -12,7 +12,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libnvfp4.so")
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "dequantize.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "dequantize.cu", "quantize_noalloc.cu"]
 HEADERS = ["device_common.cuh", "kernels.h"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",

@@ -33,7 +33,7 @@ NVFP4_COLWISE = 2
 
 EXPORTED = ("nvfp4_scale_bytes", "nvfp4_quantize_workspace_size", "nvfp4_quantize",
             "nvfp4_rht_quantize", "nvfp4_gemm", "nvfp4_dequantize", "nvfp4_status_string",
-            "nvfp4_device_error")
+            "nvfp4_device_error", "nvfp4_quantize_noalloc")
 
 
 class nvfp4_tensor(ctypes.Structure):
@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_quantize.restype = i32
     L.nvfp4_rht_quantize.argtypes = qargs + [u16, vp, sz, vp]
     L.nvfp4_rht_quantize.restype = i32
+    L.nvfp4_quantize_noalloc.argtypes = qargs + [vp]
+    L.nvfp4_quantize_noalloc.restype = i32
     L.nvfp4_gemm.argtypes = [tp, tp, vp, i64, i32, vp, sz, vp]
     L.nvfp4_gemm.restype = i32
     L.nvfp4_dequantize.argtypes = [tp, vp, i64, i32, vp]
@@ -106,6 +108,13 @@ def nvfp4_rht_quantize(x, rows, cols, ld_x, scaling, rounding, seed, stream_id, 
     return load().nvfp4_rht_quantize(x, rows, cols, ld_x, scaling, rounding, seed, stream_id,
                                      orientations, _ref(out_row), _ref(out_col), rht_sign_mask,
                                      workspace, workspace_bytes, stream)
+
+
+def nvfp4_quantize_noalloc(x, rows, cols, ld_x, scaling, rounding, seed, stream_id, orientations,
+                           out_row, out_col, stream):
+    """nvfp4_quantize without a caller-provided workspace (library-held scratch)."""
+    return load().nvfp4_quantize_noalloc(x, rows, cols, ld_x, scaling, rounding, seed, stream_id,
+                                         orientations, _ref(out_row), _ref(out_col), stream)
 
 
 def nvfp4_gemm(A, B, D, ldd, out_dtype, workspace, workspace_bytes, stream):

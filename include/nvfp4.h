@@ -205,6 +205,33 @@ NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_tensor *A, const nvfp4_tensor *B, 
 NVFP4_API nvfp4_status nvfp4_dequantize(const nvfp4_tensor *q, void *y, int64_t ldy,
                               nvfp4_dtype out_dtype, nvfp4_stream_t stream);
 
+/*
+ * nvfp4_quantize_noalloc -- nvfp4_quantize for callers that cannot provide
+ * device scratch memory (no counterpart on the pages: this is an interface
+ * convenience of this library).  Some callers cannot allocate or be handed a
+ * workspace: a plugin whose host runtime owns all device memory and passes it
+ * only inputs and outputs, or code that must not call cudaMalloc once it is
+ * running (allocation can synchronize the device or fail under memory
+ * pressure).  This entry point allocates nothing: it uses a 32 KiB scratch
+ * array compiled into the library (held on every GPU that loads the library
+ * until the process exits) and otherwise behaves exactly like nvfp4_quantize
+ * with the same arguments, workspace aside.
+ *  - The first call on a device looks up the scratch's device address (one
+ *    cudaGetSymbolAddress with that device current); make that first call
+ *    before any stream capture on the device.
+ *  - Every call shares the one scratch array and it keeps the previous call's
+ *    contents (each call writes the amax partials it reads, so nothing needs
+ *    clearing).  Calls that overlap on the GPU -- on different streams, or
+ *    from several host threads -- race on it: serialize them.
+ *  - A shape whose workspace would exceed the 32 KiB scratch returns
+ *    NVFP4_ERR_WORKSPACE; every shape nvfp4_quantize accepts fits today.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_noalloc(const void *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                              nvfp4_scaling scaling, nvfp4_rounding rounding,
+                                              uint64_t seed, uint64_t stream_id, int orientations,
+                                              const nvfp4_tensor *out_row, const nvfp4_tensor *out_col,
+                                              nvfp4_stream_t stream);
+
 /* Human-readable name of a status. */
 NVFP4_API const char *nvfp4_status_string(nvfp4_status status);
 
