@@ -165,36 +165,29 @@ class Step:
     def launches(self):
         return sum(quant_launches(self.kw[n]) for n, _, _ in QUANTS) + len(GEMMS)
 
-    def run(self, events=None):
-        """Enqueue one step; with `events`, record a (start, end) pair around
-        every quantize call and every GEMM on the current stream."""
-        ops, torch = self.ops, self.torch
-        seed = self.seed
+    def run_quantize(self, only=None):
         for name, src, _ in QUANTS:
-            kw = self.kw[name]
+            if only is not None and name != only:
+                continue
             row, col = self.q[name]
-            if events is not None:
-                e0 = torch.cuda.Event(enable_timing=True)
-                e0.record()
-            ops.quantize(self.x[src], out_row=row, out_col=col, seed=seed, workspace=self.ws, **kw)
-            if events is not None:
-                e1 = torch.cuda.Event(enable_timing=True)
-                e1.record()
-                events.append(("q:" + name, e0, e1))
+            self.ops.quantize(self.x[src], out_row=row, out_col=col, seed=self.seed, workspace=self.ws,
+                              **self.kw[name])
+
+    def run_gemms(self, only=None):
         for gname, (an, ao), (bn, bo) in GEMMS:
-            if events is not None:
-                e0 = torch.cuda.Event(enable_timing=True)
-                e0.record()
-            ops.gemm(self.operand(an, ao), self.operand(bn, bo), out=self.out[gname])
-            if events is not None:
-                e1 = torch.cuda.Event(enable_timing=True)
-                e1.record()
-                events.append(("g:" + gname, e0, e1))
+            if only is not None and gname != only:
+                continue
+            self.ops.gemm(self.operand(an, ao), self.operand(bn, bo), out=self.out[gname])
+
+    def run(self):
+        """Enqueue one step (every quantize call, then the six GEMMs)."""
+        self.run_quantize()
+        self.run_gemms()
 
 
 # ----------------------------------------------------------------- clocks --
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -208,8 +201,9 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.5)     # let the sampler start before the timed region
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -223,22 +217,29 @@ class ClockSampler:
                 self.proc.kill()
             self.f.close()
 
-    def summary(self):
+    def summary(self, windows):
+        """Median SM clock and throttle reasons over the samples taken inside
+        the timed windows [(t0, t1) host wall-clock seconds]."""
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        import datetime
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx = float(parts[2])
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    clk, mxv = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
+                if not any(t0 <= ts <= t1 for t0, t1 in windows):
+                    continue
+                sm.append(clk)
+                mx = mxv
+                for n, v in zip(names, parts[6:10]):
                     if v.lower() == "active":
                         reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
@@ -268,11 +269,13 @@ def cpu_baseline(host, mask, seed, rows_a=8, rows_b=1024):
         ops_ = []
         for qn, orient, nrows in ((an, ao, rows_a), (bn, bo, rows_b)):
             o = oracle.ROWWISE if orient == "row" else oracle.COLWISE
-            ops_.append(oracle.quantize(host[src_of[qn]], o, rows_subset=(0, nrows),
+            bits = host[src_of[qn]]
+            lrows = bits.shape[0] if o == oracle.ROWWISE else bits.shape[1]
+            ops_.append(oracle.quantize(bits, o, rows_subset=(0, min(nrows, lrows)),
                                         **_oracle_kw(kw_of[qn], mask, seed)))
         a, b = ops_
         oracle.gemm_f64(a, b, with_abs=False)
-        flops += 2 * rows_a * rows_b * a["codes"].shape[1] * 2
+        flops += 2 * a["codes"].shape[0] * b["codes"].shape[0] * a["codes"].shape[1] * 2
     dt = time.perf_counter() - t0
     desc = (f"oracle on the host cores: each of the 6 GEMMs on a {rows_a} x {rows_b} block of its "
             f"output, its operand rows quantized by the oracle (full-tensor amax pass included)")
@@ -280,6 +283,26 @@ def cpu_baseline(host, mask, seed, rows_a=8, rows_b=1024):
 
 
 # --------------------------------------------------------------- measure --
+def capture(torch, fn, stream):
+    """One CUDA graph of fn() on `stream` (launch gaps vanish on replay)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def time_replays(torch, graph, n, stream):
+    """Device milliseconds of n back-to-back replays, events on `stream`."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        graph.replay()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def measure(args):
     import torch
     world, rank, local = dist_env()
@@ -295,7 +318,7 @@ def measure(args):
     seed = 4 + 1000 * rank
     dev = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in host.items()}
     step = Step(dev, mask, seed)
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()
 
     def barrier():
         torch.cuda.synchronize()
@@ -303,58 +326,67 @@ def measure(args):
             torch.distributed.barrier()
             torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
+    # eager warm-up: first calls set kernel attributes and cache device queries
+    with torch.cuda.stream(stream):
         step.run()
     barrier()
     status = ops.device_error()
     if status != capi.NVFP4_OK:
-        raise RuntimeError(f"device status after warm-up: {capi.status_string(status)}")
+        raise RuntimeError(f"device status after the first step: {capi.status_string(status)}")
+    g_step = capture(torch, step.run, stream)
+    g_quant = {n: capture(torch, lambda n=n: step.run_quantize(n), stream) for n, _, _ in QUANTS}
+    g_gemm = {n: capture(torch, lambda n=n: step.run_gemms(n), stream) for n, _, _ in GEMMS}
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_step.replay()
+    barrier()
 
-    # ---- device-resident timing: events around the step and every launch
-    per_step_events = []
+    # ---- the timed region: exactly K steps, inputs resident in HBM
+    windows = []
     with ClockSampler(local) as clocks:
         barrier()
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for _ in range(args.steps):
-            ev = []
-            step.run(ev)
-            per_step_events.append(ev)
-        t_end.record(stream)
+        t0 = time.time()
+        with torch.cuda.stream(stream):
+            total_ms = time_replays(torch, g_step, args.steps, stream)
         barrier()
-    total_ms = t_start.elapsed_time(t_end)
+        windows.append((t0, time.time()))
+        # per kernel class: the same launches replayed alone, K times each
+        launch_ms = {}
+        t0 = time.time()
+        with torch.cuda.stream(stream):
+            for n, g in g_quant.items():
+                launch_ms["q:" + n] = time_replays(torch, g, args.steps, stream) / args.steps
+            for n, g in g_gemm.items():
+                launch_ms["g:" + n] = time_replays(torch, g, args.steps, stream) / args.steps
+        barrier()
+        windows.append((t0, time.time()))
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = t.item()
     ms_per_step = total_ms / args.steps
-    launch_ms = {}
-    for ev in per_step_events:
-        for name, e0, e1 in ev:
-            launch_ms.setdefault(name, []).append(e0.elapsed_time(e1))
-    avg = {k: sum(v) / len(v) for k, v in launch_ms.items()}
     flops = step.flops()
     value = flops * world / (ms_per_step * 1e-3) / 1e12
 
-    # ---- end to end: pinned host inputs in, outputs out, every step
+    # ---- end to end: pinned host inputs in and the six outputs out, every step
     pinned_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
                  for k, v in host.items()}
     pinned_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in step.out.items()}
     h2d = sum(t.numel() * 2 for t in pinned_in.values())
     d2h = sum(t.numel() * 2 for t in pinned_out.values())
+    e2e_steps = max(1, min(args.steps, 10))
     barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(1, min(args.steps, 5))
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        for k, t in pinned_in.items():
-            dev[k].copy_(t, non_blocking=True)
-        step.run()
-        for k, t in pinned_out.items():
-            t.copy_(step.out[k], non_blocking=True)
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for k, t in pinned_in.items():
+                dev[k].copy_(t, non_blocking=True)
+            g_step.replay()
+            for k, t in pinned_out.items():
+                t.copy_(step.out[k], non_blocking=True)
+        e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if world > 1:
@@ -367,16 +399,14 @@ def measure(args):
 
     # ---- roofline of the dominant kernel class
     peaks, peak_src = load_peaks()
-    gemm_ms = sum(v for k, v in avg.items() if k.startswith("g:"))
-    quant_ms = sum(v for k, v in avg.items() if k.startswith("q:"))
+    gemm_ms = sum(v for k, v in launch_ms.items() if k.startswith("g:"))
+    quant_ms = sum(v for k, v in launch_ms.items() if k.startswith("q:"))
     gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
-    qbytes = 0.0
-    for name, src, kw in QUANTS:
-        qbytes += quant_bytes(*SHAPES[src], step.kw[name])
+    qbytes = sum(quant_bytes(*SHAPES[src], step.kw[name]) for name, src, _ in QUANTS)
     quant_gbs = qbytes / (quant_ms * 1e-3) / 1e9
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     if gemm_ms >= quant_ms:
-        roof = {"kernel": "gemm_nvf4_kernel (6 GEMMs of the step)", "bound": "tensor",
+        roof = {"kernel": "gemm_nvf4_kernel (the step's 6 GEMMs)", "bound": "tensor",
                 "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                 "frac": round(gemm_tflops / fp4_peak, 4), "traffic": None,
                 "peak_source": f"{peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal fp4/bf16)"}
@@ -393,20 +423,21 @@ def measure(args):
         "data": "synthetic",
         "config": {"workload": workload_name(), "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
                    "gemm_gflop_per_step": round(flops / 1e9, 1), "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2 (one step touches about 2 GB)"},
+                   "l2": "inputs larger than L2 (one step touches about 2.5 GB)",
+                   "launch": "each step is one CUDA graph replay"},
         "roofline": roof,
         "gemm_tflops": round(gemm_tflops, 1),
         "gemm_frac_of_fp4_peak": round(gemm_tflops / fp4_peak, 4),
         "quantize_gbs": round(quant_gbs, 1),
         "quantize_frac_of_hbm": round(quant_gbs / peaks["hbm_gbs"], 4),
-        "per_launch_ms": {k: round(v, 4) for k, v in sorted(avg.items())},
+        "per_launch_ms": {k: round(v, 4) for k, v in sorted(launch_ms.items())},
         "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": step.launches() * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clocks.summary(windows),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        v, dt, desc, cores = cpu_baseline(host, mask, seed)
+        v, dt, desc, cores = cpu_baseline(host, mask, seed, rows_a=512, rows_b=4096)
         result["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                   "sample": desc, "seconds": round(dt, 2)}
     if world > 1:
@@ -444,7 +475,7 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
