@@ -62,57 +62,62 @@ __device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
     return out | signs;
 }
 
-// Stochastic rounding of one value to an E2M1 code with a 32-bit random word
-// ("Full-Stack FP4", Appendix 7: round up with probability d / step).  The
-// step is a power of two on every bin, so frac * 2^24 is exact.
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t word) {
+// Stochastic rounding of one value to an E2M1 code with 16 random bits
+// ("Full-Stack FP4", Appendix 7: round up with probability d / step): up iff
+// r16 < frac * 2^16.  Branch free: with m = 1 / step of |v|'s bin (2, 1 or
+// 1/2), |v| * m is exact, its floor q picks the lower grid point and
+// (|v| * m - q) * 2^16 = frac * 2^16 is exact too.
+__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
     const uint32_t sign = __float_as_uint(v) >> 31;
     const float a = fabsf(v);
-    uint32_t code;
-    if (a >= 6.0f) {
-        code = 7u;
-    } else {
-        float lo, scale;
-        if (a < 2.0f) {          // grid 0, .5, 1, 1.5 (step 0.5)
-            code = (uint32_t)__fmul_rn(a, 2.0f);
-            lo = __fmul_rn((float)code, 0.5f);
-            scale = 33554432.0f;  // 2^24 / 0.5
-        } else if (a < 4.0f) {   // grid 2, 3 (step 1)
-            lo = floorf(a);
-            code = 2u + (uint32_t)lo;
-            scale = 16777216.0f;
-        } else {                 // grid 4 (step 2)
-            lo = 4.0f;
-            code = 6u;
-            scale = 8388608.0f;
-        }
-        const float frac24 = __fmul_rn(__fsub_rn(a, lo), scale);
-        code += (__uint2float_rn(word >> 8) < frac24) ? 1u : 0u;
-    }
+    const bool below2 = a < 2.0f, below4 = a < 4.0f;
+    const float m = below2 ? 2.0f : (below4 ? 1.0f : 0.5f);
+    const float am = __fmul_rn(a, m);
+    const float q = floorf(am);
+    const uint32_t offset = below2 ? 0u : (below4 ? 2u : 4u);   // codes of the bins' first grid point minus q
+    const float frac16 = __fmul_rn(__fsub_rn(am, q), 65536.0f);
+    uint32_t code = (uint32_t)q + offset + ((__uint2float_rn(r16) < frac16) ? 1u : 0u);
+    code = (a >= 6.0f) ? 7u : code;
     return code | (sign << 3);
 }
 
 // --------------------------------------------------------------- Philox ----
-// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
+// 32x32->64 multiplies; the key is bumped by the Weyl constants between
+// rounds.  The ten round keys depend only on the seed, so they are formed once.
+struct PhiloxKeys {
+    uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
+    PhiloxKeys k;
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
 #pragma unroll
-    for (int round = 0; round < 10; ++round) {
-        if (round > 0) {
-            k0 += 0x9E3779B9u;
-            k1 += 0xBB67AE85u;
-        }
-        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    for (int r = 0; r < 10; ++r) {
+        k.k0[r] = a;
+        k.k1[r] = b;
+        a += 0x9E3779B9u;
+        b += 0xBB67AE85u;
+    }
+    return k;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& k) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k.k0[r], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k.k1[r],
+                       (uint32_t)p0);
     }
     return c;
 }
 
-// The four SR words of elements 4g .. 4g+3.
-__device__ __forceinline__ uint4 sr_words4(uint64_t seed, uint64_t stream_id, uint64_t g) {
-    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), (uint32_t)stream_id,
-                                    (uint32_t)(stream_id >> 32)),
-                         (uint32_t)seed, (uint32_t)(seed >> 32));
+// The Philox block of SR elements 8g .. 8g+7: element 8g + i takes 16 bits of
+// word i / 2, the low half for even i.
+__device__ __forceinline__ uint4 sr_words4(const PhiloxKeys& keys, uint64_t stream_id, uint64_t g) {
+    return philox4x32_10(
+        make_uint4((uint32_t)g, (uint32_t)(g >> 32), (uint32_t)stream_id, (uint32_t)(stream_id >> 32)), keys);
 }
 
 // ------------------------------------------------------------------ RHT ----
@@ -159,7 +164,7 @@ __device__ __forceinline__ uint32_t block_scale(float amax_b, float s_enc, float
 // (element 0 in the low nibble of byte 0).  idx_base is the SR index of
 // element 0 (a multiple of 16 for 1x16 blocks).
 template <bool kSR>
-__device__ __forceinline__ uint2 encode16(const float* t, float r_b, uint64_t seed, uint64_t stream_id,
+__device__ __forceinline__ uint2 encode16(const float* t, float r_b, const PhiloxKeys& keys, uint64_t stream_id,
                                           uint64_t idx_base) {
     float v[16];
 #pragma unroll
@@ -167,17 +172,14 @@ __device__ __forceinline__ uint2 encode16(const float* t, float r_b, uint64_t se
     if constexpr (!kSR) {
         return make_uint2(e2m1_rne_x8(v), e2m1_rne_x8(v + 8));
     } else {
-        uint32_t w[16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 r = sr_words4(seed, stream_id, (idx_base >> 2) + q);
-            w[4 * q + 0] = r.x; w[4 * q + 1] = r.y; w[4 * q + 2] = r.z; w[4 * q + 3] = r.w;
-        }
+        const uint4 r0 = sr_words4(keys, stream_id, idx_base >> 3);
+        const uint4 r1 = sr_words4(keys, stream_id, (idx_base >> 3) + 1);
+        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         uint32_t lo = 0, hi = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            lo |= e2m1_sr(v[i], w[i]) << (4 * i);
-            hi |= e2m1_sr(v[8 + i], w[8 + i]) << (4 * i);
+            lo |= e2m1_sr(v[i], (w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu) << (4 * i);
+            hi |= e2m1_sr(v[8 + i], (w[4 + (i >> 1)] >> (16 * (i & 1))) & 0xFFFFu) << (4 * i);
         }
         return make_uint2(lo, hi);
     }

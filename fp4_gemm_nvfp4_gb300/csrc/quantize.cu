@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
     TensorScale ts{1.0f, 1.0f};
     if constexpr (P == Pass::kEncode) ts = load_tensor_scale(a.partials_in, a.n_partials, red, a.out, nullptr);
     float local_max = 0.0f;
+    PhiloxKeys keys;
+    if constexpr (kSR) keys = philox_keys(a.seed);
     const uint32_t stride = gridDim.x * kThreads;
     for (uint32_t b = blockIdx.x * kThreads + threadIdx.x; b < a.total; b += stride) {
         const uint32_t r = b / a.bpr, j = b - r * a.bpr;
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
             float r_b;
             const uint32_t sc = block_scale(amax_b, ts.s_enc, &r_b);
             const uint64_t idx = (uint64_t)r * ((uint64_t)a.bpr * 16u) + (uint64_t)j * 16u;
-            const uint2 q = encode16<kSR>(t, r_b, a.seed, a.stream, idx);
+            const uint2 q = encode16<kSR>(t, r_b, keys, a.stream, idx);
             *reinterpret_cast<uint2*>(a.out.codes + (int64_t)r * a.out.ld_codes + (int64_t)j * 8) = q;
             a.out.scales[scale_offset(r, j, a.out.s4)] = (uint8_t)sc;
         }
@@ -126,6 +128,8 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
     float local_max = 0.0f;
+    PhiloxKeys keys;
+    if constexpr (kSR) keys = philox_keys(a.seed);
     for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const uint32_t tr = tile % a.tiles_r, tc = tile / a.tiles_r;
         const uint32_t r0 = tr * 128u + warp * 16u, c = tc * 64u + lane * 2u;
@@ -154,8 +158,8 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
             float rb0, rb1;
             const uint32_t sc0 = block_scale(m0, ts.s_enc, &rb0);
             const uint32_t sc1 = block_scale(m1, ts.s_enc, &rb1);
-            const uint2 q0 = encode16<kSR>(t0, rb0, a.seed, a.stream, (uint64_t)c * a.rows + r0);
-            const uint2 q1 = encode16<kSR>(t1, rb1, a.seed, a.stream, (uint64_t)(c + 1) * a.rows + r0);
+            const uint2 q0 = encode16<kSR>(t0, rb0, keys, a.stream, (uint64_t)c * a.rows + r0);
+            const uint2 q1 = encode16<kSR>(t1, rb1, keys, a.stream, (uint64_t)(c + 1) * a.rows + r0);
             *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
             *reinterpret_cast<uint2*>(a.out.codes + (int64_t)(c + 1) * a.out.ld_codes + r0 / 2) = q1;
             a.out.scales[scale_offset(c, r0 / 16, a.out.s4)] = (uint8_t)sc0;
@@ -182,6 +186,8 @@ __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
                           (a.emit_col && a.emit_row) ? &a.out2 : nullptr);
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
+    PhiloxKeys keys;
+    if constexpr (kSR) keys = philox_keys(a.seed);
     for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const uint32_t tr = tile % a.tiles_r, tc = tile / a.tiles_r;
         const uint32_t r0 = tr * 128u + warp * 16u, c = tc * 64u + lane * 2u;
@@ -221,11 +227,12 @@ __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 // SR index: the row-wise index of x, shared by both orientations
-                const uint64_t idx = (uint64_t)(r0 + i) * a.cols + c;     // even
-                const uint4 w = sr_words4(a.seed, a.stream, idx >> 2);
-                const bool hi = (idx & 2u) != 0;
-                const uint32_t c0 = e2m1_sr(__fmul_rn(t0[i], r_b), hi ? w.z : w.x);
-                const uint32_t c1 = e2m1_sr(__fmul_rn(t1[i], r_b), hi ? w.w : w.y);
+                const uint64_t idx = (uint64_t)(r0 + i) * a.cols + c;     // even: c and c+1 share a word
+                const uint4 w = sr_words4(keys, a.stream, idx >> 3);
+                const uint32_t sel = (uint32_t)(idx >> 1) & 3u;
+                const uint32_t word = sel == 0 ? w.x : (sel == 1 ? w.y : (sel == 2 ? w.z : w.w));
+                const uint32_t c0 = e2m1_sr(__fmul_rn(t0[i], r_b), word & 0xFFFFu);
+                const uint32_t c1 = e2m1_sr(__fmul_rn(t1[i], r_b), word >> 16);
                 if (i < 8) {
                     q0.x |= c0 << (4 * i);
                     q1.x |= c1 << (4 * i);

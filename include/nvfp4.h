@@ -65,13 +65,16 @@
  *  4. r_b = S_enc / s_b (0 if s_b = 0); v = t * r_b.
  *  5. RNE: nearest E2M1 value, ties to the even mantissa, |v| > 6 -> 6 [NV
  *     Sec. 4].  SR [FS App. 7]: round |v| up from grid point c_k to c_k+1 iff
- *     (float)(w >> 8) < ((|v| - c_k) / step_k) * 2^24, w a 32-bit Philox4x32-10
- *     word; |v| >= 6 -> 6.  The code's sign bit is the sign bit of v.
- *  6. Philox4x32-10 (Salmon et al., SC'11) word for element idx:
- *     key = (seed lo32, seed hi32), counter = (g lo32, g hi32, stream_id lo32,
- *     stream_id hi32), g = idx / 4, word idx % 4; idx = r * cols + c in the
- *     emitted logical matrix (for 16x16 scaling: the row-wise index of x, so
- *     that both orientations share one draw per element).
+ *     (float)r < ((|v| - c_k) / step_k) * 2^16, r 16 random bits (so
+ *     P(up) = ceil(frac * 2^16) / 2^16); |v| >= 6 -> 6.  The code's sign bit is
+ *     the sign bit of v.
+ *  6. Random bits of element idx: Philox4x32-10 (Salmon et al., SC'11) block
+ *     with key = (seed lo32, seed hi32), counter = (g lo32, g hi32,
+ *     stream_id lo32, stream_id hi32), g = idx / 8; the element takes word
+ *     (idx / 2) % 4, low 16 bits for even idx, high 16 bits for odd idx.
+ *     idx = r * cols + c in the emitted logical matrix (for 16x16 scaling: the
+ *     row-wise index of x, so that both orientations share one draw per
+ *     element).
  *  7. RHT [FS Eq. (2), NV Sec. 4, OT]: U = H16 * D / 4, D = diag(-1 where bit
  *     i of rht_sign_mask is set); computed as: negate per D, butterfly stages
  *     s = 0, 1, 2, 3 mapping (t[i], t[i ^ 2^s]) (i without bit s) to

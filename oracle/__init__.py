@@ -11,7 +11,7 @@ uint8 (row-major scales, one byte per 16 elements of a logical row).
 Parity status of each function (see nvfp4_oracle.c for the citations):
   e2m1_rne / e2m1_sr / e2m1_value   pinned (page grid, bins, SR statistics)
   e4m3_rne_satfinite / e4m3_value    pinned (torch float8_e4m3fn casts)
-  philox4x32_10 / sr_word            round function pinned (cuRAND host
+  philox4x32_10 / sr_bits            round function pinned (cuRAND host
                                      generator); the counter/key placement is
                                      a documented convention
   rht16                              pinned (Sylvester recursion, H H^T = 16 I)
@@ -49,7 +49,7 @@ def lib():
         L.oracle_e4m3_value.argtypes, L.oracle_e4m3_value.restype = [u8], f64
         L.oracle_e4m3_rne_satfinite.argtypes, L.oracle_e4m3_rne_satfinite.restype = [f32], u8
         L.oracle_philox4x32_10.argtypes, L.oracle_philox4x32_10.restype = [vp, vp, vp], None
-        L.oracle_sr_word.argtypes, L.oracle_sr_word.restype = [u64, u64, u64], u32
+        L.oracle_sr_bits.argtypes, L.oracle_sr_bits.restype = [u64, u64, u64], u32
         L.oracle_rht16.argtypes, L.oracle_rht16.restype = [vp, u16, vp], None
         L.oracle_tensor_scale.argtypes, L.oracle_tensor_scale.restype = [f32, vp, vp], None
         L.oracle_amax.argtypes = [vp, i64, i64, i64, i32, i32, u16]
@@ -88,8 +88,8 @@ def e2m1_rne(v):
     return lib().oracle_e2m1_rne(float(v))
 
 
-def e2m1_sr(v, word):
-    return lib().oracle_e2m1_sr(float(v), int(word))
+def e2m1_sr(v, rand16):
+    return lib().oracle_e2m1_sr(float(v), int(rand16))
 
 
 def e4m3_value(code):
@@ -108,8 +108,8 @@ def philox4x32_10(ctr, key):
     return out
 
 
-def sr_word(seed, stream_id, idx):
-    return lib().oracle_sr_word(int(seed), int(stream_id), int(idx))
+def sr_bits(seed, stream_id, idx):
+    return lib().oracle_sr_bits(int(seed), int(stream_id), int(idx))
 
 
 def rht16(x, sign_mask):

@@ -16,10 +16,12 @@
  *  - block scale: s_b = E4M3_rne_satfinite((amax_b / 6) * S_enc);
  *  - encode multiplier r_b = S_enc / s_b (0 when s_b = 0), v = x * r_b;
  *  - RNE ties go to the even mantissa; the code's sign bit is v's sign bit;
- *  - SR: round up iff (float)(word >> 8) < frac * 2^24, frac = d / step;
+ *  - SR: round up iff (float)u < frac * 2^16, frac = d / step, u a 16-bit
+ *    random value;
  *  - Philox key = (seed lo, seed hi), counter = (g lo, g hi, stream lo,
- *    stream hi), g = idx >> 2, word idx & 3, idx = row * cols + col of the
- *    emitted logical matrix (the row-wise index of x for 16x16 scaling);
+ *    stream hi), g = idx >> 3; element idx takes 16 bits of word
+ *    (idx >> 1) & 3, the low half for even idx; idx = row * cols + col of
+ *    the emitted logical matrix (the row-wise index of x for 16x16 scaling);
  *  - RHT butterfly: D first, stages s = 0..3 pairing (i, i ^ 2^s) into
  *    (a + b, a - b) with a at the lower index, then * 0.25.
  */
@@ -68,8 +70,9 @@ uint8_t oracle_e2m1_rne(float v)
 
 /* Stochastic rounding ("Full-Stack FP4", Appendix 7: for u in [c_k, c_k+1]
  * with d = u - c_k, round up to c_k+1 with probability d / step_k).  The
- * probability is realised as: up iff (float)(word >> 8) < frac * 2^24. */
-uint8_t oracle_e2m1_sr(float v, uint32_t rand_word)
+ * probability is realised with a 16-bit random value r: up iff
+ * (float)r < frac * 2^16, so P(up) = ceil(frac * 2^16) / 2^16. */
+uint8_t oracle_e2m1_sr(float v, uint32_t rand16)
 {
     uint8_t sign = signbit(v) ? 8u : 0u;
     float a = fabsf(v);
@@ -81,8 +84,8 @@ uint8_t oracle_e2m1_sr(float v, uint32_t rand_word)
     float d = a - kE2M1Magnitude[k];                     /* exact: c_k >= a/2 or c_k = 0 */
     float step = kE2M1Magnitude[k + 1] - kE2M1Magnitude[k];  /* a power of two */
     float frac = d / step;                               /* exact */
-    float u24 = (float)(rand_word >> 8);                 /* exact, < 2^24 */
-    int up = u24 < frac * 16777216.0f;                   /* both sides exact */
+    float u16 = (float)(rand16 & 0xFFFFu);               /* exact, < 2^16 */
+    int up = u16 < frac * 65536.0f;                      /* both sides exact */
     return (uint8_t)(sign | (uint8_t)(k + up));
 }
 
@@ -147,15 +150,16 @@ void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-uint32_t oracle_sr_word(uint64_t seed, uint64_t stream_id, uint64_t idx)
+uint32_t oracle_sr_bits(uint64_t seed, uint64_t stream_id, uint64_t idx)
 {
-    uint64_t g = idx >> 2;
+    uint64_t g = idx >> 3;                       /* one Philox block per 8 elements */
     uint32_t ctr[4] = {(uint32_t)g, (uint32_t)(g >> 32), (uint32_t)stream_id,
                        (uint32_t)(stream_id >> 32)};
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t out[4];
     oracle_philox4x32_10(ctr, key, out);
-    return out[idx & 3u];
+    uint32_t word = out[(idx >> 1) & 3u];
+    return (idx & 1u) ? (word >> 16) : (word & 0xFFFFu);
 }
 
 /* ------------------------------------------------------------------ */
@@ -323,7 +327,7 @@ int oracle_quantize_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t 
                                       : (uint64_t)(j * cols + lr);
                         else
                             idx = (uint64_t)(lr * lcols + j);
-                        q[u] = oracle_e2m1_sr(v, oracle_sr_word(seed, stream_id, idx));
+                        q[u] = oracle_e2m1_sr(v, oracle_sr_bits(seed, stream_id, idx));
                     }
                 }
                 crow[(16 * b + t) / 2] = (uint8_t)(q[0] | (q[1] << 4));
@@ -421,11 +425,11 @@ void oracle_e2m1_rne_array(const float *v, int64_t n, uint8_t *codes)
         codes[i] = oracle_e2m1_rne(v[i]);
 }
 
-void oracle_e2m1_sr_array(const float *v, const uint32_t *rand_words, int64_t n, uint8_t *codes)
+void oracle_e2m1_sr_array(const float *v, const uint32_t *rand16, int64_t n, uint8_t *codes)
 {
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i)
-        codes[i] = oracle_e2m1_sr(v[i], rand_words[i]);
+        codes[i] = oracle_e2m1_sr(v[i], rand16[i]);
 }
 
 void oracle_e4m3_rne_satfinite_array(const float *x, int64_t n, uint8_t *codes)

@@ -39,8 +39,8 @@ extern "C" {
 double oracle_e2m1_value(uint8_t code);
 /* Nearest E2M1 value of v, ties to the even mantissa, saturating at 6. */
 uint8_t oracle_e2m1_rne(float v);
-/* Stochastic rounding of v with one 32-bit random word. */
-uint8_t oracle_e2m1_sr(float v, uint32_t rand_word);
+/* Stochastic rounding of v with a 16-bit random value (low 16 bits). */
+uint8_t oracle_e2m1_sr(float v, uint32_t rand16);
 
 /* E4M3 (FN variant, bias 7, max 448, 0x7F = NaN) code -> value. */
 double oracle_e4m3_value(uint8_t code);
@@ -49,8 +49,8 @@ uint8_t oracle_e4m3_rne_satfinite(float x);
 
 /* Philox4x32-10 block function. */
 void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
-/* The random word that stochastic rounding of element `idx` uses. */
-uint32_t oracle_sr_word(uint64_t seed, uint64_t stream_id, uint64_t idx);
+/* The 16 random bits that stochastic rounding of element `idx` uses. */
+uint32_t oracle_sr_bits(uint64_t seed, uint64_t stream_id, uint64_t idx);
 
 /* y = (1/4) * H16 * D * x, D = diag(bit i of sign_mask ? -1 : +1). */
 void oracle_rht16(const float x[16], uint16_t sign_mask, float y[16]);
@@ -105,7 +105,7 @@ void oracle_gemm_f64(const uint8_t *a_codes, const uint8_t *a_scales, float a_sg
 
 /* Element-wise array forms of the scalar encoders above (same arithmetic). */
 void oracle_e2m1_rne_array(const float *v, int64_t n, uint8_t *codes);
-void oracle_e2m1_sr_array(const float *v, const uint32_t *rand_words, int64_t n, uint8_t *codes);
+void oracle_e2m1_sr_array(const float *v, const uint32_t *rand16, int64_t n, uint8_t *codes);
 void oracle_e4m3_rne_satfinite_array(const float *x, int64_t n, uint8_t *codes);
 
 /* Threads the OpenMP loops use (1 without OpenMP). */

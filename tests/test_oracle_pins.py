@@ -118,7 +118,7 @@ def test_e2m1_sign_bit_follows_input():
 
 
 def test_e2m1_sr_grid_points_never_move():
-    words = [0, 1, 0xFF, 0x100, 0x7FFFFFFF, 0xFFFFFFFF]
+    words = [0, 1, 0xFF, 0x100, 0x7FFF, 0xFFFF]
     for code in range(8):
         for w in words:
             assert oracle.e2m1_sr(float(GRID[code]), w) == code
@@ -126,15 +126,15 @@ def test_e2m1_sr_grid_points_never_move():
 
 
 def test_e2m1_sr_probability_threshold():
-    """P(up) = d / step realised with 24-bit words: up iff u < ceil(frac * 2^24)."""
+    """P(up) = d / step realised with 16 random bits: up iff u < ceil(frac * 2^16)."""
     for v in (0.1, 0.3, 0.74, 1.2, 1.6, 1.9, 2.2, 2.9, 3.3, 4.5, 5.9, 1e-7):
         k = int(np.searchsorted(GRID, v, side="right") - 1)
         frac = Fraction(float(np.float32(v))) - Fraction(float(GRID[k]))
         frac /= Fraction(float(GRID[k + 1] - GRID[k]))
-        thr = math.ceil(frac * 2 ** 24)
-        assert oracle.e2m1_sr(v, (thr - 1) << 8) == k + 1
-        assert oracle.e2m1_sr(v, ((thr - 1) << 8) | 0xFF) == k + 1
-        assert oracle.e2m1_sr(v, thr << 8) == k
+        thr = math.ceil(frac * 2 ** 16)
+        assert oracle.e2m1_sr(v, thr - 1) == k + 1
+        assert oracle.e2m1_sr(v, thr) == k
+        assert oracle.e2m1_sr(v, 0xFFFF) == k
 
 
 @pytest.mark.parametrize("v", [0.1, 0.3, 0.74, 1.2, 1.9, 2.2, 2.9, 3.3, 4.5, 5.9])
@@ -142,7 +142,7 @@ def test_e2m1_sr_unbiased_with_page_variance(v):
     """Appendix 7: SR is unbiased with variance d (step - d); 10^6 draws, 4 sigma."""
     n = 1_000_000
     rng = np.random.default_rng(int(v * 1000))
-    words = rng.integers(0, 2 ** 32, n, dtype=np.uint64).astype(np.uint32)
+    words = rng.integers(0, 2 ** 16, n, dtype=np.uint64).astype(np.uint32)
     q = _e2m1_values(oracle.e2m1_sr_array(np.full(n, v, np.float32), words))
     k = int(np.searchsorted(GRID, v, side="right") - 1)
     step = GRID[k + 1] - GRID[k]
@@ -229,20 +229,23 @@ def test_philox_matches_curand_host_generator(seed):
     for i in list(range(16)) + [100, 255, 511]:
         ours = oracle.philox4x32_10([0, 0, i, 0], key)
         assert np.array_equal(ours, ref[i]), i
-    # the SR word of element idx < 4 in stream s is word idx of block s
+    # the SR bits of element idx < 8 in stream s are 16 bits of block s
     for s in (0, 3, 77):
-        for idx in range(4):
-            assert oracle.sr_word(seed, s, idx) == ref[s][idx]
+        for idx in range(8):
+            word = int(ref[s][idx // 2])
+            assert oracle.sr_bits(seed, s, idx) == (word >> (16 * (idx % 2))) & 0xFFFF
 
 
-def test_sr_word_counter_layout():
-    """g = idx >> 2 goes to counter words 0-1, the stream to words 2-3."""
+def test_sr_bits_counter_layout():
+    """g = idx >> 3 goes to counter words 0-1, the stream to words 2-3; element
+    idx takes the low (even idx) or high (odd idx) half of word (idx >> 1) & 3."""
     seed, stream = 0xDEADBEEF12345678, 0x0000000A00000005
     key = [seed & 0xFFFFFFFF, seed >> 32]
-    for idx in (0, 5, 1 << 33, (1 << 40) + 3):
-        g = idx >> 2
+    for idx in (0, 5, 7, 1 << 33, (1 << 40) + 3):
+        g = idx >> 3
         block = oracle.philox4x32_10([g & 0xFFFFFFFF, g >> 32, stream & 0xFFFFFFFF, stream >> 32], key)
-        assert oracle.sr_word(seed, stream, idx) == block[idx & 3]
+        word = int(block[(idx >> 1) & 3])
+        assert oracle.sr_bits(seed, stream, idx) == (word >> (16 * (idx & 1))) & 0xFFFF
 
 
 # ----------------------------------------------------------------- RHT ----
