@@ -64,19 +64,22 @@ __device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
 
 // Stochastic rounding of one value to an E2M1 code with 16 random bits
 // ("Full-Stack FP4", Appendix 7: round up with probability d / step): up iff
-// r16 < frac * 2^16.  Branch free: with m = 1 / step of |v|'s bin (2, 1 or
-// 1/2), |v| * m is exact, its floor q picks the lower grid point and
-// (|v| * m - q) * 2^16 = frac * 2^16 is exact too.
+// r16 < frac * 2^16.  With m = 1 / step of |v|'s bin (2, 1 or 1/2), |v| * m is
+// exact and below 4; its floor q (the lower grid point) comes from a
+// round-toward-zero add of 2^23 and (|v| * m - q) * 2^16 = frac * 2^16 is
+// exact.  No int/float conversion instruction is used.
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
     const uint32_t sign = __float_as_uint(v) >> 31;
     const float a = fabsf(v);
     const bool below2 = a < 2.0f, below4 = a < 4.0f;
     const float m = below2 ? 2.0f : (below4 ? 1.0f : 0.5f);
     const float am = __fmul_rn(a, m);
-    const float q = floorf(am);
+    const float t = __fadd_rz(am, 8388608.0f);                       // 2^23 + floor(am)
+    const uint32_t q = __float_as_uint(t) & 3u;
+    const float frac16 = __fmul_rn(__fsub_rn(am, __fsub_rn(t, 8388608.0f)), 65536.0f);
+    const float r = __fsub_rn(__uint_as_float(0x4B000000u | r16), 8388608.0f);   // exactly r16
     const uint32_t offset = below2 ? 0u : (below4 ? 2u : 4u);   // codes of the bins' first grid point minus q
-    const float frac16 = __fmul_rn(__fsub_rn(am, q), 65536.0f);
-    uint32_t code = (uint32_t)q + offset + ((__uint2float_rn(r16) < frac16) ? 1u : 0u);
+    uint32_t code = q + offset + (r < frac16 ? 1u : 0u);
     code = (a >= 6.0f) ? 7u : code;
     return code | (sign << 3);
 }
