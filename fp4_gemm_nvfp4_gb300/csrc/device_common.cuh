@@ -365,6 +365,18 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
+// mbar_wait on a barrier given by its shared-memory address.
+__device__ __forceinline__ bool mbar_wait_addr(uint32_t a, uint32_t parity, uint64_t timeout_ns) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try_wait_cluster(a, parity)) return true;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
 // mbar_wait for barriers that also receive arrivals from the peer CTA.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
     const uint32_t a = smem_u32(bar);
@@ -391,6 +403,16 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* tmap, ui
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
         "l"(tmap), "r"(leader_bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+// 3-D TMA tile load completing on an mbarrier of this CTA.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y,
+                                            int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
 
@@ -454,12 +476,52 @@ __device__ __forceinline__ void mma_nvf4_pair_x4(uint32_t d_tmem, uint64_t a_des
         : "memory");
 }
 
+// The four K = 64 MMAs of one 256-deep stage.  Descriptors are built from
+// their 32-bit low words (start address >> 4 in the low 14 bits, which never
+// carry: shared memory is below 256 KiB) and the common high word, so the
+// issuing thread spends as few instructions as possible between MMAs.
+// B's descriptor is kBOff address units after A's; per K step A and B advance
+// 32 bytes (2 units) and the scale columns by 4 (A) and 8 (B), B's scales
+// starting 16 columns after A's.
+template <bool kAccumulate, uint32_t kBOff>
+__device__ __forceinline__ void mma_nvf4_pair_stage(uint32_t d_tmem, uint32_t a_lo, uint32_t desc_hi, uint32_t idesc,
+                                                    uint32_t sf_col) {
+    asm volatile(
+        "{\n\t"
+        ".reg .b32 a1, a2, a3, b0, b1, b2, b3, sa1, sa2, sa3, sb0, sb1, sb2, sb3;\n\t"
+        ".reg .b64 da0, da1, da2, da3, db0, db1, db2, db3;\n\t"
+        ".reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "add.u32 a1, %1, 2;\n\tadd.u32 a2, %1, 4;\n\tadd.u32 a3, %1, 6;\n\t"
+        "add.u32 b0, %1, %6;\n\tadd.u32 b1, b0, 2;\n\tadd.u32 b2, b0, 4;\n\tadd.u32 b3, b0, 6;\n\t"
+        "add.u32 sa1, %4, 4;\n\tadd.u32 sa2, %4, 8;\n\tadd.u32 sa3, %4, 12;\n\t"
+        "add.u32 sb0, %4, 16;\n\tadd.u32 sb1, %4, 24;\n\tadd.u32 sb2, %4, 32;\n\tadd.u32 sb3, %4, 40;\n\t"
+        "mov.b64 da0, {%1, %2};\n\tmov.b64 da1, {a1, %2};\n\tmov.b64 da2, {a2, %2};\n\tmov.b64 da3, {a3, %2};\n\t"
+        "mov.b64 db0, {b0, %2};\n\tmov.b64 db1, {b1, %2};\n\tmov.b64 db2, {b2, %2};\n\tmov.b64 db3, {b3, %2};\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da0, db0, %3, [%4], [sb0], p;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da1, db1, %3, [sa1], [sb1], 1;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da2, db2, %3, [sa2], [sb2], 1;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], da3, db3, %3, [sa3], [sb3], 1;\n\t"
+        "}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(desc_hi), "r"(idesc), "r"(sf_col), "n"(kAccumulate ? 1 : 0), "n"(kBOff)
+        : "memory");
+}
+
 // Arrive on the mbarrier at the same offset in every CTA of `cta_mask` once
 // this thread's pair MMAs so far have completed.
 __device__ __forceinline__ void tc_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
             smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// tc_commit_pair_multicast on a barrier given by its shared-memory address.
+__device__ __forceinline__ void tc_commit_pair_multicast_addr(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
         "h"(cta_mask)
         : "memory");
 }

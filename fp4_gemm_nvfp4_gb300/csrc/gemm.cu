@@ -10,20 +10,23 @@
 // output tiles.  The pair's tile is computed by tcgen05.mma.cta_group::2: each
 // CTA holds 128 rows of A and 128 of the 256 B rows in its shared memory and
 // 128 accumulator rows in its tensor memory, so each SM streams half of B.
-// Per CTA:
-//   warp 0      TMA producer: per stage (256 fp4 of K) a 128-row A box and a
-//               128-row B box (128-byte swizzle, completing on the leader
-//               CTA's mbarrier) and the stage's block scales (512-byte groups
-//               of the tile layout: this CTA's 128 A rows and all 256 B rows)
-//               by bulk copies completing on a local mbarrier;
+// Per CTA (16 warps):
+//   warps 0, 2  TMA producers, one copy per stage each: the 128-row A box and
+//               the 128-row B box (256 fp4 of K, 128-byte swizzle), both
+//               completing on the leader CTA's full barrier;
+//   warp 3      scale producer: the stage's block scales (this CTA's 128 A
+//               rows, all 256 B rows) as two 3-D TMA boxes of the tile layout
+//               onto a local barrier;
 //   warp 1      TMEM allocation for the pair; in the leader CTA, the MMA
-//               issuer: four block-scaled MMAs (K = 64 each) per stage, then a
-//               commit that releases the stage in both CTAs;
-//   warps 2-5   scale warps, one per TMEM lane quadrant: move the stage's
+//               issuer: one barrier wait, four block-scaled MMAs (K = 64 each)
+//               and one commit per stage, nothing else (the tensor pipe only
+//               stays busy while the issuing thread keeps up with it);
+//   warps 4-7   scale warps, one per TMEM lane quadrant: move the stage's
 //               scales from shared memory into the stage's TMEM columns with
-//               tcgen05.st (off the MMA pipe) and arrive on the leader's
-//               barrier;
-//   warps 6-13  epilogue, two per lane quadrant (one per 128-column half):
+//               tcgen05.st (off the MMA pipe) and arrive on the leader's full
+//               barrier, which therefore completes when both CTAs' tiles have
+//               landed and all eight scale warps are done;
+//   warps 8-15  epilogue, two per lane quadrant (one per 128-column half):
 //               drain the FP32 accumulator, scale by s_gA * s_gB, release the
 //               accumulator to the leader, stage BF16 results in 128-byte-
 //               swizzled shared memory and write them with TMA stores (FP32
@@ -45,24 +48,32 @@ static __device__ unsigned int g_gemm_status = 0;
 
 namespace {
 
+constexpr int kNumEpiWarpsStaging = 8;
 constexpr int kPairM = 256;                      // output rows per CTA pair
 constexpr int kCtaM = 128;                       // rows of A (and accumulator lanes) per CTA
 constexpr int kBN = 256;                         // output columns per tile
 constexpr int kCtaN = 128;                       // rows of B per CTA
 constexpr int kBKBytes = 128;                    // 256 fp4 of K per row per stage
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kKStepsPerStage = 4;               // K = 64 per MMA
 constexpr uint32_t kABytes = kCtaM * kBKBytes;   // 16 KiB
 constexpr uint32_t kBBytes = kCtaN * kBKBytes;   // 16 KiB
 constexpr uint32_t kSFABytes = kKStepsPerStage * 512;
 constexpr uint32_t kSFBBytes = 2 * kKStepsPerStage * 512;
 constexpr uint32_t kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
-constexpr uint32_t kStagingBytes = kCtaM * kBN * 2;   // this CTA's BF16 rows of a tile
-constexpr int kFirstSfWarp = 2;
+constexpr uint32_t kStagingBytes = kNumEpiWarpsStaging * 4096;   // 32 rows x 64 BF16 columns per epilogue warp
+constexpr int kProdAWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kProdBWarp = 2;
+constexpr int kProdSfWarp = 3;
+constexpr int kFirstSfWarp = 4;
 constexpr int kNumSfWarps = 4;
 constexpr int kFirstEpiWarp = kFirstSfWarp + kNumSfWarps;
 constexpr int kNumEpiWarps = 8;
 constexpr int kThreads = 32 * (kFirstEpiWarp + kNumEpiWarps);
+// the leader's full barrier: its A producer's arrive.expect_tx plus the scale
+// warps of both CTAs
+constexpr uint32_t kFullArrivals = 1 + 2 * kNumSfWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;                   // 256 FP32 accumulator columns
 constexpr uint32_t kSfCol0 = 256;                 // then the per-stage scale columns
@@ -79,10 +90,7 @@ struct Params {
     uint32_t m_tiles, n_tiles;   // 256-row and 256-column tiles
     uint32_t ksteps;             // ceil(K / 64): MMAs per tile, also 4-scale groups per row
     uint32_t kstages;            // ceil(ksteps / 4)
-    uint32_t sfa_row_tiles;      // ceil(M / 128)
-    uint32_t sfb_row_tiles;      // ceil(N / 128)
-    const uint8_t* sfa;
-    const uint8_t* sfb;
+    uint32_t last_nk;            // MMAs in a tile's last stage (1..4)
     const float* sga;
     const float* sgb;
     void* d;
@@ -123,15 +131,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                     const __grid_constant__ CUtensorMap tma_sfa, const __grid_constant__ CUtensorMap tma_sfb,
                      const __grid_constant__ CUtensorMap tma_d, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* staging = smem + kStages * kStageBytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStagingBytes);   // leader: both CTAs' A/B bytes
+    uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStagingBytes);   // leader: tiles + scale warps
     uint64_t* sf_full = full + kStages;          // local: this CTA's scale bytes
     uint64_t* empty = sf_full + kStages;         // local: released by the leader's commit
-    uint64_t* sf_ready = empty + kStages;        // leader: both CTAs' scale warps
-    uint64_t* acc_full = sf_ready + kStages;     // local: released by the leader's commit
+    uint64_t* acc_full = empty + kStages;        // local: released by the leader's commit
     uint64_t* acc_empty = acc_full + 1;          // leader: 2 x kNumEpiWarps arrivals
     uint64_t* drain = acc_empty + 1;             // leader
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -142,21 +150,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool leader = rank == 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], kFullArrivals);
             mbar_init(&sf_full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&sf_ready[s], 2 * kNumSfWarps);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 2 * kNumEpiWarps);
         mbar_init(drain, 1);
         *abort_flag = 0u;
         fence_barrier_init();
-        prefetch_tmap(&tma_a);
-        prefetch_tmap(&tma_b);
-        if (p.tma_store) prefetch_tmap(&tma_d);
     }
-    if (warp == 1) {
+    if (warp == kProdAWarp && lane == 0) prefetch_tmap(&tma_a);
+    if (warp == kProdBWarp && lane == 0) prefetch_tmap(&tma_b);
+    if (warp == kProdSfWarp && lane == 0) {
+        prefetch_tmap(&tma_sfa);
+        prefetch_tmap(&tma_sfb);
+    }
+    if (warp == kFirstEpiWarp && lane == 0 && p.tma_store) prefetch_tmap(&tma_d);
+    if (warp == kMmaWarp) {
         tmem_alloc_pair(tmem_slot, kTmemCols);
         tmem_relinquish_pair();
     }
@@ -168,42 +179,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t num_tiles = p.m_tiles * p.n_tiles;
     const uint32_t first_tile = cluster_id_x(), tile_stride = num_clusters_x();
 
-    if (warp == 0) {
+    if (warp == kProdAWarp || warp == kProdBWarp || warp == kProdSfWarp) {
         if (lane == 0) {
-            // -------------------------------------------------- producer
+            // ------------------------------------------------- producers
+            // Three warps, one or two copies each per stage: a single thread
+            // cannot issue a stage's five copies fast enough.
             uint32_t armed = 0, armed_parity = 0;   // per stage: copies issued, parity of their phase
             uint32_t stage = 0, phase = 0;
+            const uint32_t leader_full0 = map_to_cta(smem_u32(full), 0);
             for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
                 const uint32_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
-                const bool a_sf = (2 * mt + rank) < p.sfa_row_tiles;
-                const bool b_hi = (2 * nt + 1) < p.sfb_row_tiles;
                 for (uint32_t ks = 0; ks < p.kstages; ++ks) {
-                    if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, kTimeoutNs)) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, kTimeoutNs)) {
                         record_timeout(abort_flag);
                         break;
                     }
                     if (*abort_flag) break;
-                    const uint32_t k0 = ks * kKStepsPerStage;
-                    const uint32_t nk = min((uint32_t)kKStepsPerStage, p.ksteps - k0);
                     uint8_t* st = smem + stage * kStageBytes;
-                    uint8_t* sfa_s = st + kABytes + kBBytes;
-                    uint8_t* sfb_s = sfa_s + kSFABytes;
-                    if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (kABytes + kBBytes));
-                    mbar_arrive_expect_tx(&sf_full[stage], nk * 512u * ((a_sf ? 1u : 0u) + (b_hi ? 2u : 1u)));
+                    const uint32_t leader_full = leader_full0 + stage * 8u;
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    const uint32_t leader_full = map_to_cta(smem_u32(&full[stage]), 0);
-                    tma_load_2d_pair(st, &tma_a, leader_full, (int32_t)(ks * kBKBytes),
-                                     (int32_t)(mt * kPairM + rank * kCtaM));
-                    tma_load_2d_pair(st + kABytes, &tma_b, leader_full, (int32_t)(ks * kBKBytes),
-                                     (int32_t)(nt * kBN + rank * kCtaN));
-                    if (a_sf)
-                        bulk_load(sfa_s, p.sfa + ((size_t)(2 * mt + rank) * p.ksteps + k0) * 512u, nk * 512u,
-                                  &sf_full[stage]);
-                    bulk_load(sfb_s, p.sfb + ((size_t)(2 * nt) * p.ksteps + k0) * 512u, nk * 512u, &sf_full[stage]);
-                    if (b_hi)
-                        bulk_load(sfb_s + kKStepsPerStage * 512u, p.sfb + ((size_t)(2 * nt + 1) * p.ksteps + k0) * 512u,
-                                  nk * 512u, &sf_full[stage]);
+                    if (warp == kProdAWarp) {
+                        if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (kABytes + kBBytes));
+                        tma_load_2d_pair(st, &tma_a, leader_full, (int32_t)(ks * kBKBytes),
+                                         (int32_t)(mt * kPairM + rank * kCtaM));
+                    } else if (warp == kProdBWarp) {
+                        tma_load_2d_pair(st + kABytes, &tma_b, leader_full, (int32_t)(ks * kBKBytes),
+                                         (int32_t)(nt * kBN + rank * kCtaN));
+                    } else {
+                        // scale boxes: 4 groups of 512 bytes per 128-row tile;
+                        // groups past K and row tiles past M / N read as zero
+                        uint8_t* sfa_s = st + kABytes + kBBytes;
+                        mbar_arrive_expect_tx(&sf_full[stage], kSFABytes + kSFBBytes);
+                        tma_load_3d(sfa_s, &tma_sfa, &sf_full[stage], 0, (int32_t)(ks * kKStepsPerStage),
+                                    (int32_t)(2 * mt + rank));
+                        tma_load_3d(sfa_s + kSFABytes, &tma_sfb, &sf_full[stage], 0, (int32_t)(ks * kKStepsPerStage),
+                                    (int32_t)(2 * nt));
+                    }
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -216,14 +228,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kStages; ++s) {
                 if (!((armed >> s) & 1u)) continue;
                 const uint32_t par = (armed_parity >> s) & 1u;
-                if (leader) (void)mbar_wait_cluster(&full[s], par, kTimeoutNs);
-                (void)mbar_wait(&sf_full[s], par, kTimeoutNs);
+                if (warp == kProdAWarp && leader) (void)mbar_wait_cluster(&full[s], par, kTimeoutNs);
+                if (warp == kProdSfWarp) (void)mbar_wait(&sf_full[s], par, kTimeoutNs);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         if (leader && lane == 0) {
             // ------------------------------------------------ MMA issuer
+            // The tensor pipe only stays busy while this thread keeps up with
+            // it, so the loop body is one barrier wait, the stage's four MMAs
+            // (one asm block, descriptors built from 32-bit low words) and one
+            // commit, with every stage address advanced by an add.  (Splitting
+            // the four MMAs to wait for the next stage in between measured
+            // slower.)
+            constexpr uint32_t kStageDesc = kStageBytes >> 4;   // descriptor address units
+            constexpr uint32_t kBOff = kABytes >> 4;
+            const uint64_t desc0 = smem_desc(smem_u32(smem), 16, 1024, 2);
+            const uint32_t lo0 = (uint32_t)desc0, hi = (uint32_t)(desc0 >> 32);
+            const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
+            const uint32_t sfc0 = tmem + kSfCol0;
+            const uint32_t acc = tmem + kAccCol;
+            const uint32_t kst = p.kstages;
+            const bool tail = p.last_nk != (uint32_t)kKStepsPerStage;
             uint32_t stage = 0, phase = 0, tiles_done = 0;
+            uint32_t alo = lo0, sfc = sfc0, fa = full0, ea = empty0;
             for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
                 if (!mbar_wait_cluster(acc_empty, (tiles_done & 1u) ^ 1u, kTimeoutNs)) {
                     record_timeout(abort_flag);
@@ -231,30 +259,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 bool ok = true;
-                for (uint32_t ks = 0; ks < p.kstages; ++ks) {
-                    if (!mbar_wait_cluster(&full[stage], phase, kTimeoutNs) ||
-                        !mbar_wait_cluster(&sf_ready[stage], phase, kTimeoutNs)) {
+                for (uint32_t ks = 0; ks < kst; ++ks) {
+                    if (!mbar_wait_addr(fa, phase, kTimeoutNs)) {
                         record_timeout(abort_flag);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t nk = min((uint32_t)kKStepsPerStage, p.ksteps - ks * kKStepsPerStage);
-                    const uint32_t st = smem_u32(smem + stage * kStageBytes);
-                    const uint32_t sf_col = tmem + kSfCol0 + stage * kSfColsPerStage;
-                    const uint64_t adesc = smem_desc(st, 16, 1024, 2);
-                    const uint64_t bdesc = smem_desc(st + kABytes, 16, 1024, 2);
-                    if (nk == (uint32_t)kKStepsPerStage) {
-                        mma_nvf4_pair_x4(tmem + kAccCol, adesc, bdesc, kIdesc, sf_col, sf_col + 16, ks != 0 ? 1u : 0u);
+                    if (ks != 0 && (ks + 1u != kst || !tail)) {
+                        mma_nvf4_pair_stage<true, kBOff>(acc, alo, hi, kIdesc, sfc);
+                    } else if (ks + 1u != kst || !tail) {
+                        mma_nvf4_pair_stage<false, kBOff>(acc, alo, hi, kIdesc, sfc);
                     } else {
-                        for (uint32_t j = 0; j < nk; ++j)
-                            mma_nvf4_pair(tmem + kAccCol, adesc + 2 * j, bdesc + 2 * j, kIdesc, sf_col + 4 * j,
-                                          sf_col + 16 + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                        // last stage of a K that is not a multiple of 256
+                        const uint64_t da = ((uint64_t)hi << 32) | alo;
+                        for (uint32_t j = 0; j < p.last_nk; ++j)
+                            mma_nvf4_pair(acc, da + 2 * j, da + kBOff + 2 * j, kIdesc, sfc + 4 * j, sfc + 16 + 8 * j,
+                                          (ks | j) != 0 ? 1u : 0u);
                     }
-                    tc_commit_pair_multicast(&empty[stage], 0x3);
+                    tc_commit_pair_multicast_addr(ea, 0x3);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
+                        alo = lo0;
+                        sfc = sfc0;
+                        fa = full0;
+                        ea = empty0;
+                    } else {
+                        alo += kStageDesc;
+                        sfc += kSfColsPerStage;
+                        fa += 8u;
+                        ea += 8u;
                     }
                 }
                 if (!ok) break;
@@ -265,12 +300,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_commit_pair_multicast(drain, 0x1);
             (void)mbar_wait(drain, 0, kTimeoutNs);
         }
-    } else if (warp < kFirstEpiWarp) {
+    } else if (warp < (uint32_t)kFirstEpiWarp) {
         // ------------------------------------------------------ scale warps
         // Lane i of quadrant q holds, per K = 64 step j, 4 columns of A scales
         // (bytes 16i.. of the step's 512-byte group: rows i, i+32, i+64, i+96)
         // and 8 columns of B scales (both 128-row halves of the N tile).
         const uint32_t q = warp & 3u;
+        const uint32_t leader_full0 = map_to_cta(smem_u32(full), 0);
         uint32_t stage = 0, phase = 0;
         for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
             bool ok = true;
@@ -305,7 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&sf_ready[stage]), 0));
+                if (lane == 0) mbar_arrive_cluster(leader_full0 + stage * 8u);
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1u;
@@ -330,47 +366,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t nbase = nt * kBN + half * 128;
             const uint32_t taddr = tmem + ((q * 32u) << 16) + kAccCol + half * 128;
             if (p.tma_store) {
-                // the previous tile's stores must have read the staging buffer
-                if (lane == 0) bulk_wait_read_all();
-                __syncwarp();
+                // Two rounds of 64 columns through this warp's 4 KiB slice of
+                // the staging buffer (32 rows x 128 bytes, 128-byte swizzle).
+                // The accumulator is handed back as soon as the second
+                // round's columns are in registers.
+                uint8_t* slice = staging + (half * 4 + q) * 4096u;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr + c * 32, v);
-                    tmem_ld_wait();
-                    // 32 columns = four 16-byte pieces of one 128-byte swizzled row
-                    uint8_t* blk = staging + (2 * half + (c >> 1)) * (kCtaM * 128) + row_local * 128;
+                for (int r = 0; r < 2; ++r) {
+                    uint32_t packed[32];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t piece = (uint32_t)((c & 1) * 4 + i) ^ (row_local & 7u);
-                        const uint4 w = make_uint4(
-                            pack_bf16x2(__fmul_rn(__uint_as_float(v[8 * i + 0]), alpha),
-                                        __fmul_rn(__uint_as_float(v[8 * i + 1]), alpha)),
-                            pack_bf16x2(__fmul_rn(__uint_as_float(v[8 * i + 2]), alpha),
-                                        __fmul_rn(__uint_as_float(v[8 * i + 3]), alpha)),
-                            pack_bf16x2(__fmul_rn(__uint_as_float(v[8 * i + 4]), alpha),
-                                        __fmul_rn(__uint_as_float(v[8 * i + 5]), alpha)),
-                            pack_bf16x2(__fmul_rn(__uint_as_float(v[8 * i + 6]), alpha),
-                                        __fmul_rn(__uint_as_float(v[8 * i + 7]), alpha)));
-                        *reinterpret_cast<uint4*>(blk + piece * 16) = w;
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(taddr + (2 * r + cc) * 32, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            packed[16 * cc + i] = pack_bf16x2(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
+                                                              __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
                     }
-                }
-                tc_fence_before();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive_cluster(leader_acc_empty);
-                    const uint32_t y = row0 + q * 32;
-                    if (y < p.M) {
-#pragma unroll
-                        for (int b = 0; b < 2; ++b) {
-                            const uint32_t x = nt * kBN + (2 * half + b) * 64;
-                            if (x < p.N)
-                                tma_store_2d(&tma_d, staging + (2 * half + b) * (kCtaM * 128) + q * 32 * 128,
-                                             (int32_t)x, (int32_t)y);
-                        }
+                    if (r == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
                     }
-                    bulk_commit_group();
+                    // the slice's previous store must have read it
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<uint4*>(slice + lane * 128u + ((uint32_t)i ^ (lane & 7u)) * 16u) =
+                            make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t y = row0 + q * 32, x = nbase + r * 64;
+                        if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
+                        bulk_commit_group();
+                    }
                 }
             } else {
 #pragma unroll 1
@@ -464,6 +496,22 @@ bool make_codes_map(CUtensorMap* map, const GemmOperand& op, uint32_t box_rows) 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale map over the tile layout viewed as [row tile][4-scale group][128
+// words]: one box is 4 groups (256 of K) of 1 or 2 row tiles.  Boxes past the
+// last group or row tile read as zero.
+bool make_scale_map(CUtensorMap* map, const GemmOperand& op, uint32_t box_row_tiles) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t groups = (uint64_t)((op.cols + 63) / 64), row_tiles = (uint64_t)((op.rows + 127) / 128);
+    const cuuint64_t dims[3] = {128, (cuuint64_t)groups, (cuuint64_t)row_tiles};
+    const cuuint64_t strides[2] = {512, (cuuint64_t)(groups * 512)};
+    const cuuint32_t box[3] = {128, (cuuint32_t)kKStepsPerStage, box_row_tiles};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(op.scales), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // BF16 output map: 64-column x 32-row boxes, 128-byte swizzle.
 bool make_output_map(CUtensorMap* map, void* d, int64_t M, int64_t N, int64_t ldd) {
     EncodeTiledFn fn = encode_fn();
@@ -527,8 +575,10 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    CUtensorMap ma, mb, md;
-    if (!make_codes_map(&ma, a, kCtaM) || !make_codes_map(&mb, b, kCtaN)) return cudaErrorInvalidValue;
+    CUtensorMap ma, mb, msa, msb, md;
+    if (!make_codes_map(&ma, a, kCtaM) || !make_codes_map(&mb, b, kCtaN) || !make_scale_map(&msa, a, 1) ||
+        !make_scale_map(&msb, b, 2))
+        return cudaErrorInvalidValue;
     Params p{};
     p.M = (uint32_t)a.rows;
     p.N = (uint32_t)b.rows;
@@ -536,10 +586,7 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     p.n_tiles = (uint32_t)((b.rows + kBN - 1) / kBN);
     p.ksteps = (uint32_t)((a.cols + 63) / 64);
     p.kstages = (p.ksteps + kKStepsPerStage - 1) / kKStepsPerStage;
-    p.sfa_row_tiles = (uint32_t)((a.rows + 127) / 128);
-    p.sfb_row_tiles = (uint32_t)((b.rows + 127) / 128);
-    p.sfa = a.scales;
-    p.sfb = b.scales;
+    p.last_nk = p.ksteps - (p.kstages - 1) * kKStepsPerStage;
     p.sga = a.sg;
     p.sgb = b.sg;
     p.d = d;
@@ -552,7 +599,7 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     const uint32_t tiles = p.m_tiles * p.n_tiles;
     const uint32_t pairs = (uint32_t)max_active_pairs();
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
-    gemm_nvf4_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, md, p);
+    gemm_nvf4_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, p);
     return cudaGetLastError();
 }
 
