@@ -64,25 +64,31 @@ __device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
 
 // Stochastic rounding of one value to an E2M1 code with 16 random bits
 // ("Full-Stack FP4", Appendix 7: round up with probability d / step): up iff
-// r16 < frac * 2^16.  With m = 1 / step of |v|'s bin (2, 1 or 1/2), |v| * m is
-// exact and below 4; its floor q (the lower grid point) comes from a
-// round-toward-zero add of 2^23 and (|v| * m - q) * 2^16 = frac * 2^16 is
-// exact.  No int/float conversion instruction is used.
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) {
-    const uint32_t sign = __float_as_uint(v) >> 31;
-    const float a = fabsf(v);
-    const bool below2 = a < 2.0f, below4 = a < 4.0f;
-    const float m = below2 ? 2.0f : (below4 ? 1.0f : 0.5f);
-    const float am = __fmul_rn(a, m);
-    const float t = __fadd_rz(am, 8388608.0f);                       // 2^23 + floor(am)
-    const uint32_t q = __float_as_uint(t) & 3u;
-    const float frac16 = __fmul_rn(__fsub_rn(am, __fsub_rn(t, 8388608.0f)), 65536.0f);
-    const float r = __fsub_rn(__uint_as_float(0x4B000000u | r16), 8388608.0f);   // exactly r16
-    const uint32_t offset = below2 ? 0u : (below4 ? 2u : 4u);   // codes of the bins' first grid point minus q
-    uint32_t code = q + offset + (r < frac16 ? 1u : 0u);
-    code = (a >= 6.0f) ? 7u : code;
-    return code | (sign << 3);
+// r16 < frac * 2^16, i.e. iff r16 < ceil(frac * 2^16).
+//
+// Done on the FP32 bit pattern.  In each binade [2^e, 2^(e+1)) with e >= 0
+// the E2M1 grid keeps one mantissa bit, so frac is the low 22 mantissa bits
+// over 2^22, and adding ((2^16 - 1 - r16) << 6) + 63 to the pattern carries
+// into bit 22 exactly when r16 < ceil(frac * 2^16); shifting out the low 22
+// bits then leaves exponent and kept mantissa bit of the rounded value.
+// Below 1 the grid {0, 0.5, 1} is that of [1, 2) shifted by one and halved:
+// z = (|v| + 1) / 2, one fused multiply-add rounded upward (which keeps
+// ceil(frac * 2^16): float spacing there, 2^-24, is finer than 2^-18), lies
+// in [0.5, 1) where the same addition applies with codes two lower than the
+// [1, 2) formula gives, so one formula serves both: code = (bits + addend) /
+// 2^22 - 252.  max(|v|, (|v| + 1) / 2) selects z exactly when |v| < 1.  |v| >=
+// 6 saturates through the clamp to 6 (code 7); the code's sign bit is v's.
+__device__ __forceinline__ uint32_t sr_addend_lo(uint32_t w) { return ((~w << 6) & 0x3FFFC0u) | 63u; }
+__device__ __forceinline__ uint32_t sr_addend_hi(uint32_t w) { return ((~w >> 10) & 0x3FFFC0u) | 63u; }
+
+__device__ __forceinline__ uint32_t e2m1_sr_add(float v, uint32_t addend) {
+    const float a = fminf(fabsf(v), 6.0f);
+    const float z = fmaxf(a, __fmaf_ru(a, 0.5f, 0.5f));
+    const uint32_t code = (__float_as_uint(z) + addend - (252u << 22)) >> 22;
+    return code | ((__float_as_uint(v) >> 28) & 8u);
 }
+
+__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) { return e2m1_sr_add(v, sr_addend_lo(r16)); }
 
 // --------------------------------------------------------------- Philox ----
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
@@ -181,8 +187,9 @@ __device__ __forceinline__ uint2 encode16(const float* t, float r_b, const Philo
         uint32_t lo = 0, hi = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            lo |= e2m1_sr(v[i], (w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu) << (4 * i);
-            hi |= e2m1_sr(v[8 + i], (w[4 + (i >> 1)] >> (16 * (i & 1))) & 0xFFFFu) << (4 * i);
+            const uint32_t wl = w[i >> 1], wh = w[4 + (i >> 1)];
+            lo |= e2m1_sr_add(v[i], (i & 1) ? sr_addend_hi(wl) : sr_addend_lo(wl)) << (4 * i);
+            hi |= e2m1_sr_add(v[8 + i], (i & 1) ? sr_addend_hi(wh) : sr_addend_lo(wh)) << (4 * i);
         }
         return make_uint2(lo, hi);
     }

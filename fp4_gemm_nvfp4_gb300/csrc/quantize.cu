@@ -231,8 +231,8 @@ __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
                 const uint4 w = sr_words4(keys, a.stream, idx >> 3);
                 const uint32_t sel = (uint32_t)(idx >> 1) & 3u;
                 const uint32_t word = sel == 0 ? w.x : (sel == 1 ? w.y : (sel == 2 ? w.z : w.w));
-                const uint32_t c0 = e2m1_sr(__fmul_rn(t0[i], r_b), word & 0xFFFFu);
-                const uint32_t c1 = e2m1_sr(__fmul_rn(t1[i], r_b), word >> 16);
+                const uint32_t c0 = e2m1_sr_add(__fmul_rn(t0[i], r_b), sr_addend_lo(word));
+                const uint32_t c1 = e2m1_sr_add(__fmul_rn(t1[i], r_b), sr_addend_hi(word));
                 if (i < 8) {
                     q0.x |= c0 << (4 * i);
                     q1.x |= c1 << (4 * i);
