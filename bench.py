@@ -51,6 +51,21 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x, world, device):
+    """The slowest rank's time: the job's time (every rank gets it)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.item()
+
+
+def whole_job_tflops(flops_per_rank, world, ms):
+    """Weak scaling: every rank runs the full step on its own data."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
 # The step: (name, input, kwargs for ops.quantize) and the six GEMMs.
 QUANTS = [
     ("X.row", "X", dict(rowwise=True)),
@@ -360,13 +375,10 @@ def measure(args):
                 launch_ms["g:" + n] = time_replays(torch, g, args.steps, stream) / args.steps
         barrier()
         windows.append((t0, time.time()))
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = t.item()
+    total_ms = max_over_ranks(total_ms, world, "cuda")
     ms_per_step = total_ms / args.steps
     flops = step.flops()
-    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops, world, ms_per_step)
 
     # ---- end to end: pinned host inputs in and the six outputs out, every step
     pinned_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -389,10 +401,7 @@ def measure(args):
         e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = t.item()
+    e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
     status = ops.device_error()
     if status != capi.NVFP4_OK:
         raise RuntimeError(f"device status after timing: {capi.status_string(status)}")
@@ -431,7 +440,7 @@ def measure(args):
         "quantize_gbs": round(quant_gbs, 1),
         "quantize_frac_of_hbm": round(quant_gbs / peaks["hbm_gbs"], 4),
         "per_launch_ms": {k: round(v, 4) for k, v in sorted(launch_ms.items())},
-        "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(whole_job_tflops(flops, world, e2e_ms), 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": step.launches() * args.steps,
         "clocks": clocks.summary(windows),

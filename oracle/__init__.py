@@ -168,18 +168,21 @@ def amax(x_bits, orientation=ROWWISE, use_rht=False, sign_mask=0):
 
 
 def quantize(x_bits, orientation=ROWWISE, scaling=0, rounding=0, use_rht=False,
-             sign_mask=0, seed=0, stream_id=0, rows_subset=None):
+             sign_mask=0, seed=0, stream_id=0, rows_subset=None, amax_value=None):
     """Quantize one orientation of x (bf16 bit patterns, [rows][cols]).
 
     Returns dict(codes, scales, amax, s_enc, s_g, rows) where codes/scales
     cover the logical rows in ``rows`` (all logical rows by default; a
     contiguous range (lr0, lr1) when ``rows_subset`` is given).  The tensor
-    amax is always computed by the oracle over the full tensor.
+    amax is computed by the oracle over the full tensor unless ``amax_value``
+    gives it (a shard of a larger tensor quantized with the amax that the
+    shards agreed on).
     """
     x = _c(x_bits, np.uint16)
     rows, cols = x.shape
     lrows, lcols = (rows, cols) if orientation == ROWWISE else (cols, rows)
-    amax_value = amax(x, orientation, use_rht, sign_mask)
+    if amax_value is None:
+        amax_value = amax(x, orientation, use_rht, sign_mask)
     lr0, lr1 = (0, lrows) if rows_subset is None else rows_subset
     n = lr1 - lr0
     codes = np.zeros((n, lcols // 2), np.uint8)
