@@ -98,7 +98,22 @@ struct Params {
     int out_fp32;
     int vec_store;               // every output row starts on a 16-byte boundary
     int tma_store;               // BF16 output written through the D tensor map
+    int n_fast;                  // tile order: N tiles vary fastest (else M tiles)
 };
+
+// Output tile of a linear tile index.  Tiles that run at the same time share
+// the slow index, so its operand block is read from DRAM once and served from
+// L2 to every pair; the fast index cycles through the whole other operand,
+// which the host chooses to be the smaller one so that it stays in L2.
+__device__ __forceinline__ void tile_coords(uint32_t tile, const Params& p, uint32_t& mt, uint32_t& nt) {
+    if (p.n_fast) {
+        nt = tile % p.n_tiles;
+        mt = tile / p.n_tiles;
+    } else {
+        mt = tile % p.m_tiles;
+        nt = tile / p.m_tiles;
+    }
+}
 
 // Instruction descriptor for kind::mxf4nvf4: A and B E2M1 (format 1) at bits
 // 7 and 10, both K-major, N >> 3 at bit 17, UE4M3 scales (bit 23 = 0), M >> 7
@@ -188,7 +203,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0;
             const uint32_t leader_full0 = map_to_cta(smem_u32(full), 0);
             for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
-                const uint32_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+                uint32_t mt, nt;
+                tile_coords(tile, p, mt, nt);
                 for (uint32_t ks = 0; ks < p.kstages; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, kTimeoutNs)) {
                         record_timeout(abort_flag);
@@ -358,7 +374,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t row_local = q * 32 + lane;
         uint32_t tiles_done = 0;
         for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
-            const uint32_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+            uint32_t mt, nt;
+            tile_coords(tile, p, mt, nt);
             if (!warp_wait(acc_full, tiles_done & 1u, abort_flag)) break;
             tc_fence_after();
             const uint32_t row0 = mt * kPairM + rank * kCtaM;   // first row of this CTA's half
@@ -587,6 +604,7 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     p.ksteps = (uint32_t)((a.cols + 63) / 64);
     p.kstages = (p.ksteps + kKStepsPerStage - 1) / kKStepsPerStage;
     p.last_nk = p.ksteps - (p.kstages - 1) * kKStepsPerStage;
+    p.n_fast = b.rows <= a.rows ? 1 : 0;   // B is the smaller operand: keep it in L2
     p.sga = a.sg;
     p.sgb = b.sg;
     p.d = d;
