@@ -284,6 +284,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` (it resumes as
+// soon as the phase completes): a waiting thread then takes no issue slots
+// from the warps sharing its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `parity` to complete, giving up after timeout_ns.
 // Returns false on timeout; the caller records it.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -293,7 +308,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 256; ++i)
-            if (mbar_try_wait(a, parity)) return true;
+            if (mbar_try_wait_sleep(a, parity)) return true;
         if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
 }
@@ -372,14 +387,28 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
-// mbar_wait on a barrier given by its shared-memory address.
+// Non-blocking probe of a phase (mbarrier.test_wait).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait on a barrier given by its shared-memory address; the first probe
+// does not block (the common case on the MMA issuer's path: already complete).
 __device__ __forceinline__ bool mbar_wait_addr(uint32_t a, uint32_t parity, uint64_t timeout_ns) {
-    if (mbar_try_wait_cluster(a, parity)) return true;
+    if (mbar_test_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 256; ++i)
-            if (mbar_try_wait_cluster(a, parity)) return true;
+            if (mbar_try_wait_sleep(a, parity)) return true;
         if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
 }
@@ -392,7 +421,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 256; ++i)
-            if (mbar_try_wait_cluster(a, parity)) return true;
+            if (mbar_try_wait_sleep(a, parity)) return true;
         if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
 }

@@ -126,17 +126,13 @@ __device__ __forceinline__ void record_timeout(volatile uint32_t* abort_flag) {
     atomicOr(&g_gemm_status, kStatusTimeoutBit);
 }
 
-// Lane 0 waits and the warp shares the outcome, so a timeout never splits a
-// warp at a .sync.aligned instruction.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
-    uint32_t ok = 1;
-    if ((threadIdx.x & 31u) == 0) {
-        ok = mbar_wait_cluster(bar, parity, kTimeoutNs) ? 1u : 0u;
-        if (!ok) record_timeout(abort_flag);
-    }
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    __syncwarp();
-    return ok != 0;
+// Named barriers over the epilogue warps (id 1) and over the scale warps
+// (id 2); id 0 and the cluster barrier are used elsewhere.
+__device__ __forceinline__ void epilogue_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kNumEpiWarps) : "memory");
+}
+__device__ __forceinline__ void scale_bar() {
+    asm volatile("bar.sync 2, %0;" ::"n"(32 * kNumSfWarps) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -159,6 +155,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t* drain = acc_empty + 1;             // leader
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
+    volatile uint32_t* epi_ok = tmem_slot + 2;   // [2]: accumulator-ready verdicts, by tile parity
+    volatile uint32_t* sf_ok = tmem_slot + 4;    // [2]: scales-landed verdicts, by stage-count parity
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t rank = cluster_ctarank();
@@ -323,11 +321,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // and 8 columns of B scales (both 128-row halves of the N tile).
         const uint32_t q = warp & 3u;
         const uint32_t leader_full0 = map_to_cta(smem_u32(full), 0);
-        uint32_t stage = 0, phase = 0;
-        for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
+        uint32_t stage = 0, phase = 0, count = 0;
+        for (uint32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
             bool ok = true;
-            for (uint32_t ks = 0; ks < p.kstages; ++ks) {
-                if (!warp_wait(&sf_full[stage], phase, abort_flag)) {
+            for (uint32_t ks = 0; ks < p.kstages; ++ks, ++count) {
+                // one thread waits, the other scale warps sleep in a named
+                // barrier; all leave together
+                if (warp == (uint32_t)kFirstSfWarp && lane == 0) {
+                    bool landed = !*abort_flag && mbar_wait(&sf_full[stage], phase, kTimeoutNs);
+                    if (!landed && !*abort_flag) record_timeout(abort_flag);
+                    sf_ok[count & 1u] = landed ? 1u : 0u;
+                }
+                __syncwarp();
+                scale_bar();
+                if (!sf_ok[count & 1u]) {
                     ok = false;
                     break;
                 }
@@ -373,10 +380,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t leader_acc_empty = map_to_cta(smem_u32(acc_empty), 0);
         const uint32_t row_local = q * 32 + lane;
         uint32_t tiles_done = 0;
-        for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
+        for (uint32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
             uint32_t mt, nt;
             tile_coords(tile, p, mt, nt);
-            if (!warp_wait(acc_full, tiles_done & 1u, abort_flag)) break;
+            // One thread waits for the accumulator and the other epilogue
+            // warps sleep in a named barrier (waiting threads would take
+            // issue slots from the MMA issuer); all leave the loop together.
+            if (warp == (uint32_t)kFirstEpiWarp && lane == 0) {
+                bool ready = !*abort_flag && mbar_wait_cluster(acc_full, tiles_done & 1u, kTimeoutNs);
+                if (!ready && !*abort_flag) record_timeout(abort_flag);
+                epi_ok[tiles_done & 1u] = ready ? 1u : 0u;
+            }
+            __syncwarp();
+            epilogue_bar();
+            if (!epi_ok[tiles_done & 1u]) break;
             tc_fence_after();
             const uint32_t row0 = mt * kPairM + rank * kCtaM;   // first row of this CTA's half
             const uint32_t row = row0 + row_local;
