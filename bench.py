@@ -481,6 +481,66 @@ def reference_arm(args):
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def sweep_c5(args):
+    """Quantizer bandwidth sweep: 2^20..2^29 elements at row lengths 3072,
+    9216 and 8192, Student-t(3) values, three modes.  One JSON line per case;
+    L2 is flushed before every timed call (a write of twice its size)."""
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from fp4_gemm_nvfp4_gb300 import inputs, ops
+    peaks, peak_src = load_peaks()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    ws = ops.Workspace()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    mask = inputs.rht_sign_mask(5)
+    modes = [("1x16_rne", dict(rowwise=True)),
+             ("16x16_rne", dict(rowwise=True, colwise=True, two_d=True)),
+             ("rht_1x16_sr", dict(rowwise=True, sr=True, rht_mask=mask, seed=5))]
+    stream = torch.cuda.current_stream()
+    for rows, L in inputs.c5_sweep_sizes():
+        x = torch.empty((rows, L), dtype=torch.bfloat16, device="cuda")
+        for r0 in range(0, rows, 4096):   # t(3) = Z / sqrt(chi2_3 / 3), drawn in chunks
+            r1 = min(rows, r0 + 4096)
+            z = torch.randn((r1 - r0, L), generator=gen, device="cuda")
+            chi = torch.randn((3, r1 - r0, L), generator=gen, device="cuda").square_().mean(0).sqrt_()
+            x[r0:r1] = (z / chi * 1e-3).to(torch.bfloat16)
+        del z, chi
+        n = rows * L
+        for name, kw in modes:
+            row = ops.alloc_operand(rows, L)
+            col = ops.alloc_operand(L, rows) if kw.get("colwise") else None
+            run = lambda: ops.quantize(x, out_row=row, out_col=col, workspace=ws, **kw)
+            for _ in range(max(args.warmup, 5)):
+                run()
+            times = []
+            for _ in range(max(args.steps, 20)):
+                flush.fill_(1.0)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                run()
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.median(times)
+            outs = 1 + int(bool(kw.get("colwise")))
+            unique = n * (2 + outs * (0.5 + 1 / 16))
+            alg = quant_bytes(rows, L, kw)
+            print(json.dumps({"sweep": "c5", "mode": name, "rows": rows, "row_len": L, "elements": n,
+                              "ms": round(ms, 4), "unique_gbs": round(unique / (ms * 1e-3) / 1e9, 1),
+                              "algorithmic_gbs": round(alg / (ms * 1e-3) / 1e9, 1),
+                              "frac_of_hbm": round(alg / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                              "peak_source": f"{peak_src} hbm_gbs", "l2_flush": True,
+                              "status": ops.device_error()}), flush=True)
+            del row, col
+        del x
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -488,12 +548,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", choices=["c5"], default=None,
+                    help="instead of the layer step, run the quantizer bandwidth sweep (one JSON line per case)")
     ap.add_argument("--tokens", type=int, default=TOKENS,
                     help="tokens of the layer step (16384 is the benchmarked workload)")
     args = ap.parse_args()
     set_tokens(args.tokens)
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
+    if args.sweep == "c5":
+        sweep_c5(args)
+        return
     if args.impl == "reference":
         r = reference_arm(args)
         if r is not None:
