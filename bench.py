@@ -36,6 +36,28 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # ------------------------------------------------------------------ setup --
+# DRAM bytes per step of each kernel class on the 16384-token step, summed
+# over the class's launches in one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum, one pass per launch); the figure holds while the
+# kernel sources hash to the recorded value, and is reported as null otherwise.
+TRAFFIC = {
+    "quantize": ("8ab5d8de83007e0f", ("quantize.cu", "device_common.cuh"), 3772110336),
+    "gemm": ("82d7cdd9f968b37f", ("gemm.cu", "device_common.cuh"), 1236778496),
+}
+
+
+def measured_traffic(kind):
+    import hashlib
+    digest, files, nbytes = TRAFFIC[kind]
+    if TOKENS != 16384:
+        return None
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "fp4_gemm_nvfp4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return nbytes if h.hexdigest()[:16] == digest else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -417,12 +439,15 @@ def measure(args):
     if gemm_ms >= quant_ms:
         roof = {"kernel": "gemm_nvf4_kernel (the step's 6 GEMMs)", "bound": "tensor",
                 "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
-                "frac": round(gemm_tflops / fp4_peak, 4), "traffic": None,
+                "frac": round(gemm_tflops / fp4_peak, 4), "traffic": measured_traffic("gemm"),
+                "traffic_basis": "DRAM bytes per step over the class's launches (ncu)",
                 "peak_source": f"{peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal fp4/bf16)"}
     else:
         roof = {"kernel": "quantize (amax + encode passes of the step)", "bound": "hbm",
                 "achieved": round(quant_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "traffic": measured_traffic("quantize"),
+                "traffic_basis": "DRAM bytes per step over the class's launches (ncu)",
+                "algorithmic_bytes_per_step": round(qbytes),
                 "peak_source": f"{peak_src} hbm_gbs"}
 
     result = {
