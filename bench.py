@@ -90,27 +90,23 @@ def whole_job_tflops(flops_per_rank, world, ms):
 
 # The step: (name, input, kwargs for ops.quantize) and the six GEMMs.
 QUANTS = [
-    ("X.row", "X", dict(rowwise=True)),
-    ("X.col_rht", "X", dict(rowwise=False, colwise=True, rht_mask="mask")),
+    # X, H and the two output gradients give a row-wise operand (Fprop /
+    # Dgrad) and a col-wise RHT operand (Wgrad) from one call; weights 16x16.
+    ("X.pair", "X", dict(pair=True, rht_mask="mask")),
     ("W_up.2d", "W_up", dict(rowwise=True, colwise=True, two_d=True)),
-    ("H.row", "H", dict(rowwise=True)),
-    ("H.col_rht", "H", dict(rowwise=False, colwise=True, rht_mask="mask")),
+    ("H.pair", "H", dict(pair=True, rht_mask="mask")),
     ("W_down.2d", "W_down", dict(rowwise=True, colwise=True, two_d=True)),
-    ("dY_down.row_sr", "dY_down", dict(rowwise=True, sr=True, stream_id=1)),
-    ("dY_down.col_rht_sr", "dY_down", dict(rowwise=False, colwise=True, sr=True, rht_mask="mask",
-                                           stream_id=2)),
-    ("dY_up.row_sr", "dY_up", dict(rowwise=True, sr=True, stream_id=3)),
-    ("dY_up.col_rht_sr", "dY_up", dict(rowwise=False, colwise=True, sr=True, rht_mask="mask",
-                                       stream_id=4)),
+    ("dY_down.pair", "dY_down", dict(pair=True, rht_mask="mask", sr=True, stream_row=1, stream_col=2)),
+    ("dY_up.pair", "dY_up", dict(pair=True, rht_mask="mask", sr=True, stream_row=3, stream_col=4)),
 ]
 GEMMS = [
     # name, A (quant name, orientation), B (quant name, orientation)
-    ("fprop_up", ("X.row", "row"), ("W_up.2d", "row")),
-    ("fprop_down", ("H.row", "row"), ("W_down.2d", "row")),
-    ("dgrad_down", ("dY_down.row_sr", "row"), ("W_down.2d", "col")),
-    ("dgrad_up", ("dY_up.row_sr", "row"), ("W_up.2d", "col")),
-    ("wgrad_down", ("dY_down.col_rht_sr", "col"), ("H.col_rht", "col")),
-    ("wgrad_up", ("dY_up.col_rht_sr", "col"), ("X.col_rht", "col")),
+    ("fprop_up", ("X.pair", "row"), ("W_up.2d", "row")),
+    ("fprop_down", ("H.pair", "row"), ("W_down.2d", "row")),
+    ("dgrad_down", ("dY_down.pair", "row"), ("W_down.2d", "col")),
+    ("dgrad_up", ("dY_up.pair", "row"), ("W_up.2d", "col")),
+    ("wgrad_down", ("dY_down.pair", "col"), ("H.pair", "col")),
+    ("wgrad_up", ("dY_up.pair", "col"), ("X.pair", "col")),
 ]
 SHAPES = {}
 
@@ -137,7 +133,10 @@ def host_inputs(seed_base=4):
 
 def quant_launches(kw):
     """Kernels one quantize call launches: an amax pass and an encode pass per
-    RHT orientation, else one amax pass plus one encode pass."""
+    RHT orientation, else one amax pass plus one encode pass (row-wise plus
+    col-wise RHT of one input: one shared amax pass and two encode passes)."""
+    if kw.get("pair"):
+        return 3
     if kw.get("rht_mask") is not None:
         return 2 * (int(kw.get("rowwise", True)) + int(kw.get("colwise", False)))
     if kw.get("two_d"):
@@ -150,6 +149,8 @@ def quant_bytes(rows, cols, kw):
     input once, each encode pass reads it again and writes 0.5 B of codes and
     1/16 B of scales per element per emitted orientation."""
     n = rows * cols
+    if kw.get("pair"):                      # one amax pass, two encode passes, two orientations
+        return n * 2 * 3 + n * 2 * (0.5 + 1 / 16)
     outs = int(kw.get("rowwise", True)) + int(kw.get("colwise", False))
     if kw.get("rht_mask") is not None:      # one amax and one encode pass per orientation
         amax_passes, encode_reads = outs, outs
@@ -177,8 +178,9 @@ class Step:
             if kw.get("rht_mask") == "mask":
                 kw["rht_mask"] = mask
             rows, cols = SHAPES[src]
-            row = ops.alloc_operand(rows, cols) if kw.get("rowwise", True) else None
-            col = ops.alloc_operand(cols, rows) if kw.get("colwise", False) else None
+            pair = kw.get("pair", False)
+            row = ops.alloc_operand(rows, cols) if pair or kw.get("rowwise", True) else None
+            col = ops.alloc_operand(cols, rows) if pair or kw.get("colwise", False) else None
             self.q[name] = (row, col)
             self.kw[name] = kw
         self.out = {}
@@ -207,8 +209,14 @@ class Step:
             if only is not None and name != only:
                 continue
             row, col = self.q[name]
-            self.ops.quantize(self.x[src], out_row=row, out_col=col, seed=self.seed, workspace=self.ws,
-                              **self.kw[name])
+            kw = self.kw[name]
+            if kw.get("pair"):
+                self.ops.quantize_row_col_rht(self.x[src], kw["rht_mask"], sr=kw.get("sr", False), seed=self.seed,
+                                              stream_row=kw.get("stream_row", 0),
+                                              stream_col=kw.get("stream_col", 0), out_row=row, out_col=col,
+                                              workspace=self.ws)
+            else:
+                self.ops.quantize(self.x[src], out_row=row, out_col=col, seed=self.seed, workspace=self.ws, **kw)
 
     def run_gemms(self, only=None):
         for gname, (an, ao), (bn, bo) in GEMMS:
@@ -284,7 +292,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ CPU oracle --
-def _oracle_kw(kw, mask, seed):
+def _oracle_kw(kw, mask, seed, orient):
+    if kw.get("pair"):   # row-wise without RHT, col-wise with RHT, each on its own stream
+        rht = orient == "col"
+        return dict(scaling=0, rounding=1 if kw.get("sr") else 0, use_rht=rht, sign_mask=mask if rht else 0,
+                    seed=seed, stream_id=kw.get("stream_col" if rht else "stream_row", 0))
     return dict(scaling=1 if kw.get("two_d") else 0, rounding=1 if kw.get("sr") else 0,
                 use_rht=kw.get("rht_mask") is not None,
                 sign_mask=mask if kw.get("rht_mask") is not None else 0,
@@ -309,7 +321,7 @@ def cpu_baseline(host, mask, seed, rows_a=8, rows_b=1024):
             bits = host[src_of[qn]]
             lrows = bits.shape[0] if o == oracle.ROWWISE else bits.shape[1]
             ops_.append(oracle.quantize(bits, o, rows_subset=(0, min(nrows, lrows)),
-                                        **_oracle_kw(kw_of[qn], mask, seed)))
+                                        **_oracle_kw(kw_of[qn], mask, seed, orient)))
         a, b = ops_
         oracle.gemm_f64(a, b, with_abs=False)
         flops += 2 * a["codes"].shape[0] * b["codes"].shape[0] * a["codes"].shape[1] * 2

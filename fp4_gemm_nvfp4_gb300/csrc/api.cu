@@ -70,6 +70,19 @@ nvfp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+// Shape, pointer and workspace checks shared by the quantize entry points.
+nvfp4_status check_quantize_input(const void* x, int64_t rows, int64_t cols, int64_t ld_x) {
+    if (rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+    if (rows > 0 && cols > 0) {
+        if (!x) return NVFP4_ERR_INVALID_ARG;
+        if (ld_x < cols) return NVFP4_ERR_SHAPE;
+        if (ld_x % 8 != 0 || !aligned16(x)) return NVFP4_ERR_ALIGNMENT;
+    }
+    if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return NVFP4_ERR_UNSUPPORTED;
+    if (rows * (cols / 16) >= (int64_t(1) << 32) - 1) return NVFP4_ERR_UNSUPPORTED;
+    return NVFP4_OK;
+}
+
 nvfp4_status check_operand(const nvfp4_tensor* t) {
     if (!t || !t->codes || !t->scales || !t->global_scale) return NVFP4_ERR_INVALID_ARG;
     if (t->rows < 0 || t->cols < 0) return NVFP4_ERR_SHAPE;
@@ -114,6 +127,27 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64
                                 void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
     return quantize_impl(x, rows, cols, ld_x, scaling, rounding, seed, stream_id, orientations, out_row, out_col,
                          true, rht_sign_mask, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_quantize_row_col_rht(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                        nvfp4_rounding rounding, uint64_t seed, uint64_t stream_row,
+                                        uint64_t stream_col, uint16_t rht_sign_mask, const nvfp4_tensor* out_row,
+                                        const nvfp4_tensor* out_col, void* workspace, size_t workspace_bytes,
+                                        nvfp4_stream_t stream) {
+    if (rounding != NVFP4_ROUND_RNE && rounding != NVFP4_ROUND_SR) return NVFP4_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+    if (cols % 16 != 0 || rows % 16 != 0) return NVFP4_ERR_SHAPE;
+    nvfp4_status s;
+    if ((s = check_quantize_input(x, rows, cols, ld_x)) != NVFP4_OK) return s;
+    if ((s = check_target(out_row, rows, cols)) != NVFP4_OK) return s;
+    if ((s = check_target(out_col, cols, rows)) != NVFP4_OK) return s;
+    if (!workspace || workspace_bytes < nvfp4::kQuantizeWorkspaceBytes || !aligned16(workspace))
+        return NVFP4_ERR_WORKSPACE;
+    const QuantTarget tr = to_target(out_row), tc = to_target(out_col);
+    const cudaError_t e = nvfp4::launch_quantize_row_col_rht(
+        static_cast<const uint16_t*>(x), rows, cols, ld_x, rounding == NVFP4_ROUND_SR, rht_sign_mask, seed, stream_row,
+        stream_col, &tr, &tc, static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, int64_t ldd,

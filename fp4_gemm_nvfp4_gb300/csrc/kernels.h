@@ -30,6 +30,13 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
                             const QuantTarget* row, const QuantTarget* col, float* workspace,
                             cudaStream_t stream);
 
+// Row-wise 1x16 without RHT and col-wise 1x16 with RHT of one input, sharing
+// one amax pass (workspace as for launch_quantize).
+cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool sr,
+                                       uint32_t sign_mask, uint64_t seed, uint64_t stream_row, uint64_t stream_col,
+                                       const QuantTarget* row, const QuantTarget* col, float* workspace,
+                                       cudaStream_t stream);
+
 struct GemmOperand {
     const uint8_t* codes;
     int64_t ld_codes;

@@ -113,21 +113,24 @@ struct ColArgs {
     const float* partials_in;
     int n_partials;
     float* partials_out;
+    float* partials_out_plain;   // kAmax with kDual: max |x| before the RHT
     uint32_t mask;
     uint64_t seed, stream;
 };
 
 // One warp covers 16 rows x 64 columns (lane = 2 adjacent columns, so each
 // load instruction reads 128 contiguous bytes); a CTA of 8 warps covers a
-// 128 x 64 tile.  Each thread owns two column blocks of 16 rows.
-template <Pass P, bool kRHT, bool kSR>
+// 128 x 64 tile.  Each thread owns two column blocks of 16 rows.  kDual (amax
+// pass with RHT only) also takes the plain max |x| for a row-wise operand
+// quantized without RHT from the same input, so one read serves both.
+template <Pass P, bool kRHT, bool kSR, bool kDual = false>
 __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
     __shared__ float red[32];
     TensorScale ts{1.0f, 1.0f};
     if constexpr (P == Pass::kEncode) ts = load_tensor_scale(a.partials_in, a.n_partials, red, a.out, nullptr);
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
-    float local_max = 0.0f;
+    float local_max = 0.0f, plain_max = 0.0f;
     PhiloxKeys keys;
     if constexpr (kSR) keys = philox_keys(a.seed);
     for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -141,6 +144,10 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
             const uint32_t w = ld_nc_u32(src + (int64_t)i * a.ld_x);
             t0[i] = bf16lo(w);
             t1[i] = bf16hi(w);
+        }
+        if constexpr (kDual) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) plain_max = fmaxf(plain_max, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
         }
         if constexpr (kRHT) {
             rht16(t0, a.mask);
@@ -166,7 +173,13 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
             a.out.scales[scale_offset(c + 1, r0 / 16, a.out.s4)] = (uint8_t)sc1;
         }
     }
-    if constexpr (P == Pass::kAmax) block_max_store(local_max, a.partials_out, red);
+    if constexpr (P == Pass::kAmax) {
+        block_max_store(local_max, a.partials_out, red);
+        if constexpr (kDual) {
+            __syncthreads();
+            block_max_store(plain_max, a.partials_out_plain, red);
+        }
+    }
 }
 
 // -------------------------------------------------------------- 16x16 -----
@@ -396,6 +409,69 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
         else if (rht) launch(colwise_kernel<Pass::kEncode, true, false>);
         else if (sr) launch(colwise_kernel<Pass::kEncode, false, true>);
         else launch(colwise_kernel<Pass::kEncode, false, false>);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool sr,
+                                       uint32_t sign_mask, uint64_t seed, uint64_t stream_row, uint64_t stream_col,
+                                       const QuantTarget* row, const QuantTarget* col, float* workspace,
+                                       cudaStream_t st) {
+    cudaError_t err;
+    if ((err = clear_scale_padding(row, st)) != cudaSuccess) return err;
+    if ((err = clear_scale_padding(col, st)) != cudaSuccess) return err;
+    float* part_plain = workspace;
+    float* part_rht = workspace + kMaxAmaxPartials;
+
+    ColArgs ca{};
+    ca.x = x;
+    ca.ld_x = ld_x;
+    ca.rows = (uint32_t)rows;
+    ca.cols = (uint32_t)cols;
+    ca.tiles_r = (uint32_t)((rows + 127) / 128);
+    ca.tiles_c = (uint32_t)((cols + 63) / 64);
+    ca.mask = sign_mask;
+    ca.seed = seed;
+    const int64_t ntiles = (int64_t)ca.tiles_r * ca.tiles_c;
+
+    // one amax pass: the RHT amax for the col-wise operand and the plain
+    // amax for the row-wise one
+    int n = 0;
+    {
+        ColArgs c = ca;
+        c.partials_out = part_rht;
+        c.partials_out_plain = part_plain;
+        auto k = colwise_kernel<Pass::kAmax, true, false, true>;
+        n = persistent_grid(k, ntiles);
+        if (n > kMaxAmaxPartials) n = kMaxAmaxPartials;
+        k<<<n, kThreads, 0, st>>>(c);
+    }
+    {
+        RowArgs r{};
+        r.x = x;
+        r.ld_x = ld_x;
+        r.bpr = (uint32_t)(cols / 16);
+        r.total = (uint32_t)(rows * (cols / 16));
+        r.seed = seed;
+        r.stream = stream_row;
+        r.out = make_target(row);
+        r.partials_in = part_plain;
+        r.n_partials = n;
+        auto launch = [&](auto k) {
+            k<<<persistent_grid(k, ((int64_t)r.total + kThreads - 1) / kThreads), kThreads, 0, st>>>(r);
+        };
+        if (sr) launch(rowwise_kernel<Pass::kEncode, false, true>);
+        else launch(rowwise_kernel<Pass::kEncode, false, false>);
+    }
+    {
+        ColArgs c = ca;
+        c.stream = stream_col;
+        c.out = make_target(col);
+        c.partials_in = part_rht;
+        c.n_partials = n;
+        auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(c); };
+        if (sr) launch(colwise_kernel<Pass::kEncode, true, true>);
+        else launch(colwise_kernel<Pass::kEncode, true, false>);
     }
     return cudaGetLastError();
 }

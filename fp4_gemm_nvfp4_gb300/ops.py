@@ -111,6 +111,27 @@ def quantize(x: torch.Tensor, *, two_d: bool = False, sr: bool = False, rht_mask
     return (out_row if rowwise else None), (out_col if colwise else None)
 
 
+def quantize_row_col_rht(x: torch.Tensor, rht_mask: int, *, sr: bool = False, seed: int = 0,
+                         stream_row: int = 0, stream_col: int = 0, out_row: Optional[NVFP4Operand] = None,
+                         out_col: Optional[NVFP4Operand] = None, workspace: Optional[Workspace] = None,
+                         stream=None) -> Tuple[NVFP4Operand, NVFP4Operand]:
+    """Row-wise 1x16 (no RHT) and col-wise 1x16 with RHT of one bf16 matrix
+    (nvfp4_quantize_row_col_rht): the Fprop/Dgrad and the Wgrad operand."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    if out_row is None:
+        out_row = alloc_operand(rows, cols, x.device)
+    if out_col is None:
+        out_col = alloc_operand(cols, rows, x.device)
+    ws = workspace or _workspace(x.device)
+    status = capi.nvfp4_quantize_row_col_rht(x.data_ptr(), rows, cols, x.stride(0),
+                                             capi.NVFP4_ROUND_SR if sr else capi.NVFP4_ROUND_RNE, seed,
+                                             stream_row, stream_col, rht_mask, out_row.struct(), out_col.struct(),
+                                             ws.ptr, ws.nbytes, stream_handle(stream))
+    capi.check(status, "nvfp4_quantize_row_col_rht")
+    return out_row, out_col
+
+
 def gemm(a: NVFP4Operand, b: NVFP4Operand, out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None,
          stream=None) -> torch.Tensor:
     """D = A * B^T (nvfp4_gemm)."""

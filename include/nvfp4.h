@@ -182,6 +182,28 @@ NVFP4_API nvfp4_status nvfp4_rht_quantize(const void *x, int64_t rows, int64_t c
                                 void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_row_col_rht -- the two operands a linear layer takes from one
+ * activation or output gradient x [FS Sec. 2, Eq. (1)-(2); NV Sec. 4: the RHT
+ * goes to the Wgrad inputs only]: the ROWWISE 1x16 operand without the
+ * transform (Fprop / Dgrad) and the COLWISE 1x16 operand with the RHT along
+ * the rows of x (Wgrad).  Both outputs are required.  The results are
+ * bit-identical to
+ *   nvfp4_quantize(x, ..., NVFP4_SCALE_1X16, rounding, seed, stream_row,
+ *                  NVFP4_ROWWISE, out_row, NULL, ...)
+ *   nvfp4_rht_quantize(x, ..., NVFP4_SCALE_1X16, rounding, seed, stream_col,
+ *                      NVFP4_COLWISE, NULL, out_col, rht_sign_mask, ...)
+ * but one amax pass over x serves both (three reads of x instead of four).
+ * Requirements, workspace and errors as nvfp4_quantize with both
+ * orientations (rows % 16 == 0, cols % 16 == 0).
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_row_col_rht(const void *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                nvfp4_rounding rounding, uint64_t seed,
+                                uint64_t stream_row, uint64_t stream_col,
+                                uint16_t rht_sign_mask,
+                                const nvfp4_tensor *out_row, const nvfp4_tensor *out_col,
+                                void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
  * nvfp4_gemm -- D = A * B^T with NVFP4 operands and FP32 accumulation
  * [FS Sec. 2; NV Sec. 4: FP4 inputs, BF16 or FP32 outputs]:
  *   D[m][n] = s_gA * s_gB * sum_k e2m1(a_mk) s_A(m, k/16) e2m1(b_nk) s_B(n, k/16)

@@ -104,6 +104,28 @@ def test_quantize_validation(lib):
     assert quantize(rows=-1) == E.NVFP4_ERR_SHAPE
 
 
+def row_col_rht(**kw):
+    args = dict(x=A16 * 4, rows=64, cols=96, ld_x=96, rounding=0, seed=0, stream_row=0, stream_col=1,
+                rht_sign_mask=0x1234, out_row=tensor(64, 96), out_col=tensor(96, 64),
+                workspace=A16 * 5, workspace_bytes=capi.nvfp4_quantize_workspace_size(64, 96, 3), stream=None)
+    args.update(kw)
+    return capi.nvfp4_quantize_row_col_rht(*args.values())
+
+
+def test_row_col_rht_validation(lib):
+    E = capi
+    assert row_col_rht(rows=24, out_col=tensor(96, 24)) == E.NVFP4_ERR_SHAPE        # rows % 16 (col-wise)
+    assert row_col_rht(cols=40, ld_x=40) == E.NVFP4_ERR_SHAPE                        # cols % 16
+    assert row_col_rht(rounding=3) == E.NVFP4_ERR_INVALID_ARG
+    assert row_col_rht(out_row=None) == E.NVFP4_ERR_INVALID_ARG                      # both outputs required
+    assert row_col_rht(out_col=None) == E.NVFP4_ERR_INVALID_ARG
+    assert row_col_rht(out_col=tensor(64, 96)) == E.NVFP4_ERR_INVALID_ARG            # transposed shape expected
+    assert row_col_rht(x=A16 + 8) == E.NVFP4_ERR_ALIGNMENT
+    assert row_col_rht(x=None) == E.NVFP4_ERR_INVALID_ARG
+    assert row_col_rht(workspace_bytes=16) == E.NVFP4_ERR_WORKSPACE
+    assert row_col_rht(rows=-16) == E.NVFP4_ERR_SHAPE
+
+
 def test_rht_quantize_rejects_2d(lib):
     ws = capi.nvfp4_quantize_workspace_size(64, 64, 3)
     st = capi.nvfp4_rht_quantize(A16 * 4, 64, 64, 64, capi.NVFP4_SCALE_16X16, 0, 0, 0, 1,

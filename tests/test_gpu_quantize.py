@@ -155,3 +155,50 @@ def test_quantize_parity_full_size(name, rows, cols, kind, orientation, scaling,
         assert amax == ref["amax"] and sg == ref["s_g"]
         assert np.array_equal(codes[lr0:lr1], ref["codes"])
         assert np.array_equal(scales[lr0:lr1], ref["scales"])
+
+
+def _check_against_oracle(g, ref):
+    codes, scales, amax, sg, tiled = helpers.operand_to_host(g)
+    assert amax == ref["amax"] and sg == ref["s_g"]
+    assert np.array_equal(codes, ref["codes"]), "codes differ"
+    assert np.array_equal(scales, ref["scales"]), "scales differ"
+    assert not tiled[helpers.padding_mask(g.rows, g.cols)].any(), "scale padding not zero"
+
+
+@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("shape", [(16, 16), (272, 336), (128, 1024), (400, 192), (1040, 3072)])
+def test_row_col_rht_matches_oracle_and_separate_calls(shape, rounding):
+    """nvfp4_quantize_row_col_rht: row-wise without RHT and col-wise with RHT
+    from one shared amax pass, identical to the two separate calls."""
+    rows, cols = shape
+    bits = inputs.student_t(rows, cols, seed=rows + 3 * cols) if rounding else \
+        inputs.normal(rows, cols, seed=rows + 3 * cols, outlier_channels=2)
+    mask, seed = 0x6C3A, 987654321
+    x = helpers.to_device_bf16(bits)
+    row, col = ops.quantize_row_col_rht(x, mask, sr=rounding == 1, seed=seed, stream_row=3, stream_col=4)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    _check_against_oracle(row, oracle.quantize(bits, oracle.ROWWISE, rounding=rounding, seed=seed, stream_id=3))
+    _check_against_oracle(col, oracle.quantize(bits, oracle.COLWISE, rounding=rounding, use_rht=True,
+                                               sign_mask=mask, seed=seed, stream_id=4))
+    r2, _ = ops.quantize(x, sr=rounding == 1, seed=seed, stream_id=3)
+    _, c2 = ops.quantize(x, sr=rounding == 1, seed=seed, stream_id=4, rht_mask=mask, rowwise=False, colwise=True)
+    torch.cuda.synchronize()
+    for a, b in ((row, r2), (col, c2)):
+        ha, hb = helpers.operand_to_host(a), helpers.operand_to_host(b)
+        assert all(np.array_equal(u, v) for u, v in zip(ha, hb))
+
+
+def test_row_col_rht_zero_tensor():
+    """amax 0 gives s_g = 1 on both outputs; the col-wise codes are the
+    oracle's (the sign flips of D turn some zeros into -0, code 0x8)."""
+    bits = np.zeros((64, 128), np.uint16)
+    x = helpers.to_device_bf16(bits)
+    row, col = ops.quantize_row_col_rht(x, 0x1)
+    torch.cuda.synchronize()
+    _check_against_oracle(row, oracle.quantize(bits, oracle.ROWWISE))
+    _check_against_oracle(col, oracle.quantize(bits, oracle.COLWISE, use_rht=True, sign_mask=0x1))
+    for g in (row, col):
+        codes, scales, amax, sg, _ = helpers.operand_to_host(g)
+        assert amax == 0 and sg == 1 and not scales.any()
+    assert not helpers.operand_to_host(row)[0].any()
