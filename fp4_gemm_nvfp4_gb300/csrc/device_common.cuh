@@ -42,8 +42,9 @@ __device__ __forceinline__ float e4m3_decode(uint32_t c) {
 }
 
 // Eight values -> eight E2M1 codes (RNE, saturating), element 0 in the low
-// nibble.  The code's sign bit is forced to the value's sign bit so that
-// negative values rounding to zero encode as 0x8.
+// nibble.  The conversion keeps each value's sign bit also when the value
+// rounds to zero (-0, -0.1 and -1e-40 give 0x8 on sm_103a) and rounds ties
+// to the even code, which is the oracle's rule; the GPU tests check both.
 __device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
     uint32_t out;
     asm("{\n\t"
@@ -56,10 +57,7 @@ __device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
         "}"
         : "=r"(out)
         : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
-    uint32_t signs = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) signs |= (__float_as_uint(v[i]) >> 31) << (4 * i + 3);
-    return out | signs;
+    return out;
 }
 
 // Stochastic rounding of one value to an E2M1 code with 16 random bits
@@ -166,6 +164,23 @@ __device__ __forceinline__ uint32_t block_scale(float amax_b, float s_enc, float
     const uint32_t code = e4m3_encode_satfinite(sb32);
     const float sb = e4m3_decode(code);
     *r_b = (sb == 0.0f) ? 0.0f : __fdiv_rn(s_enc, sb);
+    return code;
+}
+
+// The multipliers r_b = S_enc / s_b of all 127 finite non-negative E4M3
+// codes, for a CTA to look up instead of dividing per block (the same single
+// division, done once per code).  Threads 0..127 fill it; callers sync.
+__device__ __forceinline__ void fill_rb_table(float* table, float s_enc) {
+    if (threadIdx.x < 128) {
+        const float sb = e4m3_decode(threadIdx.x);
+        table[threadIdx.x] = (threadIdx.x == 0 || threadIdx.x == 127) ? 0.0f : __fdiv_rn(s_enc, sb);
+    }
+}
+
+__device__ __forceinline__ uint32_t block_scale_tab(float amax_b, float s_enc, const float* table, float* r_b) {
+    const float sb32 = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
+    const uint32_t code = e4m3_encode_satfinite(sb32);
+    *r_b = table[code];
     return code;
 }
 

@@ -70,14 +70,22 @@ struct RowArgs {
 template <Pass P, bool kRHT, bool kSR>
 __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
     __shared__ float red[32];
+    __shared__ float rb_table[128];
     TensorScale ts{1.0f, 1.0f};
-    if constexpr (P == Pass::kEncode) ts = load_tensor_scale(a.partials_in, a.n_partials, red, a.out, nullptr);
+    if constexpr (P == Pass::kEncode) {
+        ts = load_tensor_scale(a.partials_in, a.n_partials, red, a.out, nullptr);
+        fill_rb_table(rb_table, ts.s_enc);
+        __syncthreads();
+    }
     float local_max = 0.0f;
     PhiloxKeys keys;
     if constexpr (kSR) keys = philox_keys(a.seed);
+    // block b = r * bpr + j; (r, j) advance by the grid stride without a division
     const uint32_t stride = gridDim.x * kThreads;
-    for (uint32_t b = blockIdx.x * kThreads + threadIdx.x; b < a.total; b += stride) {
-        const uint32_t r = b / a.bpr, j = b - r * a.bpr;
+    const uint32_t stride_r = stride / a.bpr, stride_j = stride - stride_r * a.bpr;
+    uint32_t b = blockIdx.x * kThreads + threadIdx.x;
+    uint32_t r = b / a.bpr, j = b - r * a.bpr;
+    for (; b < a.total; b += stride) {
         const uint16_t* src = a.x + (int64_t)r * a.ld_x + (int64_t)j * 16;
         const uint4 u0 = ld_nc_v4(src), u1 = ld_nc_v4(src + 8);
         float t[16] = {bf16lo(u0.x), bf16hi(u0.x), bf16lo(u0.y), bf16hi(u0.y), bf16lo(u0.z), bf16hi(u0.z),
@@ -91,11 +99,17 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
             local_max = fmaxf(local_max, amax_b);
         } else {
             float r_b;
-            const uint32_t sc = block_scale(amax_b, ts.s_enc, &r_b);
+            const uint32_t sc = block_scale_tab(amax_b, ts.s_enc, rb_table, &r_b);
             const uint64_t idx = (uint64_t)r * ((uint64_t)a.bpr * 16u) + (uint64_t)j * 16u;
             const uint2 q = encode16<kSR>(t, r_b, keys, a.stream, idx);
             *reinterpret_cast<uint2*>(a.out.codes + (int64_t)r * a.out.ld_codes + (int64_t)j * 8) = q;
             a.out.scales[scale_offset(r, j, a.out.s4)] = (uint8_t)sc;
+        }
+        j += stride_j;
+        r += stride_r;
+        if (j >= a.bpr) {
+            j -= a.bpr;
+            ++r;
         }
     }
     if constexpr (P == Pass::kAmax) block_max_store(local_max, a.partials_out, red);
@@ -126,8 +140,13 @@ struct ColArgs {
 template <Pass P, bool kRHT, bool kSR, bool kDual = false>
 __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
     __shared__ float red[32];
+    __shared__ float rb_table[128];
     TensorScale ts{1.0f, 1.0f};
-    if constexpr (P == Pass::kEncode) ts = load_tensor_scale(a.partials_in, a.n_partials, red, a.out, nullptr);
+    if constexpr (P == Pass::kEncode) {
+        ts = load_tensor_scale(a.partials_in, a.n_partials, red, a.out, nullptr);
+        fill_rb_table(rb_table, ts.s_enc);
+        __syncthreads();
+    }
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
     float local_max = 0.0f, plain_max = 0.0f;
@@ -163,8 +182,8 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
             local_max = fmaxf(local_max, fmaxf(m0, m1));
         } else {
             float rb0, rb1;
-            const uint32_t sc0 = block_scale(m0, ts.s_enc, &rb0);
-            const uint32_t sc1 = block_scale(m1, ts.s_enc, &rb1);
+            const uint32_t sc0 = block_scale_tab(m0, ts.s_enc, rb_table, &rb0);
+            const uint32_t sc1 = block_scale_tab(m1, ts.s_enc, rb_table, &rb1);
             const uint2 q0 = encode16<kSR>(t0, rb0, keys, a.stream, (uint64_t)c * a.rows + r0);
             const uint2 q1 = encode16<kSR>(t1, rb1, keys, a.stream, (uint64_t)(c + 1) * a.rows + r0);
             *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
@@ -194,9 +213,12 @@ __device__ __forceinline__ uint32_t nibble(uint2 q, int i) {
 template <bool kSR>
 __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
     __shared__ float red[32];
+    __shared__ float rb_table[128];
     const TensorScale ts =
         load_tensor_scale(a.partials_in, a.n_partials, red, a.emit_col ? a.out : a.out2,
                           (a.emit_col && a.emit_row) ? &a.out2 : nullptr);
+    fill_rb_table(rb_table, ts.s_enc);
+    __syncthreads();
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
     PhiloxKeys keys;
@@ -223,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
         if (!valid) continue;
         float r_b;
-        const uint32_t sc = block_scale(m, ts.s_enc, &r_b);
+        const uint32_t sc = block_scale_tab(m, ts.s_enc, rb_table, &r_b);
         uint2 q0, q1;
         if constexpr (!kSR) {
             float v0[16], v1[16];
