@@ -134,9 +134,9 @@ def host_inputs(seed_base=4):
 def quant_launches(kw):
     """Kernels one quantize call launches: an amax pass and an encode pass per
     RHT orientation, else one amax pass plus one encode pass (row-wise plus
-    col-wise RHT of one input: one shared amax pass and two encode passes)."""
+    col-wise RHT of one input: one shared amax pass and one encode pass)."""
     if kw.get("pair"):
-        return 3
+        return 2
     if kw.get("rht_mask") is not None:
         return 2 * (int(kw.get("rowwise", True)) + int(kw.get("colwise", False)))
     if kw.get("two_d"):
@@ -149,8 +149,8 @@ def quant_bytes(rows, cols, kw):
     input once, each encode pass reads it again and writes 0.5 B of codes and
     1/16 B of scales per element per emitted orientation."""
     n = rows * cols
-    if kw.get("pair"):                      # one amax pass, two encode passes, two orientations
-        return n * 2 * 3 + n * 2 * (0.5 + 1 / 16)
+    if kw.get("pair"):                      # one amax pass, one encode pass emitting both orientations
+        return n * 2 * 2 + n * 2 * (0.5 + 1 / 16)
     outs = int(kw.get("rowwise", True)) + int(kw.get("colwise", False))
     if kw.get("rht_mask") is not None:      # one amax and one encode pass per orientation
         amax_passes, encode_reads = outs, outs

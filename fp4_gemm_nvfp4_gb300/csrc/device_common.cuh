@@ -177,6 +177,15 @@ __device__ __forceinline__ void fill_rb_table(float* table, float s_enc) {
     }
 }
 
+// fill_rb_table by threads [first, first + 128).
+__device__ __forceinline__ void fill_rb_table_at(float* table, float s_enc, uint32_t first) {
+    const uint32_t c = threadIdx.x - first;
+    if (threadIdx.x >= first && c < 128) {
+        const float sb = e4m3_decode(c);
+        table[c] = (c == 0 || c == 127) ? 0.0f : __fdiv_rn(s_enc, sb);
+    }
+}
+
 __device__ __forceinline__ uint32_t block_scale_tab(float amax_b, float s_enc, const float* table, float* r_b) {
     const float sb32 = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
     const uint32_t code = e4m3_encode_satfinite(sb32);

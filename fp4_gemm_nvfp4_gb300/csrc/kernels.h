@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace nvfp4 {
@@ -54,6 +55,12 @@ cudaError_t gemm_read_and_clear_status(unsigned int* status);
 cudaError_t launch_dequantize(const uint8_t* codes, int64_t ld_codes, const uint8_t* scales, const float* sg,
                               int64_t rows, int64_t cols, void* y, int64_t ldy, bool out_fp32,
                               cudaStream_t stream);
+
+// cuTensorMapEncodeTiled from the driver (null if unavailable).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

@@ -294,6 +294,162 @@ __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
     }
 }
 
+// ------------------------------------------- row + col-RHT pair encode -----
+// The encode pass of nvfp4_quantize_row_col_rht in one read of x: each warp
+// takes 16-row x 64-column slices of x by TMA (128-byte swizzle, two slots per
+// warp so the next slice is in flight while this one is encoded) and encodes
+// every element twice from shared memory:
+//   col-wise with RHT: lane = 2 columns x 16 rows (as colwise_kernel);
+//   row-wise without RHT: lane = 2 row blocks of 16 (row = lane / 2), 16
+//   bytes of codes and 2 scale bytes per lane.
+struct PairArgs {
+    uint32_t rows, cols;
+    uint32_t tiles_r, tiles_c;   // 128-row x 64-column CTA tiles
+    Target row, col;
+    const float* part_plain;
+    const float* part_rht;
+    int n_partials;
+    uint32_t mask;
+    uint64_t seed, stream_row, stream_col;
+};
+
+constexpr int kPairSlots = 2;
+constexpr uint32_t kSliceBytes = 16 * 128;   // 16 rows x 64 bf16
+
+template <bool kSR>
+__global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                                                               const PairArgs a) {
+    __shared__ float red[32];
+    __shared__ float rb_row[128], rb_col[128];
+    __shared__ __align__(1024) uint8_t ring[kThreads / 32][kPairSlots][kSliceBytes];
+    __shared__ uint64_t full[kThreads / 32][kPairSlots];
+    const TensorScale ts_row = load_tensor_scale(a.part_plain, a.n_partials, red, a.row, nullptr);
+    const TensorScale ts_col = load_tensor_scale(a.part_rht, a.n_partials, red, a.col, nullptr);
+    fill_rb_table_at(rb_row, ts_row.s_enc, 0);
+    fill_rb_table_at(rb_col, ts_col.s_enc, 128);
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        for (int sl = 0; sl < kPairSlots; ++sl) mbar_init(&full[warp][sl], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    PhiloxKeys keys;
+    if constexpr (kSR) keys = philox_keys(a.seed);
+    const uint32_t ntiles = a.tiles_r * a.tiles_c;
+    // this warp's slice of the CTA's k-th tile, if it holds rows
+    auto slice_of = [&](uint32_t k, uint32_t& r0, uint32_t& c0) -> bool {
+        const uint32_t tile = blockIdx.x + k * gridDim.x;
+        if (tile >= ntiles) return false;
+        r0 = (tile % a.tiles_r) * 128u + warp * 16u;
+        c0 = (tile / a.tiles_r) * 64u;
+        return r0 < a.rows;
+    };
+    auto issue = [&](uint32_t k) {
+        uint32_t r0, c0;
+        if (lane == 0 && slice_of(k, r0, c0)) {
+            uint64_t* bar = &full[warp][k & 1u];
+            mbar_arrive_expect_tx(bar, kSliceBytes);
+            tma_load_2d(ring[warp][k & 1u], &tmap_x, bar, (int32_t)c0, (int32_t)r0);
+        }
+    };
+    const uint32_t kcount = (ntiles > blockIdx.x) ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
+    uint32_t parity = 0;   // bit s: parity of the next wait on slot s
+    issue(0);
+    for (uint32_t k = 0; k < kcount; ++k) {
+        __syncwarp();   // every lane is done with the slot the next copy fills
+        issue(k + 1);
+        uint32_t r0, c0;
+        if (!slice_of(k, r0, c0)) continue;
+        const uint32_t sl = k & 1u;
+        if (!mbar_wait(&full[warp][sl], (parity >> sl) & 1u, 2000000000ull)) {
+            // a copy that never landed: let the next one (issued above) land
+            // before this CTA can exit, then stop
+            uint32_t r1, c1;
+            if (slice_of(k + 1, r1, c1))
+                (void)mbar_wait(&full[warp][sl ^ 1u], (parity >> (sl ^ 1u)) & 1u, 2000000000ull);
+            break;
+        }
+        parity ^= 1u << sl;
+        const uint8_t* src = ring[warp][sl];
+
+        // ---- col-wise with RHT: lane = columns c0 + 2 lane, c0 + 2 lane + 1
+        {
+            const uint32_t c = c0 + lane * 2u;
+            float t0[16], t1[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t off = (uint32_t)i * 128u + (((lane >> 2) ^ (uint32_t)(i & 7)) << 4) + (lane & 3u) * 4u;
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(src + off);
+                t0[i] = bf16lo(w);
+                t1[i] = bf16hi(w);
+            }
+            if (c < a.cols) {
+                rht16(t0, a.mask);
+                rht16(t1, a.mask);
+                float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    m0 = fmaxf(m0, fabsf(t0[i]));
+                    m1 = fmaxf(m1, fabsf(t1[i]));
+                }
+                float rb0, rb1;
+                const uint32_t sc0 = block_scale_tab(m0, ts_col.s_enc, rb_col, &rb0);
+                const uint32_t sc1 = block_scale_tab(m1, ts_col.s_enc, rb_col, &rb1);
+                const uint2 q0 = encode16<kSR>(t0, rb0, keys, a.stream_col, (uint64_t)c * a.rows + r0);
+                const uint2 q1 = encode16<kSR>(t1, rb1, keys, a.stream_col, (uint64_t)(c + 1) * a.rows + r0);
+                *reinterpret_cast<uint2*>(a.col.codes + (int64_t)c * a.col.ld_codes + r0 / 2) = q0;
+                *reinterpret_cast<uint2*>(a.col.codes + (int64_t)(c + 1) * a.col.ld_codes + r0 / 2) = q1;
+                a.col.scales[scale_offset(c, r0 / 16, a.col.s4)] = (uint8_t)sc0;
+                a.col.scales[scale_offset(c + 1, r0 / 16, a.col.s4)] = (uint8_t)sc1;
+            }
+        }
+        // ---- row-wise without RHT: lane = row r0 + lane / 2, 32 columns
+        {
+            const uint32_t i = lane >> 1, h = lane & 1u;
+            const uint32_t r = r0 + i, cb = c0 + 32u * h;
+            if (cb < a.cols) {
+                float v[32];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t off = i * 128u + (((4u * h + (uint32_t)kk) ^ (i & 7u)) << 4);
+                    const uint4 u = *reinterpret_cast<const uint4*>(src + off);
+                    v[8 * kk + 0] = bf16lo(u.x);
+                    v[8 * kk + 1] = bf16hi(u.x);
+                    v[8 * kk + 2] = bf16lo(u.y);
+                    v[8 * kk + 3] = bf16hi(u.y);
+                    v[8 * kk + 4] = bf16lo(u.z);
+                    v[8 * kk + 5] = bf16hi(u.z);
+                    v[8 * kk + 6] = bf16lo(u.w);
+                    v[8 * kk + 7] = bf16hi(u.w);
+                }
+                const bool two = cb + 16u < a.cols;
+                uint2 q[2];
+                uint32_t sc[2];
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    float m = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[16 * jj + e]));
+                    float rb;
+                    sc[jj] = block_scale_tab(m, ts_row.s_enc, rb_row, &rb);
+                    q[jj] = encode16<kSR>(v + 16 * jj, rb, keys, a.stream_row,
+                                          (uint64_t)r * a.cols + cb + 16u * (uint32_t)jj);
+                }
+                uint8_t* dst = a.row.codes + (int64_t)r * a.row.ld_codes + cb / 2;
+                const uint32_t j0 = cb / 16u;
+                if (two) {
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
+                    *reinterpret_cast<uint16_t*>(a.row.scales + scale_offset(r, j0, a.row.s4)) =
+                        (uint16_t)(sc[0] | (sc[1] << 8));
+                } else {
+                    *reinterpret_cast<uint2*>(dst) = q[0];
+                    a.row.scales[scale_offset(r, j0, a.row.s4)] = (uint8_t)sc[0];
+                }
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------- launch -----
 template <typename K>
 int persistent_grid(K kernel, int64_t work) {
@@ -468,33 +624,35 @@ cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t
         if (n > kMaxAmaxPartials) n = kMaxAmaxPartials;
         k<<<n, kThreads, 0, st>>>(c);
     }
-    {
-        RowArgs r{};
-        r.x = x;
-        r.ld_x = ld_x;
-        r.bpr = (uint32_t)(cols / 16);
-        r.total = (uint32_t)(rows * (cols / 16));
-        r.seed = seed;
-        r.stream = stream_row;
-        r.out = make_target(row);
-        r.partials_in = part_plain;
-        r.n_partials = n;
-        auto launch = [&](auto k) {
-            k<<<persistent_grid(k, ((int64_t)r.total + kThreads - 1) / kThreads), kThreads, 0, st>>>(r);
-        };
-        if (sr) launch(rowwise_kernel<Pass::kEncode, false, true>);
-        else launch(rowwise_kernel<Pass::kEncode, false, false>);
-    }
-    {
-        ColArgs c = ca;
-        c.stream = stream_col;
-        c.out = make_target(col);
-        c.partials_in = part_rht;
-        c.n_partials = n;
-        auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(c); };
-        if (sr) launch(colwise_kernel<Pass::kEncode, true, true>);
-        else launch(colwise_kernel<Pass::kEncode, true, false>);
-    }
+    // one encode pass for both orientations, x staged through TMA
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    CUtensorMap tmap;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld_x * 2u};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t elem[2] = {1, 1};
+    if (fn(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, elem,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    PairArgs pa{};
+    pa.rows = (uint32_t)rows;
+    pa.cols = (uint32_t)cols;
+    pa.tiles_r = ca.tiles_r;
+    pa.tiles_c = ca.tiles_c;
+    pa.row = make_target(row);
+    pa.col = make_target(col);
+    pa.part_plain = part_plain;
+    pa.part_rht = part_rht;
+    pa.n_partials = n;
+    pa.mask = sign_mask;
+    pa.seed = seed;
+    pa.stream_row = stream_row;
+    pa.stream_col = stream_col;
+    auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(tmap, pa); };
+    if (sr) launch(pair_encode_kernel<true>);
+    else launch(pair_encode_kernel<false>);
     return cudaGetLastError();
 }
 

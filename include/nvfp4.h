@@ -192,7 +192,8 @@ NVFP4_API nvfp4_status nvfp4_rht_quantize(const void *x, int64_t rows, int64_t c
  *                  NVFP4_ROWWISE, out_row, NULL, ...)
  *   nvfp4_rht_quantize(x, ..., NVFP4_SCALE_1X16, rounding, seed, stream_col,
  *                      NVFP4_COLWISE, NULL, out_col, rht_sign_mask, ...)
- * but one amax pass over x serves both (three reads of x instead of four).
+ * but one amax pass and one encode pass over x serve both (two reads of x
+ * instead of four).
  * Requirements, workspace and errors as nvfp4_quantize with both
  * orientations (rows % 16 == 0, cols % 16 == 0).
  */
