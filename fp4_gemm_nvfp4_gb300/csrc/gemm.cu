@@ -97,7 +97,7 @@ struct Params {
     int64_t ldd;
     int out_fp32;
     int vec_store;               // every output row starts on a 16-byte boundary
-    int tma_store;               // BF16 output written through the D tensor map
+    int tma_store;               // output written through the D tensor map (BF16 or FP32)
     int n_fast;                  // tile order: N tiles vary fastest (else M tiles)
 };
 
@@ -399,7 +399,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t row = row0 + row_local;
             const uint32_t nbase = nt * kBN + half * 128;
             const uint32_t taddr = tmem + ((q * 32u) << 16) + kAccCol + half * 128;
-            if (p.tma_store) {
+            if (p.tma_store && !p.out_fp32) {
                 // Two rounds of 64 columns through this warp's 4 KiB slice of
                 // the staging buffer (32 rows x 128 bytes, 128-byte swizzle).
                 // The accumulator is handed back as soon as the second
@@ -434,6 +434,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         const uint32_t y = row0 + q * 32, x = nbase + r * 64;
+                        if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (p.tma_store && p.out_fp32) {
+                // FP32: four rounds of 32 columns through this warp's 4 KiB
+                // slice (32 rows x 128 bytes, 128-byte swizzle); the
+                // accumulator goes back after the last round's load.
+                uint8_t* slice = staging + (half * 4 + q) * 4096u;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + c * 32, v);
+                    tmem_ld_wait();
+                    if (c == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
+                    }
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<uint4*>(slice + lane * 128u + ((uint32_t)i ^ (lane & 7u)) * 16u) =
+                            make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(v[4 * i]), alpha)),
+                                       __float_as_uint(__fmul_rn(__uint_as_float(v[4 * i + 1]), alpha)),
+                                       __float_as_uint(__fmul_rn(__uint_as_float(v[4 * i + 2]), alpha)),
+                                       __float_as_uint(__fmul_rn(__uint_as_float(v[4 * i + 3]), alpha)));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t y = row0 + q * 32, x = nbase + (uint32_t)c * 32u;
                         if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
                         bulk_commit_group();
                     }
@@ -528,15 +560,17 @@ bool make_scale_map(CUtensorMap* map, const GemmOperand& op, uint32_t box_row_ti
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// BF16 output map: 64-column x 32-row boxes, 128-byte swizzle.
-bool make_output_map(CUtensorMap* map, void* d, int64_t M, int64_t N, int64_t ldd) {
+// Output map: 128-byte x 32-row boxes (64 BF16 or 32 FP32 columns), 128-byte
+// swizzle.
+bool make_output_map(CUtensorMap* map, void* d, int64_t M, int64_t N, int64_t ldd, bool fp32) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)(ldd * 2)};
-    const cuuint32_t box[2] = {64, 32};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ldd * (fp32 ? 4 : 2))};
+    const cuuint32_t box[2] = {fp32 ? 32u : 64u, 32};
     const cuuint32_t elem[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    return fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box,
+              elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -625,7 +659,7 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     p.out_fp32 = out_fp32 ? 1 : 0;
     const int64_t esz = out_fp32 ? 4 : 2;
     p.vec_store = ((reinterpret_cast<uintptr_t>(d) & 15u) == 0 && (ldd * esz) % 16 == 0) ? 1 : 0;
-    p.tma_store = (!out_fp32 && p.vec_store && make_output_map(&md, d, a.rows, b.rows, ldd)) ? 1 : 0;
+    p.tma_store = (p.vec_store && make_output_map(&md, d, a.rows, b.rows, ldd, out_fp32)) ? 1 : 0;
     if (!p.tma_store) md = ma;   // unused by the kernel; any valid map
     const uint32_t tiles = p.m_tiles * p.n_tiles;
     const uint32_t pairs = (uint32_t)max_active_pairs();
