@@ -450,6 +450,142 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     }
 }
 
+// ------------------------------------------------ 16x16, RNE, via TMA -----
+// The RNE 16x16 encode from TMA-staged 16-row x 64-column slices (as
+// pair_kernel): the col-wise codes come from the col layout (lane = 2 columns
+// x 16 rows, tile amax by three shuffles), the row-wise codes from the row
+// layout (lane = half a row), each with 16-byte code stores; both encode
+// every element with the tile's r_b, so the two are exact transposes.
+struct Tile2dArgs {
+    uint32_t rows, cols;
+    uint32_t tiles_r, tiles_c;   // 128-row x 64-column CTA tiles
+    Target row, col;
+    bool emit_row, emit_col;
+    const float* partials;
+    int n_partials;
+};
+
+__global__ void __launch_bounds__(kThreads) tile2d_rne_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                                                              const Tile2dArgs a) {
+    __shared__ float red[32];
+    __shared__ float rb_tab[128];
+    __shared__ __align__(1024) uint8_t ring[kThreads / 32][kPairSlots][kSliceBytes];
+    __shared__ uint64_t full[kThreads / 32][kPairSlots];
+    const TensorScale ts = load_tensor_scale(a.partials, a.n_partials, red, a.emit_col ? a.col : a.row,
+                                             (a.emit_col && a.emit_row) ? &a.row : nullptr);
+    fill_rb_table(rb_tab, ts.s_enc);
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        for (int sl = 0; sl < kPairSlots; ++sl) mbar_init(&full[warp][sl], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const uint32_t ntiles = a.tiles_r * a.tiles_c;
+    auto slice_of = [&](uint32_t k, uint32_t& r0, uint32_t& c0) -> bool {
+        const uint32_t tile = blockIdx.x + k * gridDim.x;
+        if (tile >= ntiles) return false;
+        r0 = (tile % a.tiles_r) * 128u + warp * 16u;
+        c0 = (tile / a.tiles_r) * 64u;
+        return r0 < a.rows;
+    };
+    auto issue = [&](uint32_t k) {
+        uint32_t r0, c0;
+        if (lane == 0 && slice_of(k, r0, c0)) {
+            uint64_t* bar = &full[warp][k & 1u];
+            mbar_arrive_expect_tx(bar, kSliceBytes);
+            tma_load_2d(ring[warp][k & 1u], &tmap_x, bar, (int32_t)c0, (int32_t)r0);
+        }
+    };
+    const uint32_t kcount = (ntiles > blockIdx.x) ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
+    uint32_t parity = 0;
+    issue(0);
+    for (uint32_t k = 0; k < kcount; ++k) {
+        __syncwarp();
+        issue(k + 1);
+        uint32_t r0, c0;
+        if (!slice_of(k, r0, c0)) continue;
+        const uint32_t sl = k & 1u;
+        if (!mbar_wait(&full[warp][sl], (parity >> sl) & 1u, 2000000000ull)) {
+            uint32_t r1, c1;
+            if (slice_of(k + 1, r1, c1))
+                (void)mbar_wait(&full[warp][sl ^ 1u], (parity >> (sl ^ 1u)) & 1u, 2000000000ull);
+            break;
+        }
+        parity ^= 1u << sl;
+        const uint8_t* src = ring[warp][sl];
+        // col layout: tile amax and scale; col-wise codes
+        const uint32_t c = c0 + lane * 2u;
+        float t0[16], t1[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(
+                src + (uint32_t)i * 128u + (((lane >> 2) ^ (uint32_t)(i & 7)) << 4) + (lane & 3u) * 4u);
+            t0[i] = bf16lo(w);
+            t1[i] = bf16hi(w);
+        }
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        float rb;
+        const uint32_t sc = block_scale_tab(m, ts.s_enc, rb_tab, &rb);
+        if (a.emit_col && c < a.cols) {
+            float v0[16], v1[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                v0[i] = __fmul_rn(t0[i], rb);
+                v1[i] = __fmul_rn(t1[i], rb);
+            }
+            const uint2 q0 = make_uint2(e2m1_rne_x8(v0), e2m1_rne_x8(v0 + 8));
+            const uint2 q1 = make_uint2(e2m1_rne_x8(v1), e2m1_rne_x8(v1 + 8));
+            *reinterpret_cast<uint2*>(a.col.codes + (int64_t)c * a.col.ld_codes + r0 / 2) = q0;
+            *reinterpret_cast<uint2*>(a.col.codes + (int64_t)(c + 1) * a.col.ld_codes + r0 / 2) = q1;
+            a.col.scales[scale_offset(c, r0 / 16, a.col.s4)] = (uint8_t)sc;
+            a.col.scales[scale_offset(c + 1, r0 / 16, a.col.s4)] = (uint8_t)sc;
+        }
+        if (a.emit_row) {
+            // row layout: row r0 + lane / 2, columns c0 + 32 (lane & 1) .. + 31
+            // = tiles 2h and 2h+1 of the slice, whose scales lanes 16h and
+            // 16h + 8 hold
+            const uint32_t i = lane >> 1, h = lane & 1u;
+            const uint32_t r = r0 + i, cb = c0 + 32u * h;
+            const float rbt0 = __shfl_sync(0xFFFFFFFFu, rb, 16 * h), rbt1 = __shfl_sync(0xFFFFFFFFu, rb, 16 * h + 8);
+            const uint32_t sct0 = __shfl_sync(0xFFFFFFFFu, sc, 16 * h),
+                           sct1 = __shfl_sync(0xFFFFFFFFu, sc, 16 * h + 8);
+            if (cb < a.cols) {
+                float v[32];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t off = i * 128u + (((4u * h + (uint32_t)kk) ^ (i & 7u)) << 4);
+                    const uint4 u = *reinterpret_cast<const uint4*>(src + off);
+                    const float rbk = kk < 2 ? rbt0 : rbt1;
+                    v[8 * kk + 0] = __fmul_rn(bf16lo(u.x), rbk);
+                    v[8 * kk + 1] = __fmul_rn(bf16hi(u.x), rbk);
+                    v[8 * kk + 2] = __fmul_rn(bf16lo(u.y), rbk);
+                    v[8 * kk + 3] = __fmul_rn(bf16hi(u.y), rbk);
+                    v[8 * kk + 4] = __fmul_rn(bf16lo(u.z), rbk);
+                    v[8 * kk + 5] = __fmul_rn(bf16hi(u.z), rbk);
+                    v[8 * kk + 6] = __fmul_rn(bf16lo(u.w), rbk);
+                    v[8 * kk + 7] = __fmul_rn(bf16hi(u.w), rbk);
+                }
+                uint8_t* dst = a.row.codes + (int64_t)r * a.row.ld_codes + cb / 2;
+                const uint32_t j0 = cb / 16u;
+                if (cb + 16u < a.cols) {
+                    *reinterpret_cast<uint4*>(dst) =
+                        make_uint4(e2m1_rne_x8(v), e2m1_rne_x8(v + 8), e2m1_rne_x8(v + 16), e2m1_rne_x8(v + 24));
+                    *reinterpret_cast<uint16_t*>(a.row.scales + scale_offset(r, j0, a.row.s4)) =
+                        (uint16_t)(sct0 | (sct1 << 8));
+                } else {
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(e2m1_rne_x8(v), e2m1_rne_x8(v + 8));
+                    a.row.scales[scale_offset(r, j0, a.row.s4)] = (uint8_t)sct0;
+                }
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------- launch -----
 template <typename K>
 int persistent_grid(K kernel, int64_t work) {
@@ -540,10 +676,31 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
         if (sr) {
             auto k = tile2d_kernel<true>;
             k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(ca);
-        } else {
-            auto k = tile2d_kernel<false>;
-            k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(ca);
+            return cudaGetLastError();
         }
+        EncodeTiledFn fn = encode_fn();
+        CUtensorMap tmap;
+        const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)ld_x * 2u};
+        const cuuint32_t box[2] = {64, 16};
+        const cuuint32_t elem[2] = {1, 1};
+        if (!fn || fn(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, elem,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        Tile2dArgs ta{};
+        ta.rows = (uint32_t)rows;
+        ta.cols = (uint32_t)cols;
+        ta.tiles_r = ca.tiles_r;
+        ta.tiles_c = ca.tiles_c;
+        ta.row = make_target(row);
+        ta.col = make_target(col);
+        ta.emit_row = row != nullptr;
+        ta.emit_col = col != nullptr;
+        ta.partials = part_a;
+        ta.n_partials = ca.n_partials;
+        auto k = tile2d_rne_kernel;
+        k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(tmap, ta);
         return cudaGetLastError();
     }
 
