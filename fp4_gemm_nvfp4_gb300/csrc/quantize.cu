@@ -307,8 +307,9 @@ struct PairArgs {
     uint32_t tiles_r, tiles_c;   // 128-row x 64-column CTA tiles
     Target row, col;
     const float* part_plain;
-    const float* part_rht;
+    const float* part_rht;       // the col-wise operand's partials (with or without RHT)
     int n_partials;
+    bool emit_row, emit_col;
     uint32_t mask;
     uint64_t seed, stream_row, stream_col;
 };
@@ -316,15 +317,18 @@ struct PairArgs {
 constexpr int kPairSlots = 2;
 constexpr uint32_t kSliceBytes = 16 * 128;   // 16 rows x 64 bf16
 
-template <bool kSR>
+// kColRHT: the col-wise operand gets the RHT (else none); the row-wise
+// operand never does.  Either orientation may be left out (emit_*).
+template <bool kSR, bool kColRHT>
 __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                                const PairArgs a) {
     __shared__ float red[32];
     __shared__ float rb_row[128], rb_col[128];
     __shared__ __align__(1024) uint8_t ring[kThreads / 32][kPairSlots][kSliceBytes];
     __shared__ uint64_t full[kThreads / 32][kPairSlots];
-    const TensorScale ts_row = load_tensor_scale(a.part_plain, a.n_partials, red, a.row, nullptr);
-    const TensorScale ts_col = load_tensor_scale(a.part_rht, a.n_partials, red, a.col, nullptr);
+    TensorScale ts_row{1.0f, 1.0f}, ts_col{1.0f, 1.0f};
+    if (a.emit_row) ts_row = load_tensor_scale(a.part_plain, a.n_partials, red, a.row, nullptr);
+    if (a.emit_col) ts_col = load_tensor_scale(a.part_rht, a.n_partials, red, a.col, nullptr);
     fill_rb_table_at(rb_row, ts_row.s_enc, 0);
     fill_rb_table_at(rb_col, ts_col.s_enc, 128);
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
@@ -383,9 +387,11 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                 t0[i] = bf16lo(w);
                 t1[i] = bf16hi(w);
             }
-            if (c < a.cols) {
-                rht16(t0, a.mask);
-                rht16(t1, a.mask);
+            if (a.emit_col && c < a.cols) {
+                if constexpr (kColRHT) {
+                    rht16(t0, a.mask);
+                    rht16(t1, a.mask);
+                }
                 float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -407,7 +413,7 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
         {
             const uint32_t i = lane >> 1, h = lane & 1u;
             const uint32_t r = r0 + i, cb = c0 + 32u * h;
-            if (cb < a.cols) {
+            if (a.emit_row && cb < a.cols) {
                 float v[32];
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
@@ -632,6 +638,48 @@ int row_amax(const RowArgs& base, float* partials, cudaStream_t st) {
     return g;
 }
 
+// The slice-staged encode (pair_encode_kernel): optional row-wise operand
+// without RHT and optional col-wise operand with or without RHT.
+cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool sr, bool col_rht,
+                               uint32_t sign_mask, uint64_t seed, uint64_t stream_row, uint64_t stream_col,
+                               const QuantTarget* row, const QuantTarget* col, const float* part_row,
+                               const float* part_col, int n_partials, cudaStream_t st) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    CUtensorMap tmap;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld_x * 2u};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t elem[2] = {1, 1};
+    if (fn(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, elem,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    PairArgs pa{};
+    pa.rows = (uint32_t)rows;
+    pa.cols = (uint32_t)cols;
+    pa.tiles_r = (uint32_t)((rows + 127) / 128);
+    pa.tiles_c = (uint32_t)((cols + 63) / 64);
+    pa.row = make_target(row);
+    pa.col = make_target(col);
+    pa.emit_row = row != nullptr;
+    pa.emit_col = col != nullptr;
+    pa.part_plain = part_row;
+    pa.part_rht = part_col;
+    pa.n_partials = n_partials;
+    pa.mask = sign_mask;
+    pa.seed = seed;
+    pa.stream_row = stream_row;
+    pa.stream_col = stream_col;
+    const int64_t ntiles = (int64_t)pa.tiles_r * pa.tiles_c;
+    auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(tmap, pa); };
+    if (sr && col_rht) launch(pair_encode_kernel<true, true>);
+    else if (col_rht) launch(pair_encode_kernel<false, true>);
+    else if (sr) launch(pair_encode_kernel<true, false>);
+    else launch(pair_encode_kernel<false, false>);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool scale_2d, bool sr,
@@ -721,7 +769,10 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
         }
     }
 
-    if (row) {
+    // row-wise: the thread-per-block kernel, unless a plain col-wise operand
+    // is emitted too (then one slice-staged pass emits both)
+    const bool joint = row && col && !rht;
+    if (row && !joint) {
         RowArgs r = ra;
         r.out = make_target(row);
         r.partials_in = part_a;
@@ -734,17 +785,9 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
         else if (sr) launch(rowwise_kernel<Pass::kEncode, false, true>);
         else launch(rowwise_kernel<Pass::kEncode, false, false>);
     }
-    if (col) {
-        ColArgs c = ca;
-        c.out = make_target(col);
-        c.partials_in = part_b;
-        c.n_partials = n_col;
-        auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(c); };
-        if (rht && sr) launch(colwise_kernel<Pass::kEncode, true, true>);
-        else if (rht) launch(colwise_kernel<Pass::kEncode, true, false>);
-        else if (sr) launch(colwise_kernel<Pass::kEncode, false, true>);
-        else launch(colwise_kernel<Pass::kEncode, false, false>);
-    }
+    if (col)
+        return launch_pair_encode(x, rows, cols, ld_x, sr, rht, sign_mask, seed, stream_id, stream_id,
+                                  joint ? row : nullptr, col, part_a, part_b, joint ? n_row : n_col, st);
     return cudaGetLastError();
 }
 
@@ -803,13 +846,14 @@ cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t
     pa.part_plain = part_plain;
     pa.part_rht = part_rht;
     pa.n_partials = n;
+    pa.emit_row = pa.emit_col = true;
     pa.mask = sign_mask;
     pa.seed = seed;
     pa.stream_row = stream_row;
     pa.stream_col = stream_col;
     auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(tmap, pa); };
-    if (sr) launch(pair_encode_kernel<true>);
-    else launch(pair_encode_kernel<false>);
+    if (sr) launch(pair_encode_kernel<true, true>);
+    else launch(pair_encode_kernel<false, true>);
     return cudaGetLastError();
 }
 
