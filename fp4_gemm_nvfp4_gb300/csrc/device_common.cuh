@@ -60,33 +60,35 @@ __device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
     return out;
 }
 
-// Stochastic rounding of one value to an E2M1 code with 16 random bits
+// Stochastic rounding of one value to the E2M1 grid with 16 random bits
 // ("Full-Stack FP4", Appendix 7: round up with probability d / step): up iff
 // r16 < frac * 2^16, i.e. iff r16 < ceil(frac * 2^16).
 //
 // Done on the FP32 bit pattern.  In each binade [2^e, 2^(e+1)) with e >= 0
 // the E2M1 grid keeps one mantissa bit, so frac is the low 22 mantissa bits
 // over 2^22, and adding ((2^16 - 1 - r16) << 6) + 63 to the pattern carries
-// into bit 22 exactly when r16 < ceil(frac * 2^16); shifting out the low 22
-// bits then leaves exponent and kept mantissa bit of the rounded value.
-// Below 1 the grid {0, 0.5, 1} is that of [1, 2) shifted by one and halved:
-// z = (|v| + 1) / 2, one fused multiply-add rounded upward (which keeps
-// ceil(frac * 2^16): float spacing there, 2^-24, is finer than 2^-18), lies
-// in [0.5, 1) where the same addition applies with codes two lower than the
-// [1, 2) formula gives, so one formula serves both: code = (bits + addend) /
-// 2^22 - 252.  max(|v|, (|v| + 1) / 2) selects z exactly when |v| < 1.  |v| >=
-// 6 saturates through the clamp to 6 (code 7); the code's sign bit is v's.
+// into bit 22 exactly when r16 < ceil(frac * 2^16); clearing the low 22 bits
+// then leaves the rounded value.  Below 1 the grid {0, 0.5, 1} is that of
+// [1, 2) shifted by one and halved: z = (|v| + 1) / 2, one fused multiply-add
+// rounded upward (which keeps ceil(frac * 2^16): float spacing there, 2^-24,
+// is finer than 2^-18), lies in [0.5, 1) where the same addition applies,
+// and 2 z - 1 maps the rounded z back.  max(|v|, (|v| + 1) / 2) selects z
+// exactly when |v| < 1, and min(q, 2 q - 1) selects 2 q - 1 exactly when
+// q < 1.  The result is |v|'s rounded value with v's sign: a grid value, or
+// a value >= 6 (|v| > 6 can round to 8 or 12), which the saturating RNE
+// conversion e2m1_rne_x8 then turns into the code without rounding, so no
+// clamp to 6 is needed.  With finite v, |v| here stays below 9 (the block
+// scale's E4M3 rounding error is at most 1/2 of its smallest subnormal step).
 __device__ __forceinline__ uint32_t sr_addend_lo(uint32_t w) { return ((~w << 6) & 0x3FFFC0u) | 63u; }
-__device__ __forceinline__ uint32_t sr_addend_hi(uint32_t w) { return ((~w >> 10) & 0x3FFFC0u) | 63u; }
+__device__ __forceinline__ uint32_t sr_addend_hi(uint32_t w) { return (~w >> 10) | 63u; }
 
-__device__ __forceinline__ uint32_t e2m1_sr_add(float v, uint32_t addend) {
-    const float a = fminf(fabsf(v), 6.0f);
+__device__ __forceinline__ float e2m1_sr_grid(float v, uint32_t addend) {
+    const float a = fabsf(v);
     const float z = fmaxf(a, __fmaf_ru(a, 0.5f, 0.5f));
-    const uint32_t code = (__float_as_uint(z) + addend - (252u << 22)) >> 22;
-    return code | ((__float_as_uint(v) >> 28) & 8u);
+    const float zt = __uint_as_float((__float_as_uint(z) + addend) & 0xFFC00000u);
+    const float q = fminf(zt, __fmaf_rn(zt, 2.0f, -1.0f));
+    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(v) & 0x80000000u));
 }
-
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t r16) { return e2m1_sr_add(v, sr_addend_lo(r16)); }
 
 // --------------------------------------------------------------- Philox ----
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
@@ -208,14 +210,13 @@ __device__ __forceinline__ uint2 encode16(const float* t, float r_b, const Philo
         const uint4 r0 = sr_words4(keys, stream_id, idx_base >> 3);
         const uint4 r1 = sr_words4(keys, stream_id, (idx_base >> 3) + 1);
         const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        uint32_t lo = 0, hi = 0;
+        float q[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t wl = w[i >> 1], wh = w[4 + (i >> 1)];
-            lo |= e2m1_sr_add(v[i], (i & 1) ? sr_addend_hi(wl) : sr_addend_lo(wl)) << (4 * i);
-            hi |= e2m1_sr_add(v[8 + i], (i & 1) ? sr_addend_hi(wh) : sr_addend_lo(wh)) << (4 * i);
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t wi = w[i >> 1];
+            q[i] = e2m1_sr_grid(v[i], (i & 1) ? sr_addend_hi(wi) : sr_addend_lo(wi));
         }
-        return make_uint2(lo, hi);
+        return make_uint2(e2m1_rne_x8(q), e2m1_rne_x8(q + 8));
     }
 }
 

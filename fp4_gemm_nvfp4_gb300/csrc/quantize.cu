@@ -257,8 +257,7 @@ __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
             q0 = make_uint2(e2m1_rne_x8(v0), e2m1_rne_x8(v0 + 8));
             q1 = make_uint2(e2m1_rne_x8(v1), e2m1_rne_x8(v1 + 8));
         } else {
-            q0 = make_uint2(0u, 0u);
-            q1 = make_uint2(0u, 0u);
+            float g0[16], g1[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 // SR index: the row-wise index of x, shared by both orientations
@@ -266,16 +265,11 @@ __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
                 const uint4 w = sr_words4(keys, a.stream, idx >> 3);
                 const uint32_t sel = (uint32_t)(idx >> 1) & 3u;
                 const uint32_t word = sel == 0 ? w.x : (sel == 1 ? w.y : (sel == 2 ? w.z : w.w));
-                const uint32_t c0 = e2m1_sr_add(__fmul_rn(t0[i], r_b), sr_addend_lo(word));
-                const uint32_t c1 = e2m1_sr_add(__fmul_rn(t1[i], r_b), sr_addend_hi(word));
-                if (i < 8) {
-                    q0.x |= c0 << (4 * i);
-                    q1.x |= c1 << (4 * i);
-                } else {
-                    q0.y |= c0 << (4 * (i - 8));
-                    q1.y |= c1 << (4 * (i - 8));
-                }
+                g0[i] = e2m1_sr_grid(__fmul_rn(t0[i], r_b), sr_addend_lo(word));
+                g1[i] = e2m1_sr_grid(__fmul_rn(t1[i], r_b), sr_addend_hi(word));
             }
+            q0 = make_uint2(e2m1_rne_x8(g0), e2m1_rne_x8(g0 + 8));
+            q1 = make_uint2(e2m1_rne_x8(g1), e2m1_rne_x8(g1 + 8));
         }
         if (a.emit_col) {
             *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
