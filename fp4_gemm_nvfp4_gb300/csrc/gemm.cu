@@ -401,22 +401,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t taddr = tmem + ((q * 32u) << 16) + kAccCol + half * 128;
             if (p.tma_store && !p.out_fp32) {
                 // Two rounds of 64 columns through this warp's 4 KiB slice of
-                // the staging buffer (32 rows x 128 bytes, 128-byte swizzle).
-                // The accumulator is handed back as soon as the second
-                // round's columns are in registers.
+                // the staging buffer (32 rows x 128 bytes, 128-byte swizzle),
+                // each round's two loads in flight under one wait.  The
+                // accumulator is handed back as soon as the second round's
+                // columns are in registers.
                 uint8_t* slice = staging + (half * 4 + q) * 4096u;
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     uint32_t packed[32];
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        uint32_t v[32];
-                        tmem_ld_32x32b_x32(taddr + (2 * r + cc) * 32, v);
+                    {
+                        uint32_t v0[32], v1[32];
+                        tmem_ld_32x32b_x32(taddr + (2 * r) * 32, v0);
+                        tmem_ld_32x32b_x32(taddr + (2 * r + 1) * 32, v1);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            packed[16 * cc + i] = pack_bf16x2(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
-                                                              __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+                        for (int i = 0; i < 16; ++i) {
+                            packed[i] = pack_bf16x2(__fmul_rn(__uint_as_float(v0[2 * i]), alpha),
+                                                    __fmul_rn(__uint_as_float(v0[2 * i + 1]), alpha));
+                            packed[16 + i] = pack_bf16x2(__fmul_rn(__uint_as_float(v1[2 * i]), alpha),
+                                                         __fmul_rn(__uint_as_float(v1[2 * i + 1]), alpha));
+                        }
                     }
                     if (r == 1) {
                         tc_fence_before();
@@ -440,34 +444,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             } else if (p.tma_store && p.out_fp32) {
                 // FP32: four rounds of 32 columns through this warp's 4 KiB
-                // slice (32 rows x 128 bytes, 128-byte swizzle); the
-                // accumulator goes back after the last round's load.
+                // slice (32 rows x 128 bytes, 128-byte swizzle), loaded two
+                // rounds at a time under one wait; the accumulator goes back
+                // once the last two rounds are in registers.
                 uint8_t* slice = staging + (half * 4 + q) * 4096u;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr + c * 32, v);
+                for (int c2 = 0; c2 < 4; c2 += 2) {
+                    uint32_t v[2][32];
+                    tmem_ld_32x32b_x32(taddr + c2 * 32, v[0]);
+                    tmem_ld_32x32b_x32(taddr + (c2 + 1) * 32, v[1]);
                     tmem_ld_wait();
-                    if (c == 3) {
+                    if (c2 == 2) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
                     }
-                    if (lane == 0) bulk_wait_read_all();
-                    __syncwarp();
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        *reinterpret_cast<uint4*>(slice + lane * 128u + ((uint32_t)i ^ (lane & 7u)) * 16u) =
-                            make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(v[4 * i]), alpha)),
-                                       __float_as_uint(__fmul_rn(__uint_as_float(v[4 * i + 1]), alpha)),
-                                       __float_as_uint(__fmul_rn(__uint_as_float(v[4 * i + 2]), alpha)),
-                                       __float_as_uint(__fmul_rn(__uint_as_float(v[4 * i + 3]), alpha)));
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const uint32_t y = row0 + q * 32, x = nbase + (uint32_t)c * 32u;
-                        if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
-                        bulk_commit_group();
+                    for (int h = 0; h < 2; ++h) {
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            *reinterpret_cast<uint4*>(slice + lane * 128u + ((uint32_t)i ^ (lane & 7u)) * 16u) =
+                                make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(v[h][4 * i]), alpha)),
+                                           __float_as_uint(__fmul_rn(__uint_as_float(v[h][4 * i + 1]), alpha)),
+                                           __float_as_uint(__fmul_rn(__uint_as_float(v[h][4 * i + 2]), alpha)),
+                                           __float_as_uint(__fmul_rn(__uint_as_float(v[h][4 * i + 3]), alpha)));
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const uint32_t y = row0 + q * 32, x = nbase + (uint32_t)(c2 + h) * 32u;
+                            if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
+                            bulk_commit_group();
+                        }
                     }
                 }
             } else {
