@@ -93,12 +93,14 @@ __device__ __forceinline__ float e2m1_sr_grid(float v, uint32_t addend) {
 // --------------------------------------------------------------- Philox ----
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
 // 32x32->64 multiplies; the key is bumped by the Weyl constants between
-// rounds.  The ten round keys depend only on the seed, so they are formed once.
+// rounds.  The ten round keys depend only on the seed, so the host forms them
+// once and the kernels read them from their parameters (no registers, no
+// per-round key additions).
 struct PhiloxKeys {
     uint32_t k0[10], k1[10];
 };
 
-__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
+__host__ __device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
     PhiloxKeys k;
     uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
 #pragma unroll

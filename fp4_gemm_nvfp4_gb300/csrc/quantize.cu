@@ -62,7 +62,8 @@ struct RowArgs {
     int n_partials;
     float* partials_out;
     uint32_t mask;
-    uint64_t seed, stream;
+    PhiloxKeys keys;             // SR round keys of the seed
+    uint64_t stream;
 };
 
 // One thread = one 1x16 block: two 16-byte loads, RHT in registers (optional),
@@ -78,8 +79,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
         __syncthreads();
     }
     float local_max = 0.0f;
-    PhiloxKeys keys;
-    if constexpr (kSR) keys = philox_keys(a.seed);
+    const PhiloxKeys& keys = a.keys;   // SR round keys, formed by the host
     // block b = r * bpr + j; (r, j) advance by the grid stride without a division
     const uint32_t stride = gridDim.x * kThreads;
     const uint32_t stride_r = stride / a.bpr, stride_j = stride - stride_r * a.bpr;
@@ -129,7 +129,8 @@ struct ColArgs {
     float* partials_out;
     float* partials_out_plain;   // kAmax with kDual: max |x| before the RHT
     uint32_t mask;
-    uint64_t seed, stream;
+    PhiloxKeys keys;             // SR round keys of the seed
+    uint64_t stream;
 };
 
 // One warp covers 16 rows x 64 columns (lane = 2 adjacent columns, so each
@@ -150,8 +151,7 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
     float local_max = 0.0f, plain_max = 0.0f;
-    PhiloxKeys keys;
-    if constexpr (kSR) keys = philox_keys(a.seed);
+    const PhiloxKeys& keys = a.keys;   // SR round keys, formed by the host
     for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const uint32_t tr = tile % a.tiles_r, tc = tile / a.tiles_r;
         const uint32_t r0 = tr * 128u + warp * 16u, c = tc * 64u + lane * 2u;
@@ -221,8 +221,7 @@ __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
     __syncthreads();
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
-    PhiloxKeys keys;
-    if constexpr (kSR) keys = philox_keys(a.seed);
+    const PhiloxKeys& keys = a.keys;   // SR round keys, formed by the host
     for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const uint32_t tr = tile % a.tiles_r, tc = tile / a.tiles_r;
         const uint32_t r0 = tr * 128u + warp * 16u, c = tc * 64u + lane * 2u;
@@ -305,7 +304,8 @@ struct PairArgs {
     int n_partials;
     bool emit_row, emit_col;
     uint32_t mask;
-    uint64_t seed, stream_row, stream_col;
+    PhiloxKeys keys;             // SR round keys of the seed
+    uint64_t stream_row, stream_col;
 };
 
 constexpr int kPairSlots = 2;
@@ -331,8 +331,7 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
         fence_barrier_init();
     }
     __syncthreads();
-    PhiloxKeys keys;
-    if constexpr (kSR) keys = philox_keys(a.seed);
+    const PhiloxKeys& keys = a.keys;   // SR round keys, formed by the host
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
     // this warp's slice of the CTA's k-th tile, if it holds rows
     auto slice_of = [&](uint32_t k, uint32_t& r0, uint32_t& c0) -> bool {
@@ -662,7 +661,7 @@ cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, in
     pa.part_rht = part_col;
     pa.n_partials = n_partials;
     pa.mask = sign_mask;
-    pa.seed = seed;
+    pa.keys = philox_keys(seed);
     pa.stream_row = stream_row;
     pa.stream_col = stream_col;
     const int64_t ntiles = (int64_t)pa.tiles_r * pa.tiles_c;
@@ -690,7 +689,7 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
     ra.bpr = (uint32_t)(cols / 16);
     ra.total = (uint32_t)(rows * (cols / 16));
     ra.mask = sign_mask;
-    ra.seed = seed;
+    ra.keys = philox_keys(seed);
     ra.stream = stream_id;
 
     ColArgs ca{};
@@ -701,7 +700,7 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
     ca.tiles_r = (uint32_t)((rows + 127) / 128);
     ca.tiles_c = (uint32_t)((cols + 63) / 64);
     ca.mask = sign_mask;
-    ca.seed = seed;
+    ca.keys = philox_keys(seed);
     ca.stream = stream_id;
     const int64_t ntiles = (int64_t)ca.tiles_r * ca.tiles_c;
 
@@ -803,7 +802,7 @@ cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t
     ca.tiles_r = (uint32_t)((rows + 127) / 128);
     ca.tiles_c = (uint32_t)((cols + 63) / 64);
     ca.mask = sign_mask;
-    ca.seed = seed;
+    ca.keys = philox_keys(seed);
     const int64_t ntiles = (int64_t)ca.tiles_r * ca.tiles_c;
 
     // one amax pass: the RHT amax for the col-wise operand and the plain
@@ -842,7 +841,7 @@ cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t
     pa.n_partials = n;
     pa.emit_row = pa.emit_col = true;
     pa.mask = sign_mask;
-    pa.seed = seed;
+    pa.keys = philox_keys(seed);
     pa.stream_row = stream_row;
     pa.stream_col = stream_col;
     auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(tmap, pa); };
