@@ -132,8 +132,11 @@ __device__ __forceinline__ uint4 sr_words4(const PhiloxKeys& keys, uint64_t stre
 }
 
 // ------------------------------------------------------------------ RHT ----
-// t <- H16 * D * t / 4: negate per mask, butterfly stages 0..3, times 0.25.
-__device__ __forceinline__ void rht16(float* t, uint32_t sign_mask) {
+// t <- H16 * D * t (without the 1/4): negate per mask, butterfly stages 0..3.
+// With bf16 inputs every value here is a multiple of 2^-133, so t / 4 is
+// exact even when subnormal: max|t| / 4 is the amax of the scaled transform,
+// and RN((t / 4) r) = RN(t (r / 4)) whenever r / 4 is exact.
+__device__ __forceinline__ void rht16_unscaled(float* t, uint32_t sign_mask) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) t[i] = __uint_as_float(__float_as_uint(t[i]) ^ (((sign_mask >> i) & 1u) << 31));
 #pragma unroll
@@ -146,8 +149,17 @@ __device__ __forceinline__ void rht16(float* t, uint32_t sign_mask) {
             t[i | (1 << s)] = __fsub_rn(a, b);
         }
     }
+}
+
+__device__ __forceinline__ void scale16(float* t, float f) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) t[i] = __fmul_rn(t[i], 0.25f);
+    for (int i = 0; i < 16; ++i) t[i] = __fmul_rn(t[i], f);
+}
+
+// t <- H16 * D * t / 4: negate per mask, butterfly stages 0..3, times 0.25.
+__device__ __forceinline__ void rht16(float* t, uint32_t sign_mask) {
+    rht16_unscaled(t, sign_mask);
+    scale16(t, 0.25f);
 }
 
 // ------------------------------------------------------------ tensor scale -
@@ -162,9 +174,24 @@ __device__ __forceinline__ TensorScale tensor_scale(float amax) {
     return {s, __fdiv_rn(1.0f, s)};
 }
 
+// RN(a / 6) for a >= 0 without a division: q0 = RN(a * RN(1/6)), the exact
+// remainder a - 6 q0 by one fused multiply-add, and one correction step
+// q0 + remainder * RN(1/6) (Markstein's method for division by a constant,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", 1990).  An exhaustive comparison with IEEE division on sm_103a
+// over every non-negative float found it exact from 2^-125 up; below that
+// the quotient is subnormal and the division is done as such.
+__device__ __forceinline__ float div6_rn(float a) {
+    if (a < 0x1p-125f) return __fdiv_rn(a, 6.0f);
+    const float c6 = 0x1.555556p-3f;
+    const float q0 = __fmul_rn(a, c6);
+    const float r = __fmaf_rn(-q0, 6.0f, a);
+    return __fmaf_rn(r, c6, q0);
+}
+
 // Block scale code and encode multiplier r_b from the block amax.
 __device__ __forceinline__ uint32_t block_scale(float amax_b, float s_enc, float* r_b) {
-    const float sb32 = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
+    const float sb32 = __fmul_rn(div6_rn(amax_b), s_enc);
     const uint32_t code = e4m3_encode_satfinite(sb32);
     const float sb = e4m3_decode(code);
     *r_b = (sb == 0.0f) ? 0.0f : __fdiv_rn(s_enc, sb);
@@ -174,24 +201,31 @@ __device__ __forceinline__ uint32_t block_scale(float amax_b, float s_enc, float
 // The multipliers r_b = S_enc / s_b of all 127 finite non-negative E4M3
 // codes, for a CTA to look up instead of dividing per block (the same single
 // division, done once per code).  Threads 0..127 fill it; callers sync.
-__device__ __forceinline__ void fill_rb_table(float* table, float s_enc) {
+__device__ __forceinline__ void fill_rb_table(float* table, float s_enc, float mult = 1.0f) {
     if (threadIdx.x < 128) {
         const float sb = e4m3_decode(threadIdx.x);
-        table[threadIdx.x] = (threadIdx.x == 0 || threadIdx.x == 127) ? 0.0f : __fdiv_rn(s_enc, sb);
+        table[threadIdx.x] =
+            (threadIdx.x == 0 || threadIdx.x == 127) ? 0.0f : __fmul_rn(__fdiv_rn(s_enc, sb), mult);
     }
 }
 
+// Whether an RHT encode may take the transform's 1/4 into its multipliers
+// (table entries r_b / 4): exact for every code when the smallest r_b,
+// S_enc / 448, is at least 2^-124, so that r_b / 4 stays normal.  Otherwise
+// (tensor amax above about 1.3e38) the 1/4 is applied to the values.
+__device__ __forceinline__ bool rht_quarter_foldable(float s_enc) { return __fdiv_rn(s_enc, 448.0f) >= 0x1p-124f; }
+
 // fill_rb_table by threads [first, first + 128).
-__device__ __forceinline__ void fill_rb_table_at(float* table, float s_enc, uint32_t first) {
+__device__ __forceinline__ void fill_rb_table_at(float* table, float s_enc, uint32_t first, float mult = 1.0f) {
     const uint32_t c = threadIdx.x - first;
     if (threadIdx.x >= first && c < 128) {
         const float sb = e4m3_decode(c);
-        table[c] = (c == 0 || c == 127) ? 0.0f : __fdiv_rn(s_enc, sb);
+        table[c] = (c == 0 || c == 127) ? 0.0f : __fmul_rn(__fdiv_rn(s_enc, sb), mult);
     }
 }
 
 __device__ __forceinline__ uint32_t block_scale_tab(float amax_b, float s_enc, const float* table, float* r_b) {
-    const float sb32 = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
+    const float sb32 = __fmul_rn(div6_rn(amax_b), s_enc);
     const uint32_t code = e4m3_encode_satfinite(sb32);
     *r_b = table[code];
     return code;

@@ -73,9 +73,11 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
     __shared__ float red[32];
     __shared__ float rb_table[128];
     TensorScale ts{1.0f, 1.0f};
+    bool fold = false;   // the RHT's 1/4 lives in the multipliers (rht_quarter_foldable)
     if constexpr (P == Pass::kEncode) {
         ts = load_tensor_scale(a.partials_in, a.n_partials, red, a.out, nullptr);
-        fill_rb_table(rb_table, ts.s_enc);
+        if constexpr (kRHT) fold = rht_quarter_foldable(ts.s_enc);
+        fill_rb_table(rb_table, ts.s_enc, fold ? 0.25f : 1.0f);
         __syncthreads();
     }
     float local_max = 0.0f;
@@ -91,13 +93,17 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
         float t[16] = {bf16lo(u0.x), bf16hi(u0.x), bf16lo(u0.y), bf16hi(u0.y), bf16lo(u0.z), bf16hi(u0.z),
                        bf16lo(u0.w), bf16hi(u0.w), bf16lo(u1.x), bf16hi(u1.x), bf16lo(u1.y), bf16hi(u1.y),
                        bf16lo(u1.z), bf16hi(u1.z), bf16lo(u1.w), bf16hi(u1.w)};
-        if constexpr (kRHT) rht16(t, a.mask);
+        if constexpr (kRHT) {
+            rht16_unscaled(t, a.mask);   // the 1/4 comes below
+            if (P == Pass::kEncode && !fold) scale16(t, 0.25f);
+        }
         float amax_b = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(t[i]));
         if constexpr (P == Pass::kAmax) {
             local_max = fmaxf(local_max, amax_b);
         } else {
+            if (fold) amax_b = __fmul_rn(amax_b, 0.25f);
             float r_b;
             const uint32_t sc = block_scale_tab(amax_b, ts.s_enc, rb_table, &r_b);
             const uint64_t idx = (uint64_t)r * ((uint64_t)a.bpr * 16u) + (uint64_t)j * 16u;
@@ -112,7 +118,10 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
             ++r;
         }
     }
-    if constexpr (P == Pass::kAmax) block_max_store(local_max, a.partials_out, red);
+    if constexpr (P == Pass::kAmax) {
+        if constexpr (kRHT) local_max = __fmul_rn(local_max, 0.25f);
+        block_max_store(local_max, a.partials_out, red);
+    }
 }
 
 // ----------------------------------------------------------- col-wise -----
@@ -143,9 +152,11 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
     __shared__ float red[32];
     __shared__ float rb_table[128];
     TensorScale ts{1.0f, 1.0f};
+    bool fold = false;   // the RHT's 1/4 lives in the multipliers (rht_quarter_foldable)
     if constexpr (P == Pass::kEncode) {
         ts = load_tensor_scale(a.partials_in, a.n_partials, red, a.out, nullptr);
-        fill_rb_table(rb_table, ts.s_enc);
+        if constexpr (kRHT) fold = rht_quarter_foldable(ts.s_enc);
+        fill_rb_table(rb_table, ts.s_enc, fold ? 0.25f : 1.0f);
         __syncthreads();
     }
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
@@ -169,8 +180,12 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
             for (int i = 0; i < 16; ++i) plain_max = fmaxf(plain_max, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
         }
         if constexpr (kRHT) {
-            rht16(t0, a.mask);
-            rht16(t1, a.mask);
+            rht16_unscaled(t0, a.mask);   // the 1/4 comes below
+            rht16_unscaled(t1, a.mask);
+            if (P == Pass::kEncode && !fold) {
+                scale16(t0, 0.25f);
+                scale16(t1, 0.25f);
+            }
         }
         float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
@@ -181,6 +196,10 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
         if constexpr (P == Pass::kAmax) {
             local_max = fmaxf(local_max, fmaxf(m0, m1));
         } else {
+            if (fold) {
+                m0 = __fmul_rn(m0, 0.25f);
+                m1 = __fmul_rn(m1, 0.25f);
+            }
             float rb0, rb1;
             const uint32_t sc0 = block_scale_tab(m0, ts.s_enc, rb_table, &rb0);
             const uint32_t sc1 = block_scale_tab(m1, ts.s_enc, rb_table, &rb1);
@@ -193,6 +212,7 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
         }
     }
     if constexpr (P == Pass::kAmax) {
+        if constexpr (kRHT) local_max = __fmul_rn(local_max, 0.25f);
         block_max_store(local_max, a.partials_out, red);
         if constexpr (kDual) {
             __syncthreads();
@@ -323,8 +343,10 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     TensorScale ts_row{1.0f, 1.0f}, ts_col{1.0f, 1.0f};
     if (a.emit_row) ts_row = load_tensor_scale(a.part_plain, a.n_partials, red, a.row, nullptr);
     if (a.emit_col) ts_col = load_tensor_scale(a.part_rht, a.n_partials, red, a.col, nullptr);
+    // the col-wise RHT's 1/4 lives in its multipliers (rht_quarter_foldable)
+    const bool fold = kColRHT && rht_quarter_foldable(ts_col.s_enc);
     fill_rb_table_at(rb_row, ts_row.s_enc, 0);
-    fill_rb_table_at(rb_col, ts_col.s_enc, 128);
+    fill_rb_table_at(rb_col, ts_col.s_enc, 128, fold ? 0.25f : 1.0f);
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     if (lane == 0) {
         for (int sl = 0; sl < kPairSlots; ++sl) mbar_init(&full[warp][sl], 1);
@@ -382,14 +404,22 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
             }
             if (a.emit_col && c < a.cols) {
                 if constexpr (kColRHT) {
-                    rht16(t0, a.mask);
-                    rht16(t1, a.mask);
+                    rht16_unscaled(t0, a.mask);   // the 1/4 comes below
+                    rht16_unscaled(t1, a.mask);
+                    if (!fold) {
+                        scale16(t0, 0.25f);
+                        scale16(t1, 0.25f);
+                    }
                 }
                 float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     m0 = fmaxf(m0, fabsf(t0[i]));
                     m1 = fmaxf(m1, fabsf(t1[i]));
+                }
+                if (fold) {
+                    m0 = __fmul_rn(m0, 0.25f);
+                    m1 = __fmul_rn(m1, 0.25f);
                 }
                 float rb0, rb1;
                 const uint32_t sc0 = block_scale_tab(m0, ts_col.s_enc, rb_col, &rb0);
