@@ -264,6 +264,8 @@ int oracle_quantize_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t 
     int64_t lcols = (orientation == ORACLE_ROWWISE) ? cols : rows;
     if (lcols % 16 != 0 || lr0 < 0 || lr1 > lrows || lr0 > lr1)
         return 2;
+    if (scaling < 0 || scaling > 2)
+        return 5;
     if (scaling == 1 && (rows % 16 != 0 || cols % 16 != 0))
         return 3;
     if (scaling == 1 && use_rht)
@@ -290,7 +292,7 @@ int oracle_quantize_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t 
             /* block amax: the 1x16 block, or the 16x16 tile of x that holds it
              * ("Full-Stack FP4", Sec. 2: blocks of 16x16 or 1x16) */
             float amax_b = 0.0f;
-            if (scaling == 0) {
+            if (scaling != 1) {
                 for (int t = 0; t < 16; ++t)
                     if (fabsf(blk[t]) > amax_b)
                         amax_b = fabsf(blk[t]);
@@ -310,6 +312,36 @@ int oracle_quantize_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t 
             uint8_t sb_code = oracle_e4m3_rne_satfinite(sb32);
             float sb = (float)oracle_e4m3_value(sb_code);
             float r_b = (sb == 0.0f) ? 0.0f : s_enc / sb;
+
+            /* 4/6 adaptive scaling ("Full-Stack FP4", Sec. 1 and related
+             * work: 4/6 adds MSE-optimal adaptive block scaling; the rule is
+             * not printed).  Reading: the block is also encoded with its amax
+             * mapped to 4; each candidate is encoded with RNE and measured by
+             * sum_i (x_i S_enc - e2m1(q_i) s)^2 in binary32 (x_i S_enc and
+             * the difference rounded once each, the squares accumulated in
+             * index order by fused multiply-adds); the 4 candidate is kept
+             * only when strictly closer.  With SR the chosen scale is then
+             * used for the stochastic encode. */
+            if (scaling == 2) {
+                float sb32_4 = (amax_b / 4.0f) * s_enc;
+                uint8_t code4 = oracle_e4m3_rne_satfinite(sb32_4);
+                float sb4 = (float)oracle_e4m3_value(code4);
+                float r4 = (sb4 == 0.0f) ? 0.0f : s_enc / sb4;
+                float err6 = 0.0f, err4 = 0.0f;
+                for (int t = 0; t < 16; ++t) {
+                    float xs = blk[t] * s_enc;
+                    float g6 = (float)oracle_e2m1_value(oracle_e2m1_rne(blk[t] * r_b));
+                    float g4 = (float)oracle_e2m1_value(oracle_e2m1_rne(blk[t] * r4));
+                    float d6 = xs - g6 * sb;
+                    float d4 = xs - g4 * sb4;
+                    err6 = fmaf(d6, d6, err6);
+                    err4 = fmaf(d4, d4, err4);
+                }
+                if (err4 < err6) {
+                    sb_code = code4;
+                    r_b = r4;
+                }
+            }
             srow[b] = sb_code;
 
             for (int t = 0; t < 16; t += 2) {

@@ -75,7 +75,9 @@ float oracle_amax(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld,
  * its columns are the reduction dimension.  amax is oracle_amax() of the
  * same orientation.  Output: codes [(lr1-lr0)][Lc/2] (lower column index in
  * the low nibble) and scales [(lr1-lr0)][Lc/16] row-major, Lc = logical cols.
- * scaling: 0 = 1x16 blocks, 1 = 16x16 tiles of x.  rounding: 0 RNE, 1 SR.
+ * scaling: 0 = 1x16 blocks, 1 = 16x16 tiles of x, 2 = 1x16 blocks with the
+ * 4/6 choice (amax mapped to 6 or to 4, whichever RNE candidate is closer).
+ * rounding: 0 RNE, 1 SR.
  * Returns 0 on success, nonzero on a bad shape.
  */
 int oracle_quantize_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld,

@@ -453,6 +453,103 @@ def test_quantize_rejects_bad_shapes():
         oracle.quantize(np.zeros((24, 32), np.uint16), scaling=1)
 
 
+# ------------------------------------------------- 4/6 adaptive scaling ----
+# "Full-Stack FP4" names 4/6 scaling (its related-work section: MSE-optimal
+# adaptive block scaling) without printing the rule; the oracle's reading is
+# "encode each 1x16 block with its amax mapped to 6 and to 4 (RNE), keep the
+# closer one in squared error".  These pins check that reading against
+# hand-built blocks and an independent float64 computation of both errors.
+SCALE_46 = 2
+
+
+def _e4m3_code_of(value):
+    t = torch.tensor([value], dtype=torch.float32).to(torch.float8_e4m3fn)
+    return int(t.view(torch.uint8).item())
+
+
+def test_46_keeps_exact_four_and_exact_six_blocks():
+    """S_enc = 2688 / 42 = 64.  Block 1 holds values of {0, 0.5 ... 4}: with its
+    amax mapped to 4 the scale is 64 and every value is on the grid; with the
+    amax mapped to 6 the scale is E4M3(42.67) = 44 and most are not.  Block 2
+    holds values of {0 ... 6}: exact with the amax mapped to 6 (scale 64),
+    inexact mapped to 4 (scale 96).  Block 0 holds the tensor amax, where
+    both mappings saturate at 448 and the tie keeps 6."""
+    blk0 = [42.0] + [0.0] * 15
+    blk1 = [4, 3, 2, 1.5, 1, 0.5, 0, -4, -3, -2, -1.5, -1, -0.5, 0, 2, 4]
+    blk2 = [6, 4, 3, 2, 1.5, 1, 0.5, 0, -6, -4, -3, -2, -1.5, -1, -0.5, 6]
+    xf = np.array([blk0 + blk1 + blk2], np.float32)
+    x = inputs.to_bf16_bits(xf)
+    q46 = oracle.quantize(x, scaling=SCALE_46)
+    q6 = oracle.quantize(x)
+    assert float(q46["s_enc"]) == 64.0
+    assert list(q46["scales"][0]) == [0x7E, _e4m3_code_of(64.0), _e4m3_code_of(64.0)]
+    assert list(q6["scales"][0]) == [0x7E, _e4m3_code_of(44.0), _e4m3_code_of(64.0)]
+    deq46 = oracle.dequantize(q46["codes"], q46["scales"], q46["s_g"])[0]
+    deq6 = oracle.dequantize(q6["codes"], q6["scales"], q6["s_g"])[0]
+    assert np.array_equal(deq46[16:], xf[0, 16:].astype(np.float64))
+    assert not np.array_equal(deq6[16:32], xf[0, 16:32].astype(np.float64))
+    assert np.array_equal(deq6[32:], xf[0, 32:].astype(np.float64))
+
+
+def _block_errors_f64(xf, s_enc, amax_b):
+    """Squared error of both candidates in float64, from the pinned E4M3 and
+    E2M1 primitives; the encode multiplications stay binary32 as read."""
+    out = {}
+    for m in (6.0, 4.0):
+        sb32 = np.float32(np.float32(np.float32(amax_b) / np.float32(m)) * np.float32(s_enc))
+        code = _e4m3_code_of(float(min(sb32, np.float32(448.0))))
+        sb = float(_torch_e4m3_values(np.array([code], np.uint8))[0])
+        r = np.float32(0.0) if sb == 0 else np.float32(np.float32(s_enc) / np.float32(sb))
+        v = (xf.astype(np.float32) * r).astype(np.float32)
+        g = _e2m1_values(oracle.e2m1_rne_array(v).astype(np.int64))
+        err = float(np.sum((xf.astype(np.float64) * float(s_enc) - g * sb) ** 2))
+        out[m] = (code, err)
+    return out
+
+
+@pytest.mark.parametrize("gen", ["normal", "student_t"])
+def test_46_choice_is_the_lower_squared_error(gen):
+    x = (inputs.normal(64, 256, 31, outlier_channels=2) if gen == "normal"
+         else inputs.student_t(64, 256, 32))
+    xf = inputs.bf16_bits_to_f32(x)
+    q = oracle.quantize(x, scaling=SCALE_46)
+    s_enc = float(q["s_enc"])
+    checked = fours = 0
+    for r in range(64):
+        for b in range(16):
+            blk = xf[r, 16 * b:16 * b + 16]
+            e = _block_errors_f64(blk, s_enc, np.abs(blk).max())
+            (c6, e6), (c4, e4) = e[6.0], e[4.0]
+            if abs(e4 - e6) <= 1e-6 * max(e4, e6, 1e-30):
+                continue   # too close for a float64 reference to decide a binary32 choice
+            want = c4 if e4 < e6 else c6
+            assert q["scales"][r, b] == want, (r, b, e6, e4)
+            fours += want == c4 and c4 != c6
+            checked += 1
+    assert checked > 900 and fours > 50
+
+
+def test_46_error_never_above_plain_scaling():
+    x = inputs.student_t(32, 512, 33)
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    q46 = oracle.quantize(x, scaling=SCALE_46)
+    q6 = oracle.quantize(x)
+    d46 = (oracle.dequantize(q46["codes"], q46["scales"], q46["s_g"]) - xf) ** 2
+    d6 = (oracle.dequantize(q6["codes"], q6["scales"], q6["s_g"]) - xf) ** 2
+    b46 = d46.reshape(32, 32, 16).sum(axis=2)
+    b6 = d6.reshape(32, 32, 16).sum(axis=2)
+    assert np.all(b46 <= b6 * (1 + 1e-5) + 1e-30)
+    assert b46.sum() < b6.sum()
+
+
+def test_46_sr_uses_the_rne_choice_of_scale():
+    x = _rand_bits(32, 256, 34, outliers=1)
+    rne = oracle.quantize(x, scaling=SCALE_46)
+    sr = oracle.quantize(x, scaling=SCALE_46, rounding=1, seed=3, stream_id=1)
+    assert np.array_equal(rne["scales"], sr["scales"])
+    assert not np.array_equal(rne["codes"], sr["codes"])
+
+
 # ---------------------------------------------------------- dequantize ----
 def test_dequantize_grid_values():
     codes4 = np.arange(16, dtype=np.uint8)
