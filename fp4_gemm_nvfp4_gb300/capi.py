@@ -24,6 +24,7 @@ NVFP4_ERR_WORKSPACE = 7
 # enums
 NVFP4_SCALE_1X16 = 0
 NVFP4_SCALE_16X16 = 1
+NVFP4_SCALE_1X16_46 = 2
 NVFP4_ROUND_RNE = 0
 NVFP4_ROUND_SR = 1
 NVFP4_OUT_BF16 = 0

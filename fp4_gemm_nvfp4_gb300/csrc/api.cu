@@ -38,7 +38,8 @@ nvfp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld
                            nvfp4_rounding rounding, uint64_t seed, uint64_t stream_id, int orientations,
                            const nvfp4_tensor* out_row, const nvfp4_tensor* out_col, bool rht, uint16_t mask,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    if (scaling != NVFP4_SCALE_1X16 && scaling != NVFP4_SCALE_16X16) return NVFP4_ERR_INVALID_ARG;
+    if (scaling != NVFP4_SCALE_1X16 && scaling != NVFP4_SCALE_16X16 && scaling != NVFP4_SCALE_1X16_46)
+        return NVFP4_ERR_INVALID_ARG;
     if (rounding != NVFP4_ROUND_RNE && rounding != NVFP4_ROUND_SR) return NVFP4_ERR_INVALID_ARG;
     if (orientations < 1 || orientations > 3) return NVFP4_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
@@ -65,7 +66,8 @@ nvfp4_status quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld
     if (want_row) tr = to_target(out_row);
     if (want_col) tc = to_target(out_col);
     const cudaError_t e = nvfp4::launch_quantize(
-        static_cast<const uint16_t*>(x), rows, cols, ld_x, two_d, rounding == NVFP4_ROUND_SR, rht, mask, seed,
+        static_cast<const uint16_t*>(x), rows, cols, ld_x, two_d, scaling == NVFP4_SCALE_1X16_46,
+        rounding == NVFP4_ROUND_SR, rht, mask, seed,
         stream_id, want_row ? &tr : nullptr, want_col ? &tc : nullptr, static_cast<float*>(workspace), stream);
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }

@@ -231,6 +231,71 @@ __device__ __forceinline__ uint32_t block_scale_tab(float amax_b, float s_enc, c
     return code;
 }
 
+// The values of eight E2M1 codes (element 0 in the low nibble), signed.
+__device__ __forceinline__ void e2m1_decode_x8(uint32_t w, float* g) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float lo, hi;
+        asm("{\n\t"
+            ".reg .b8 t;\n\t"
+            ".reg .b32 h2;\n\t"
+            ".reg .f16 l, h;\n\t"
+            "cvt.u8.u32 t, %2;\n\t"
+            "cvt.rn.f16x2.e2m1x2 h2, t;\n\t"
+            "mov.b32 {l, h}, h2;\n\t"
+            "cvt.f32.f16 %0, l;\n\t"
+            "cvt.f32.f16 %1, h;\n\t"
+            "}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(w >> (8 * k)));
+        g[2 * k] = lo;
+        g[2 * k + 1] = hi;
+    }
+}
+
+// 4/6 adaptive scaling of one 1x16 block (the oracle's reading of the 4/6
+// scaling "Full-Stack FP4" names): the block's amax mapped to 6 (the plain
+// scale) or to 4, each candidate encoded with RNE and measured by
+// sum_i (x_i S_enc - e2m1(q_i) s)^2 in binary32, accumulated in index order by
+// fused multiply-adds; the 4 candidate only when strictly closer.  t holds the
+// values the multipliers of `table` apply to and xs_mult * t_i = x_i S_enc
+// (both carry the RHT's 1/4 when it is folded into the multipliers).  Returns
+// the chosen scale code and its multiplier in *r_b.
+__device__ __forceinline__ uint32_t block_scale_46(const float* t, float amax_b, float s_enc, float xs_mult,
+                                                   const float* table, float* r_b) {
+    float r6;
+    const uint32_t c6 = block_scale_tab(amax_b, s_enc, table, &r6);
+    const uint32_t c4 = e4m3_encode_satfinite(__fmul_rn(__fmul_rn(amax_b, 0.25f), s_enc));
+    const float r4 = table[c4];
+    const float sb6 = e4m3_decode(c6), sb4 = e4m3_decode(c4);
+    float v6[16], v4[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        v6[i] = __fmul_rn(t[i], r6);
+        v4[i] = __fmul_rn(t[i], r4);
+    }
+    float g6[16], g4[16];
+    e2m1_decode_x8(e2m1_rne_x8(v6), g6);
+    e2m1_decode_x8(e2m1_rne_x8(v6 + 8), g6 + 8);
+    e2m1_decode_x8(e2m1_rne_x8(v4), g4);
+    e2m1_decode_x8(e2m1_rne_x8(v4 + 8), g4 + 8);
+    float e6 = 0.0f, e4 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float xs = __fmul_rn(t[i], xs_mult);
+        const float d6 = __fsub_rn(xs, __fmul_rn(g6[i], sb6));
+        const float d4 = __fsub_rn(xs, __fmul_rn(g4[i], sb4));
+        e6 = __fmaf_rn(d6, d6, e6);
+        e4 = __fmaf_rn(d4, d4, e4);
+    }
+    if (e4 < e6) {
+        *r_b = r4;
+        return c4;
+    }
+    *r_b = r6;
+    return c6;
+}
+
 // Encode the 16 values t of one block with multiplier r_b: codes in a uint2
 // (element 0 in the low nibble of byte 0).  idx_base is the SR index of
 // element 0 (a multiple of 16 for 1x16 blocks).

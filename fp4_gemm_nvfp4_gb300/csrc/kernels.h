@@ -27,7 +27,7 @@ constexpr int kMaxAmaxPartials = 4096;
 constexpr size_t kQuantizeWorkspaceBytes = 2 * kMaxAmaxPartials * sizeof(float);
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool scale_2d,
-                            bool sr, bool rht, uint32_t sign_mask, uint64_t seed, uint64_t stream_id,
+                            bool scale_46, bool sr, bool rht, uint32_t sign_mask, uint64_t seed, uint64_t stream_id,
                             const QuantTarget* row, const QuantTarget* col, float* workspace,
                             cudaStream_t stream);
 

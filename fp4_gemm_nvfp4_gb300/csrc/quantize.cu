@@ -64,6 +64,7 @@ struct RowArgs {
     uint32_t mask;
     PhiloxKeys keys;             // SR round keys of the seed
     uint64_t stream;
+    bool s46;                    // 4/6 adaptive block scales (block_scale_46)
 };
 
 // One thread = one 1x16 block: two 16-byte loads, RHT in registers (optional),
@@ -105,7 +106,9 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
         } else {
             if (fold) amax_b = __fmul_rn(amax_b, 0.25f);
             float r_b;
-            const uint32_t sc = block_scale_tab(amax_b, ts.s_enc, rb_table, &r_b);
+            const uint32_t sc =
+                a.s46 ? block_scale_46(t, amax_b, ts.s_enc, fold ? __fmul_rn(ts.s_enc, 0.25f) : ts.s_enc, rb_table, &r_b)
+                      : block_scale_tab(amax_b, ts.s_enc, rb_table, &r_b);
             const uint64_t idx = (uint64_t)r * ((uint64_t)a.bpr * 16u) + (uint64_t)j * 16u;
             const uint2 q = encode16<kSR>(t, r_b, keys, a.stream, idx);
             *reinterpret_cast<uint2*>(a.out.codes + (int64_t)r * a.out.ld_codes + (int64_t)j * 8) = q;
@@ -326,6 +329,7 @@ struct PairArgs {
     uint32_t mask;
     PhiloxKeys keys;             // SR round keys of the seed
     uint64_t stream_row, stream_col;
+    bool s46;                    // 4/6 adaptive block scales (block_scale_46), both orientations
 };
 
 constexpr int kPairSlots = 2;
@@ -422,8 +426,15 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                     m1 = __fmul_rn(m1, 0.25f);
                 }
                 float rb0, rb1;
-                const uint32_t sc0 = block_scale_tab(m0, ts_col.s_enc, rb_col, &rb0);
-                const uint32_t sc1 = block_scale_tab(m1, ts_col.s_enc, rb_col, &rb1);
+                uint32_t sc0, sc1;
+                if (a.s46) {
+                    const float xs_mult = fold ? __fmul_rn(ts_col.s_enc, 0.25f) : ts_col.s_enc;
+                    sc0 = block_scale_46(t0, m0, ts_col.s_enc, xs_mult, rb_col, &rb0);
+                    sc1 = block_scale_46(t1, m1, ts_col.s_enc, xs_mult, rb_col, &rb1);
+                } else {
+                    sc0 = block_scale_tab(m0, ts_col.s_enc, rb_col, &rb0);
+                    sc1 = block_scale_tab(m1, ts_col.s_enc, rb_col, &rb1);
+                }
                 const uint2 q0 = encode16<kSR>(t0, rb0, keys, a.stream_col, (uint64_t)c * a.rows + r0);
                 const uint2 q1 = encode16<kSR>(t1, rb1, keys, a.stream_col, (uint64_t)(c + 1) * a.rows + r0);
                 *reinterpret_cast<uint2*>(a.col.codes + (int64_t)c * a.col.ld_codes + r0 / 2) = q0;
@@ -460,7 +471,8 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
 #pragma unroll
                     for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[16 * jj + e]));
                     float rb;
-                    sc[jj] = block_scale_tab(m, ts_row.s_enc, rb_row, &rb);
+                    sc[jj] = a.s46 ? block_scale_46(v + 16 * jj, m, ts_row.s_enc, ts_row.s_enc, rb_row, &rb)
+                                   : block_scale_tab(m, ts_row.s_enc, rb_row, &rb);
                     q[jj] = encode16<kSR>(v + 16 * jj, rb, keys, a.stream_row,
                                           (uint64_t)r * a.cols + cb + 16u * (uint32_t)jj);
                 }
@@ -666,7 +678,7 @@ int row_amax(const RowArgs& base, float* partials, cudaStream_t st) {
 cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool sr, bool col_rht,
                                uint32_t sign_mask, uint64_t seed, uint64_t stream_row, uint64_t stream_col,
                                const QuantTarget* row, const QuantTarget* col, const float* part_row,
-                               const float* part_col, int n_partials, cudaStream_t st) {
+                               const float* part_col, int n_partials, bool s46, cudaStream_t st) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     CUtensorMap tmap;
@@ -694,6 +706,7 @@ cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, in
     pa.keys = philox_keys(seed);
     pa.stream_row = stream_row;
     pa.stream_col = stream_col;
+    pa.s46 = s46;
     const int64_t ntiles = (int64_t)pa.tiles_r * pa.tiles_c;
     auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(tmap, pa); };
     if (sr && col_rht) launch(pair_encode_kernel<true, true>);
@@ -705,7 +718,8 @@ cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, in
 
 }  // namespace
 
-cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool scale_2d, bool sr,
+cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool scale_2d, bool scale_46,
+                            bool sr,
                             bool rht, uint32_t sign_mask, uint64_t seed, uint64_t stream_id,
                             const QuantTarget* row, const QuantTarget* col, float* workspace,
                             cudaStream_t st) {
@@ -721,6 +735,7 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
     ra.mask = sign_mask;
     ra.keys = philox_keys(seed);
     ra.stream = stream_id;
+    ra.s46 = scale_46;
 
     ColArgs ca{};
     ca.x = x;
@@ -810,7 +825,7 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
     }
     if (col)
         return launch_pair_encode(x, rows, cols, ld_x, sr, rht, sign_mask, seed, stream_id, stream_id,
-                                  joint ? row : nullptr, col, part_a, part_b, joint ? n_row : n_col, st);
+                                  joint ? row : nullptr, col, part_a, part_b, joint ? n_row : n_col, scale_46, st);
     return cudaGetLastError();
 }
 

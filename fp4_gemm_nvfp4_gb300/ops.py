@@ -85,9 +85,10 @@ def _workspace(device) -> Workspace:
 def quantize(x: torch.Tensor, *, two_d: bool = False, sr: bool = False, rht_mask: Optional[int] = None,
              seed: int = 0, stream_id: int = 0, rowwise: bool = True, colwise: bool = False,
              out_row: Optional[NVFP4Operand] = None, out_col: Optional[NVFP4Operand] = None,
-             workspace: Optional[Workspace] = None, stream=None
+             workspace: Optional[Workspace] = None, stream=None, scale46: bool = False
              ) -> Tuple[Optional[NVFP4Operand], Optional[NVFP4Operand]]:
-    """Quantize a bf16 CUDA matrix (nvfp4_quantize / nvfp4_rht_quantize)."""
+    """Quantize a bf16 CUDA matrix (nvfp4_quantize / nvfp4_rht_quantize).
+    scale46 selects 1x16 blocks with 4/6 adaptive scales (NVFP4_SCALE_1X16_46)."""
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     rows, cols = x.shape
     if rowwise and out_row is None:
@@ -97,7 +98,7 @@ def quantize(x: torch.Tensor, *, two_d: bool = False, sr: bool = False, rht_mask
     ws = workspace or _workspace(x.device)
     orient = (capi.NVFP4_ROWWISE if rowwise else 0) | (capi.NVFP4_COLWISE if colwise else 0)
     sr_ = capi.NVFP4_ROUND_SR if sr else capi.NVFP4_ROUND_RNE
-    sc = capi.NVFP4_SCALE_16X16 if two_d else capi.NVFP4_SCALE_1X16
+    sc = capi.NVFP4_SCALE_16X16 if two_d else (capi.NVFP4_SCALE_1X16_46 if scale46 else capi.NVFP4_SCALE_1X16)
     trow = out_row.struct() if rowwise else None
     tcol = out_col.struct() if colwise else None
     st = stream_handle(stream)

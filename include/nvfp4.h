@@ -117,7 +117,15 @@ typedef enum {
     NVFP4_ERR_WORKSPACE = 7      /* workspace missing or too small */
 } nvfp4_status;
 
-typedef enum { NVFP4_SCALE_1X16 = 0, NVFP4_SCALE_16X16 = 1 } nvfp4_scaling;
+/* Block scaling.  NVFP4_SCALE_1X16_46 is 1x16 blocks with 4/6 adaptive
+ * scaling [FS related work: 4/6 scaling, MSE-optimal adaptive block scales;
+ * the rule is not printed there]: each block is encoded with its amax mapped
+ * to 6 (the plain 1x16 scale) and with its amax mapped to 4 (scale
+ * E4M3(RN(amax_b / 4) * S_enc)), both with RNE, and keeps the candidate with
+ * the smaller sum_i (x_i * S_enc - e2m1(q_i) * s)^2 (binary32, index order,
+ * fused multiply-adds; the 6 candidate on a tie); with SR the chosen scale is
+ * then used for the stochastic encode.  The output format is unchanged. */
+typedef enum { NVFP4_SCALE_1X16 = 0, NVFP4_SCALE_16X16 = 1, NVFP4_SCALE_1X16_46 = 2 } nvfp4_scaling;
 typedef enum { NVFP4_ROUND_RNE = 0, NVFP4_ROUND_SR = 1 } nvfp4_rounding;
 typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_FP32 = 1 } nvfp4_dtype;
 enum { NVFP4_ROWWISE = 1, NVFP4_COLWISE = 2 };   /* bit mask of orientations to emit */
@@ -141,7 +149,8 @@ NVFP4_API size_t nvfp4_quantize_workspace_size(int64_t rows, int64_t cols, int o
 /*
  * nvfp4_quantize -- quantize x (bf16, [rows][ld_x], row-major) to NVFP4
  * without the Hadamard transform [FS Sec. 2; NV Sec. 2, Sec. 4].
- *  scaling      1x16 blocks (activations, gradients) or 16x16 tiles (weights).
+ *  scaling      1x16 blocks (activations, gradients), 1x16 blocks with 4/6
+ *               adaptive scales, or 16x16 tiles (weights).
  *  rounding     RNE (weights, activations) or SR (gradients).
  *  seed, stream_id  select the Philox stream of SR (ignored for RNE); use a
  *               different stream_id for each quantization of one tensor.

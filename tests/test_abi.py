@@ -89,7 +89,8 @@ def test_quantize_validation(lib):
     assert quantize(x=None) == E.NVFP4_ERR_INVALID_ARG
     assert quantize(orientations=0) == E.NVFP4_ERR_INVALID_ARG
     assert quantize(orientations=4) == E.NVFP4_ERR_INVALID_ARG
-    assert quantize(scaling=2) == E.NVFP4_ERR_INVALID_ARG
+    assert quantize(scaling=3) == E.NVFP4_ERR_INVALID_ARG
+    assert quantize(scaling=2, orientations=2, rows=24, out_col=tensor(64, 24)) == E.NVFP4_ERR_SHAPE   # 4/6 is 1x16
     assert quantize(rounding=5) == E.NVFP4_ERR_INVALID_ARG
     assert quantize(out_row=None) == E.NVFP4_ERR_INVALID_ARG
     assert quantize(out_row=tensor(64, 32)) == E.NVFP4_ERR_INVALID_ARG               # wrong shape

@@ -23,7 +23,7 @@ def library():
 def gpu_quantize(bits, orientation, scaling=0, rounding=0, use_rht=False, sign_mask=0, seed=0,
                  stream_id=0):
     x = helpers.to_device_bf16(bits)
-    row, col = ops.quantize(x, two_d=scaling == 1, sr=rounding == 1,
+    row, col = ops.quantize(x, two_d=scaling == 1, scale46=scaling == 2, sr=rounding == 1,
                             rht_mask=sign_mask if use_rht else None, seed=seed, stream_id=stream_id,
                             rowwise=orientation == oracle.ROWWISE, colwise=orientation == oracle.COLWISE)
     torch.cuda.synchronize()
@@ -48,8 +48,9 @@ def assert_parity(bits, orientation, rows_subset=None, **kw):
 
 
 MODES = [
-    # (scaling, rounding, rht)
+    # (scaling, rounding, rht); scaling 2 = 1x16 with 4/6 adaptive scales
     (0, 0, False), (0, 1, False), (0, 0, True), (0, 1, True), (1, 0, False), (1, 1, False),
+    (2, 0, False), (2, 1, False), (2, 0, True), (2, 1, True),
 ]
 
 
@@ -96,10 +97,12 @@ def test_quantize_ties_and_negative_zero():
 def test_quantize_both_orientations_in_one_call():
     bits = inputs.normal(256, 320, seed=44, outlier_channels=3)
     x = helpers.to_device_bf16(bits)
-    for kw in (dict(), dict(sr=True, seed=4), dict(rht_mask=0x0F0F), dict(two_d=True)):
+    for kw in (dict(), dict(sr=True, seed=4), dict(rht_mask=0x0F0F), dict(two_d=True), dict(scale46=True),
+               dict(scale46=True, sr=True, seed=6), dict(scale46=True, rht_mask=0x3C3C)):
         row, col = ops.quantize(x, rowwise=True, colwise=True, stream_id=2, **kw)
         torch.cuda.synchronize()
-        common = dict(scaling=1 if kw.get("two_d") else 0, rounding=1 if kw.get("sr") else 0,
+        common = dict(scaling=1 if kw.get("two_d") else (2 if kw.get("scale46") else 0),
+                      rounding=1 if kw.get("sr") else 0,
                       use_rht="rht_mask" in kw, sign_mask=kw.get("rht_mask", 0),
                       seed=kw.get("seed", 0), stream_id=2)
         for op, orient in ((row, oracle.ROWWISE), (col, oracle.COLWISE)):
@@ -135,6 +138,8 @@ def _ranges(n, k=48):
     ("c3_dY_col", 8192, 9216, "grad", oracle.COLWISE, 0, 1, True),
     ("c3_X_col", 8192, 3072, "normal", oracle.COLWISE, 0, 0, True),
     ("c4_dY_row", 16384, 3072, "grad", oracle.ROWWISE, 0, 1, False),
+    ("c4_H_46_row", 16384, 9216, "normal", oracle.ROWWISE, 2, 0, False),
+    ("c3_dY_46_col", 8192, 9216, "grad", oracle.COLWISE, 2, 1, True),
 ])
 def test_quantize_parity_full_size(name, rows, cols, kind, orientation, scaling, rounding, rht):
     seed = zlib.crc32(name.encode()) % 1000
