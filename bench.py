@@ -154,10 +154,8 @@ def quant_bytes(rows, cols, kw):
     outs = int(kw.get("rowwise", True)) + int(kw.get("colwise", False))
     if kw.get("rht_mask") is not None:      # one amax and one encode pass per orientation
         amax_passes, encode_reads = outs, outs
-    elif kw.get("two_d"):                   # one encode pass emits both orientations
-        amax_passes, encode_reads = 1, 1
-    else:
-        amax_passes, encode_reads = 1, outs
+    else:                                   # one encode pass emits both orientations (16x16, or 1x16
+        amax_passes, encode_reads = 1, 1    # row + col through the slice-staged pair kernel)
     return n * 2 * (amax_passes + encode_reads) + n * outs * (0.5 + 1 / 16)
 
 
@@ -520,7 +518,8 @@ def reference_arm(args):
 
 def sweep_c5(args):
     """Quantizer bandwidth sweep: 2^20..2^29 elements at row lengths 3072,
-    9216 and 8192, Student-t(3) values, three modes.  One JSON line per case;
+    9216 and 8192, Student-t(3) values, five modes (the last two with 4/6
+    adaptive block scales).  One JSON line per case;
     L2 is flushed before every timed call (a write of twice its size)."""
     import torch
     torch.cuda.set_device(0)
@@ -536,7 +535,9 @@ def sweep_c5(args):
     mask = inputs.rht_sign_mask(5)
     modes = [("1x16_rne", dict(rowwise=True)),
              ("16x16_rne", dict(rowwise=True, colwise=True, two_d=True)),
-             ("rht_1x16_sr", dict(rowwise=True, sr=True, rht_mask=mask, seed=5))]
+             ("rht_1x16_sr", dict(rowwise=True, sr=True, rht_mask=mask, seed=5)),
+             ("1x16_46_rne", dict(rowwise=True, scale46=True)),
+             ("rht_1x16_46_sr", dict(rowwise=True, sr=True, rht_mask=mask, seed=5, scale46=True))]
     stream = torch.cuda.current_stream()
     for rows, L in inputs.c5_sweep_sizes():
         x = torch.empty((rows, L), dtype=torch.bfloat16, device="cuda")
