@@ -64,12 +64,12 @@ struct RowArgs {
     uint32_t mask;
     PhiloxKeys keys;             // SR round keys of the seed
     uint64_t stream;
-    bool s46;                    // 4/6 adaptive block scales (block_scale_46)
 };
 
 // One thread = one 1x16 block: two 16-byte loads, RHT in registers (optional),
 // block amax, E4M3 scale, 8 bytes of codes.
-template <Pass P, bool kRHT, bool kSR>
+// kS46: 4/6 adaptive block scales (block_scale_46).
+template <Pass P, bool kRHT, bool kSR, bool kS46 = false>
 __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
     __shared__ float red[32];
     __shared__ float rb_table[128];
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
             if (fold) amax_b = __fmul_rn(amax_b, 0.25f);
             float r_b;
             const uint32_t sc =
-                a.s46 ? block_scale_46(t, amax_b, ts.s_enc, fold ? __fmul_rn(ts.s_enc, 0.25f) : ts.s_enc, rb_table, &r_b)
+                kS46 ? block_scale_46(t, amax_b, ts.s_enc, fold ? __fmul_rn(ts.s_enc, 0.25f) : ts.s_enc, rb_table, &r_b)
                       : block_scale_tab(amax_b, ts.s_enc, rb_table, &r_b);
             const uint64_t idx = (uint64_t)r * ((uint64_t)a.bpr * 16u) + (uint64_t)j * 16u;
             const uint2 q = encode16<kSR>(t, r_b, keys, a.stream, idx);
@@ -329,7 +329,6 @@ struct PairArgs {
     uint32_t mask;
     PhiloxKeys keys;             // SR round keys of the seed
     uint64_t stream_row, stream_col;
-    bool s46;                    // 4/6 adaptive block scales (block_scale_46), both orientations
 };
 
 constexpr int kPairSlots = 2;
@@ -337,7 +336,8 @@ constexpr uint32_t kSliceBytes = 16 * 128;   // 16 rows x 64 bf16
 
 // kColRHT: the col-wise operand gets the RHT (else none); the row-wise
 // operand never does.  Either orientation may be left out (emit_*).
-template <bool kSR, bool kColRHT>
+// kS46: 4/6 adaptive block scales (block_scale_46) in both orientations.
+template <bool kSR, bool kColRHT, bool kS46 = false>
 __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                                const PairArgs a) {
     __shared__ float red[32];
@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                 }
                 float rb0, rb1;
                 uint32_t sc0, sc1;
-                if (a.s46) {
+                if constexpr (kS46) {
                     const float xs_mult = fold ? __fmul_rn(ts_col.s_enc, 0.25f) : ts_col.s_enc;
                     sc0 = block_scale_46(t0, m0, ts_col.s_enc, xs_mult, rb_col, &rb0);
                     sc1 = block_scale_46(t1, m1, ts_col.s_enc, xs_mult, rb_col, &rb1);
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
 #pragma unroll
                     for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[16 * jj + e]));
                     float rb;
-                    sc[jj] = a.s46 ? block_scale_46(v + 16 * jj, m, ts_row.s_enc, ts_row.s_enc, rb_row, &rb)
+                    sc[jj] = kS46 ? block_scale_46(v + 16 * jj, m, ts_row.s_enc, ts_row.s_enc, rb_row, &rb)
                                    : block_scale_tab(m, ts_row.s_enc, rb_row, &rb);
                     q[jj] = encode16<kSR>(v + 16 * jj, rb, keys, a.stream_row,
                                           (uint64_t)r * a.cols + cb + 16u * (uint32_t)jj);
@@ -706,13 +706,19 @@ cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, in
     pa.keys = philox_keys(seed);
     pa.stream_row = stream_row;
     pa.stream_col = stream_col;
-    pa.s46 = s46;
     const int64_t ntiles = (int64_t)pa.tiles_r * pa.tiles_c;
     auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(tmap, pa); };
-    if (sr && col_rht) launch(pair_encode_kernel<true, true>);
-    else if (col_rht) launch(pair_encode_kernel<false, true>);
-    else if (sr) launch(pair_encode_kernel<true, false>);
-    else launch(pair_encode_kernel<false, false>);
+    if (s46) {
+        if (sr && col_rht) launch(pair_encode_kernel<true, true, true>);
+        else if (col_rht) launch(pair_encode_kernel<false, true, true>);
+        else if (sr) launch(pair_encode_kernel<true, false, true>);
+        else launch(pair_encode_kernel<false, false, true>);
+    } else {
+        if (sr && col_rht) launch(pair_encode_kernel<true, true>);
+        else if (col_rht) launch(pair_encode_kernel<false, true>);
+        else if (sr) launch(pair_encode_kernel<true, false>);
+        else launch(pair_encode_kernel<false, false>);
+    }
     return cudaGetLastError();
 }
 
@@ -735,7 +741,6 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
     ra.mask = sign_mask;
     ra.keys = philox_keys(seed);
     ra.stream = stream_id;
-    ra.s46 = scale_46;
 
     ColArgs ca{};
     ca.x = x;
@@ -818,10 +823,17 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
         auto launch = [&](auto k) {
             k<<<persistent_grid(k, ((int64_t)r.total + kThreads - 1) / kThreads), kThreads, 0, st>>>(r);
         };
-        if (rht && sr) launch(rowwise_kernel<Pass::kEncode, true, true>);
-        else if (rht) launch(rowwise_kernel<Pass::kEncode, true, false>);
-        else if (sr) launch(rowwise_kernel<Pass::kEncode, false, true>);
-        else launch(rowwise_kernel<Pass::kEncode, false, false>);
+        if (scale_46) {
+            if (rht && sr) launch(rowwise_kernel<Pass::kEncode, true, true, true>);
+            else if (rht) launch(rowwise_kernel<Pass::kEncode, true, false, true>);
+            else if (sr) launch(rowwise_kernel<Pass::kEncode, false, true, true>);
+            else launch(rowwise_kernel<Pass::kEncode, false, false, true>);
+        } else {
+            if (rht && sr) launch(rowwise_kernel<Pass::kEncode, true, true>);
+            else if (rht) launch(rowwise_kernel<Pass::kEncode, true, false>);
+            else if (sr) launch(rowwise_kernel<Pass::kEncode, false, true>);
+            else launch(rowwise_kernel<Pass::kEncode, false, false>);
+        }
     }
     if (col)
         return launch_pair_encode(x, rows, cols, ld_x, sr, rht, sign_mask, seed, stream_id, stream_id,
