@@ -58,6 +58,9 @@ def lib():
                                            i32, f32, i64, i64, vp, vp]
         L.oracle_quantize_rows.restype = i32
         L.oracle_dequantize.argtypes = [vp, vp, f32, i64, i64, vp]
+        L.oracle_requantize_col_rht.argtypes = [vp, vp, f32, i64, i64, i32, u16, u64, u64, f32, i64, i64,
+                                                vp, vp, vp]
+        L.oracle_requantize_col_rht.restype = i32
         L.oracle_dequantize.restype = None
         L.oracle_round_bf16.argtypes, L.oracle_round_bf16.restype = [f64], u16
         L.oracle_gemm_f64.argtypes = [vp, vp, f32, vp, vp, f32, i64, i64, i64, vp, i64, vp, vp]
@@ -196,6 +199,31 @@ def quantize(x_bits, orientation=ROWWISE, scaling=0, rounding=0, use_rht=False,
     s_enc, s_g = tensor_scale(amax_value)
     return dict(codes=codes, scales=scales, amax=np.float32(amax_value), s_enc=s_enc,
                 s_g=s_g, rows=(lr0, lr1))
+
+
+def requantize_col_rht(q_row, sign_mask, rounding=0, seed=0, stream_id=0, rows_subset=None,
+                       amax_value=None):
+    """Wgrad's second operand from a row-wise operand (a dict from quantize()):
+    dequantize, RHT along the rows, col-wise 1x16 quantization ("Full-Stack
+    FP4", Sec. 3.2 Eq. (2)).  Returns the same dict as quantize() for the
+    [cols][rows] output."""
+    codes = _c(q_row["codes"], np.uint8)
+    scales = _c(q_row["scales"], np.uint8)
+    rows, cols = codes.shape[0], codes.shape[1] * 2
+    lr0, lr1 = (0, cols) if rows_subset is None else rows_subset
+    n = lr1 - lr0
+    out_codes = np.zeros((n, rows // 2), np.uint8)
+    out_scales = np.zeros((n, rows // 16), np.uint8)
+    amax_out = np.zeros(1, np.float32)
+    rc = lib().oracle_requantize_col_rht(_ptr(codes), _ptr(scales), float(q_row["s_g"]), rows, cols,
+                                         int(rounding), int(sign_mask), int(seed), int(stream_id),
+                                         -1.0 if amax_value is None else float(amax_value), lr0, lr1,
+                                         _ptr(out_codes), _ptr(out_scales), _ptr(amax_out))
+    if rc != 0:
+        raise ValueError(f"oracle_requantize_col_rht rejected the arguments (code {rc})")
+    s_enc, s_g = tensor_scale(amax_out[0])
+    return dict(codes=out_codes, scales=out_scales, amax=np.float32(amax_out[0]), s_enc=s_enc, s_g=s_g,
+                rows=(lr0, lr1))
 
 
 def dequantize(codes, scales, s_g):

@@ -29,6 +29,7 @@
 
 #include <float.h>
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #ifdef _OPENMP
@@ -209,16 +210,39 @@ static float bf16_bits_to_float(uint16_t h)
     return f;
 }
 
+/* The matrix being quantized: bf16 bit patterns, or binary32 values (a
+ * dequantized operand), [rows][ld] row-major. */
+struct source {
+    const uint16_t *bf16;
+    const float *f32;
+    int64_t ld;
+};
+
+static float src_elem(const struct source *x, int64_t r, int64_t c)
+{
+    return x->f32 ? x->f32[r * x->ld + c] : bf16_bits_to_float(x->bf16[r * x->ld + c]);
+}
+
 /* Element j of logical row lr of one orientation. */
-static float logical_elem(const uint16_t *x, int64_t ld, int orientation, int64_t lr, int64_t j)
+static float logical_elem(const struct source *x, int orientation, int64_t lr, int64_t j)
 {
     if (orientation == ORACLE_ROWWISE)
-        return bf16_bits_to_float(x[lr * ld + j]);
-    return bf16_bits_to_float(x[j * ld + lr]);
+        return src_elem(x, lr, j);
+    return src_elem(x, j, lr);
 }
+
+static float amax_src(const struct source *x, int64_t rows, int64_t cols,
+                      int orientation, int use_rht, uint16_t sign_mask);
 
 float oracle_amax(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld,
                   int orientation, int use_rht, uint16_t sign_mask)
+{
+    struct source src = {x, NULL, ld};
+    return amax_src(&src, rows, cols, orientation, use_rht, sign_mask);
+}
+
+static float amax_src(const struct source *x, int64_t rows, int64_t cols,
+                      int orientation, int use_rht, uint16_t sign_mask)
 {
     int64_t lrows = (orientation == ORACLE_ROWWISE) ? rows : cols;
     int64_t lcols = (orientation == ORACLE_ROWWISE) ? cols : rows;
@@ -227,7 +251,7 @@ float oracle_amax(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld,
 #pragma omp parallel for reduction(max : amax) schedule(static)
         for (int64_t r = 0; r < rows; ++r)
             for (int64_t c = 0; c < cols; ++c) {
-                float a = fabsf(bf16_bits_to_float(x[r * ld + c]));
+                float a = fabsf(src_elem(x, r, c));
                 if (a > amax)
                     amax = a;
             }
@@ -240,7 +264,7 @@ float oracle_amax(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld,
         for (int64_t b = 0; b < lcols / 16; ++b) {
             float blk[16], rot[16];
             for (int t = 0; t < 16; ++t)
-                blk[t] = logical_elem(x, ld, orientation, lr, 16 * b + t);
+                blk[t] = logical_elem(x, orientation, lr, 16 * b + t);
             oracle_rht16(blk, sign_mask, rot);
             for (int t = 0; t < 16; ++t) {
                 float a = fabsf(rot[t]);
@@ -252,11 +276,28 @@ float oracle_amax(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld,
     return amax;
 }
 
+static int quantize_src(const struct source *x, int64_t rows, int64_t cols,
+                        int scaling, int rounding, int use_rht, uint16_t sign_mask,
+                        uint64_t seed, uint64_t stream_id, int orientation,
+                        float amax, int64_t lr0, int64_t lr1,
+                        uint8_t *codes, uint8_t *scales);
+
 int oracle_quantize_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld,
                          int scaling, int rounding, int use_rht, uint16_t sign_mask,
                          uint64_t seed, uint64_t stream_id, int orientation,
                          float amax, int64_t lr0, int64_t lr1,
                          uint8_t *codes, uint8_t *scales)
+{
+    struct source src = {x, NULL, ld};
+    return quantize_src(&src, rows, cols, scaling, rounding, use_rht, sign_mask, seed, stream_id,
+                        orientation, amax, lr0, lr1, codes, scales);
+}
+
+static int quantize_src(const struct source *x, int64_t rows, int64_t cols,
+                        int scaling, int rounding, int use_rht, uint16_t sign_mask,
+                        uint64_t seed, uint64_t stream_id, int orientation,
+                        float amax, int64_t lr0, int64_t lr1,
+                        uint8_t *codes, uint8_t *scales)
 {
     if (orientation != ORACLE_ROWWISE && orientation != ORACLE_COLWISE)
         return 1;
@@ -282,7 +323,7 @@ int oracle_quantize_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t 
         for (int64_t b = 0; b < nblk; ++b) {
             float blk[16];
             for (int t = 0; t < 16; ++t)
-                blk[t] = logical_elem(x, ld, orientation, lr, 16 * b + t);
+                blk[t] = logical_elem(x, orientation, lr, 16 * b + t);
             if (use_rht) {
                 float rot[16];
                 oracle_rht16(blk, sign_mask, rot);
@@ -301,7 +342,7 @@ int oracle_quantize_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t 
                 int64_t c0 = (orientation == ORACLE_ROWWISE) ? 16 * b : (lr / 16) * 16;
                 for (int64_t i = 0; i < 16; ++i)
                     for (int64_t j = 0; j < 16; ++j) {
-                        float a = fabsf(bf16_bits_to_float(x[(r0 + i) * ld + c0 + j]));
+                        float a = fabsf(src_elem(x, r0 + i, c0 + j));
                         if (a > amax_b)
                             amax_b = a;
                     }
@@ -382,6 +423,47 @@ void oracle_dequantize(const uint8_t *codes, const uint8_t *scales, float s_g,
             double s = oracle_e4m3_value(scales[r * (cols / 16) + c / 16]);
             out[r * cols + c] = oracle_e2m1_value(code) * s * (double)s_g;
         }
+}
+
+/* ------------------------------------------------------------------ */
+/* Wgrad's second operand re-quantized from the forward's quantized input
+ * ("Full-Stack FP4", Sec. 3.2 Eq. (2): Q_16x1(H16^T Q_1x16(X))).  The row-wise
+ * operand (codes [rows][cols/2], scales [rows][cols/16] row-major, s_g) is
+ * dequantized to binary32, x^ = RN(RN(e2m1 * s_b) * s_g) (the first product is
+ * exact), and then quantized like oracle_quantize_rows with the RHT in the
+ * COLWISE orientation: 16 consecutive rows of a column form a block, the
+ * output is [cols][rows] (K-major along rows).  amax < 0 asks for the tensor
+ * amax of the rotated dequantized values; it is returned in *amax_out. */
+int oracle_requantize_col_rht(const uint8_t *codes, const uint8_t *scales, float s_g,
+                              int64_t rows, int64_t cols, int rounding, uint16_t sign_mask,
+                              uint64_t seed, uint64_t stream_id, float amax,
+                              int64_t lr0, int64_t lr1, uint8_t *out_codes, uint8_t *out_scales,
+                              float *amax_out)
+{
+    if (rows % 16 != 0 || cols % 16 != 0)
+        return 2;
+    float *xf = (float *)malloc((size_t)(rows * cols) * sizeof(float));
+    if (!xf)
+        return 6;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            uint8_t byte = codes[r * (cols / 2) + c / 2];
+            uint8_t code = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xFu);
+            float g = (float)oracle_e2m1_value(code);
+            float sb = (float)oracle_e4m3_value(scales[r * (cols / 16) + c / 16]);
+            float gs = g * sb;
+            xf[r * cols + c] = gs * s_g;
+        }
+    struct source src = {NULL, xf, cols};
+    if (amax < 0.0f)
+        amax = amax_src(&src, rows, cols, ORACLE_COLWISE, 1, sign_mask);
+    if (amax_out)
+        *amax_out = amax;
+    int rc = quantize_src(&src, rows, cols, 0, rounding, 1, sign_mask, seed, stream_id, ORACLE_COLWISE,
+                          amax, lr0, lr1, out_codes, out_scales);
+    free(xf);
+    return rc;
 }
 
 uint16_t oracle_round_bf16(double v)

@@ -113,6 +113,20 @@ void oracle_e4m3_rne_satfinite_array(const float *x, int64_t n, uint8_t *codes);
 /* Threads the OpenMP loops use (1 without OpenMP). */
 int oracle_num_threads(void);
 
+/*
+ * Wgrad's second operand from the forward's quantized input ("Full-Stack
+ * FP4", Sec. 3.2 Eq. (2)): dequantize the row-wise 1x16 operand (codes
+ * [rows][cols/2], row-major scales [rows][cols/16], s_g) to binary32, apply
+ * the RHT along the rows and quantize col-wise with 1x16 blocks along the
+ * rows.  Logical rows [lr0, lr1) of the [cols][rows] output; amax < 0
+ * computes the tensor amax (returned in *amax_out).  Returns 0 on success.
+ */
+int oracle_requantize_col_rht(const uint8_t *codes, const uint8_t *scales, float s_g,
+                              int64_t rows, int64_t cols, int rounding, uint16_t sign_mask,
+                              uint64_t seed, uint64_t stream_id, float amax,
+                              int64_t lr0, int64_t lr1, uint8_t *out_codes, uint8_t *out_scales,
+                              float *amax_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -550,6 +550,41 @@ def test_46_sr_uses_the_rne_choice_of_scale():
     assert not np.array_equal(rne["codes"], sr["codes"])
 
 
+# ------------------------------------------ Wgrad re-quantization (Eq. 2) ----
+@pytest.mark.parametrize("k", [0, 2])
+@pytest.mark.parametrize("rounding", [0, 1])
+def test_requantize_equals_quantizing_the_dequantized_values(k, rounding):
+    """With s_g a power of two (tensor amax 2688 * 2^k) every dequantized value
+    e2m1 * s_b * s_g has at most 6 significant bits, so it is a bf16 value, and
+    re-quantizing the operand must equal the (separately pinned) col-wise RHT
+    quantization of those bf16 values ("Full-Stack FP4", Sec. 3.2 Eq. (2):
+    Q_16x1(H^T Q_1x16(X)))."""
+    xf = inputs.bf16_bits_to_f32(inputs.normal(96, 64, 40 + k, outlier_channels=1)).copy()
+    xf[5, 7] = 2688.0 * 2 ** k
+    x = inputs.to_bf16_bits(xf)
+    q = oracle.quantize(x)
+    assert float(q["s_g"]) == 2.0 ** k
+    xhat = oracle.dequantize(q["codes"], q["scales"], q["s_g"])
+    bits = inputs.to_bf16_bits(xhat.astype(np.float32))
+    assert np.array_equal(inputs.bf16_bits_to_f32(bits).astype(np.float64), xhat)
+    want = oracle.quantize(bits, oracle.COLWISE, rounding=rounding, use_rht=True, sign_mask=0x6C39,
+                           seed=9, stream_id=4)
+    got = oracle.requantize_col_rht(q, 0x6C39, rounding=rounding, seed=9, stream_id=4)
+    assert got["amax"] == want["amax"]
+    assert np.array_equal(got["codes"], want["codes"]) and np.array_equal(got["scales"], want["scales"])
+
+
+def test_requantize_row_subset_and_zero_operand():
+    q = oracle.quantize(_rand_bits(64, 48, 41, outliers=1))
+    full = oracle.requantize_col_rht(q, 0x0F0F, rounding=1, seed=2)
+    part = oracle.requantize_col_rht(q, 0x0F0F, rounding=1, seed=2, rows_subset=(16, 40))
+    assert np.array_equal(full["codes"][16:40], part["codes"])
+    assert np.array_equal(full["scales"][16:40], part["scales"])
+    z = oracle.requantize_col_rht(oracle.quantize(np.zeros((32, 32), np.uint16)), 0xFFFF)
+    # all values zero (the sign flips of the RHT leave negative zeros, code 0x8)
+    assert z["amax"] == 0 and not (z["codes"] & 0x77).any() and not z["scales"].any()
+
+
 # ---------------------------------------------------------- dequantize ----
 def test_dequantize_grid_values():
     codes4 = np.arange(16, dtype=np.uint8)
