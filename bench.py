@@ -518,8 +518,9 @@ def reference_arm(args):
 
 def sweep_c5(args):
     """Quantizer bandwidth sweep: 2^20..2^29 elements at row lengths 3072,
-    9216 and 8192, Student-t(3) values, five modes (the last two with 4/6
-    adaptive block scales).  One JSON line per case;
+    9216 and 8192, Student-t(3) values, six modes (two with 4/6 adaptive
+    block scales; the last re-quantizes the row-wise operand of x into the
+    col-wise RHT operand).  One JSON line per case;
     L2 is flushed before every timed call (a write of twice its size)."""
     import torch
     torch.cuda.set_device(0)
@@ -537,7 +538,8 @@ def sweep_c5(args):
              ("16x16_rne", dict(rowwise=True, colwise=True, two_d=True)),
              ("rht_1x16_sr", dict(rowwise=True, sr=True, rht_mask=mask, seed=5)),
              ("1x16_46_rne", dict(rowwise=True, scale46=True)),
-             ("rht_1x16_46_sr", dict(rowwise=True, sr=True, rht_mask=mask, seed=5, scale46=True))]
+             ("rht_1x16_46_sr", dict(rowwise=True, sr=True, rht_mask=mask, seed=5, scale46=True)),
+             ("requant_col_rht_sr", dict(requant=True, rht_mask=mask, seed=5))]
     stream = torch.cuda.current_stream()
     for rows, L in inputs.c5_sweep_sizes():
         x = torch.empty((rows, L), dtype=torch.bfloat16, device="cuda")
@@ -550,8 +552,16 @@ def sweep_c5(args):
         n = rows * L
         for name, kw in modes:
             row = ops.alloc_operand(rows, L)
-            col = ops.alloc_operand(L, rows) if kw.get("colwise") else None
-            run = lambda: ops.quantize(x, out_row=row, out_col=col, workspace=ws, **kw)
+            if kw.get("requant"):
+                # Wgrad's operand re-quantized from the row-wise operand of x
+                # (input: 0.5625 B per element, read by both passes)
+                ops.quantize(x, out_row=row, workspace=ws)
+                col = ops.alloc_operand(L, rows)
+                run = lambda: ops.requantize_col_rht(row, kw["rht_mask"], sr=True, seed=kw["seed"], out_col=col,
+                                                     workspace=ws)
+            else:
+                col = ops.alloc_operand(L, rows) if kw.get("colwise") else None
+                run = lambda: ops.quantize(x, out_row=row, out_col=col, workspace=ws, **kw)
             for _ in range(max(args.warmup, 5)):
                 run()
             times = []
@@ -565,9 +575,13 @@ def sweep_c5(args):
                 e1.synchronize()
                 times.append(e0.elapsed_time(e1))
             ms = statistics.median(times)
-            outs = 1 + int(bool(kw.get("colwise")))
-            unique = n * (2 + outs * (0.5 + 1 / 16))
-            alg = quant_bytes(rows, L, kw)
+            if kw.get("requant"):
+                unique = n * 2 * (0.5 + 1 / 16)
+                alg = n * 3 * (0.5 + 1 / 16)
+            else:
+                outs = 1 + int(bool(kw.get("colwise")))
+                unique = n * (2 + outs * (0.5 + 1 / 16))
+                alg = quant_bytes(rows, L, kw)
             print(json.dumps({"sweep": "c5", "mode": name, "rows": rows, "row_len": L, "elements": n,
                               "ms": round(ms, 4), "unique_gbs": round(unique / (ms * 1e-3) / 1e9, 1),
                               "algorithmic_gbs": round(alg / (ms * 1e-3) / 1e9, 1),

@@ -34,7 +34,8 @@ NVFP4_COLWISE = 2
 
 EXPORTED = ("nvfp4_scale_bytes", "nvfp4_quantize_workspace_size", "nvfp4_quantize",
             "nvfp4_rht_quantize", "nvfp4_gemm", "nvfp4_dequantize", "nvfp4_status_string",
-            "nvfp4_device_error", "nvfp4_quantize_noalloc", "nvfp4_quantize_row_col_rht")
+            "nvfp4_device_error", "nvfp4_quantize_noalloc", "nvfp4_quantize_row_col_rht",
+            "nvfp4_requantize_col_rht")
 
 
 class nvfp4_tensor(ctypes.Structure):
@@ -77,6 +78,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_quantize_noalloc.restype = i32
     L.nvfp4_quantize_row_col_rht.argtypes = [vp, i64, i64, i64, i32, u64, u64, u64, u16, tp, tp, vp, sz, vp]
     L.nvfp4_quantize_row_col_rht.restype = i32
+    L.nvfp4_requantize_col_rht.argtypes = [tp, i32, u64, u64, u16, tp, vp, sz, vp]
+    L.nvfp4_requantize_col_rht.restype = i32
     L.nvfp4_gemm.argtypes = [tp, tp, vp, i64, i32, vp, sz, vp]
     L.nvfp4_gemm.restype = i32
     L.nvfp4_dequantize.argtypes = [tp, vp, i64, i32, vp]
@@ -126,6 +129,13 @@ def nvfp4_quantize_row_col_rht(x, rows, cols, ld_x, rounding, seed, stream_row, 
     return load().nvfp4_quantize_row_col_rht(x, rows, cols, ld_x, rounding, seed, stream_row, stream_col,
                                              rht_sign_mask, _ref(out_row), _ref(out_col), workspace,
                                              workspace_bytes, stream)
+
+
+def nvfp4_requantize_col_rht(in_row, rounding, seed, stream_id, rht_sign_mask, out_col, workspace,
+                             workspace_bytes, stream):
+    """Wgrad's second operand re-quantized from a row-wise operand (Eq. (2))."""
+    return load().nvfp4_requantize_col_rht(_ref(in_row), rounding, seed, stream_id, rht_sign_mask, _ref(out_col),
+                                           workspace, workspace_bytes, stream)
 
 
 def nvfp4_gemm(A, B, D, ldd, out_dtype, workspace, workspace_bytes, stream):

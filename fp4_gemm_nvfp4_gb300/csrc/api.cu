@@ -152,6 +152,31 @@ nvfp4_status nvfp4_quantize_row_col_rht(const void* x, int64_t rows, int64_t col
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+nvfp4_status nvfp4_requantize_col_rht(const nvfp4_tensor* in_row, nvfp4_rounding rounding, uint64_t seed,
+                                      uint64_t stream_id, uint16_t rht_sign_mask, const nvfp4_tensor* out_col,
+                                      void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    if (rounding != NVFP4_ROUND_RNE && rounding != NVFP4_ROUND_SR) return NVFP4_ERR_INVALID_ARG;
+    if (!in_row || !out_col) return NVFP4_ERR_INVALID_ARG;
+    const int64_t rows = in_row->rows, cols = in_row->cols;
+    if (rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+    if (rows % 16 != 0 || cols % 16 != 0) return NVFP4_ERR_SHAPE;
+    nvfp4_status s;
+    if ((s = check_target(in_row, rows, cols)) != NVFP4_OK) return s;
+    if ((s = check_target(out_col, cols, rows)) != NVFP4_OK) return s;
+    if (out_col->global_scale == in_row->global_scale ||
+        (rows > 0 && cols > 0 && (out_col->codes == in_row->codes || out_col->scales == in_row->scales)))
+        return NVFP4_ERR_INVALID_ARG;
+    if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return NVFP4_ERR_UNSUPPORTED;
+    if (cols * (rows / 16) >= (int64_t(1) << 32) - 1) return NVFP4_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < nvfp4::kQuantizeWorkspaceBytes || !aligned16(workspace))
+        return NVFP4_ERR_WORKSPACE;
+    const QuantTarget ti = to_target(in_row), to = to_target(out_col);
+    const cudaError_t e = nvfp4::launch_requantize_col_rht(&ti, rounding == NVFP4_ROUND_SR, rht_sign_mask, seed,
+                                                           stream_id, &to, static_cast<float*>(workspace),
+                                                           reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, int64_t ldd,
                         nvfp4_dtype out_dtype, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
     (void)workspace;

@@ -253,6 +253,22 @@ __device__ __forceinline__ void e2m1_decode_x8(uint32_t w, float* g) {
     }
 }
 
+// The two E2M1 codes of one byte (low nibble first), as values.
+__device__ __forceinline__ void e2m1_decode_byte(uint32_t b, float& lo, float& hi) {
+    asm("{\n\t"
+        ".reg .b8 t;\n\t"
+        ".reg .b32 h2;\n\t"
+        ".reg .f16 l, h;\n\t"
+        "cvt.u8.u32 t, %2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h2, t;\n\t"
+        "mov.b32 {l, h}, h2;\n\t"
+        "cvt.f32.f16 %0, l;\n\t"
+        "cvt.f32.f16 %1, h;\n\t"
+        "}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(b));
+}
+
 // 4/6 adaptive scaling of one 1x16 block (the oracle's reading of the 4/6
 // scaling "Full-Stack FP4" names): the block's amax mapped to 6 (the plain
 // scale) or to 4, each candidate encoded with RNE and measured by

@@ -26,6 +26,12 @@ struct QuantTarget {
 constexpr int kMaxAmaxPartials = 4096;
 constexpr size_t kQuantizeWorkspaceBytes = 2 * kMaxAmaxPartials * sizeof(float);
 
+// Wgrad's second operand from a row-wise operand (in: [lrows][lcols]; out:
+// [lcols][lrows]): dequantize, RHT along the rows, col-wise 1x16.
+cudaError_t launch_requantize_col_rht(const QuantTarget* in, bool sr, uint32_t sign_mask, uint64_t seed,
+                                      uint64_t stream_id, const QuantTarget* out, float* workspace,
+                                      cudaStream_t stream);
+
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool scale_2d,
                             bool scale_46, bool sr, bool rht, uint32_t sign_mask, uint64_t seed, uint64_t stream_id,
                             const QuantTarget* row, const QuantTarget* col, float* workspace,

@@ -224,6 +224,94 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
     }
 }
 
+// --------------------------------------------- Wgrad re-quantization -----
+// Q_16x1(H^T Q_1x16(X)) ("Full-Stack FP4", Sec. 3.2 Eq. (2)): the forward's
+// row-wise operand of X is dequantized (RN(RN(e2m1 * s_b) * s_g); the first
+// product is exact), rotated along its rows and quantized col-wise, so Wgrad
+// sees the same quantized activations as Fprop.  Thread layout of
+// colwise_kernel: lane = 2 columns x 16 rows (one code byte per row), a warp
+// 16 rows x 64 columns, a CTA 128 x 64.
+struct RequantArgs {
+    const uint8_t* in_codes;     // [rows][in_ld] bytes
+    int64_t in_ld;
+    const uint8_t* in_scales;    // tile layout of a [rows][cols] operand
+    uint32_t in_s4;
+    const float* in_sg;
+    uint32_t rows, cols;
+    uint32_t tiles_r, tiles_c;   // tiles of 128 rows x 64 columns
+    Target out;                  // logical [cols][rows]
+    const float* partials_in;
+    int n_partials;
+    float* partials_out;
+    uint32_t mask;
+    PhiloxKeys keys;             // SR round keys of the seed
+    uint64_t stream;
+};
+
+template <Pass P, bool kSR>
+__global__ void __launch_bounds__(kThreads) requant_kernel(const RequantArgs a) {
+    __shared__ float red[32];
+    __shared__ float rb_table[128];
+    __shared__ float sb_tab[128];     // E4M3 scale code -> value
+    __shared__ float2 g_tab[256];     // code byte -> its two E2M1 values (low nibble first)
+    static_assert(kThreads >= 256, "one table entry per thread");
+    {
+        float lo, hi;
+        e2m1_decode_byte(threadIdx.x, lo, hi);
+        g_tab[threadIdx.x] = make_float2(lo, hi);
+        if (threadIdx.x < 128) sb_tab[threadIdx.x] = e4m3_decode(threadIdx.x);
+    }
+    TensorScale ts{1.0f, 1.0f};
+    if constexpr (P == Pass::kEncode) {
+        ts = load_tensor_scale(a.partials_in, a.n_partials, red, a.out, nullptr);
+        fill_rb_table(rb_table, ts.s_enc);
+    }
+    __syncthreads();
+    const float sg = *a.in_sg;
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint32_t ntiles = a.tiles_r * a.tiles_c;
+    float local_max = 0.0f;
+    const PhiloxKeys& keys = a.keys;
+    for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const uint32_t tr = tile % a.tiles_r, tc = tile / a.tiles_r;
+        const uint32_t r0 = tr * 128u + warp * 16u, c = tc * 64u + lane * 2u;
+        if (r0 >= a.rows || c >= a.cols) continue;
+        // rows r0 .. r0+15 of one 32-row quadrant: their scales are 16 bytes apart
+        const uint8_t* srow = a.in_scales + scale_offset(r0, c / 16, a.in_s4);
+        const uint8_t* crow = a.in_codes + (int64_t)r0 * a.in_ld + c / 2;
+        float t0[16], t1[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float2 g = g_tab[__ldg(crow + (int64_t)i * a.in_ld)];
+            const float sb = sb_tab[__ldg(srow + 16 * i) & 0x7Fu];
+            t0[i] = __fmul_rn(__fmul_rn(g.x, sb), sg);
+            t1[i] = __fmul_rn(__fmul_rn(g.y, sb), sg);
+        }
+        rht16(t0, a.mask);
+        rht16(t1, a.mask);
+        float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            m0 = fmaxf(m0, fabsf(t0[i]));
+            m1 = fmaxf(m1, fabsf(t1[i]));
+        }
+        if constexpr (P == Pass::kAmax) {
+            local_max = fmaxf(local_max, fmaxf(m0, m1));
+        } else {
+            float rb0, rb1;
+            const uint32_t sc0 = block_scale_tab(m0, ts.s_enc, rb_table, &rb0);
+            const uint32_t sc1 = block_scale_tab(m1, ts.s_enc, rb_table, &rb1);
+            const uint2 q0 = encode16<kSR>(t0, rb0, keys, a.stream, (uint64_t)c * a.rows + r0);
+            const uint2 q1 = encode16<kSR>(t1, rb1, keys, a.stream, (uint64_t)(c + 1) * a.rows + r0);
+            *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
+            *reinterpret_cast<uint2*>(a.out.codes + (int64_t)(c + 1) * a.out.ld_codes + r0 / 2) = q1;
+            a.out.scales[scale_offset(c, r0 / 16, a.out.s4)] = (uint8_t)sc0;
+            a.out.scales[scale_offset(c + 1, r0 / 16, a.out.s4)] = (uint8_t)sc1;
+        }
+    }
+    if constexpr (P == Pass::kAmax) block_max_store(local_max, a.partials_out, red);
+}
+
 // -------------------------------------------------------------- 16x16 -----
 __device__ __forceinline__ uint32_t nibble(uint2 q, int i) {
     return ((i < 8 ? q.x : q.y) >> (4 * (i & 7))) & 0xFu;
@@ -904,6 +992,41 @@ cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t
     auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(tmap, pa); };
     if (sr) launch(pair_encode_kernel<true, true>);
     else launch(pair_encode_kernel<false, true>);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_requantize_col_rht(const QuantTarget* in, bool sr, uint32_t sign_mask, uint64_t seed,
+                                      uint64_t stream_id, const QuantTarget* out, float* workspace, cudaStream_t st) {
+    cudaError_t err;
+    if ((err = clear_scale_padding(out, st)) != cudaSuccess) return err;
+    RequantArgs ra{};
+    ra.in_codes = in->codes;
+    ra.in_ld = in->ld_codes;
+    ra.in_scales = in->scales;
+    ra.in_s4 = (uint32_t)((in->lcols + 63) / 64);
+    ra.in_sg = in->sg;
+    ra.rows = (uint32_t)in->lrows;
+    ra.cols = (uint32_t)in->lcols;
+    ra.tiles_r = (uint32_t)((in->lrows + 127) / 128);
+    ra.tiles_c = (uint32_t)((in->lcols + 63) / 64);
+    ra.out = make_target(out);
+    ra.mask = sign_mask;
+    ra.keys = philox_keys(seed);
+    ra.stream = stream_id;
+    const int64_t ntiles = (int64_t)ra.tiles_r * ra.tiles_c;
+    {
+        RequantArgs a = ra;
+        a.partials_out = workspace;
+        auto k = requant_kernel<Pass::kAmax, false>;
+        int g = persistent_grid(k, ntiles);
+        if (g > kMaxAmaxPartials) g = kMaxAmaxPartials;
+        k<<<g, kThreads, 0, st>>>(a);
+        ra.n_partials = g;
+    }
+    ra.partials_in = workspace;
+    auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(ra); };
+    if (sr) launch(requant_kernel<Pass::kEncode, true>);
+    else launch(requant_kernel<Pass::kEncode, false>);
     return cudaGetLastError();
 }
 

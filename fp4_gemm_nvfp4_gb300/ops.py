@@ -112,6 +112,21 @@ def quantize(x: torch.Tensor, *, two_d: bool = False, sr: bool = False, rht_mask
     return (out_row if rowwise else None), (out_col if colwise else None)
 
 
+def requantize_col_rht(q_row: NVFP4Operand, rht_mask: int, *, sr: bool = False, seed: int = 0,
+                       stream_id: int = 0, out_col: Optional[NVFP4Operand] = None,
+                       workspace: Optional[Workspace] = None, stream=None) -> NVFP4Operand:
+    """Wgrad's second operand from a row-wise operand (nvfp4_requantize_col_rht):
+    dequantize, RHT along the rows, col-wise 1x16."""
+    if out_col is None:
+        out_col = alloc_operand(q_row.cols, q_row.rows, q_row.codes.device)
+    ws = workspace or _workspace(q_row.codes.device)
+    status = capi.nvfp4_requantize_col_rht(q_row.struct(), capi.NVFP4_ROUND_SR if sr else capi.NVFP4_ROUND_RNE,
+                                           seed, stream_id, rht_mask, out_col.struct(), ws.ptr, ws.nbytes,
+                                           stream_handle(stream))
+    capi.check(status, "nvfp4_requantize_col_rht")
+    return out_col
+
+
 def quantize_row_col_rht(x: torch.Tensor, rht_mask: int, *, sr: bool = False, seed: int = 0,
                          stream_row: int = 0, stream_col: int = 0, out_row: Optional[NVFP4Operand] = None,
                          out_col: Optional[NVFP4Operand] = None, workspace: Optional[Workspace] = None,

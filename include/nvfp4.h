@@ -191,6 +191,27 @@ NVFP4_API nvfp4_status nvfp4_rht_quantize(const void *x, int64_t rows, int64_t c
                                 void *workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_requantize_col_rht -- Wgrad's second operand re-quantized from the
+ * forward pass's quantized input [FS Sec. 3.2 Eq. (2): Q_16x1(H16^T Q_1x16(X))],
+ * so that Wgrad uses the same quantized activations as Fprop.  in_row is a
+ * ROWWISE 1x16 operand ([rows][cols], e.g. from nvfp4_quantize); each value
+ * is dequantized to binary32 as RN(RN(e2m1 * s_b) * s_g), the 16-point RHT
+ * U = H16 * D / 4 is applied along the rows (16 consecutive rows of a
+ * column), and the result is quantized col-wise with 1x16 blocks along the
+ * rows into out_col ([cols][rows], K-major along rows) with its own tensor
+ * amax and s_g, RNE or SR as for nvfp4_rht_quantize (stream_id selects the
+ * Philox stream).  Two kernels: an amax pass and an encode pass over the FP4
+ * input (0.5625 B read per element each).
+ * Requirements: rows % 16 == 0 and cols % 16 == 0 [SHAPE]; in_row and
+ * out_col as for nvfp4_quantize's outputs and not sharing codes, scales or
+ * s_g [INVALID_ARG]; workspace of nvfp4_quantize_workspace_size() bytes.
+ */
+NVFP4_API nvfp4_status nvfp4_requantize_col_rht(const nvfp4_tensor *in_row, nvfp4_rounding rounding,
+                                                uint64_t seed, uint64_t stream_id, uint16_t rht_sign_mask,
+                                                const nvfp4_tensor *out_col, void *workspace,
+                                                size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
  * nvfp4_quantize_row_col_rht -- the two operands a linear layer takes from one
  * activation or output gradient x [FS Sec. 2, Eq. (1)-(2); NV Sec. 4: the RHT
  * goes to the Wgrad inputs only]: the ROWWISE 1x16 operand without the

@@ -127,6 +127,29 @@ def test_row_col_rht_validation(lib):
     assert row_col_rht(rows=-16) == E.NVFP4_ERR_SHAPE
 
 
+def requant(**kw):
+    args = dict(in_row=tensor(64, 96, codes=A16 * 6, scales=A16 * 7, sg=A16 * 8), rounding=0, seed=0,
+                stream_id=0, mask=0x1234, out_col=tensor(96, 64), workspace=A16 * 5,
+                workspace_bytes=capi.nvfp4_quantize_workspace_size(64, 96, 3), stream=None)
+    args.update(kw)
+    return capi.nvfp4_requantize_col_rht(*args.values())
+
+
+def test_requantize_validation(lib):
+    """Every call here is rejected on the host (no kernel ever sees the fake addresses)."""
+    E = capi
+    assert requant(in_row=None) == E.NVFP4_ERR_INVALID_ARG
+    assert requant(out_col=None) == E.NVFP4_ERR_INVALID_ARG
+    assert requant(rounding=2) == E.NVFP4_ERR_INVALID_ARG
+    assert requant(in_row=tensor(24, 96, codes=A16 * 6, scales=A16 * 7, sg=A16 * 8),
+                   out_col=tensor(96, 24)) == E.NVFP4_ERR_SHAPE                      # rows % 16
+    assert requant(out_col=tensor(64, 96)) == E.NVFP4_ERR_INVALID_ARG                 # transposed shape expected
+    assert requant(out_col=tensor(96, 64, sg=A16 * 8)) == E.NVFP4_ERR_INVALID_ARG     # shares s_g with the input
+    assert requant(out_col=tensor(96, 64, codes=A16 * 6)) == E.NVFP4_ERR_INVALID_ARG  # shares codes
+    assert requant(in_row=tensor(64, 96, codes=A16 + 8, scales=A16 * 7, sg=A16 * 8)) == E.NVFP4_ERR_ALIGNMENT
+    assert requant(workspace_bytes=16) == E.NVFP4_ERR_WORKSPACE
+
+
 def test_rht_quantize_rejects_2d(lib):
     ws = capi.nvfp4_quantize_workspace_size(64, 64, 3)
     st = capi.nvfp4_rht_quantize(A16 * 4, 64, 64, 64, capi.NVFP4_SCALE_16X16, 0, 0, 0, 1,

@@ -207,3 +207,34 @@ def test_row_col_rht_zero_tensor():
         codes, scales, amax, sg, _ = helpers.operand_to_host(g)
         assert amax == 0 and sg == 1 and not scales.any()
     assert not helpers.operand_to_host(row)[0].any()
+
+
+# ---- Wgrad re-quantization from the forward's row-wise operand (Eq. (2)) ----
+@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("shape", [(16, 16), (272, 336), (128, 1024), (400, 192), (1040, 3072)])
+def test_requantize_col_rht_matches_oracle(shape, rounding):
+    rows, cols = shape
+    bits = inputs.normal(rows, cols, seed=rows + 3 * cols, outlier_channels=2)
+    x = helpers.to_device_bf16(bits)
+    row, _ = ops.quantize(x)
+    col = ops.requantize_col_rht(row, 0x5AA5, sr=rounding == 1, seed=77, stream_id=6)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    ref = oracle.requantize_col_rht(oracle.quantize(bits), 0x5AA5, rounding=rounding, seed=77, stream_id=6)
+    _check_against_oracle(col, ref)
+
+
+def test_requantize_col_rht_full_size_sampled():
+    rows, cols = 16384, 3072
+    bits = inputs.normal(rows, cols, 8, outlier_channels=inputs.outlier_count(cols))
+    row, _ = ops.quantize(helpers.to_device_bf16(bits))
+    col = ops.requantize_col_rht(row, inputs.rht_sign_mask(8), sr=True, seed=8, stream_id=2)
+    torch.cuda.synchronize()
+    codes, scales, amax, sg, _ = helpers.operand_to_host(col)
+    q = oracle.quantize(bits)
+    for lr0, lr1 in _ranges(cols):
+        ref = oracle.requantize_col_rht(q, inputs.rht_sign_mask(8), rounding=1, seed=8, stream_id=2,
+                                        rows_subset=(lr0, lr1))
+        assert amax == ref["amax"] and sg == ref["s_g"]
+        assert np.array_equal(codes[lr0:lr1], ref["codes"])
+        assert np.array_equal(scales[lr0:lr1], ref["scales"])
