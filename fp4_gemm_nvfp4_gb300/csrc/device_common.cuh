@@ -82,6 +82,18 @@ __device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
 __device__ __forceinline__ uint32_t sr_addend_lo(uint32_t w) { return ((~w << 6) & 0x3FFFC0u) | 63u; }
 __device__ __forceinline__ uint32_t sr_addend_hi(uint32_t w) { return (~w >> 10) | 63u; }
 
+// Both addends of one Philox word, 0x3FFFFF - 64 r for r = its low and its
+// high 16 bits (the same values as sr_addend_lo / sr_addend_hi), as integer
+// multiply-adds: they run on the FMA pipe while the rounding itself keeps
+// the integer ALU busy.
+__device__ __forceinline__ void sr_addends(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    uint32_t h16, t;
+    asm("mul.hi.u32 %0, %1, 65536;" : "=r"(h16) : "r"(w));
+    asm("mad.lo.u32 %0, %1, 4294967232, 4194303;" : "=r"(hi) : "r"(h16));       // 0x3FFFFF - 64 h16
+    asm("mad.lo.u32 %0, %1, 4194304, 4194303;" : "=r"(t) : "r"(h16));            // 0x3FFFFF + 2^22 h16
+    asm("mad.lo.u32 %0, %1, 4294967232, %2;" : "=r"(lo) : "r"(w), "r"(t));     // 0x3FFFFF - 64 (w - 2^16 h16)
+}
+
 __device__ __forceinline__ float e2m1_sr_grid(float v, uint32_t addend) {
     const float a = fabsf(v);
     const float z = fmaxf(a, __fmaf_ru(a, 0.5f, 0.5f));
@@ -329,9 +341,11 @@ __device__ __forceinline__ uint2 encode16(const float* t, float r_b, const Philo
         const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         float q[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t wi = w[i >> 1];
-            q[i] = e2m1_sr_grid(v[i], (i & 1) ? sr_addend_hi(wi) : sr_addend_lo(wi));
+        for (int k = 0; k < 8; ++k) {
+            uint32_t alo, ahi;
+            sr_addends(w[k], alo, ahi);
+            q[2 * k] = e2m1_sr_grid(v[2 * k], alo);
+            q[2 * k + 1] = e2m1_sr_grid(v[2 * k + 1], ahi);
         }
         return make_uint2(e2m1_rne_x8(q), e2m1_rne_x8(q + 8));
     }
