@@ -35,7 +35,7 @@ NVFP4_COLWISE = 2
 EXPORTED = ("nvfp4_scale_bytes", "nvfp4_quantize_workspace_size", "nvfp4_quantize",
             "nvfp4_rht_quantize", "nvfp4_gemm", "nvfp4_dequantize", "nvfp4_status_string",
             "nvfp4_device_error", "nvfp4_quantize_noalloc", "nvfp4_quantize_row_col_rht",
-            "nvfp4_requantize_col_rht")
+            "nvfp4_requantize_col_rht", "nvfp4_gemm_lora", "nvfp4_gemm_lora_workspace_size")
 
 
 class nvfp4_tensor(ctypes.Structure):
@@ -81,6 +81,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_requantize_col_rht.argtypes = [tp, i32, u64, u64, u16, tp, vp, sz, vp]
     L.nvfp4_requantize_col_rht.restype = i32
     L.nvfp4_gemm.argtypes = [tp, tp, vp, i64, i32, vp, sz, vp]
+    L.nvfp4_gemm_lora_workspace_size.argtypes = [i64, i64]
+    L.nvfp4_gemm_lora_workspace_size.restype = sz
+    L.nvfp4_gemm_lora.argtypes = [tp, tp, vp, i64, i32, vp, i64, vp, i64, i64, ctypes.c_float, vp, sz, vp]
+    L.nvfp4_gemm_lora.restype = i32
     L.nvfp4_gemm.restype = i32
     L.nvfp4_dequantize.argtypes = [tp, vp, i64, i32, vp]
     L.nvfp4_dequantize.restype = i32
@@ -140,6 +144,16 @@ def nvfp4_requantize_col_rht(in_row, rounding, seed, stream_id, rht_sign_mask, o
 
 def nvfp4_gemm(A, B, D, ldd, out_dtype, workspace, workspace_bytes, stream):
     return load().nvfp4_gemm(_ref(A), _ref(B), D, ldd, out_dtype, workspace, workspace_bytes, stream)
+
+
+def nvfp4_gemm_lora_workspace_size(M, r):
+    return load().nvfp4_gemm_lora_workspace_size(M, r)
+
+
+def nvfp4_gemm_lora(A, B, D, ldd, out_dtype, U, ldu, V, ldv, r, beta, workspace, workspace_bytes, stream):
+    """D = s_gA s_gB A B^T + beta U V^T (the LoRA-SVD projection's low-rank branch fused)."""
+    return load().nvfp4_gemm_lora(_ref(A), _ref(B), D, ldd, out_dtype, U, ldu, V, ldv, r, beta, workspace,
+                                  workspace_bytes, stream)
 
 
 def nvfp4_dequantize(q, y, ldy, out_dtype, stream):

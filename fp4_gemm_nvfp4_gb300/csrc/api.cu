@@ -4,6 +4,7 @@
 // status means no kernel was launched (except NVFP4_ERR_CUDA from a launch).
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 
 #include "../../include/nvfp4.h"
@@ -199,6 +200,41 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, i
                    ? NVFP4_OK
                    : NVFP4_ERR_CUDA;
     const cudaError_t e = nvfp4::launch_gemm(to_operand(A), to_operand(B), D, ldd, out_dtype == NVFP4_OUT_FP32, st);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+size_t nvfp4_gemm_lora_workspace_size(int64_t M, int64_t r) {
+    if (M < 0 || r < 0) return 0;
+    return (size_t)(M * r * 2) + 16;
+}
+
+nvfp4_status nvfp4_gemm_lora(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, int64_t ldd,
+                             nvfp4_dtype out_dtype, const void* U, int64_t ldu, const void* V, int64_t ldv,
+                             int64_t r, float beta, void* workspace, size_t workspace_bytes,
+                             nvfp4_stream_t stream) {
+    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status s;
+    if ((s = check_operand(A)) != NVFP4_OK) return s;
+    if ((s = check_operand(B)) != NVFP4_OK) return s;
+    if (A->cols != B->cols) return NVFP4_ERR_SHAPE;
+    if (!D || !U || !V) return NVFP4_ERR_INVALID_ARG;
+    const int64_t M = A->rows, N = B->rows, K = A->cols;
+    const int64_t esz = out_dtype == NVFP4_OUT_FP32 ? 4 : 2;
+    if (ldd < N) return NVFP4_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(D) % (uintptr_t)esz) != 0) return NVFP4_ERR_ALIGNMENT;
+    if (r <= 0 || r % 64 != 0 || r > 4096) return NVFP4_ERR_UNSUPPORTED;
+    if (ldu < r || ldv < r) return NVFP4_ERR_SHAPE;
+    if (!aligned16(U) || !aligned16(V) || ldu % 8 != 0 || ldv % 8 != 0) return NVFP4_ERR_ALIGNMENT;
+    if (!std::isfinite(beta)) return NVFP4_ERR_INVALID_ARG;
+    if (ceil_div(M, 128) * ceil_div(N, 256) >= (int64_t(1) << 32)) return NVFP4_ERR_UNSUPPORTED;
+    if (K == 0) return NVFP4_ERR_UNSUPPORTED;   // no FP4 product to carry the low-rank term
+    if (!workspace || !aligned16(workspace) || workspace_bytes < nvfp4_gemm_lora_workspace_size(M, r))
+        return NVFP4_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (M == 0 || N == 0) return NVFP4_OK;
+    const nvfp4::LowRank lr{U, ldu, V, ldv, r, beta, workspace};
+    const cudaError_t e =
+        nvfp4::launch_gemm(to_operand(A), to_operand(B), D, ldd, out_dtype == NVFP4_OUT_FP32, st, &lr);
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 

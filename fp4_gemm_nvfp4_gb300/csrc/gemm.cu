@@ -99,6 +99,7 @@ struct Params {
     int vec_store;               // every output row starts on a 16-byte boundary
     int tma_store;               // output written through the D tensor map (BF16 or FP32)
     int n_fast;                  // tile order: N tiles vary fastest (else M tiles)
+    uint32_t lora_stages;        // 64-deep BF16 stages of the low-rank term per tile (0: none)
 };
 
 // Output tile of a linear tile index.  Tiles that run at the same time share
@@ -120,6 +121,36 @@ __device__ __forceinline__ void tile_coords(uint32_t tile, const Params& p, uint
 // at bit 27 (M = 256 for the pair), scale-factor ids 0.
 constexpr uint32_t kIdesc =
     (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kPairM >> 7) << 27);
+
+// Instruction descriptor for kind::f16 (the low-rank term): FP32 D (bit 4),
+// A and B BF16 (format 1 at bits 7 and 10), both K-major, N >> 3 at bit 17,
+// M >> 4 at bit 24 (M = 256 for the pair).
+constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                                ((uint32_t)(kPairM >> 4) << 24);
+
+// Four pair MMAs of kind::f16 over one 64-deep BF16 stage (16 per MMA; the
+// descriptors advance by 32 bytes like the FP4 steps); accumulates onto D
+// unless the stage is the first MMA work of the tile.
+__device__ __forceinline__ void mma_bf16_pair_stage(uint32_t d_tmem, uint32_t a_lo, uint32_t desc_hi,
+                                                    uint32_t b_off, uint32_t accumulate_first) {
+    asm volatile(
+        "{\n\t"
+        ".reg .b32 a1, a2, a3, b0, b1, b2, b3;\n\t"
+        ".reg .b64 da0, da1, da2, da3, db0, db1, db2, db3;\n\t"
+        ".reg .pred p;\n\t"
+        "setp.ne.b32 p, %3, 0;\n\t"
+        "add.u32 a1, %1, 2;\n\tadd.u32 a2, %1, 4;\n\tadd.u32 a3, %1, 6;\n\t"
+        "add.u32 b0, %1, %4;\n\tadd.u32 b1, b0, 2;\n\tadd.u32 b2, b0, 4;\n\tadd.u32 b3, b0, 6;\n\t"
+        "mov.b64 da0, {%1, %2};\n\tmov.b64 da1, {a1, %2};\n\tmov.b64 da2, {a2, %2};\n\tmov.b64 da3, {a3, %2};\n\t"
+        "mov.b64 db0, {b0, %2};\n\tmov.b64 db1, {b1, %2};\n\tmov.b64 db2, {b2, %2};\n\tmov.b64 db3, {b3, %2};\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], da0, db0, %5, p;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], da1, db1, %5, 1;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], da2, db2, %5, 1;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], da3, db3, %5, 1;\n\t"
+        "}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(desc_hi), "r"(accumulate_first), "r"(b_off), "n"(kIdescBf16)
+        : "memory");
+}
 
 __device__ __forceinline__ void record_timeout(volatile uint32_t* abort_flag) {
     *abort_flag = 1u;
@@ -143,7 +174,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                      const __grid_constant__ CUtensorMap tma_sfa, const __grid_constant__ CUtensorMap tma_sfb,
-                     const __grid_constant__ CUtensorMap tma_d, const Params p) {
+                     const __grid_constant__ CUtensorMap tma_d, const __grid_constant__ CUtensorMap tma_u,
+                     const __grid_constant__ CUtensorMap tma_v, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* staging = smem + kStages * kStageBytes;
@@ -173,8 +205,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         *abort_flag = 0u;
         fence_barrier_init();
     }
-    if (warp == kProdAWarp && lane == 0) prefetch_tmap(&tma_a);
-    if (warp == kProdBWarp && lane == 0) prefetch_tmap(&tma_b);
+    if (warp == kProdAWarp && lane == 0) {
+        prefetch_tmap(&tma_a);
+        if (p.lora_stages) prefetch_tmap(&tma_u);
+    }
+    if (warp == kProdBWarp && lane == 0) {
+        prefetch_tmap(&tma_b);
+        if (p.lora_stages) prefetch_tmap(&tma_v);
+    }
     if (warp == kProdSfWarp && lane == 0) {
         prefetch_tmap(&tma_sfa);
         prefetch_tmap(&tma_sfb);
@@ -229,6 +267,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     (int32_t)(2 * mt + rank));
                         tma_load_3d(sfa_s + kSFABytes, &tma_sfb, &sf_full[stage], 0, (int32_t)(ks * kKStepsPerStage),
                                     (int32_t)(2 * nt));
+                    }
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                // the low-rank term: 64 BF16 columns of U' and V per stage in
+                // the A and B slots (the same 16 KiB boxes), no scales
+                for (uint32_t ls = 0; ls < p.lora_stages && !*abort_flag; ++ls) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, kTimeoutNs)) {
+                        record_timeout(abort_flag);
+                        break;
+                    }
+                    uint8_t* st = smem + stage * kStageBytes;
+                    const uint32_t leader_full = leader_full0 + stage * 8u;
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (warp == kProdAWarp) {
+                        if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (kABytes + kBBytes));
+                        tma_load_2d_pair(st, &tma_u, leader_full, (int32_t)(ls * 64u),
+                                         (int32_t)(mt * kPairM + rank * kCtaM));
+                    } else if (warp == kProdBWarp) {
+                        tma_load_2d_pair(st + kABytes, &tma_v, leader_full, (int32_t)(ls * 64u),
+                                         (int32_t)(nt * kBN + rank * kCtaN));
+                    } else {
+                        mbar_arrive(&sf_full[stage]);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -306,6 +370,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ea += 8u;
                     }
                 }
+                for (uint32_t ls = 0; ok && ls < p.lora_stages; ++ls) {
+                    if (!mbar_wait_addr(fa, phase, kTimeoutNs)) {
+                        record_timeout(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_bf16_pair_stage(acc, alo, hi, kBOff, (kst | ls) != 0 ? 1u : 0u);
+                    tc_commit_pair_multicast_addr(ea, 0x3);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                        alo = lo0;
+                        sfc = sfc0;
+                        fa = full0;
+                        ea = empty0;
+                    } else {
+                        alo += kStageDesc;
+                        sfc += kSfColsPerStage;
+                        fa += 8u;
+                        ea += 8u;
+                    }
+                }
                 if (!ok) break;
                 tc_commit_pair_multicast(acc_full, 0x3);
                 ++tiles_done;
@@ -364,6 +451,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(leader_full0 + stage * 8u);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            // low-rank stages carry no scales: only the arrival on full
+            for (uint32_t ls = 0; ok && ls < p.lora_stages; ++ls, ++count) {
+                if (warp == (uint32_t)kFirstSfWarp && lane == 0) {
+                    bool landed = !*abort_flag && mbar_wait(&sf_full[stage], phase, kTimeoutNs);
+                    if (!landed && !*abort_flag) record_timeout(abort_flag);
+                    sf_ok[count & 1u] = landed ? 1u : 0u;
+                }
+                __syncwarp();
+                scale_bar();
+                if (!sf_ok[count & 1u]) {
+                    ok = false;
+                    break;
+                }
                 if (lane == 0) mbar_arrive_cluster(leader_full0 + stage * 8u);
                 if (++stage == kStages) {
                     stage = 0;
@@ -584,6 +690,46 @@ bool make_output_map(CUtensorMap* map, void* d, int64_t M, int64_t N, int64_t ld
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over a BF16 [rows][ld] matrix, 64 columns (128 bytes) by 128 rows
+// per box with the 128-byte swizzle: the low-rank operands' K-major tiles.
+bool make_bf16_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t elem[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// U'[m][k] = bf16(RN(U[m][k] * g)), g = RN(beta / RN(s_gA * s_gB)): the
+// low-rank term rides on the accumulator that the epilogue multiplies by
+// s_gA * s_gB.
+__global__ void lora_prescale_kernel(const uint16_t* __restrict__ u, int64_t ldu, int64_t rows, int64_t r,
+                                     float beta, const float* sga, const float* sgb, uint16_t* __restrict__ out) {
+    const float g = __fdiv_rn(beta, __fmul_rn(*sga, *sgb));
+    const int64_t n = rows * r;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / r, col = i - row * r;
+        const float x = __uint_as_float((uint32_t)u[row * ldu + col] << 16);
+        const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(x, g));
+        out[i] = *reinterpret_cast<const uint16_t*>(&h);
+    }
+}
+
+cudaError_t launch_lora_prescale(const void* u, int64_t ldu, int64_t rows, int64_t r, float beta, const float* sga,
+                                 const float* sgb, void* out, cudaStream_t stream) {
+    const int64_t n = rows * r;
+    int blocks = (int)((n + 255) / 256);
+    if (blocks > 4 * device_sm_count()) blocks = 4 * device_sm_count();
+    if (blocks < 1) blocks = 1;
+    lora_prescale_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(u), ldu, rows, r, beta, sga, sgb,
+                                                     static_cast<uint16_t*>(out));
+    return cudaGetLastError();
+}
+
 // Number of CTA pairs that can be resident at once (cached per device).
 int max_active_pairs() {
     static int pairs[64];
@@ -638,7 +784,7 @@ int device_sm_count() {
 }
 
 cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int64_t ldd, bool out_fp32,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const LowRank* lora) {
     static bool attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
@@ -670,10 +816,22 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     p.vec_store = ((reinterpret_cast<uintptr_t>(d) & 15u) == 0 && (ldd * esz) % 16 == 0) ? 1 : 0;
     p.tma_store = (p.vec_store && make_output_map(&md, d, a.rows, b.rows, ldd, out_fp32)) ? 1 : 0;
     if (!p.tma_store) md = ma;   // unused by the kernel; any valid map
+    CUtensorMap mu = ma, mv = ma;  // unused without a low-rank term
+    if (lora) {
+        if (!make_bf16_rows_map(&mu, lora->u_scaled, a.rows, lora->r, lora->r) ||
+            !make_bf16_rows_map(&mv, lora->v, b.rows, lora->r, lora->ldv))
+            return cudaErrorInvalidValue;
+        p.lora_stages = (uint32_t)(lora->r / 64);
+        // U' = U * (beta / (s_gA s_gB)), so that the epilogue's factor
+        // s_gA s_gB leaves beta * U V^T
+        const cudaError_t e = launch_lora_prescale(lora->u, lora->ldu, a.rows, lora->r, lora->beta, a.sg, b.sg,
+                                                   lora->u_scaled, stream);
+        if (e != cudaSuccess) return e;
+    }
     const uint32_t tiles = p.m_tiles * p.n_tiles;
     const uint32_t pairs = (uint32_t)max_active_pairs();
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
-    gemm_nvf4_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, p);
+    gemm_nvf4_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, mu, mv, p);
     return cudaGetLastError();
 }
 

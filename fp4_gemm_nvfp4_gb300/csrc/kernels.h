@@ -52,8 +52,21 @@ struct GemmOperand {
     int64_t rows, cols;
 };
 
+// The low-rank term of a LoRA-SVD projection, D += beta * U V^T: U [M][r]
+// and V [N][r] row-major BF16, r a multiple of 64; u_scaled is scratch for
+// U * beta / (s_gA s_gB) ([M][r] BF16, 16-byte aligned).
+struct LowRank {
+    const void* u;
+    int64_t ldu;
+    const void* v;
+    int64_t ldv;
+    int64_t r;
+    float beta;
+    void* u_scaled;
+};
+
 cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int64_t ldd, bool out_fp32,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const LowRank* lora = nullptr);
 
 // Read and clear the GEMM kernels' device status word (synchronous).
 cudaError_t gemm_read_and_clear_status(unsigned int* status);

@@ -160,6 +160,26 @@ def gemm(a: NVFP4Operand, b: NVFP4Operand, out_dtype=torch.bfloat16, out: Option
     return out
 
 
+
+def gemm_lora(a: NVFP4Operand, b: NVFP4Operand, u: torch.Tensor, v: torch.Tensor, beta: float,
+              out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None, scratch: Optional[torch.Tensor] = None,
+              stream=None) -> torch.Tensor:
+    """D = A * B^T + beta * U V^T (nvfp4_gemm_lora): U [M][r], V [N][r] bf16, r a multiple of 64."""
+    assert u.dtype == torch.bfloat16 and v.dtype == torch.bfloat16 and u.stride(1) == 1 and v.stride(1) == 1
+    r = u.shape[1]
+    assert v.shape[1] == r and u.shape[0] == a.rows and v.shape[0] == b.rows
+    if out is None:
+        out = torch.empty((a.rows, b.rows), dtype=out_dtype, device=a.codes.device)
+    nbytes = capi.nvfp4_gemm_lora_workspace_size(a.rows, r)
+    if scratch is None or scratch.numel() < nbytes:
+        scratch = torch.empty(nbytes, dtype=torch.uint8, device=a.codes.device)
+    dt = capi.NVFP4_OUT_FP32 if out.dtype == torch.float32 else capi.NVFP4_OUT_BF16
+    status = capi.nvfp4_gemm_lora(a.struct(), b.struct(), out.data_ptr(), out.stride(0), dt, u.data_ptr(),
+                                  u.stride(0), v.data_ptr(), v.stride(0), r, float(beta), scratch.data_ptr(),
+                                  scratch.numel(), stream_handle(stream))
+    capi.check(status, "nvfp4_gemm_lora")
+    return out
+
 def dequantize(q: NVFP4Operand, out_dtype=torch.float32, stream=None) -> torch.Tensor:
     """x^ = e2m1 * s_b * s_g (nvfp4_dequantize)."""
     y = torch.empty((q.rows, q.cols), dtype=out_dtype, device=q.codes.device)

@@ -254,6 +254,30 @@ NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_tensor *A, const nvfp4_tensor *B, 
                         nvfp4_stream_t stream);
 
 /*
+ * nvfp4_gemm_lora -- nvfp4_gemm plus the BF16 low-rank branch of a LoRA-SVD
+ * linear projection [FS Sec. 3.2 Eq. (1): Y = Q(X) Q(W_res)^T + beta (X L1^T) L2^T,
+ * dX = Q(dY) Q(W_res) + beta (dY L2) L1; fused into the GEMM as FS App. 9
+ * discusses]:
+ *   D = s_gA * s_gB * (A B^T) + beta * U V^T
+ *  U            device, BF16 [M][ldu] row-major, r columns (e.g. X L1^T).
+ *  V            device, BF16 [N][ldv] row-major, r columns (e.g. L2).
+ *  r            the rank, a multiple of 64 up to 4096 [UNSUPPORTED otherwise].
+ *  beta         finite FP32 scalar.
+ *  workspace    device scratch of nvfp4_gemm_lora_workspace_size(M, r) bytes,
+ *               16-byte aligned: holds U * beta / (s_gA s_gB) in BF16.
+ * The low-rank product runs on the tensor cores (BF16 MMAs into the same FP32
+ * accumulator, after the tile's FP4 MMAs), so U is rounded once more to BF16
+ * after scaling (relative error 2^-9 on that term).  K = 0 is UNSUPPORTED.
+ * Other requirements and errors as nvfp4_gemm; U and V 16-byte aligned,
+ * ldu, ldv multiples of 8 and >= r [ALIGNMENT / SHAPE].
+ */
+NVFP4_API size_t nvfp4_gemm_lora_workspace_size(int64_t M, int64_t r);
+NVFP4_API nvfp4_status nvfp4_gemm_lora(const nvfp4_tensor *A, const nvfp4_tensor *B, void *D, int64_t ldd,
+                                       nvfp4_dtype out_dtype, const void *U, int64_t ldu, const void *V,
+                                       int64_t ldv, int64_t r, float beta, void *workspace,
+                                       size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
  * nvfp4_dequantize -- y = e2m1(code) * s_b * s_g for every element of q
  * [FS Sec. 2], rounded once (nearest even) to out_dtype; y is row-major
  * [q->rows][ldy].  Requirements: y 16-byte aligned, ldy * sizeof(out) % 16 == 0.

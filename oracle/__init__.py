@@ -237,6 +237,22 @@ def dequantize(codes, scales, s_g):
     return out
 
 
+def gemm_lora_f64(a, b, u_bits, v_bits, beta, row_ids=None):
+    """The LoRA-SVD projection of "Full-Stack FP4", Sec. 3.2 Eq. (1):
+    y = A * B^T (gemm_f64, the NVFP4 GEMM) + beta * U V^T (the BF16 low-rank
+    branch, U = [M][r] and V = [N][r] bf16 bit patterns), in float64.
+    Returns (y, abs_sum, lora_abs_sum): the sums of |a b| and of |beta u v|
+    over the reduction, for tolerances."""
+    y, ab = gemm_f64(a, b, row_ids=row_ids)
+    u = (np.ascontiguousarray(u_bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    v = (np.ascontiguousarray(v_bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if row_ids is not None:
+        u = u[np.asarray(row_ids)]
+    lora = float(beta) * (u @ v.T)
+    lora_abs = abs(float(beta)) * (np.abs(u) @ np.abs(v).T)
+    return y + lora, ab, lora_abs
+
+
 def gemm_f64(a, b, row_ids=None, with_abs=True):
     """y = A * B^T for two oracle-quantized operands (dicts from quantize()).
 

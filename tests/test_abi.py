@@ -150,6 +150,30 @@ def test_requantize_validation(lib):
     assert requant(workspace_bytes=16) == E.NVFP4_ERR_WORKSPACE
 
 
+def gemm_lora(**kw):
+    args = dict(A=tensor(64, 128), B=tensor(96, 128), D=A16 * 9, ldd=96, out_dtype=0, U=A16 * 10, ldu=64,
+                V=A16 * 11, ldv=64, r=64, beta=0.5, workspace=A16 * 12,
+                workspace_bytes=capi.nvfp4_gemm_lora_workspace_size(64, 64), stream=None)
+    args.update(kw)
+    return capi.nvfp4_gemm_lora(*args.values())
+
+
+def test_gemm_lora_validation(lib):
+    """Every call here is rejected on the host (no kernel ever sees the fake addresses)."""
+    E = capi
+    assert gemm_lora(r=32, ldu=32, ldv=32) == E.NVFP4_ERR_UNSUPPORTED                # r % 64
+    assert gemm_lora(r=0) == E.NVFP4_ERR_UNSUPPORTED
+    assert gemm_lora(ldu=32) == E.NVFP4_ERR_SHAPE                                     # ldu < r
+    assert gemm_lora(U=A16 + 8) == E.NVFP4_ERR_ALIGNMENT
+    assert gemm_lora(ldv=68) == E.NVFP4_ERR_ALIGNMENT                                 # ldv % 8
+    assert gemm_lora(U=None) == E.NVFP4_ERR_INVALID_ARG
+    assert gemm_lora(beta=float("nan")) == E.NVFP4_ERR_INVALID_ARG
+    assert gemm_lora(workspace_bytes=16) == E.NVFP4_ERR_WORKSPACE
+    assert gemm_lora(A=tensor(64, 0), B=tensor(96, 0)) == E.NVFP4_ERR_UNSUPPORTED     # K = 0
+    assert gemm_lora(B=tensor(96, 64)) == E.NVFP4_ERR_SHAPE                           # K mismatch
+    assert capi.nvfp4_gemm_lora_workspace_size(100, 64) >= 100 * 64 * 2
+
+
 def test_rht_quantize_rejects_2d(lib):
     ws = capi.nvfp4_quantize_workspace_size(64, 64, 3)
     st = capi.nvfp4_rht_quantize(A16 * 4, 64, 64, 64, capi.NVFP4_SCALE_16X16, 0, 0, 0, 1,

@@ -175,3 +175,64 @@ def test_wgrad_rht_cancels_in_the_product():
                                dict(orientation=oracle.COLWISE, use_rht=True, sign_mask=0xECA8))
     y2 = ops.gemm(ga2, gb2, out_dtype=torch.float32).cpu().numpy().astype(np.float64)
     assert np.linalg.norm(y2 - exact) / np.linalg.norm(exact) > 0.8
+
+
+# ---- LoRA-SVD projection: the BF16 low-rank branch fused into the GEMM ----
+@pytest.mark.parametrize("M,N,K,r,beta", [(128, 256, 256, 64, 0.5), (200, 300, 320, 128, -1.25),
+                                          (384, 512, 3072, 64, 2.0), (130, 260, 80, 192, 0.75)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_lora_matches_oracle(M, N, K, r, beta, out_dtype):
+    """D = s_gA s_gB A B^T + beta U V^T ("Full-Stack FP4", Sec. 3.2 Eq. (1)).
+    Tolerance: the GEMM bound plus 2^-8 of sum |beta u v| (U is scaled and
+    rounded to BF16 once more on its way into the tensor cores)."""
+    rng = np.random.default_rng(M * 7 + N * 11 + K * 13 + r)
+    a_h = _random_operand_host(rng, M, K)
+    b_h = _random_operand_host(rng, N, K)
+    a, b = _upload(a_h, M, K), _upload(b_h, N, K)
+    u_bits = inputs.to_bf16_bits(rng.standard_normal((M, r)).astype(np.float32) * 4.0)
+    v_bits = inputs.to_bf16_bits(rng.standard_normal((N, r)).astype(np.float32) * 0.5)
+    u = helpers.to_device_bf16(u_bits)
+    v = helpers.to_device_bf16(v_bits)
+    y = ops.gemm_lora(a, b, u, v, beta, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    y_ref, abs_sum, lora_abs = oracle.gemm_lora_f64(a_h, b_h, u_bits, v_bits, beta)
+    bound = helpers.gemm_bound(abs_sum, y_ref, out_dtype == torch.bfloat16) + 2.0 ** -8 * lora_abs
+    err = np.abs(y.float().cpu().numpy().astype(np.float64) - y_ref)
+    worst = np.unravel_index(np.argmax(err / bound), err.shape)
+    assert np.all(err <= bound), (int((err > bound).sum()), worst, y_ref[worst], bound[worst])
+    if out_dtype == torch.float32:
+        # the low-rank term on its own: the same GEMM without it differs by
+        # beta U V^T up to U's BF16 rounding and the roundings of the FP32
+        # accumulator as each of the r/16 BF16 MMAs adds onto it
+        y_plain = ops.gemm(a, b, out_dtype=torch.float32).cpu().numpy().astype(np.float64)
+        y_l = y.cpu().numpy().astype(np.float64)
+        lora_ref = y_ref - oracle.gemm_f64(a_h, b_h)[0]
+        tight = 2.0 ** -8 * lora_abs + (r / 16 + 2) * 2.0 ** -23 * (np.abs(y_plain) + np.abs(y_l)) + 1e-30
+        dev = np.abs((y_l - y_plain) - lora_ref)
+        bad = np.argwhere(dev > tight)
+        assert bad.size == 0, (len(bad), bad[:6].tolist(), [(float(dev[i, j]), float(tight[i, j]),
+                               float(lora_ref[i, j]), float(y_l[i, j] - y_plain[i, j])) for i, j in bad[:4]])
+
+
+def test_gemm_lora_full_size_fprop_up_sampled():
+    """The 16384x9216x3072 Fprop of the up projection with a rank-64 branch
+    (U = X L1^T, V = L2 as random BF16), sampled rows."""
+    M, N, K, r = 16384, 9216, 3072, 64
+    x_bits = inputs.normal(M, K, 3, outlier_channels=inputs.outlier_count(K))
+    w_bits = inputs.normal(N, K, 4, std=0.02)
+    a, _ = ops.quantize(helpers.to_device_bf16(x_bits))
+    b, _ = ops.quantize(helpers.to_device_bf16(w_bits), two_d=True)
+    rng = np.random.default_rng(5)
+    u_bits = inputs.to_bf16_bits(rng.standard_normal((M, r)).astype(np.float32))
+    v_bits = inputs.to_bf16_bits(rng.standard_normal((N, r)).astype(np.float32) * 0.02)
+    y = ops.gemm_lora(a, b, helpers.to_device_bf16(u_bits), helpers.to_device_bf16(v_bits), 0.5)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    rows = np.sort(np.random.default_rng(6).choice(M, 96, replace=False))
+    qa = oracle.quantize(x_bits, rows_subset=None)
+    qb = oracle.quantize(w_bits, scaling=1)
+    y_ref, abs_sum, lora_abs = oracle.gemm_lora_f64(qa, qb, u_bits, v_bits, 0.5, row_ids=rows)
+    bound = helpers.gemm_bound(abs_sum, y_ref, True) + 2.0 ** -8 * lora_abs
+    err = np.abs(y.float().cpu().numpy()[rows].astype(np.float64) - y_ref)
+    assert np.all(err <= bound), int((err > bound).sum())

@@ -585,6 +585,28 @@ def test_requantize_row_subset_and_zero_operand():
     assert z["amax"] == 0 and not (z["codes"] & 0x77).any() and not z["scales"].any()
 
 
+# ------------------------------------------------ LoRA-SVD branch (Eq. 1) ----
+def test_gemm_lora_adds_the_low_rank_product():
+    """Full-Stack FP4, Sec. 3.2 Eq. (1): Y = Q(X) Q(W)^T + beta (X L1^T) L2^T.
+    With an all-zero FP4 operand the result is exactly beta U V^T, checked
+    against a triple loop on small integers; otherwise the low-rank term is
+    added to the FP4 GEMM."""
+    u_f = (np.arange(8 * 64, dtype=np.float32).reshape(8, 64) % 5) - 2
+    v_f = (np.arange(6 * 64, dtype=np.float32).reshape(6, 64) % 3) - 1
+    u, v = inputs.to_bf16_bits(u_f), inputs.to_bf16_bits(v_f)
+    brute = np.array([[-0.75 * sum(int(u_f[i, k]) * int(v_f[j, k]) for k in range(64)) for j in range(6)]
+                      for i in range(8)])
+    zero = oracle.quantize(np.zeros((8, 64), np.uint16))
+    b = oracle.quantize(inputs.normal(6, 64, 2))
+    y, ab, la = oracle.gemm_lora_f64(zero, b, u, v, -0.75)
+    assert np.array_equal(y, brute) and not ab.any()
+    assert np.array_equal(la, np.abs(brute) * 0 + 0.75 * (np.abs(u_f).astype(np.float64) @ np.abs(v_f).T))
+    a = oracle.quantize(inputs.normal(8, 64, 1))
+    y, _, _ = oracle.gemm_lora_f64(a, b, u, v, -0.75)
+    y0, _ = oracle.gemm_f64(a, b)
+    assert np.allclose(y - y0, brute, rtol=0, atol=1e-9)
+
+
 # ---------------------------------------------------------- dequantize ----
 def test_dequantize_grid_values():
     codes4 = np.arange(16, dtype=np.uint8)
