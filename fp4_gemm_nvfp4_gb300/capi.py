@@ -35,7 +35,8 @@ NVFP4_COLWISE = 2
 EXPORTED = ("nvfp4_scale_bytes", "nvfp4_quantize_workspace_size", "nvfp4_quantize",
             "nvfp4_rht_quantize", "nvfp4_gemm", "nvfp4_dequantize", "nvfp4_status_string",
             "nvfp4_device_error", "nvfp4_quantize_noalloc", "nvfp4_quantize_row_col_rht",
-            "nvfp4_requantize_col_rht", "nvfp4_gemm_lora", "nvfp4_gemm_lora_workspace_size")
+            "nvfp4_requantize_col_rht", "nvfp4_gemm_lora", "nvfp4_gemm_lora_workspace_size",
+            "nvfp4_gemm_amax", "nvfp4_quantize_row_col_rht_amax")
 
 
 class nvfp4_tensor(ctypes.Structure):
@@ -81,6 +82,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_requantize_col_rht.argtypes = [tp, i32, u64, u64, u16, tp, vp, sz, vp]
     L.nvfp4_requantize_col_rht.restype = i32
     L.nvfp4_gemm.argtypes = [tp, tp, vp, i64, i32, vp, sz, vp]
+    L.nvfp4_gemm_amax.argtypes = [tp, tp, vp, i64, vp, u16, vp, sz, vp]
+    L.nvfp4_gemm_amax.restype = i32
+    L.nvfp4_quantize_row_col_rht_amax.argtypes = [vp, i64, i64, i64, i32, u64, u64, u64, u16, vp, tp, tp, vp]
+    L.nvfp4_quantize_row_col_rht_amax.restype = i32
     L.nvfp4_gemm_lora_workspace_size.argtypes = [i64, i64]
     L.nvfp4_gemm_lora_workspace_size.restype = sz
     L.nvfp4_gemm_lora.argtypes = [tp, tp, vp, i64, i32, vp, i64, vp, i64, i64, ctypes.c_float, vp, sz, vp]
@@ -144,6 +149,19 @@ def nvfp4_requantize_col_rht(in_row, rounding, seed, stream_id, rht_sign_mask, o
 
 def nvfp4_gemm(A, B, D, ldd, out_dtype, workspace, workspace_bytes, stream):
     return load().nvfp4_gemm(_ref(A), _ref(B), D, ldd, out_dtype, workspace, workspace_bytes, stream)
+
+
+def nvfp4_gemm_amax(A, B, D, ldd, amax_out, rht_sign_mask, workspace, workspace_bytes, stream):
+    """nvfp4_gemm (BF16 out) that also writes max |D| and the rotated amax of D."""
+    return load().nvfp4_gemm_amax(_ref(A), _ref(B), D, ldd, amax_out, rht_sign_mask, workspace, workspace_bytes,
+                                  stream)
+
+
+def nvfp4_quantize_row_col_rht_amax(x, rows, cols, ld_x, rounding, seed, stream_row, stream_col, rht_sign_mask,
+                                    amax_in, out_row, out_col, stream):
+    """nvfp4_quantize_row_col_rht with the two tensor amaxes given (no amax pass)."""
+    return load().nvfp4_quantize_row_col_rht_amax(x, rows, cols, ld_x, rounding, seed, stream_row, stream_col,
+                                                  rht_sign_mask, amax_in, _ref(out_row), _ref(out_col), stream)
 
 
 def nvfp4_gemm_lora_workspace_size(M, r):

@@ -203,6 +203,54 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, i
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, int64_t ldd, float* amax_out,
+                             uint16_t rht_sign_mask, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    nvfp4_status s;
+    if ((s = check_operand(A)) != NVFP4_OK) return s;
+    if ((s = check_operand(B)) != NVFP4_OK) return s;
+    if (A->cols != B->cols) return NVFP4_ERR_SHAPE;
+    if (!D || !amax_out) return NVFP4_ERR_INVALID_ARG;
+    const int64_t M = A->rows, N = B->rows, K = A->cols;
+    if (ldd < N) return NVFP4_ERR_SHAPE;
+    if (M % 16 != 0) return NVFP4_ERR_SHAPE;   // 16-row blocks of the rotated amax
+    if (!aligned16(D) || ldd % 8 != 0 || (reinterpret_cast<uintptr_t>(amax_out) & 3u) != 0)
+        return NVFP4_ERR_ALIGNMENT;
+    if (ceil_div(M, 128) * ceil_div(N, 256) >= (int64_t(1) << 32)) return NVFP4_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (M == 0 || N == 0 || K == 0) {
+        // D = 0 (or empty): both maxima are 0
+        if (M && N &&
+            cudaMemset2DAsync(D, (size_t)(ldd * 2), 0, (size_t)(N * 2), (size_t)M, st) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        return cudaMemsetAsync(amax_out, 0, 2 * sizeof(float), st) == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+    }
+    const cudaError_t e = nvfp4::launch_gemm(to_operand(A), to_operand(B), D, ldd, false, st, nullptr, amax_out,
+                                             rht_sign_mask);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status nvfp4_quantize_row_col_rht_amax(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                             nvfp4_rounding rounding, uint64_t seed, uint64_t stream_row,
+                                             uint64_t stream_col, uint16_t rht_sign_mask, const float* amax_in,
+                                             const nvfp4_tensor* out_row, const nvfp4_tensor* out_col,
+                                             nvfp4_stream_t stream) {
+    if (rounding != NVFP4_ROUND_RNE && rounding != NVFP4_ROUND_SR) return NVFP4_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
+    if (cols % 16 != 0 || rows % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (!amax_in || (reinterpret_cast<uintptr_t>(amax_in) & 3u) != 0) return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status s;
+    if ((s = check_quantize_input(x, rows, cols, ld_x)) != NVFP4_OK) return s;
+    if ((s = check_target(out_row, rows, cols)) != NVFP4_OK) return s;
+    if ((s = check_target(out_col, cols, rows)) != NVFP4_OK) return s;
+    const QuantTarget tr = to_target(out_row), tc = to_target(out_col);
+    const cudaError_t e = nvfp4::launch_quantize_row_col_rht_amax(
+        static_cast<const uint16_t*>(x), rows, cols, ld_x, rounding == NVFP4_ROUND_SR, rht_sign_mask, seed, stream_row,
+        stream_col, amax_in, &tr, &tc, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 size_t nvfp4_gemm_lora_workspace_size(int64_t M, int64_t r) {
     if (M < 0 || r < 0) return 0;
     return (size_t)(M * r * 2) + 16;

@@ -100,6 +100,8 @@ struct Params {
     int tma_store;               // output written through the D tensor map (BF16 or FP32)
     int n_fast;                  // tile order: N tiles vary fastest (else M tiles)
     uint32_t lora_stages;        // 64-deep BF16 stages of the low-rank term per tile (0: none)
+    float* amax_out;             // [2]: max |D| and max |RHT along D's rows| (BF16 TMA path), or null
+    uint32_t rht_mask;
 };
 
 // Output tile of a linear tile index.  Tiles that run at the same time share
@@ -171,6 +173,48 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// The amax contributions of one 32-row x 64-column BF16 slice of the output
+// (128-byte swizzled, row j at j * 128 bytes): lane c takes columns 2c and
+// 2c + 1 down the 32 rows, i.e. two 16-row blocks per column, and folds in
+// max |x| and max |H16 D x| of each block, the transform in the quantizer's
+// order (signs, then butterfly stages 0..3 as (a + b, a - b)); the 1/4 is
+// applied to the final maximum, exactly.
+__device__ __forceinline__ void slice_amax(const uint8_t* slice, uint32_t lane, uint32_t rht_mask,
+                                           float& amax_plain, float& amax_rht) {
+    const uint32_t chunk = lane >> 2, word = (lane & 3u) * 4u;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        float t0[16], t1[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t j = 16u * blk + i;
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(slice + j * 128u + ((chunk ^ (j & 7u)) << 4) + word);
+            const uint32_t sgn = ((rht_mask >> i) & 1u) << 31;
+            t0[i] = __uint_as_float(w << 16);
+            t1[i] = __uint_as_float(w & 0xFFFF0000u);
+            amax_plain = fmaxf(amax_plain, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
+            t0[i] = __uint_as_float(__float_as_uint(t0[i]) ^ sgn);
+            t1[i] = __uint_as_float(__float_as_uint(t1[i]) ^ sgn);
+        }
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (i & (1 << st)) continue;
+                const float a0 = t0[i], b0 = t0[i | (1 << st)], a1 = t1[i], b1 = t1[i | (1 << st)];
+                t0[i] = __fadd_rn(a0, b0);
+                t0[i | (1 << st)] = __fsub_rn(a0, b0);
+                t1[i] = __fadd_rn(a1, b1);
+                t1[i | (1 << st)] = __fsub_rn(a1, b1);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax_rht = fmaxf(amax_rht, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
+    }
+}
+
+// kAmax: the epilogue also takes the output's two tensor amaxes (p.amax_out).
+template <bool kAmax>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                      const __grid_constant__ CUtensorMap tma_sfa, const __grid_constant__ CUtensorMap tma_sfb,
@@ -484,6 +528,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t half = (warp - kFirstEpiWarp) >> 2;     // 128-column half of the tile
         const float alpha = __fmul_rn(*p.sga, *p.sgb);
         const uint32_t leader_acc_empty = map_to_cta(smem_u32(acc_empty), 0);
+        // amax of the BF16 output for its quantization (rows of one warp are
+        // lanes, so a 16-row block of a column is 16 lanes): the plain max
+        // and the max after the RHT along the rows (sign of this lane's row,
+        // then butterfly stages by shuffles; stage s: lanes with bit s set
+        // take partner - t, the others t + partner)
+        float amax_plain = 0.0f, amax_rht = 0.0f;
         const uint32_t row_local = q * 32 + lane;
         uint32_t tiles_done = 0;
         for (uint32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
@@ -547,6 +597,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
                         bulk_commit_group();
                     }
+                    // the slice now holds this warp's 32 rows x 64 columns: read
+                    // it back by columns for the output's amax
+                    if constexpr (kAmax) slice_amax(slice, lane, p.rht_mask, amax_plain, amax_rht);
                 }
             } else if (p.tma_store && p.out_fp32) {
                 // FP32: four rounds of 32 columns through this warp's 4 KiB
@@ -635,6 +688,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++tiles_done;
         }
         if (p.tma_store && lane == 0) bulk_wait_all();
+        if constexpr (kAmax) {
+            amax_plain = warp_max(amax_plain);
+            amax_rht = warp_max(amax_rht);
+            if (lane == 0) {
+                // non-negative floats order like their bit patterns
+                atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(amax_plain));
+                atomicMax(reinterpret_cast<unsigned int*>(p.amax_out) + 1,
+                          __float_as_uint(__fmul_rn(amax_rht, 0.25f)));
+            }
+        }
     }
 
     // neither CTA frees tensor memory or exits while its peer may still use it
@@ -748,7 +811,7 @@ int max_active_pairs() {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvf4_kernel, &cfg) != cudaSuccess || n < 1)
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvf4_kernel<false>, &cfg) != cudaSuccess || n < 1)
             n = device_sm_count() / 2;
         pairs[dev] = n > 0 ? n : 1;
     }
@@ -784,13 +847,16 @@ int device_sm_count() {
 }
 
 cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int64_t ldd, bool out_fp32,
-                        cudaStream_t stream, const LowRank* lora) {
+                        cudaStream_t stream, const LowRank* lora, float* amax_out, uint32_t rht_mask) {
     static bool attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
         cudaError_t e =
-            cudaFuncSetAttribute(gemm_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+            cudaFuncSetAttribute(gemm_nvf4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_nvf4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -816,6 +882,14 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     p.vec_store = ((reinterpret_cast<uintptr_t>(d) & 15u) == 0 && (ldd * esz) % 16 == 0) ? 1 : 0;
     p.tma_store = (p.vec_store && make_output_map(&md, d, a.rows, b.rows, ldd, out_fp32)) ? 1 : 0;
     if (!p.tma_store) md = ma;   // unused by the kernel; any valid map
+    if (amax_out) {
+        // the amax is taken in the BF16 TMA-store epilogue
+        if (out_fp32 || !p.tma_store) return cudaErrorInvalidValue;
+        const cudaError_t e = cudaMemsetAsync(amax_out, 0, 2 * sizeof(float), stream);
+        if (e != cudaSuccess) return e;
+        p.amax_out = amax_out;
+        p.rht_mask = rht_mask;
+    }
     CUtensorMap mu = ma, mv = ma;  // unused without a low-rank term
     if (lora) {
         if (!make_bf16_rows_map(&mu, lora->u_scaled, a.rows, lora->r, lora->r) ||
@@ -831,7 +905,10 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     const uint32_t tiles = p.m_tiles * p.n_tiles;
     const uint32_t pairs = (uint32_t)max_active_pairs();
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
-    gemm_nvf4_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, mu, mv, p);
+    if (p.amax_out)
+        gemm_nvf4_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, mu, mv, p);
+    else
+        gemm_nvf4_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, mu, mv, p);
     return cudaGetLastError();
 }
 

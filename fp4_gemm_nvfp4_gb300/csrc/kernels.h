@@ -39,6 +39,13 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
 
 // Row-wise 1x16 without RHT and col-wise 1x16 with RHT of one input, sharing
 // one amax pass (workspace as for launch_quantize).
+// As launch_quantize_row_col_rht with the two tensor amaxes given (amax_in[0]
+// plain, amax_in[1] rotated; e.g. from the producing GEMM): no amax pass.
+cudaError_t launch_quantize_row_col_rht_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool sr,
+                                             uint32_t sign_mask, uint64_t seed, uint64_t stream_row,
+                                             uint64_t stream_col, const float* amax_in, const QuantTarget* row,
+                                             const QuantTarget* col, cudaStream_t stream);
+
 cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool sr,
                                        uint32_t sign_mask, uint64_t seed, uint64_t stream_row, uint64_t stream_col,
                                        const QuantTarget* row, const QuantTarget* col, float* workspace,
@@ -65,8 +72,12 @@ struct LowRank {
     void* u_scaled;
 };
 
+// amax_out (BF16 output only): [0] = max |D|, [1] = max |U d| over the 16-row
+// blocks of each column (the RHT U = H16 diag(rht_mask) / 4 along D's rows),
+// the two tensor amaxes nvfp4_quantize_row_col_rht takes of D.
 cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int64_t ldd, bool out_fp32,
-                        cudaStream_t stream, const LowRank* lora = nullptr);
+                        cudaStream_t stream, const LowRank* lora = nullptr, float* amax_out = nullptr,
+                        uint32_t rht_mask = 0);
 
 // Read and clear the GEMM kernels' device status word (synchronous).
 cudaError_t gemm_read_and_clear_status(unsigned int* status);

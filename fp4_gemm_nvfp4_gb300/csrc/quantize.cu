@@ -995,6 +995,18 @@ cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t
     return cudaGetLastError();
 }
 
+cudaError_t launch_quantize_row_col_rht_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool sr,
+                                             uint32_t sign_mask, uint64_t seed, uint64_t stream_row,
+                                             uint64_t stream_col, const float* amax_in, const QuantTarget* row,
+                                             const QuantTarget* col, cudaStream_t st) {
+    cudaError_t err;
+    if ((err = clear_scale_padding(row, st)) != cudaSuccess) return err;
+    if ((err = clear_scale_padding(col, st)) != cudaSuccess) return err;
+    // the encode pass reduces "partials": here one value each
+    return launch_pair_encode(x, rows, cols, ld_x, sr, true, sign_mask, seed, stream_row, stream_col, row, col,
+                              amax_in, amax_in + 1, 1, false, st);
+}
+
 cudaError_t launch_requantize_col_rht(const QuantTarget* in, bool sr, uint32_t sign_mask, uint64_t seed,
                                       uint64_t stream_id, const QuantTarget* out, float* workspace, cudaStream_t st) {
     cudaError_t err;

@@ -161,6 +161,39 @@ def gemm(a: NVFP4Operand, b: NVFP4Operand, out_dtype=torch.bfloat16, out: Option
 
 
 
+def gemm_amax(a: NVFP4Operand, b: NVFP4Operand, rht_mask: int, out: Optional[torch.Tensor] = None,
+              amax: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """D = A * B^T in BF16 plus D's two tensor amaxes (nvfp4_gemm_amax): amax[0]
+    plain, amax[1] after the RHT along D's rows with rht_mask."""
+    if out is None:
+        out = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.codes.device)
+    if amax is None:
+        amax = torch.empty(2, dtype=torch.float32, device=a.codes.device)
+    status = capi.nvfp4_gemm_amax(a.struct(), b.struct(), out.data_ptr(), out.stride(0), amax.data_ptr(),
+                                  rht_mask, None, 0, stream_handle(stream))
+    capi.check(status, "nvfp4_gemm_amax")
+    return out, amax
+
+
+def quantize_row_col_rht_amax(x: torch.Tensor, rht_mask: int, amax: torch.Tensor, *, sr: bool = False,
+                              seed: int = 0, stream_row: int = 0, stream_col: int = 0,
+                              out_row: Optional[NVFP4Operand] = None, out_col: Optional[NVFP4Operand] = None,
+                              stream=None) -> Tuple[NVFP4Operand, NVFP4Operand]:
+    """quantize_row_col_rht with the two tensor amaxes given (nvfp4_quantize_row_col_rht_amax)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    assert amax.dtype == torch.float32 and amax.numel() >= 2
+    rows, cols = x.shape
+    if out_row is None:
+        out_row = alloc_operand(rows, cols, x.device)
+    if out_col is None:
+        out_col = alloc_operand(cols, rows, x.device)
+    status = capi.nvfp4_quantize_row_col_rht_amax(
+        x.data_ptr(), rows, cols, x.stride(0), capi.NVFP4_ROUND_SR if sr else capi.NVFP4_ROUND_RNE, seed,
+        stream_row, stream_col, rht_mask, amax.data_ptr(), out_row.struct(), out_col.struct(), stream_handle(stream))
+    capi.check(status, "nvfp4_quantize_row_col_rht_amax")
+    return out_row, out_col
+
+
 def gemm_lora(a: NVFP4Operand, b: NVFP4Operand, u: torch.Tensor, v: torch.Tensor, beta: float,
               out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None, scratch: Optional[torch.Tensor] = None,
               stream=None) -> torch.Tensor:

@@ -254,6 +254,37 @@ NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_tensor *A, const nvfp4_tensor *B, 
                         nvfp4_stream_t stream);
 
 /*
+ * nvfp4_gemm_amax -- nvfp4_gemm with BF16 output that also takes, in its
+ * epilogue, the two tensor amaxes the quantization of D needs [FS App. 9:
+ * quantization fused with the operation that produces its input; SURVEY f1]:
+ *  amax_out[0]  max |D| over the BF16 outputs (the row-wise operand's amax);
+ *  amax_out[1]  max |U d| over the 16-row blocks d of each column of D, with
+ *               U = H16 * diag(rht_sign_mask) / 4 (the col-wise RHT operand's
+ *               amax), in the rounding order of nvfp4_quantize_row_col_rht.
+ * amax_out is device memory (2 floats, 4-byte aligned), overwritten.  Feed it
+ * to nvfp4_quantize_row_col_rht_amax with the same mask: the result equals
+ * nvfp4_quantize_row_col_rht of D without its amax pass.
+ * Requirements as nvfp4_gemm plus: M % 16 == 0 [SHAPE]; D 16-byte aligned
+ * and ldd % 8 == 0 [ALIGNMENT].
+ */
+NVFP4_API nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor *A, const nvfp4_tensor *B, void *D, int64_t ldd,
+                                       float *amax_out, uint16_t rht_sign_mask, void *workspace,
+                                       size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_quantize_row_col_rht_amax -- nvfp4_quantize_row_col_rht with the two
+ * tensor amaxes given (amax_in[0] plain, amax_in[1] rotated; device memory,
+ * e.g. from nvfp4_gemm_amax): one encode pass over x, no amax pass, no
+ * workspace.  Codes and scales are bit-identical to nvfp4_quantize_row_col_rht
+ * when amax_in holds the true maxima.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_row_col_rht_amax(const void *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                                       nvfp4_rounding rounding, uint64_t seed, uint64_t stream_row,
+                                                       uint64_t stream_col, uint16_t rht_sign_mask,
+                                                       const float *amax_in, const nvfp4_tensor *out_row,
+                                                       const nvfp4_tensor *out_col, nvfp4_stream_t stream);
+
+/*
  * nvfp4_gemm_lora -- nvfp4_gemm plus the BF16 low-rank branch of a LoRA-SVD
  * linear projection [FS Sec. 3.2 Eq. (1): Y = Q(X) Q(W_res)^T + beta (X L1^T) L2^T,
  * dX = Q(dY) Q(W_res) + beta (dY L2) L1; fused into the GEMM as FS App. 9

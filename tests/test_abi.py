@@ -174,6 +174,27 @@ def test_gemm_lora_validation(lib):
     assert capi.nvfp4_gemm_lora_workspace_size(100, 64) >= 100 * 64 * 2
 
 
+def test_fused_amax_validation(lib):
+    """Rejected on the host (no kernel ever sees the fake addresses)."""
+    E = capi
+    ws = None
+    assert capi.nvfp4_gemm_amax(tensor(24, 128), tensor(96, 128), A16 * 9, 96, A16 * 13, 0x1234, ws, 0,
+                                None) == E.NVFP4_ERR_SHAPE                                      # M % 16
+    assert capi.nvfp4_gemm_amax(tensor(64, 128), tensor(96, 128), A16 * 9 + 8, 96, A16 * 13, 0x1234, ws, 0,
+                                None) == E.NVFP4_ERR_ALIGNMENT
+    assert capi.nvfp4_gemm_amax(tensor(64, 128), tensor(96, 128), A16 * 9, 100, A16 * 13, 0x1234, ws, 0,
+                                None) == E.NVFP4_ERR_ALIGNMENT                                  # ldd % 8
+    assert capi.nvfp4_gemm_amax(tensor(64, 128), tensor(96, 128), A16 * 9, 96, None, 0x1234, ws, 0,
+                                None) == E.NVFP4_ERR_INVALID_ARG
+    q = capi.nvfp4_quantize_row_col_rht_amax
+    assert q(A16 * 4, 64, 64, 64, 0, 0, 0, 0, 0x1234, None, tensor(64, 64), tensor(64, 64),
+             None) == E.NVFP4_ERR_INVALID_ARG                                                   # amax_in
+    assert q(A16 * 4, 24, 64, 64, 0, 0, 0, 0, 0x1234, A16 * 13, tensor(24, 64), tensor(64, 24),
+             None) == E.NVFP4_ERR_SHAPE
+    assert q(A16 * 4, 64, 64, 64, 7, 0, 0, 0, 0x1234, A16 * 13, tensor(64, 64), tensor(64, 64),
+             None) == E.NVFP4_ERR_INVALID_ARG
+
+
 def test_rht_quantize_rejects_2d(lib):
     ws = capi.nvfp4_quantize_workspace_size(64, 64, 3)
     st = capi.nvfp4_rht_quantize(A16 * 4, 64, 64, 64, capi.NVFP4_SCALE_16X16, 0, 0, 0, 1,
