@@ -108,7 +108,21 @@ GEMMS = [
     ("wgrad_down", ("dY_down.pair", "col"), ("H.pair", "col")),
     ("wgrad_up", ("dY_up.pair", "col"), ("X.pair", "col")),
 ]
+# The layer's dataflow: H is the Fprop-up output and dY_up the Dgrad-down
+# output (the activation between is not part of this step), so those two
+# GEMMs write them and take their two tensor amaxes in the epilogue, and the
+# pair quantization of H and dY_up runs without its amax pass.  Off with
+# --no-fuse-amax (then H and dY_up are inputs like X and dY_down).
+FUSE_AMAX = True
+PRODUCED = {"H": "fprop_up", "dY_up": "dgrad_down"}
+ORDER = [("q", "X.pair"), ("q", "W_up.2d"), ("q", "W_down.2d"), ("g", "fprop_up"), ("q", "H.pair"),
+         ("g", "fprop_down"), ("q", "dY_down.pair"), ("g", "dgrad_down"), ("q", "dY_up.pair"),
+         ("g", "wgrad_down"), ("g", "dgrad_up"), ("g", "wgrad_up")]
 SHAPES = {}
+
+
+def produced(src):
+    return FUSE_AMAX and src in PRODUCED
 
 
 def set_tokens(tokens):
@@ -134,9 +148,10 @@ def host_inputs(seed_base=4):
 def quant_launches(kw):
     """Kernels one quantize call launches: an amax pass and an encode pass per
     RHT orientation, else one amax pass plus one encode pass (row-wise plus
-    col-wise RHT of one input: one shared amax pass and one encode pass)."""
+    col-wise RHT of one input: one shared amax pass and one encode pass; with
+    the amax taken by the producing GEMM, the encode pass only)."""
     if kw.get("pair"):
-        return 2
+        return 1 if kw.get("amax_given") else 2
     if kw.get("rht_mask") is not None:
         return 2 * (int(kw.get("rowwise", True)) + int(kw.get("colwise", False)))
     if kw.get("two_d"):
@@ -150,7 +165,7 @@ def quant_bytes(rows, cols, kw):
     1/16 B of scales per element per emitted orientation."""
     n = rows * cols
     if kw.get("pair"):                      # one amax pass, one encode pass emitting both orientations
-        return n * 2 * 2 + n * 2 * (0.5 + 1 / 16)
+        return n * 2 * (1 if kw.get("amax_given") else 2) + n * 2 * (0.5 + 1 / 16)
     outs = int(kw.get("rowwise", True)) + int(kw.get("colwise", False))
     if kw.get("rht_mask") is not None:      # one amax and one encode pass per orientation
         amax_passes, encode_reads = outs, outs
@@ -175,6 +190,8 @@ class Step:
             kw = dict(kw)
             if kw.get("rht_mask") == "mask":
                 kw["rht_mask"] = mask
+            if produced(src):
+                kw["amax_given"] = True
             rows, cols = SHAPES[src]
             pair = kw.get("pair", False)
             row = ops.alloc_operand(rows, cols) if pair or kw.get("rowwise", True) else None
@@ -182,10 +199,16 @@ class Step:
             self.q[name] = (row, col)
             self.kw[name] = kw
         self.out = {}
+        self.amax = {}
         for gname, (an, ao), (bn, bo) in GEMMS:
             a = self.operand(an, ao)
             b = self.operand(bn, bo)
-            self.out[gname] = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device="cuda")
+            src = [k for k, g in PRODUCED.items() if g == gname]
+            if FUSE_AMAX and src:
+                self.out[gname] = self.x[src[0]]      # the GEMM writes the tensor the step quantizes next
+                self.amax[gname] = torch.zeros(2, dtype=torch.float32, device="cuda")
+            else:
+                self.out[gname] = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device="cuda")
         self.ws = ops.Workspace()
 
     def operand(self, name, orient):
@@ -208,7 +231,12 @@ class Step:
                 continue
             row, col = self.q[name]
             kw = self.kw[name]
-            if kw.get("pair"):
+            if kw.get("amax_given"):
+                self.ops.quantize_row_col_rht_amax(self.x[src], kw["rht_mask"], self.amax[PRODUCED[src]],
+                                                   sr=kw.get("sr", False), seed=self.seed,
+                                                   stream_row=kw.get("stream_row", 0),
+                                                   stream_col=kw.get("stream_col", 0), out_row=row, out_col=col)
+            elif kw.get("pair"):
                 self.ops.quantize_row_col_rht(self.x[src], kw["rht_mask"], sr=kw.get("sr", False), seed=self.seed,
                                               stream_row=kw.get("stream_row", 0),
                                               stream_col=kw.get("stream_col", 0), out_row=row, out_col=col,
@@ -220,12 +248,21 @@ class Step:
         for gname, (an, ao), (bn, bo) in GEMMS:
             if only is not None and gname != only:
                 continue
-            self.ops.gemm(self.operand(an, ao), self.operand(bn, bo), out=self.out[gname])
+            if gname in self.amax:
+                self.ops.gemm_amax(self.operand(an, ao), self.operand(bn, bo), self.mask, out=self.out[gname],
+                                   amax=self.amax[gname])
+            else:
+                self.ops.gemm(self.operand(an, ao), self.operand(bn, bo), out=self.out[gname])
 
     def run(self):
-        """Enqueue one step (every quantize call, then the six GEMMs)."""
-        self.run_quantize()
-        self.run_gemms()
+        """Enqueue one step: in the layer's dataflow order when the producing
+        GEMMs take the amax, else every quantize call, then the six GEMMs."""
+        if FUSE_AMAX:
+            for kind, name in ORDER:
+                (self.run_quantize if kind == "q" else self.run_gemms)(name)
+        else:
+            self.run_quantize()
+            self.run_gemms()
 
 
 # ----------------------------------------------------------------- clocks --
@@ -414,7 +451,7 @@ def measure(args):
 
     # ---- end to end: pinned host inputs in and the six outputs out, every step
     pinned_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
-                 for k, v in host.items()}
+                 for k, v in host.items() if not produced(k)}
     pinned_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in step.out.items()}
     h2d = sum(t.numel() * 2 for t in pinned_in.values())
     d2h = sum(t.numel() * 2 for t in pinned_out.values())
@@ -452,6 +489,10 @@ def measure(args):
                 "frac": round(gemm_tflops / fp4_peak, 4), "traffic": measured_traffic("gemm"),
                 "traffic_basis": "DRAM bytes per step over the class's launches (ncu)",
                 "peak_source": f"{peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal fp4/bf16)"}
+        if FUSE_AMAX:
+            roof["note"] = ("fprop_up and dgrad_down also take their BF16 output's two tensor amaxes in the "
+                            "epilogue (the work of the quantizer's amax pass, moved there); achieved counts "
+                            "only the FP4 GEMM FLOPs")
     else:
         roof = {"kernel": "quantize (amax + encode passes of the step)", "bound": "hbm",
                 "achieved": round(quant_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -468,6 +509,8 @@ def measure(args):
         "config": {"workload": workload_name(), "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
                    "gemm_gflop_per_step": round(flops / 1e9, 1), "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (one step touches about 2.5 GB)",
+                   "dataflow": ("H and dY_up written by fprop_up and dgrad_down, their tensor amax taken in "
+                                "those GEMMs' epilogue" if FUSE_AMAX else "all six bf16 tensors are inputs"),
                    "launch": "each step is one CUDA graph replay"},
         "roofline": roof,
         "gemm_tflops": round(gemm_tflops, 1),
@@ -600,12 +643,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fuse-amax", action="store_true",
+                    help="quantize H and dY_up as inputs with their own amax pass (no fused GEMM amax)")
     ap.add_argument("--sweep", choices=["c5"], default=None,
                     help="instead of the layer step, run the quantizer bandwidth sweep (one JSON line per case)")
     ap.add_argument("--tokens", type=int, default=TOKENS,
                     help="tokens of the layer step (16384 is the benchmarked workload)")
     args = ap.parse_args()
     set_tokens(args.tokens)
+    global FUSE_AMAX
+    FUSE_AMAX = not args.no_fuse_amax
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
     if args.sweep == "c5":
