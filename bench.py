@@ -1,6 +1,8 @@
 """Benchmark: the full NVFP4 linear-layer step of the 3B model's FFN at 16384
-tokens on one GB300 (quantize every operand, then Fprop / Dgrad / Wgrad of the
-up 3072->9216 and down 9216->3072 projections).
+tokens on one GB300 (Fprop / Dgrad / Wgrad of the up 3072->9216 and down
+9216->3072 projections, each operand quantized before its first use; H and
+dY_up are the outputs of Fprop-up and Dgrad-down, whose epilogues take their
+tensor amaxes).
 
 Prints one JSON line.  `value` is the step's GEMM work (6 GEMMs x 2*M*N*K)
 divided by the device time of the whole step (all quantize and GEMM kernels),

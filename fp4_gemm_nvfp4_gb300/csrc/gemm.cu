@@ -173,43 +173,62 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Packed binary32 pairs (two columns in one 64-bit register pair): each lane
+// of an add.f32x2 / sub.f32x2 rounds like the scalar operation.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ void f32x2_butterfly(uint64_t& a, uint64_t& b) {
+    uint64_t s, d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(a), "l"(b));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    a = s;
+    b = d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // The amax contributions of one 32-row x 64-column BF16 slice of the output
 // (128-byte swizzled, row j at j * 128 bytes): lane c takes columns 2c and
 // 2c + 1 down the 32 rows, i.e. two 16-row blocks per column, and folds in
 // max |x| and max |H16 D x| of each block, the transform in the quantizer's
-// order (signs, then butterfly stages 0..3 as (a + b, a - b)); the 1/4 is
-// applied to the final maximum, exactly.
+// order (signs, then butterfly stages 0..3 as (a + b, a - b)), both columns
+// at once in packed pairs; the 1/4 is applied to the final maximum, exactly.
 __device__ __forceinline__ void slice_amax(const uint8_t* slice, uint32_t lane, uint32_t rht_mask,
                                            float& amax_plain, float& amax_rht) {
     const uint32_t chunk = lane >> 2, word = (lane & 3u) * 4u;
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
-        float t0[16], t1[16];
+        uint64_t t[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint32_t j = 16u * blk + i;
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(slice + j * 128u + ((chunk ^ (j & 7u)) << 4) + word);
-            const uint32_t sgn = ((rht_mask >> i) & 1u) << 31;
-            t0[i] = __uint_as_float(w << 16);
-            t1[i] = __uint_as_float(w & 0xFFFF0000u);
-            amax_plain = fmaxf(amax_plain, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
-            t0[i] = __uint_as_float(__float_as_uint(t0[i]) ^ sgn);
-            t1[i] = __uint_as_float(__float_as_uint(t1[i]) ^ sgn);
+            uint32_t w = *reinterpret_cast<const uint32_t*>(slice + j * 128u + ((chunk ^ (j & 7u)) << 4) + word);
+            w ^= ((rht_mask >> i) & 1u) * 0x80008000u;     // D: both columns' sign bits
+            const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+            amax_plain = fmax3(amax_plain, fabsf(lo), fabsf(hi));
+            t[i] = f32x2_pack(lo, hi);
         }
 #pragma unroll
         for (int st = 0; st < 4; ++st) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                if (i & (1 << st)) continue;
-                const float a0 = t0[i], b0 = t0[i | (1 << st)], a1 = t1[i], b1 = t1[i | (1 << st)];
-                t0[i] = __fadd_rn(a0, b0);
-                t0[i | (1 << st)] = __fsub_rn(a0, b0);
-                t1[i] = __fadd_rn(a1, b1);
-                t1[i | (1 << st)] = __fsub_rn(a1, b1);
-            }
+            for (int i = 0; i < 16; ++i)
+                if (!(i & (1 << st))) f32x2_butterfly(t[i], t[i | (1 << st)]);
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) amax_rht = fmaxf(amax_rht, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
+        for (int i = 0; i < 16; ++i) {
+            float lo, hi;
+            f32x2_unpack(t[i], lo, hi);
+            amax_rht = fmax3(amax_rht, fabsf(lo), fabsf(hi));
+        }
     }
 }
 
@@ -582,6 +601,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
+                        // round 0's columns, still in the slice: their amax
+                        // waits until the accumulator is back with the MMAs
+                        if constexpr (kAmax) slice_amax(slice, lane, p.rht_mask, amax_plain, amax_rht);
                     }
                     // the slice's previous store must have read it
                     if (lane == 0) bulk_wait_read_all();
@@ -598,8 +620,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         bulk_commit_group();
                     }
                     // the slice now holds this warp's 32 rows x 64 columns: read
-                    // it back by columns for the output's amax
-                    if constexpr (kAmax) slice_amax(slice, lane, p.rht_mask, amax_plain, amax_rht);
+                    // it back by columns for the output's amax (round 0's is
+                    // taken in round 1, after the accumulator's release)
+                    if constexpr (kAmax)
+                        if (r == 1) slice_amax(slice, lane, p.rht_mask, amax_plain, amax_rht);
                 }
             } else if (p.tma_store && p.out_fp32) {
                 // FP32: four rounds of 32 columns through this warp's 4 KiB
