@@ -27,10 +27,13 @@
 //               barrier, which therefore completes when both CTAs' tiles have
 //               landed and all eight scale warps are done;
 //   warps 8-15  epilogue, two per lane quadrant (one per 128-column half):
-//               drain the FP32 accumulator, scale by s_gA * s_gB, release the
-//               accumulator to the leader, stage BF16 results in 128-byte-
-//               swizzled shared memory and write them with TMA stores (FP32
-//               and unaligned outputs: direct stores).
+//               load the warp's 128 accumulator columns into registers under
+//               one wait, release the accumulator to the leader, scale by
+//               s_gA * s_gB, stage the results in 128-byte-swizzled shared
+//               memory and write them with TMA stores (unaligned outputs:
+//               direct stores).
+// The warp groups split the register file with setmaxnreg (64 / 72 / 184 x2
+// per thread) so that the epilogue holds a whole accumulator half.
 // Every mbarrier wait is bounded (2 s); a wait that runs out sets the status
 // word read by nvfp4_device_error and both CTAs drain and exit.
 #include <cuda.h>
@@ -159,11 +162,8 @@ __device__ __forceinline__ void record_timeout(volatile uint32_t* abort_flag) {
     atomicOr(&g_gemm_status, kStatusTimeoutBit);
 }
 
-// Named barriers over the epilogue warps (id 1) and over the scale warps
-// (id 2); id 0 and the cluster barrier are used elsewhere.
-__device__ __forceinline__ void epilogue_bar() {
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kNumEpiWarps) : "memory");
-}
+// Named barrier over the scale warps (id 2); id 0 and the cluster barrier
+// are used elsewhere.
 __device__ __forceinline__ void scale_bar() {
     asm volatile("bar.sync 2, %0;" ::"n"(32 * kNumSfWarps) : "memory");
 }
@@ -250,7 +250,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t* drain = acc_empty + 1;             // leader
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
-    volatile uint32_t* epi_ok = tmem_slot + 2;   // [2]: accumulator-ready verdicts, by tile parity
     volatile uint32_t* sf_ok = tmem_slot + 4;    // [2]: scales-landed verdicts, by stage-count parity
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
@@ -293,178 +292,187 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t num_tiles = p.m_tiles * p.n_tiles;
     const uint32_t first_tile = cluster_id_x(), tile_stride = num_clusters_x();
 
-    if (warp == kProdAWarp || warp == kProdBWarp || warp == kProdSfWarp) {
-        if (lane == 0) {
-            // ------------------------------------------------- producers
-            // Three warps, one or two copies each per stage: a single thread
-            // cannot issue a stage's five copies fast enough.
-            uint32_t armed = 0, armed_parity = 0;   // per stage: copies issued, parity of their phase
-            uint32_t stage = 0, phase = 0;
-            const uint32_t leader_full0 = map_to_cta(smem_u32(full), 0);
-            for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
-                uint32_t mt, nt;
-                tile_coords(tile, p, mt, nt);
-                for (uint32_t ks = 0; ks < p.kstages; ++ks) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, kTimeoutNs)) {
-                        record_timeout(abort_flag);
-                        break;
+    // Registers per thread by warp group (setmaxnreg): producers and MMA
+    // issuer 64, scale warps 72, epilogue 184, so that each epilogue warp
+    // holds its whole 128-column accumulator half in registers and hands the
+    // accumulator back after one wait.  The launch gives all 512 threads 128
+    // (checked on the host): 128 * (64 + 72) + 256 * 184 = 64512 <= 65536.
+    if (warp < (uint32_t)kFirstSfWarp) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
+        if (warp != (uint32_t)kMmaWarp) {
+            if (lane == 0) {
+                // ------------------------------------------------- producers
+                // Three warps, one or two copies each per stage: a single thread
+                // cannot issue a stage's five copies fast enough.
+                uint32_t armed = 0, armed_parity = 0;   // per stage: copies issued, parity of their phase
+                uint32_t stage = 0, phase = 0;
+                const uint32_t leader_full0 = map_to_cta(smem_u32(full), 0);
+                for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
+                    uint32_t mt, nt;
+                    tile_coords(tile, p, mt, nt);
+                    for (uint32_t ks = 0; ks < p.kstages; ++ks) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, kTimeoutNs)) {
+                            record_timeout(abort_flag);
+                            break;
+                        }
+                        if (*abort_flag) break;
+                        uint8_t* st = smem + stage * kStageBytes;
+                        const uint32_t leader_full = leader_full0 + stage * 8u;
+                        armed |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        if (warp == kProdAWarp) {
+                            if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (kABytes + kBBytes));
+                            tma_load_2d_pair(st, &tma_a, leader_full, (int32_t)(ks * kBKBytes),
+                                             (int32_t)(mt * kPairM + rank * kCtaM));
+                        } else if (warp == kProdBWarp) {
+                            tma_load_2d_pair(st + kABytes, &tma_b, leader_full, (int32_t)(ks * kBKBytes),
+                                             (int32_t)(nt * kBN + rank * kCtaN));
+                        } else {
+                            // scale boxes: 4 groups of 512 bytes per 128-row tile;
+                            // groups past K and row tiles past M / N read as zero
+                            uint8_t* sfa_s = st + kABytes + kBBytes;
+                            mbar_arrive_expect_tx(&sf_full[stage], kSFABytes + kSFBBytes);
+                            tma_load_3d(sfa_s, &tma_sfa, &sf_full[stage], 0, (int32_t)(ks * kKStepsPerStage),
+                                        (int32_t)(2 * mt + rank));
+                            tma_load_3d(sfa_s + kSFABytes, &tma_sfb, &sf_full[stage], 0,
+                                        (int32_t)(ks * kKStepsPerStage), (int32_t)(2 * nt));
+                        }
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    if (*abort_flag) break;
-                    uint8_t* st = smem + stage * kStageBytes;
-                    const uint32_t leader_full = leader_full0 + stage * 8u;
-                    armed |= 1u << stage;
-                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    if (warp == kProdAWarp) {
-                        if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (kABytes + kBBytes));
-                        tma_load_2d_pair(st, &tma_a, leader_full, (int32_t)(ks * kBKBytes),
-                                         (int32_t)(mt * kPairM + rank * kCtaM));
-                    } else if (warp == kProdBWarp) {
-                        tma_load_2d_pair(st + kABytes, &tma_b, leader_full, (int32_t)(ks * kBKBytes),
-                                         (int32_t)(nt * kBN + rank * kCtaN));
-                    } else {
-                        // scale boxes: 4 groups of 512 bytes per 128-row tile;
-                        // groups past K and row tiles past M / N read as zero
-                        uint8_t* sfa_s = st + kABytes + kBBytes;
-                        mbar_arrive_expect_tx(&sf_full[stage], kSFABytes + kSFBBytes);
-                        tma_load_3d(sfa_s, &tma_sfa, &sf_full[stage], 0, (int32_t)(ks * kKStepsPerStage),
-                                    (int32_t)(2 * mt + rank));
-                        tma_load_3d(sfa_s + kSFABytes, &tma_sfb, &sf_full[stage], 0, (int32_t)(ks * kKStepsPerStage),
-                                    (int32_t)(2 * nt));
-                    }
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    // the low-rank term: 64 BF16 columns of U' and V per stage in
+                    // the A and B slots (the same 16 KiB boxes), no scales
+                    for (uint32_t ls = 0; ls < p.lora_stages && !*abort_flag; ++ls) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, kTimeoutNs)) {
+                            record_timeout(abort_flag);
+                            break;
+                        }
+                        uint8_t* st = smem + stage * kStageBytes;
+                        const uint32_t leader_full = leader_full0 + stage * 8u;
+                        armed |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        if (warp == kProdAWarp) {
+                            if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (kABytes + kBBytes));
+                            tma_load_2d_pair(st, &tma_u, leader_full, (int32_t)(ls * 64u),
+                                             (int32_t)(mt * kPairM + rank * kCtaM));
+                        } else if (warp == kProdBWarp) {
+                            tma_load_2d_pair(st + kABytes, &tma_v, leader_full, (int32_t)(ls * 64u),
+                                             (int32_t)(nt * kBN + rank * kCtaN));
+                        } else {
+                            mbar_arrive(&sf_full[stage]);
+                        }
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
-                // the low-rank term: 64 BF16 columns of U' and V per stage in
-                // the A and B slots (the same 16 KiB boxes), no scales
-                for (uint32_t ls = 0; ls < p.lora_stages && !*abort_flag; ++ls) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, kTimeoutNs)) {
-                        record_timeout(abort_flag);
-                        break;
-                    }
-                    uint8_t* st = smem + stage * kStageBytes;
-                    const uint32_t leader_full = leader_full0 + stage * 8u;
-                    armed |= 1u << stage;
-                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    if (warp == kProdAWarp) {
-                        if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (kABytes + kBBytes));
-                        tma_load_2d_pair(st, &tma_u, leader_full, (int32_t)(ls * 64u),
-                                         (int32_t)(mt * kPairM + rank * kCtaM));
-                    } else if (warp == kProdBWarp) {
-                        tma_load_2d_pair(st + kABytes, &tma_v, leader_full, (int32_t)(ls * 64u),
-                                         (int32_t)(nt * kBN + rank * kCtaN));
-                    } else {
-                        mbar_arrive(&sf_full[stage]);
-                    }
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                // every copy must land before the pair exits: the leader's full
+                // barriers count both CTAs' tile bytes, sf_full this CTA's scales
+    #pragma unroll
+                for (int s = 0; s < kStages; ++s) {
+                    if (!((armed >> s) & 1u)) continue;
+                    const uint32_t par = (armed_parity >> s) & 1u;
+                    if (warp == kProdAWarp && leader) (void)mbar_wait_cluster(&full[s], par, kTimeoutNs);
+                    if (warp == kProdSfWarp) (void)mbar_wait(&sf_full[s], par, kTimeoutNs);
                 }
             }
-            // every copy must land before the pair exits: the leader's full
-            // barriers count both CTAs' tile bytes, sf_full this CTA's scales
-#pragma unroll
-            for (int s = 0; s < kStages; ++s) {
-                if (!((armed >> s) & 1u)) continue;
-                const uint32_t par = (armed_parity >> s) & 1u;
-                if (warp == kProdAWarp && leader) (void)mbar_wait_cluster(&full[s], par, kTimeoutNs);
-                if (warp == kProdSfWarp) (void)mbar_wait(&sf_full[s], par, kTimeoutNs);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        if (leader && lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            // The tensor pipe only stays busy while this thread keeps up with
-            // it, so the loop body is one barrier wait, the stage's four MMAs
-            // (one asm block, descriptors built from 32-bit low words) and one
-            // commit, with every stage address advanced by an add.  (Splitting
-            // the four MMAs to wait for the next stage in between measured
-            // slower.)
-            constexpr uint32_t kStageDesc = kStageBytes >> 4;   // descriptor address units
-            constexpr uint32_t kBOff = kABytes >> 4;
-            const uint64_t desc0 = smem_desc(smem_u32(smem), 16, 1024, 2);
-            const uint32_t lo0 = (uint32_t)desc0, hi = (uint32_t)(desc0 >> 32);
-            const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
-            const uint32_t sfc0 = tmem + kSfCol0;
-            const uint32_t acc = tmem + kAccCol;
-            const uint32_t kst = p.kstages;
-            const bool tail = p.last_nk != (uint32_t)kKStepsPerStage;
-            uint32_t stage = 0, phase = 0, tiles_done = 0;
-            uint32_t alo = lo0, sfc = sfc0, fa = full0, ea = empty0;
-            for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
-                if (!mbar_wait_cluster(acc_empty, (tiles_done & 1u) ^ 1u, kTimeoutNs)) {
-                    record_timeout(abort_flag);
-                    break;
-                }
-                tc_fence_after();
-                bool ok = true;
-                for (uint32_t ks = 0; ks < kst; ++ks) {
-                    if (!mbar_wait_addr(fa, phase, kTimeoutNs)) {
+        } else {
+            if (leader && lane == 0) {
+                // ------------------------------------------------ MMA issuer
+                // The tensor pipe only stays busy while this thread keeps up with
+                // it, so the loop body is one barrier wait, the stage's four MMAs
+                // (one asm block, descriptors built from 32-bit low words) and one
+                // commit, with every stage address advanced by an add.  (Splitting
+                // the four MMAs to wait for the next stage in between measured
+                // slower.)
+                constexpr uint32_t kStageDesc = kStageBytes >> 4;   // descriptor address units
+                constexpr uint32_t kBOff = kABytes >> 4;
+                const uint64_t desc0 = smem_desc(smem_u32(smem), 16, 1024, 2);
+                const uint32_t lo0 = (uint32_t)desc0, hi = (uint32_t)(desc0 >> 32);
+                const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
+                const uint32_t sfc0 = tmem + kSfCol0;
+                const uint32_t acc = tmem + kAccCol;
+                const uint32_t kst = p.kstages;
+                const bool tail = p.last_nk != (uint32_t)kKStepsPerStage;
+                uint32_t stage = 0, phase = 0, tiles_done = 0;
+                uint32_t alo = lo0, sfc = sfc0, fa = full0, ea = empty0;
+                for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
+                    if (!mbar_wait_cluster(acc_empty, (tiles_done & 1u) ^ 1u, kTimeoutNs)) {
                         record_timeout(abort_flag);
-                        ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (ks != 0 && (ks + 1u != kst || !tail)) {
-                        mma_nvf4_pair_stage<true, kBOff>(acc, alo, hi, kIdesc, sfc);
-                    } else if (ks + 1u != kst || !tail) {
-                        mma_nvf4_pair_stage<false, kBOff>(acc, alo, hi, kIdesc, sfc);
-                    } else {
-                        // last stage of a K that is not a multiple of 256
-                        const uint64_t da = ((uint64_t)hi << 32) | alo;
-                        for (uint32_t j = 0; j < p.last_nk; ++j)
-                            mma_nvf4_pair(acc, da + 2 * j, da + kBOff + 2 * j, kIdesc, sfc + 4 * j, sfc + 16 + 8 * j,
-                                          (ks | j) != 0 ? 1u : 0u);
+                    bool ok = true;
+                    for (uint32_t ks = 0; ks < kst; ++ks) {
+                        if (!mbar_wait_addr(fa, phase, kTimeoutNs)) {
+                            record_timeout(abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (ks != 0 && (ks + 1u != kst || !tail)) {
+                            mma_nvf4_pair_stage<true, kBOff>(acc, alo, hi, kIdesc, sfc);
+                        } else if (ks + 1u != kst || !tail) {
+                            mma_nvf4_pair_stage<false, kBOff>(acc, alo, hi, kIdesc, sfc);
+                        } else {
+                            // last stage of a K that is not a multiple of 256
+                            const uint64_t da = ((uint64_t)hi << 32) | alo;
+                            for (uint32_t j = 0; j < p.last_nk; ++j)
+                                mma_nvf4_pair(acc, da + 2 * j, da + kBOff + 2 * j, kIdesc, sfc + 4 * j,
+                                              sfc + 16 + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                        }
+                        tc_commit_pair_multicast_addr(ea, 0x3);
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                            alo = lo0;
+                            sfc = sfc0;
+                            fa = full0;
+                            ea = empty0;
+                        } else {
+                            alo += kStageDesc;
+                            sfc += kSfColsPerStage;
+                            fa += 8u;
+                            ea += 8u;
+                        }
                     }
-                    tc_commit_pair_multicast_addr(ea, 0x3);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                        alo = lo0;
-                        sfc = sfc0;
-                        fa = full0;
-                        ea = empty0;
-                    } else {
-                        alo += kStageDesc;
-                        sfc += kSfColsPerStage;
-                        fa += 8u;
-                        ea += 8u;
+                    for (uint32_t ls = 0; ok && ls < p.lora_stages; ++ls) {
+                        if (!mbar_wait_addr(fa, phase, kTimeoutNs)) {
+                            record_timeout(abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        mma_bf16_pair_stage(acc, alo, hi, kBOff, (kst | ls) != 0 ? 1u : 0u);
+                        tc_commit_pair_multicast_addr(ea, 0x3);
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                            alo = lo0;
+                            sfc = sfc0;
+                            fa = full0;
+                            ea = empty0;
+                        } else {
+                            alo += kStageDesc;
+                            sfc += kSfColsPerStage;
+                            fa += 8u;
+                            ea += 8u;
+                        }
                     }
+                    if (!ok) break;
+                    tc_commit_pair_multicast(acc_full, 0x3);
+                    ++tiles_done;
                 }
-                for (uint32_t ls = 0; ok && ls < p.lora_stages; ++ls) {
-                    if (!mbar_wait_addr(fa, phase, kTimeoutNs)) {
-                        record_timeout(abort_flag);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    mma_bf16_pair_stage(acc, alo, hi, kBOff, (kst | ls) != 0 ? 1u : 0u);
-                    tc_commit_pair_multicast_addr(ea, 0x3);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                        alo = lo0;
-                        sfc = sfc0;
-                        fa = full0;
-                        ea = empty0;
-                    } else {
-                        alo += kStageDesc;
-                        sfc += kSfColsPerStage;
-                        fa += 8u;
-                        ea += 8u;
-                    }
-                }
-                if (!ok) break;
-                tc_commit_pair_multicast(acc_full, 0x3);
-                ++tiles_done;
+                // all MMAs complete before either CTA frees its tensor memory
+                tc_commit_pair_multicast(drain, 0x1);
+                (void)mbar_wait(drain, 0, kTimeoutNs);
             }
-            // all MMAs complete before either CTA frees its tensor memory
-            tc_commit_pair_multicast(drain, 0x1);
-            (void)mbar_wait(drain, 0, kTimeoutNs);
         }
     } else if (warp < (uint32_t)kFirstEpiWarp) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
         // ------------------------------------------------------ scale warps
         // Lane i of quadrant q holds, per K = 64 step j, 4 columns of A scales
         // (bytes 16i.. of the step's 512-byte group: rows i, i+32, i+64, i+96)
@@ -542,6 +550,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) break;
         }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
         // --------------------------------------------------------- epilogue
         const uint32_t q = warp & 3u;                          // TMEM lane quadrant
         const uint32_t half = (warp - kFirstEpiWarp) >> 2;     // 128-column half of the tile
@@ -558,53 +567,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (uint32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
             uint32_t mt, nt;
             tile_coords(tile, p, mt, nt);
-            // One thread waits for the accumulator and the other epilogue
-            // warps sleep in a named barrier (waiting threads would take
-            // issue slots from the MMA issuer); all leave the loop together.
-            if (warp == (uint32_t)kFirstEpiWarp && lane == 0) {
-                bool ready = !*abort_flag && mbar_wait_cluster(acc_full, tiles_done & 1u, kTimeoutNs);
+            // One thread per warp waits for the accumulator, suspended in the
+            // barrier's try_wait (no issue slots taken from the MMA issuer);
+            // each warp wakes on the barrier itself, not behind a named
+            // barrier that a single waiter would have to open (about 500
+            // cycles per tile).
+            uint32_t ready = 0;
+            if (lane == 0) {
+                ready = (!*abort_flag && mbar_wait_cluster(acc_full, tiles_done & 1u, kTimeoutNs)) ? 1u : 0u;
                 if (!ready && !*abort_flag) record_timeout(abort_flag);
-                epi_ok[tiles_done & 1u] = ready ? 1u : 0u;
             }
-            __syncwarp();
-            epilogue_bar();
-            if (!epi_ok[tiles_done & 1u]) break;
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (!ready) break;
             tc_fence_after();
             const uint32_t row0 = mt * kPairM + rank * kCtaM;   // first row of this CTA's half
             const uint32_t row = row0 + row_local;
             const uint32_t nbase = nt * kBN + half * 128;
             const uint32_t taddr = tmem + ((q * 32u) << 16) + kAccCol + half * 128;
             if (p.tma_store && !p.out_fp32) {
-                // Two rounds of 64 columns through this warp's 4 KiB slice of
-                // the staging buffer (32 rows x 128 bytes, 128-byte swizzle),
-                // each round's two loads in flight under one wait.  The
-                // accumulator is handed back as soon as the second round's
-                // columns are in registers.
+                // All 128 columns are loaded under one wait and the
+                // accumulator goes back to the MMAs at once; then two rounds
+                // of 64 columns through this warp's 4 KiB slice of the staging
+                // buffer (32 rows x 128 bytes, 128-byte swizzle).
                 uint8_t* slice = staging + (half * 4 + q) * 4096u;
+                uint32_t packed2[2][32];
+                {
+                    uint32_t v[4][32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, v[c]);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            packed2[c >> 1][16 * (c & 1) + i] =
+                                pack_bf16x2(__fmul_rn(__uint_as_float(v[c][2 * i]), alpha),
+                                            __fmul_rn(__uint_as_float(v[c][2 * i + 1]), alpha));
+                }
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    uint32_t packed[32];
-                    {
-                        uint32_t v0[32], v1[32];
-                        tmem_ld_32x32b_x32(taddr + (2 * r) * 32, v0);
-                        tmem_ld_32x32b_x32(taddr + (2 * r + 1) * 32, v1);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            packed[i] = pack_bf16x2(__fmul_rn(__uint_as_float(v0[2 * i]), alpha),
-                                                    __fmul_rn(__uint_as_float(v0[2 * i + 1]), alpha));
-                            packed[16 + i] = pack_bf16x2(__fmul_rn(__uint_as_float(v1[2 * i]), alpha),
-                                                         __fmul_rn(__uint_as_float(v1[2 * i + 1]), alpha));
-                        }
-                    }
-                    if (r == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
-                        // round 0's columns, still in the slice: their amax
-                        // waits until the accumulator is back with the MMAs
-                        if constexpr (kAmax) slice_amax(slice, lane, p.rht_mask, amax_plain, amax_rht);
-                    }
+                    const uint32_t* packed = packed2[r];
                     // the slice's previous store must have read it
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
@@ -620,46 +625,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         bulk_commit_group();
                     }
                     // the slice now holds this warp's 32 rows x 64 columns: read
-                    // it back by columns for the output's amax (round 0's is
-                    // taken in round 1, after the accumulator's release)
-                    if constexpr (kAmax)
-                        if (r == 1) slice_amax(slice, lane, p.rht_mask, amax_plain, amax_rht);
+                    // it back by columns for the output's amax
+                    if constexpr (kAmax) slice_amax(slice, lane, p.rht_mask, amax_plain, amax_rht);
                 }
             } else if (p.tma_store && p.out_fp32) {
-                // FP32: four rounds of 32 columns through this warp's 4 KiB
-                // slice (32 rows x 128 bytes, 128-byte swizzle), loaded two
-                // rounds at a time under one wait; the accumulator goes back
-                // once the last two rounds are in registers.
+                // FP32: all 128 columns loaded under one wait, the
+                // accumulator handed back, then four rounds of 32 columns
+                // through this warp's 4 KiB slice (32 rows x 128 bytes,
+                // 128-byte swizzle).
                 uint8_t* slice = staging + (half * 4 + q) * 4096u;
-#pragma unroll 1
-                for (int c2 = 0; c2 < 4; c2 += 2) {
-                    uint32_t v[2][32];
-                    tmem_ld_32x32b_x32(taddr + c2 * 32, v[0]);
-                    tmem_ld_32x32b_x32(taddr + (c2 + 1) * 32, v[1]);
-                    tmem_ld_wait();
-                    if (c2 == 2) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
-                    }
+                uint32_t v[4][32];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (lane == 0) bulk_wait_read_all();
-                        __syncwarp();
+                for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, v[c]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            *reinterpret_cast<uint4*>(slice + lane * 128u + ((uint32_t)i ^ (lane & 7u)) * 16u) =
-                                make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(v[h][4 * i]), alpha)),
-                                           __float_as_uint(__fmul_rn(__uint_as_float(v[h][4 * i + 1]), alpha)),
-                                           __float_as_uint(__fmul_rn(__uint_as_float(v[h][4 * i + 2]), alpha)),
-                                           __float_as_uint(__fmul_rn(__uint_as_float(v[h][4 * i + 3]), alpha)));
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            const uint32_t y = row0 + q * 32, x = nbase + (uint32_t)(c2 + h) * 32u;
-                            if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
-                            bulk_commit_group();
-                        }
+                for (int c = 0; c < 4; ++c) {
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<uint4*>(slice + lane * 128u + ((uint32_t)i ^ (lane & 7u)) * 16u) =
+                            make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(v[c][4 * i]), alpha)),
+                                       __float_as_uint(__fmul_rn(__uint_as_float(v[c][4 * i + 1]), alpha)),
+                                       __float_as_uint(__fmul_rn(__uint_as_float(v[c][4 * i + 2]), alpha)),
+                                       __float_as_uint(__fmul_rn(__uint_as_float(v[c][4 * i + 3]), alpha)));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t y = row0 + q * 32, x = nbase + (uint32_t)c * 32u;
+                        if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
+                        bulk_commit_group();
                     }
                 }
             } else {
@@ -817,6 +815,23 @@ cudaError_t launch_lora_prescale(const void* u, int64_t ldu, int64_t rows, int64
     return cudaGetLastError();
 }
 
+// The kernel's warp groups trade registers with setmaxnreg against a launch
+// allocation of 128 per thread (512 threads); a build that allocated fewer
+// would leave the epilogue's setmaxnreg.inc waiting, so it is not launched.
+bool register_split_ok() {
+    static int ok = -1;
+    if (ok < 0) {
+        cudaFuncAttributes f0, f1;
+        ok = (cudaFuncGetAttributes(&f0, gemm_nvf4_kernel<false>) == cudaSuccess &&
+              cudaFuncGetAttributes(&f1, gemm_nvf4_kernel<true>) == cudaSuccess &&
+              f0.numRegs * kThreads >= 128 * (64 + 72) + 256 * 184 &&
+              f1.numRegs * kThreads >= 128 * (64 + 72) + 256 * 184)
+                 ? 1
+                 : 0;
+    }
+    return ok == 1;
+}
+
 // Number of CTA pairs that can be resident at once (cached per device).
 int max_active_pairs() {
     static int pairs[64];
@@ -884,6 +899,7 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
+    if (!register_split_ok()) return cudaErrorInvalidConfiguration;
     CUtensorMap ma, mb, msa, msb, md;
     if (!make_codes_map(&ma, a, kCtaM) || !make_codes_map(&mb, b, kCtaN) || !make_scale_map(&msa, a, 1) ||
         !make_scale_map(&msb, b, 2))
