@@ -20,6 +20,12 @@ Parity status of each function (see nvfp4_oracle.c for the citations):
   quantize / amax                    pinned by invariants and special cases
   dequantize / round_bf16            pinned (grid values, torch bf16 casts)
   gemm_f64                           pinned (exact rational brute force)
+  gemm_axpby_f64                     pinned (beta = 0 reduces to gemm_f64;
+                                     alpha = 0 to beta * C, exactly)
+  newton_schulz_step                 pinned (closed form p(s) = a s + b s^3
+                                     + c s^5 on scaled partial identities,
+                                     b = c = 0 gives RN(a X), distance to the
+                                     unquantized polynomial on random X)
 """
 import ctypes
 import os
@@ -63,6 +69,7 @@ def lib():
         L.oracle_requantize_col_rht.restype = i32
         L.oracle_dequantize.restype = None
         L.oracle_round_bf16.argtypes, L.oracle_round_bf16.restype = [f64], u16
+        L.oracle_round_bf16_array.argtypes, L.oracle_round_bf16_array.restype = [vp, i64, vp], None
         L.oracle_gemm_f64.argtypes = [vp, vp, f32, vp, vp, f32, i64, i64, i64, vp, i64, vp, vp]
         L.oracle_gemm_f64.restype = None
         L.oracle_num_threads.argtypes, L.oracle_num_threads.restype = [], i32
@@ -155,6 +162,19 @@ def e4m3_rne_satfinite_array(x):
 
 def round_bf16(v):
     return lib().oracle_round_bf16(float(v))
+
+
+def round_bf16_array(v):
+    """float64 array -> bf16 bit patterns (uint16), each rounded once."""
+    vv = _c(v, np.float64)
+    out = np.zeros(vv.shape, np.uint16)
+    lib().oracle_round_bf16_array(_ptr(vv), vv.size, _ptr(out))
+    return out
+
+
+def bf16_to_f64(bits):
+    """bf16 bit patterns -> float64 values (exact)."""
+    return (_c(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def num_threads():
@@ -270,3 +290,53 @@ def gemm_f64(a, b, row_ids=None, with_abs=True):
     lib().oracle_gemm_f64(_ptr(ac), _ptr(as_), float(a["s_g"]), _ptr(bc), _ptr(bs),
                           float(b["s_g"]), M, N, K, _ptr(ids), nr, _ptr(y), _ptr(ab))
     return y, ab
+
+
+def gemm_axpby_f64(a, b, alpha, c_bits, beta, row_ids=None):
+    """y = alpha * A B^T + beta * C in float64: the GEMM of two oracle-quantized
+    operands (gemm_f64) combined with a bf16 matrix C ([M][N] bit patterns, or
+    None for beta = 0), as the Newton-Schulz iteration of "Full-Stack FP4",
+    Sec. 3.4 combines b A_k + c (qA_k qA_k^16x1) and a X_k + qB_k qX_k^16x1.
+    Returns (y, abs_sum): abs_sum = |alpha| sum_k |a_k b_k| + |beta c|, the
+    magnitude a tolerance scales with."""
+    y, ab = gemm_f64(a, b, row_ids=row_ids)
+    y = float(alpha) * y
+    ab = abs(float(alpha)) * ab
+    if c_bits is not None and float(beta) != 0.0:
+        c = bf16_to_f64(c_bits)
+        if row_ids is not None:
+            c = c[np.asarray(row_ids)]
+        y = y + float(beta) * c
+        ab = ab + abs(float(beta)) * np.abs(c)
+    return y, ab
+
+
+def newton_schulz_step(x_bits, a, b, c, sign_mask):
+    """One NVFP4 Newton-Schulz iteration of the Root optimizer ("Full-Stack
+    FP4", Sec. 3.4, the quantized NS iteration):
+
+        qX  = Q_1x16(X H),        A  = qX qX^T
+        qA  = Q_1x16(A H),        qA' = Q_16x1(H^T A),   B = b A + c qA qA'
+        qB  = Q_1x16(B H),        qX' = Q_16x1(H^T X),   X_next = a X + qB qX'
+
+    X is bf16 [m][n] (bit patterns).  Every quantization is RTN with 4/6
+    scaling (the page: "all NVFP4 quantizations adopt RTN and 4/6 scaling");
+    H = H16 diag(sign_mask) / 4 along each product's reduction dimension, one
+    mask for the whole step so that H H^T = I cancels in each product.  The
+    page leaves the storage of A, B and X_next open; here each is a bf16
+    tensor rounded once from its float64 value, and (a, b, c) are binary32
+    inputs (the page's shape-optimised coefficients are not printed).
+
+    Returns a dict of the intermediate and final tensors: qX, A (bf16 bits),
+    qA, qAc, B (bf16 bits), qB, qXc, X (bf16 bits of X_next).
+    """
+    x_bits = _c(x_bits, np.uint16)
+    a, b, c = (float(np.float32(v)) for v in (a, b, c))   # binary32, as the library takes them
+    q = lambda t, o: quantize(t, o, scaling=2, rounding=0, use_rht=True, sign_mask=sign_mask)
+    qX = q(x_bits, ROWWISE)
+    A = round_bf16_array(gemm_f64(qX, qX, with_abs=False)[0])
+    qA, qAc = q(A, ROWWISE), q(A, COLWISE)
+    B = round_bf16_array(gemm_axpby_f64(qA, qAc, c, A, b)[0])
+    qB, qXc = q(B, ROWWISE), q(x_bits, COLWISE)
+    X = round_bf16_array(gemm_axpby_f64(qB, qXc, 1.0, x_bits, a)[0])
+    return dict(qX=qX, A=A, qA=qA, qAc=qAc, B=B, qB=qB, qXc=qXc, X=X)

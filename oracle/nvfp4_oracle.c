@@ -491,6 +491,12 @@ uint16_t oracle_round_bf16(double v)
     return (uint16_t)(sign | (uint16_t)(u >> 16));
 }
 
+void oracle_round_bf16_array(const double *v, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_round_bf16(v[i]);
+}
+
 /* ------------------------------------------------------------------ */
 /* y = s_gA s_gB sum_k (e2m1(a_k) s_A)(e2m1(b_k) s_B): the three linear-layer
  * GEMMs with FP4 inputs ("Full-Stack FP4", Sec. 2 Linear projection;

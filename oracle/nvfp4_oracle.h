@@ -92,6 +92,8 @@ void oracle_dequantize(const uint8_t *codes, const uint8_t *scales, float s_g,
 
 /* Round binary64 to bfloat16 (nearest, ties to even) in a single step. */
 uint16_t oracle_round_bf16(double v);
+/* oracle_round_bf16 of each of n values. */
+void oracle_round_bf16_array(const double *v, int64_t n, uint16_t *out);
 
 /*
  * y[i][n] = s_gA*s_gB * sum_k (e2m1(a)*s_A)(e2m1(b)*s_B) in binary64 for the
