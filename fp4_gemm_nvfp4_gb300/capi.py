@@ -36,7 +36,8 @@ EXPORTED = ("nvfp4_scale_bytes", "nvfp4_quantize_workspace_size", "nvfp4_quantiz
             "nvfp4_rht_quantize", "nvfp4_gemm", "nvfp4_dequantize", "nvfp4_status_string",
             "nvfp4_device_error", "nvfp4_quantize_noalloc", "nvfp4_quantize_row_col_rht",
             "nvfp4_requantize_col_rht", "nvfp4_gemm_lora", "nvfp4_gemm_lora_workspace_size",
-            "nvfp4_gemm_amax", "nvfp4_quantize_row_col_rht_amax")
+            "nvfp4_gemm_amax", "nvfp4_quantize_row_col_rht_amax", "nvfp4_gemm_axpby",
+            "nvfp4_newton_schulz_workspace_size", "nvfp4_newton_schulz_step")
 
 
 class nvfp4_tensor(ctypes.Structure):
@@ -91,6 +92,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_gemm_lora.argtypes = [tp, tp, vp, i64, i32, vp, i64, vp, i64, i64, ctypes.c_float, vp, sz, vp]
     L.nvfp4_gemm_lora.restype = i32
     L.nvfp4_gemm.restype = i32
+    f32 = ctypes.c_float
+    L.nvfp4_gemm_axpby.argtypes = [tp, tp, vp, i64, i32, f32, vp, i64, f32, vp, sz, vp]
+    L.nvfp4_gemm_axpby.restype = i32
+    L.nvfp4_newton_schulz_workspace_size.argtypes = [i64, i64]
+    L.nvfp4_newton_schulz_workspace_size.restype = sz
+    L.nvfp4_newton_schulz_step.argtypes = [vp, i64, i64, i64, f32, f32, f32, u16, vp, i64, vp, sz, vp]
+    L.nvfp4_newton_schulz_step.restype = i32
     L.nvfp4_dequantize.argtypes = [tp, vp, i64, i32, vp]
     L.nvfp4_dequantize.restype = i32
     L.nvfp4_status_string.argtypes, L.nvfp4_status_string.restype = [i32], ctypes.c_char_p
@@ -172,6 +180,23 @@ def nvfp4_gemm_lora(A, B, D, ldd, out_dtype, U, ldu, V, ldv, r, beta, workspace,
     """D = s_gA s_gB A B^T + beta U V^T (the LoRA-SVD projection's low-rank branch fused)."""
     return load().nvfp4_gemm_lora(_ref(A), _ref(B), D, ldd, out_dtype, U, ldu, V, ldv, r, beta, workspace,
                                   workspace_bytes, stream)
+
+
+def nvfp4_gemm_axpby(A, B, D, ldd, out_dtype, alpha, C, ldc, beta, workspace, workspace_bytes, stream):
+    """D = alpha s_gA s_gB A B^T + beta C (C of D's dtype, may be D itself)."""
+    return load().nvfp4_gemm_axpby(_ref(A), _ref(B), D, ldd, out_dtype, alpha, C, ldc, beta, workspace,
+                                   workspace_bytes, stream)
+
+
+def nvfp4_newton_schulz_workspace_size(m, n):
+    return load().nvfp4_newton_schulz_workspace_size(m, n)
+
+
+def nvfp4_newton_schulz_step(X, m, n, ldx, a, b, c, rht_sign_mask, X_out, ld_out, workspace, workspace_bytes,
+                             stream):
+    """One NVFP4 Newton-Schulz iteration X_out = a X + b (X X^T) X + c (X X^T)^2 X with NVFP4 products."""
+    return load().nvfp4_newton_schulz_step(X, m, n, ldx, a, b, c, rht_sign_mask, X_out, ld_out, workspace,
+                                           workspace_bytes, stream)
 
 
 def nvfp4_dequantize(q, y, ldy, out_dtype, stream):

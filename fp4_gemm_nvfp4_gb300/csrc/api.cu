@@ -100,6 +100,84 @@ nvfp4::GemmOperand to_operand(const nvfp4_tensor* t) {
     return nvfp4::GemmOperand{t->codes, t->ld_codes, t->scales, t->global_scale, t->rows, t->cols};
 }
 
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Carves one [rows][cols] NVFP4 operand (codes with a 16-byte multiple row
+// stride, tile-layout scales, s_g, amax) out of a workspace at *off.
+nvfp4_tensor carve_operand(uint8_t* base, size_t* off, int64_t rows, int64_t cols) {
+    nvfp4_tensor t{};
+    t.rows = rows;
+    t.cols = cols;
+    t.ld_codes = (cols / 2 + 15) / 16 * 16;
+    t.codes = base ? base + *off : nullptr;
+    *off = align256(*off + (size_t)(rows * t.ld_codes));
+    t.scales = base ? base + *off : nullptr;
+    *off = align256(*off + nvfp4_scale_bytes(rows, cols));
+    t.global_scale = base ? reinterpret_cast<float*>(base + *off) : nullptr;
+    t.amax = base ? reinterpret_cast<float*>(base + *off) + 1 : nullptr;
+    *off = align256(*off + 2 * sizeof(float));
+    return t;
+}
+
+// The Newton-Schulz step's workspace: A_k and B_k (bf16 [m][m]) first, then
+// the five quantized operands and the quantizer's scratch.
+struct NsWorkspace {
+    void* a;
+    void* b;
+    nvfp4_tensor qx, qxc, qa, qac, qb;
+    void* qws;
+    size_t bytes;
+};
+
+NsWorkspace ns_layout(void* workspace, int64_t m, int64_t n) {
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    NsWorkspace w{};
+    size_t off = 0;
+    w.a = base ? base + off : nullptr;
+    off = align256(off + (size_t)(m * m * 2));
+    w.b = base ? base + off : nullptr;
+    off = align256(off + (size_t)(m * m * 2));
+    w.qx = carve_operand(base, &off, m, n);
+    w.qxc = carve_operand(base, &off, n, m);
+    w.qa = carve_operand(base, &off, m, m);
+    w.qac = carve_operand(base, &off, m, m);
+    w.qb = carve_operand(base, &off, m, m);
+    w.qws = base ? base + off : nullptr;
+    off = align256(off + nvfp4::kQuantizeWorkspaceBytes);
+    w.bytes = off;
+    return w;
+}
+
+nvfp4_status gemm_axpby_impl(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, int64_t ldd,
+                             nvfp4_dtype out_dtype, float alpha, const void* C, int64_t ldc, float beta,
+                             cudaStream_t st) {
+    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
+    if (!std::isfinite(alpha) || !std::isfinite(beta)) return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status s;
+    if ((s = check_operand(A)) != NVFP4_OK) return s;
+    if ((s = check_operand(B)) != NVFP4_OK) return s;
+    if (A->cols != B->cols) return NVFP4_ERR_SHAPE;
+    if (!D) return NVFP4_ERR_INVALID_ARG;
+    const int64_t M = A->rows, N = B->rows, K = A->cols;
+    const int64_t esz = out_dtype == NVFP4_OUT_FP32 ? 4 : 2;
+    if (ldd < N) return NVFP4_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(D) % (uintptr_t)esz) != 0) return NVFP4_ERR_ALIGNMENT;
+    const bool with_c = beta != 0.0f;
+    if (with_c) {
+        if (!C) return NVFP4_ERR_INVALID_ARG;
+        if (ldc < N) return NVFP4_ERR_SHAPE;
+        if ((reinterpret_cast<uintptr_t>(C) % (uintptr_t)esz) != 0) return NVFP4_ERR_ALIGNMENT;
+        if (C == D && ldc != ldd) return NVFP4_ERR_INVALID_ARG;
+    }
+    if (ceil_div(M, 128) * ceil_div(N, 256) >= (int64_t(1) << 32)) return NVFP4_ERR_UNSUPPORTED;
+    if (K == 0) return NVFP4_ERR_UNSUPPORTED;   // no product to carry the C term
+    if (M == 0 || N == 0) return NVFP4_OK;
+    const nvfp4::Axpby ax{alpha, with_c ? C : nullptr, with_c ? ldc : 0, with_c ? beta : 0.0f};
+    const cudaError_t e = nvfp4::launch_gemm(to_operand(A), to_operand(B), D, ldd, out_dtype == NVFP4_OUT_FP32, st,
+                                             nullptr, nullptr, 0, &ax);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -284,6 +362,54 @@ nvfp4_status nvfp4_gemm_lora(const nvfp4_tensor* A, const nvfp4_tensor* B, void*
     const cudaError_t e =
         nvfp4::launch_gemm(to_operand(A), to_operand(B), D, ldd, out_dtype == NVFP4_OUT_FP32, st, &lr);
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status nvfp4_gemm_axpby(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, int64_t ldd,
+                              nvfp4_dtype out_dtype, float alpha, const void* C, int64_t ldc, float beta,
+                              void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    return gemm_axpby_impl(A, B, D, ldd, out_dtype, alpha, C, ldc, beta, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t nvfp4_newton_schulz_workspace_size(int64_t m, int64_t n) {
+    if (m <= 0 || n <= 0) return 0;
+    return ns_layout(nullptr, m, n).bytes;
+}
+
+nvfp4_status nvfp4_newton_schulz_step(const void* X, int64_t m, int64_t n, int64_t ldx, float a, float b, float c,
+                                      uint16_t rht_sign_mask, void* X_out, int64_t ld_out, void* workspace,
+                                      size_t workspace_bytes, nvfp4_stream_t stream) {
+    if (!std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c)) return NVFP4_ERR_INVALID_ARG;
+    if (m <= 0 || n <= 0 || m % 16 != 0 || n % 16 != 0) return NVFP4_ERR_SHAPE;
+    nvfp4_status s;
+    if ((s = check_quantize_input(X, m, n, ldx)) != NVFP4_OK) return s;
+    if ((s = check_quantize_input(X_out, m, n, ld_out)) != NVFP4_OK) return s;
+    if (X_out == X && ld_out != ldx) return NVFP4_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < nvfp4_newton_schulz_workspace_size(m, n))
+        return NVFP4_ERR_WORKSPACE;
+    const NsWorkspace w = ns_layout(workspace, m, n);
+    const size_t qb = nvfp4::kQuantizeWorkspaceBytes;
+    // qX = Q_1x16(X H) and qX' = Q_16x1(H^T X), one call
+    if ((s = nvfp4_rht_quantize(X, m, n, ldx, NVFP4_SCALE_1X16_46, NVFP4_ROUND_RNE, 0, 0,
+                                NVFP4_ROWWISE | NVFP4_COLWISE, &w.qx, &w.qxc, rht_sign_mask, w.qws, qb,
+                                stream)) != NVFP4_OK)
+        return s;
+    // A = qX qX^T
+    if ((s = nvfp4_gemm(&w.qx, &w.qx, w.a, m, NVFP4_OUT_BF16, nullptr, 0, stream)) != NVFP4_OK) return s;
+    // qA = Q_1x16(A H), qA' = Q_16x1(H^T A); B = b A + c qA qA'
+    if ((s = nvfp4_rht_quantize(w.a, m, m, m, NVFP4_SCALE_1X16_46, NVFP4_ROUND_RNE, 0, 0,
+                                NVFP4_ROWWISE | NVFP4_COLWISE, &w.qa, &w.qac, rht_sign_mask, w.qws, qb,
+                                stream)) != NVFP4_OK)
+        return s;
+    if ((s = nvfp4_gemm_axpby(&w.qa, &w.qac, w.b, m, NVFP4_OUT_BF16, c, w.a, m, b, nullptr, 0, stream)) !=
+        NVFP4_OK)
+        return s;
+    // qB = Q_1x16(B H); X_out = a X + qB qX'
+    if ((s = nvfp4_rht_quantize(w.b, m, m, m, NVFP4_SCALE_1X16_46, NVFP4_ROUND_RNE, 0, 0, NVFP4_ROWWISE, &w.qb,
+                                nullptr, rht_sign_mask, w.qws, qb, stream)) != NVFP4_OK)
+        return s;
+    return nvfp4_gemm_axpby(&w.qb, &w.qxc, X_out, ld_out, NVFP4_OUT_BF16, 1.0f, X, ldx, a, nullptr, 0, stream);
 }
 
 nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, void* y, int64_t ldy, nvfp4_dtype out_dtype,

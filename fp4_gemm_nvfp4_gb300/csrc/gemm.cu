@@ -105,7 +105,58 @@ struct Params {
     uint32_t lora_stages;        // 64-deep BF16 stages of the low-rank term per tile (0: none)
     float* amax_out;             // [2]: max |D| and max |RHT along D's rows| (BF16 TMA path), or null
     uint32_t rht_mask;
+    float alpha;                 // extra factor on the product (1 for a plain GEMM)
+    const void* c;               // D = alpha s_gA s_gB A B^T + beta C: C [M][ldc] of D's dtype, or null
+    int64_t ldc;
+    float beta;
+    int c_vec;                   // every row of C starts on a 16-byte boundary
 };
+
+// 32 consecutive values of C's row `row` from column n0 (zeros past M or N):
+// BF16 as 16 packed pairs, FP32 as 32 floats.
+__device__ __forceinline__ void load_c_bf16x32(const Params& p, uint32_t row, uint32_t n0, uint32_t* w) {
+    const uint16_t* src = static_cast<const uint16_t*>(p.c) + (int64_t)row * p.ldc + n0;
+    if (row < p.M && p.c_vec && n0 + 32 <= p.N) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 u = *reinterpret_cast<const uint4*>(src + 8 * j);
+            w[4 * j] = u.x;
+            w[4 * j + 1] = u.y;
+            w[4 * j + 2] = u.z;
+            w[4 * j + 3] = u.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t lo = (row < p.M && n0 + 2 * i < p.N) ? src[2 * i] : 0u;
+            const uint32_t hi = (row < p.M && n0 + 2 * i + 1 < p.N) ? src[2 * i + 1] : 0u;
+            w[i] = lo | (hi << 16);
+        }
+    }
+}
+__device__ __forceinline__ void load_c_f32x32(const Params& p, uint32_t row, uint32_t n0, float* f) {
+    const float* src = static_cast<const float*>(p.c) + (int64_t)row * p.ldc + n0;
+    if (row < p.M && p.c_vec && n0 + 32 <= p.N) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 u = *reinterpret_cast<const float4*>(src + 4 * j);
+            f[4 * j] = u.x;
+            f[4 * j + 1] = u.y;
+            f[4 * j + 2] = u.z;
+            f[4 * j + 3] = u.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) f[i] = (row < p.M && n0 + i < p.N) ? src[i] : 0.0f;
+    }
+}
+
+// One output value: RN(acc * alpha) + RN(beta * c) in binary32 (the C term
+// only when the call has one).
+__device__ __forceinline__ float epi_value(uint32_t acc_bits, float alpha, bool has_c, float beta, float c) {
+    const float y = __fmul_rn(__uint_as_float(acc_bits), alpha);
+    return has_c ? __fadd_rn(y, __fmul_rn(beta, c)) : y;
+}
 
 // Output tile of a linear tile index.  Tiles that run at the same time share
 // the slow index, so its operand block is read from DRAM once and served from
@@ -232,8 +283,11 @@ __device__ __forceinline__ void slice_amax(const uint8_t* slice, uint32_t lane, 
     }
 }
 
-// kAmax: the epilogue also takes the output's two tensor amaxes (p.amax_out).
-template <bool kAmax>
+// Epilogue variants: the plain product; the product plus the output's two
+// tensor amaxes (p.amax_out); alpha times the product plus beta C (p.c).
+enum EpiMode { kEpiPlain = 0, kEpiAmax = 1, kEpiC = 2 };
+
+template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                      const __grid_constant__ CUtensorMap tma_sfa, const __grid_constant__ CUtensorMap tma_sfb,
@@ -554,7 +608,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // --------------------------------------------------------- epilogue
         const uint32_t q = warp & 3u;                          // TMEM lane quadrant
         const uint32_t half = (warp - kFirstEpiWarp) >> 2;     // 128-column half of the tile
-        const float alpha = __fmul_rn(*p.sga, *p.sgb);
+        const float alpha = __fmul_rn(__fmul_rn(*p.sga, *p.sgb), p.alpha);
+        constexpr bool kAmax = kMode == kEpiAmax;
+        constexpr bool has_c = kMode == kEpiC;
         const uint32_t leader_acc_empty = map_to_cta(smem_u32(acc_empty), 0);
         // amax of the BF16 output for its quantization (rows of one warp are
         // lanes, so a 16-row block of a column is 16 lanes): the plain max
@@ -600,12 +656,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t cw[16];
+                        if constexpr (has_c) {
+                            // one chunk of C in flight at a time (registers)
+                            asm volatile("" ::: "memory");
+                            load_c_bf16x32(p, row, nbase + 32 * c, cw);
+                        }
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             packed2[c >> 1][16 * (c & 1) + i] =
-                                pack_bf16x2(__fmul_rn(__uint_as_float(v[c][2 * i]), alpha),
-                                            __fmul_rn(__uint_as_float(v[c][2 * i + 1]), alpha));
+                                pack_bf16x2(epi_value(v[c][2 * i], alpha, has_c, p.beta, bf16lo(cw[i])),
+                                            epi_value(v[c][2 * i + 1], alpha, has_c, p.beta, bf16hi(cw[i])));
+                    }
                 }
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
@@ -643,15 +706,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
+                    float cf[32];
+                    if constexpr (has_c) load_c_f32x32(p, row, nbase + 32 * c, cf);
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         *reinterpret_cast<uint4*>(slice + lane * 128u + ((uint32_t)i ^ (lane & 7u)) * 16u) =
-                            make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(v[c][4 * i]), alpha)),
-                                       __float_as_uint(__fmul_rn(__uint_as_float(v[c][4 * i + 1]), alpha)),
-                                       __float_as_uint(__fmul_rn(__uint_as_float(v[c][4 * i + 2]), alpha)),
-                                       __float_as_uint(__fmul_rn(__uint_as_float(v[c][4 * i + 3]), alpha)));
+                            make_uint4(__float_as_uint(epi_value(v[c][4 * i], alpha, has_c, p.beta, cf[4 * i])),
+                                       __float_as_uint(epi_value(v[c][4 * i + 1], alpha, has_c, p.beta, cf[4 * i + 1])),
+                                       __float_as_uint(epi_value(v[c][4 * i + 2], alpha, has_c, p.beta, cf[4 * i + 2])),
+                                       __float_as_uint(epi_value(v[c][4 * i + 3], alpha, has_c, p.beta, cf[4 * i + 3])));
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -671,26 +736,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (row >= p.M) continue;
                     if (p.out_fp32) {
                         float* dst = reinterpret_cast<float*>(p.d) + (int64_t)row * p.ldd + n0;
+                        float cf[32];
+                        if constexpr (has_c) load_c_f32x32(p, row, n0, cf);
                         if (p.vec_store && n0 + 32 <= p.N) {
 #pragma unroll
                             for (int i = 0; i < 32; i += 4)
                                 *reinterpret_cast<float4*>(dst + i) =
-                                    make_float4(__fmul_rn(__uint_as_float(v[i]), alpha),
-                                                __fmul_rn(__uint_as_float(v[i + 1]), alpha),
-                                                __fmul_rn(__uint_as_float(v[i + 2]), alpha),
-                                                __fmul_rn(__uint_as_float(v[i + 3]), alpha));
+                                    make_float4(epi_value(v[i], alpha, has_c, p.beta, cf[i]),
+                                                epi_value(v[i + 1], alpha, has_c, p.beta, cf[i + 1]),
+                                                epi_value(v[i + 2], alpha, has_c, p.beta, cf[i + 2]),
+                                                epi_value(v[i + 3], alpha, has_c, p.beta, cf[i + 3]));
                         } else {
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
-                                if (n0 + i < p.N) dst[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
+                                if (n0 + i < p.N) dst[i] = epi_value(v[i], alpha, has_c, p.beta, cf[i]);
                         }
                     } else {
                         uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + (int64_t)row * p.ldd + n0;
-                        uint32_t packed[16];
+                        uint32_t packed[16], cw[16];
+                        if constexpr (has_c) load_c_bf16x32(p, row, n0, cw);
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            packed[i] = pack_bf16x2(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
-                                                    __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+                            packed[i] = pack_bf16x2(epi_value(v[2 * i], alpha, has_c, p.beta, bf16lo(cw[i])),
+                                                    epi_value(v[2 * i + 1], alpha, has_c, p.beta, bf16hi(cw[i])));
                         if (p.vec_store && n0 + 32 <= p.N) {
 #pragma unroll
                             for (int i = 0; i < 16; i += 4)
@@ -822,10 +890,13 @@ bool register_split_ok() {
     static int ok = -1;
     if (ok < 0) {
         cudaFuncAttributes f0, f1;
-        ok = (cudaFuncGetAttributes(&f0, gemm_nvf4_kernel<false>) == cudaSuccess &&
-              cudaFuncGetAttributes(&f1, gemm_nvf4_kernel<true>) == cudaSuccess &&
+        cudaFuncAttributes f2;
+        ok = (cudaFuncGetAttributes(&f0, gemm_nvf4_kernel<kEpiPlain>) == cudaSuccess &&
+              cudaFuncGetAttributes(&f1, gemm_nvf4_kernel<kEpiAmax>) == cudaSuccess &&
+              cudaFuncGetAttributes(&f2, gemm_nvf4_kernel<kEpiC>) == cudaSuccess &&
               f0.numRegs * kThreads >= 128 * (64 + 72) + 256 * 184 &&
-              f1.numRegs * kThreads >= 128 * (64 + 72) + 256 * 184)
+              f1.numRegs * kThreads >= 128 * (64 + 72) + 256 * 184 &&
+              f2.numRegs * kThreads >= 128 * (64 + 72) + 256 * 184)
                  ? 1
                  : 0;
     }
@@ -850,7 +921,7 @@ int max_active_pairs() {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvf4_kernel<false>, &cfg) != cudaSuccess || n < 1)
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvf4_kernel<kEpiPlain>, &cfg) != cudaSuccess || n < 1)
             n = device_sm_count() / 2;
         pairs[dev] = n > 0 ? n : 1;
     }
@@ -886,15 +957,20 @@ int device_sm_count() {
 }
 
 cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int64_t ldd, bool out_fp32,
-                        cudaStream_t stream, const LowRank* lora, float* amax_out, uint32_t rht_mask) {
+                        cudaStream_t stream, const LowRank* lora, float* amax_out, uint32_t rht_mask,
+                        const Axpby* axpby) {
     static bool attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
         cudaError_t e =
-            cudaFuncSetAttribute(gemm_nvf4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+            cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemm_nvf4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiAmax>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_nvf4_kernel<kEpiC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
@@ -918,7 +994,17 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     p.d = d;
     p.ldd = ldd;
     p.out_fp32 = out_fp32 ? 1 : 0;
+    p.alpha = 1.0f;
     const int64_t esz = out_fp32 ? 4 : 2;
+    if (axpby) {
+        // the C term goes with the plain product only
+        if (lora || amax_out) return cudaErrorInvalidValue;
+        p.alpha = axpby->alpha;
+        p.c = axpby->c;
+        p.ldc = axpby->ldc;
+        p.beta = axpby->beta;
+        p.c_vec = ((reinterpret_cast<uintptr_t>(axpby->c) & 15u) == 0 && (axpby->ldc * esz) % 16 == 0) ? 1 : 0;
+    }
     p.vec_store = ((reinterpret_cast<uintptr_t>(d) & 15u) == 0 && (ldd * esz) % 16 == 0) ? 1 : 0;
     p.tma_store = (p.vec_store && make_output_map(&md, d, a.rows, b.rows, ldd, out_fp32)) ? 1 : 0;
     if (!p.tma_store) md = ma;   // unused by the kernel; any valid map
@@ -946,9 +1032,11 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     const uint32_t pairs = (uint32_t)max_active_pairs();
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
     if (p.amax_out)
-        gemm_nvf4_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, mu, mv, p);
+        gemm_nvf4_kernel<kEpiAmax><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, mu, mv, p);
+    else if (p.c)
+        gemm_nvf4_kernel<kEpiC><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, mu, mv, p);
     else
-        gemm_nvf4_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, mu, mv, p);
+        gemm_nvf4_kernel<kEpiPlain><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, mu, mv, p);
     return cudaGetLastError();
 }
 

@@ -72,12 +72,21 @@ struct LowRank {
     void* u_scaled;
 };
 
+// D = alpha * (s_gA s_gB A B^T) + beta * C with C [M][ldc] of D's dtype
+// (C may be D itself: each element is read before it is written).
+struct Axpby {
+    float alpha;
+    const void* c;
+    int64_t ldc;
+    float beta;
+};
+
 // amax_out (BF16 output only): [0] = max |D|, [1] = max |U d| over the 16-row
 // blocks of each column (the RHT U = H16 diag(rht_mask) / 4 along D's rows),
 // the two tensor amaxes nvfp4_quantize_row_col_rht takes of D.
 cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int64_t ldd, bool out_fp32,
                         cudaStream_t stream, const LowRank* lora = nullptr, float* amax_out = nullptr,
-                        uint32_t rht_mask = 0);
+                        uint32_t rht_mask = 0, const Axpby* axpby = nullptr);
 
 // Read and clear the GEMM kernels' device status word (synchronous).
 cudaError_t gemm_read_and_clear_status(unsigned int* status);

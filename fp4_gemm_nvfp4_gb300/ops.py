@@ -213,6 +213,48 @@ def gemm_lora(a: NVFP4Operand, b: NVFP4Operand, u: torch.Tensor, v: torch.Tensor
     capi.check(status, "nvfp4_gemm_lora")
     return out
 
+def gemm_axpby(a: NVFP4Operand, b: NVFP4Operand, alpha: float, c: Optional[torch.Tensor], beta: float,
+               out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """D = alpha * A * B^T + beta * C (nvfp4_gemm_axpby); C has D's dtype and may be `out` itself."""
+    if out is None:
+        out = torch.empty((a.rows, b.rows), dtype=out_dtype, device=a.codes.device)
+    dt = capi.NVFP4_OUT_FP32 if out.dtype == torch.float32 else capi.NVFP4_OUT_BF16
+    if c is not None:
+        assert c.dtype == out.dtype and c.dim() == 2 and c.stride(1) == 1
+    status = capi.nvfp4_gemm_axpby(a.struct(), b.struct(), out.data_ptr(), out.stride(0), dt, float(alpha),
+                                   None if c is None else c.data_ptr(), 0 if c is None else c.stride(0),
+                                   float(beta), None, 0, stream_handle(stream))
+    capi.check(status, "nvfp4_gemm_axpby")
+    return out
+
+
+def newton_schulz_step(x: torch.Tensor, a: float, b: float, c: float, rht_mask: int,
+                       out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """One NVFP4 Newton-Schulz iteration of a bf16 [m][n] matrix (nvfp4_newton_schulz_step).
+    After the call the workspace begins with A_k and then B_k (bf16 [m][m]; see ns_intermediates)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    m, n = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    nbytes = capi.nvfp4_newton_schulz_workspace_size(m, n)
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    status = capi.nvfp4_newton_schulz_step(x.data_ptr(), m, n, x.stride(0), float(a), float(b), float(c),
+                                           rht_mask, out.data_ptr(), out.stride(0), workspace.data_ptr(),
+                                           workspace.numel(), stream_handle(stream))
+    capi.check(status, "nvfp4_newton_schulz_step")
+    return out
+
+
+def ns_intermediates(workspace: torch.Tensor, m: int) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Views of A_k and B_k (bf16 [m][m]) at the start of a Newton-Schulz step's workspace."""
+    off_b = (2 * m * m + 255) // 256 * 256
+    a = workspace[:2 * m * m].view(torch.bfloat16).view(m, m)
+    b = workspace[off_b:off_b + 2 * m * m].view(torch.bfloat16).view(m, m)
+    return a, b
+
+
 def dequantize(q: NVFP4Operand, out_dtype=torch.float32, stream=None) -> torch.Tensor:
     """x^ = e2m1 * s_b * s_g (nvfp4_dequantize)."""
     y = torch.empty((q.rows, q.cols), dtype=out_dtype, device=q.codes.device)

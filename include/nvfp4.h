@@ -309,6 +309,55 @@ NVFP4_API nvfp4_status nvfp4_gemm_lora(const nvfp4_tensor *A, const nvfp4_tensor
                                        size_t workspace_bytes, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_gemm_axpby -- the NVFP4 GEMM plus a scaled C term, as the Newton-
+ * Schulz iteration of the Root optimizer combines its products [FS Sec. 3.4:
+ * B_k = b A_k + c qA_k qA_k^16x1, X_k+1 = a X_k + qB_k qX_k^16x1]:
+ *   D = alpha * (s_gA * s_gB * A B^T) + beta * C
+ * per element in binary32: RN(acc * RN(RN(s_gA * s_gB) * alpha)) + RN(beta * c),
+ * then one rounding to out_dtype.
+ *  C            device, row-major [M][ldc] of out_dtype; read only when
+ *               beta != 0 (may be NULL then).  C may be D itself (same
+ *               leading dimension): every element is read before it is
+ *               written; any other overlap is undefined.
+ *  alpha, beta  finite FP32 scalars [INVALID_ARG].
+ * Requirements and errors as nvfp4_gemm, plus ldc >= N [SHAPE] and C aligned
+ * to its element size [ALIGNMENT]; K = 0 is UNSUPPORTED.
+ */
+NVFP4_API nvfp4_status nvfp4_gemm_axpby(const nvfp4_tensor *A, const nvfp4_tensor *B, void *D, int64_t ldd,
+                                        nvfp4_dtype out_dtype, float alpha, const void *C, int64_t ldc,
+                                        float beta, void *workspace, size_t workspace_bytes,
+                                        nvfp4_stream_t stream);
+
+/*
+ * nvfp4_newton_schulz_step -- one NVFP4 Newton-Schulz iteration of the Root
+ * (Muon) optimizer, with every matrix product an NVFP4 GEMM [FS Sec. 3.4, the
+ * quantized NS iteration]:
+ *   qX = Q_1x16(X H),  A = qX qX^T
+ *   qA = Q_1x16(A H),  qA' = Q_16x1(H^T A),  B = b A + c qA qA'
+ *   qB = Q_1x16(B H),  qX' = Q_16x1(H^T X),  X_out = a X + qB qX'
+ * Every quantization is RNE with 4/6 adaptive block scales
+ * (NVFP4_SCALE_1X16_46) and the RHT H = H16 * D / 4 with D from rht_sign_mask
+ * along the product's reduction dimension (one mask for the whole step, so
+ * H H^T = I cancels in each product).  A and B are BF16 [m][m]; X and X_out
+ * are BF16 [m][n] row-major (ldx, ld_out in elements).  The page's
+ * shape-optimised (a, b, c) are not printed: the caller passes them.
+ *  workspace    device scratch of nvfp4_newton_schulz_workspace_size(m, n)
+ *               bytes, 16-byte aligned.  After the call it begins with A
+ *               (bf16, row stride m) and, at byte offset 256 * ceil(2 m^2 /
+ *               256), B; the rest (the five quantized operands) is internal.
+ * Work on `stream`: three quantize calls and three GEMMs.  X_out may be X
+ * itself (same leading dimension).
+ * Requirements: m % 16 == 0, n % 16 == 0, m, n > 0 [SHAPE]; X and X_out
+ * 16-byte aligned with leading dimensions multiples of 8 and >= n
+ * [ALIGNMENT / SHAPE]; finite a, b, c [INVALID_ARG].
+ */
+NVFP4_API size_t nvfp4_newton_schulz_workspace_size(int64_t m, int64_t n);
+NVFP4_API nvfp4_status nvfp4_newton_schulz_step(const void *X, int64_t m, int64_t n, int64_t ldx, float a,
+                                                float b, float c, uint16_t rht_sign_mask, void *X_out,
+                                                int64_t ld_out, void *workspace, size_t workspace_bytes,
+                                                nvfp4_stream_t stream);
+
+/*
  * nvfp4_dequantize -- y = e2m1(code) * s_b * s_g for every element of q
  * [FS Sec. 2], rounded once (nearest even) to out_dtype; y is row-major
  * [q->rows][ldy].  Requirements: y 16-byte aligned, ldy * sizeof(out) % 16 == 0.
