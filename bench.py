@@ -638,6 +638,89 @@ def sweep_c5(args):
         torch.cuda.empty_cache()
 
 
+def sweep_ns(args):
+    """The NVFP4 Newton-Schulz step ("Full-Stack FP4", Sec. 3.4) on the 3B
+    model's weight shapes (X is [m][n] with m the smaller dimension: FFN 3072 x
+    9216, QKV 3072 x 6144, O 3072 x 3072), Muon coefficients, inputs G / ||G||_F.
+    One JSON line per shape: the step through nvfp4_newton_schulz_step, and its
+    three quantize calls and three GEMMs timed one by one (CUDA events on the
+    launching stream, L2 flushed before every timed call)."""
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from fp4_gemm_nvfp4_gb300 import capi, inputs, ops
+    peaks, peak_src = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    a, b, c = 3.4445, -4.7750, 2.0315
+    mask = inputs.rht_sign_mask(6)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(6)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        times = []
+        for _ in range(max(args.steps, 10)):
+            flush.fill_(1.0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    for name, m, n in [("ffn", 3072, 9216), ("qkv", 3072, 6144), ("o", 3072, 3072)]:
+        g = torch.randn((m, n), generator=gen, device="cuda")
+        x = (g / g.norm()).to(torch.bfloat16)
+        del g
+        ws = torch.empty(capi.nvfp4_newton_schulz_workspace_size(m, n), dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(x)
+        step_ms = timed(lambda: ops.newton_schulz_step(x, a, b, c, mask, out=out, workspace=ws))
+        # the same work call by call
+        qws = ops.Workspace()
+        qx, qxc = ops.alloc_operand(m, n), ops.alloc_operand(n, m)
+        qa, qac, qb = ops.alloc_operand(m, m), ops.alloc_operand(m, m), ops.alloc_operand(m, m)
+        A = torch.empty((m, m), dtype=torch.bfloat16, device="cuda")
+        B = torch.empty_like(A)
+        parts = [
+            ("q_x_pair", lambda: ops.quantize(x, rht_mask=mask, rowwise=True, colwise=True, scale46=True,
+                                              out_row=qx, out_col=qxc, workspace=qws), None),
+            ("gemm_xxt", lambda: ops.gemm(qx, qx, out=A), 2 * m * m * n),
+            ("q_a_pair", lambda: ops.quantize(A, rht_mask=mask, rowwise=True, colwise=True, scale46=True,
+                                              out_row=qa, out_col=qac, workspace=qws), None),
+            ("gemm_aa", lambda: ops.gemm_axpby(qa, qac, c, A, b, out=B), 2 * m * m * m),
+            ("q_b_row", lambda: ops.quantize(B, rht_mask=mask, rowwise=True, scale46=True, out_row=qb,
+                                             workspace=qws), None),
+            ("gemm_bx", lambda: ops.gemm_axpby(qb, qxc, 1.0, x, a, out=out), 2 * m * n * m),
+        ]
+        for _, fn, _ in parts:   # intermediates for the later parts
+            fn()
+        res = {}
+        gemm_ms = gemm_flop = 0.0
+        for pname, fn, flop in parts:
+            ms = timed(fn)
+            res[pname] = {"ms": round(ms, 4)}
+            if flop:
+                res[pname]["tflops"] = round(flop / (ms * 1e-3) / 1e12, 1)
+                gemm_ms += ms
+                gemm_flop += flop
+        flop = 4 * m * m * n + 2 * m ** 3
+        print(json.dumps({"sweep": "newton_schulz", "weight": name, "m": m, "n": n, "coefficients": [a, b, c],
+                          "step_ms": round(step_ms, 4), "step_tflops": round(flop / (step_ms * 1e-3) / 1e12, 1),
+                          "gemm_tflops": round(gemm_flop / (gemm_ms * 1e-3) / 1e12, 1),
+                          "gemm_frac_of_fp4_peak": round(gemm_flop / (gemm_ms * 1e-3) / 1e12 / fp4_peak, 4),
+                          "peak_source": f"{peak_src} bf16 burst x 6", "parts": res, "l2_flush": True,
+                          "status": ops.device_error()}), flush=True)
+        del x, ws, out, qx, qxc, qa, qac, qb, A, B
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -647,8 +730,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fuse-amax", action="store_true",
                     help="quantize H and dY_up as inputs with their own amax pass (no fused GEMM amax)")
-    ap.add_argument("--sweep", choices=["c5"], default=None,
-                    help="instead of the layer step, run the quantizer bandwidth sweep (one JSON line per case)")
+    ap.add_argument("--sweep", choices=["c5", "ns"], default=None,
+                    help="instead of the layer step, run the quantizer bandwidth sweep (c5) or the NVFP4 "
+                         "Newton-Schulz step on the 3B weight shapes (ns); one JSON line per case")
     ap.add_argument("--tokens", type=int, default=TOKENS,
                     help="tokens of the layer step (16384 is the benchmarked workload)")
     args = ap.parse_args()
@@ -659,6 +743,9 @@ def main():
         args.warmup = 3
     if args.sweep == "c5":
         sweep_c5(args)
+        return
+    if args.sweep == "ns":
+        sweep_ns(args)
         return
     if args.impl == "reference":
         r = reference_arm(args)
