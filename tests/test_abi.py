@@ -224,6 +224,48 @@ def test_gemm_validation(lib):
     assert gemm(A=tensor(0, 256)) == E.NVFP4_OK
 
 
+def test_gemm_axpby_validation(lib):
+    E = capi
+
+    def axpby(A=None, B=None, D=A16 * 6, ldd=128, dt=0, alpha=1.0, C=A16 * 7, ldc=128, beta=0.5):
+        A = A or tensor(128, 256)
+        B = B or tensor(128, 256)
+        return capi.nvfp4_gemm_axpby(A, B, D, ldd, dt, alpha, C, ldc, beta, None, 0, None)
+    assert axpby(alpha=float("nan")) == E.NVFP4_ERR_INVALID_ARG
+    assert axpby(beta=float("inf")) == E.NVFP4_ERR_INVALID_ARG
+    assert axpby(C=None) == E.NVFP4_ERR_INVALID_ARG                  # beta != 0 reads C
+    assert axpby(ldc=100) == E.NVFP4_ERR_SHAPE                       # ldc < N
+    assert axpby(C=A16 * 7 + 1) == E.NVFP4_ERR_ALIGNMENT
+    assert axpby(C=A16 * 6, ldc=136) == E.NVFP4_ERR_INVALID_ARG      # C == D needs the same ld
+    assert axpby(B=tensor(128, 128)) == E.NVFP4_ERR_SHAPE            # K mismatch
+    assert axpby(A=tensor(128, 0), B=tensor(128, 0)) == E.NVFP4_ERR_UNSUPPORTED   # K = 0
+    assert axpby(dt=3) == E.NVFP4_ERR_INVALID_ARG
+    assert axpby(A=tensor(0, 256)) == E.NVFP4_OK                     # empty output: nothing enqueued
+
+
+def test_newton_schulz_validation(lib):
+    E = capi
+    ws_bytes = capi.nvfp4_newton_schulz_workspace_size(64, 128)
+    assert ws_bytes > 2 * (2 * 64 * 64)   # A and B, then the quantized operands
+    assert capi.nvfp4_newton_schulz_workspace_size(0, 128) == 0
+
+    def ns(X=A16 * 4, m=64, n=128, ldx=128, a=1.5, b=-0.5, c=0.0, out=A16 * 8, ld_out=128,
+           ws=A16 * 9, ws_bytes=ws_bytes):
+        return capi.nvfp4_newton_schulz_step(X, m, n, ldx, a, b, c, 0x1234, out, ld_out, ws, ws_bytes, None)
+    assert ns(m=40) == E.NVFP4_ERR_SHAPE
+    assert ns(n=72, ldx=72, ld_out=72) == E.NVFP4_ERR_SHAPE
+    assert ns(m=0) == E.NVFP4_ERR_SHAPE
+    assert ns(a=float("nan")) == E.NVFP4_ERR_INVALID_ARG
+    assert ns(X=None) == E.NVFP4_ERR_INVALID_ARG
+    assert ns(X=A16 * 4 + 8) == E.NVFP4_ERR_ALIGNMENT
+    assert ns(ldx=100) == E.NVFP4_ERR_SHAPE
+    assert ns(ldx=132) == E.NVFP4_ERR_ALIGNMENT
+    assert ns(out=A16 * 4, ld_out=136) == E.NVFP4_ERR_INVALID_ARG    # in place needs the same ld
+    assert ns(ws=None) == E.NVFP4_ERR_WORKSPACE
+    assert ns(ws_bytes=ws_bytes - 1) == E.NVFP4_ERR_WORKSPACE
+    assert ns(ws=A16 * 9 + 8) == E.NVFP4_ERR_WORKSPACE
+
+
 def test_dequantize_validation(lib):
     E = capi
     q = tensor(64, 64)
