@@ -401,14 +401,17 @@ __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
 // ------------------------------------------- row + col-RHT pair encode -----
 // The encode pass of nvfp4_quantize_row_col_rht in one read of x: each warp
 // takes 16-row x 64-column slices of x by TMA (128-byte swizzle, two slots per
-// warp so the next slice is in flight while this one is encoded) and encodes
-// every element twice from shared memory:
-//   col-wise with RHT: lane = 2 columns x 16 rows (as colwise_kernel);
+// warp so the next slice is in flight while this one is encoded), four of them
+// down its 64 rows of a 512-row CTA tile, and encodes every element twice from
+// shared memory:
+//   col-wise with RHT: lane = 2 columns x 16 rows (as colwise_kernel); the
+//   four slices' codes of a column (32 bytes) and scales (4 bytes) are kept
+//   in registers and stored together after the fourth;
 //   row-wise without RHT: lane = 2 row blocks of 16 (row = lane / 2), 16
 //   bytes of codes and 2 scale bytes per lane.
 struct PairArgs {
     uint32_t rows, cols;
-    uint32_t tiles_r, tiles_c;   // 128-row x 64-column CTA tiles
+    uint32_t tiles_r, tiles_c;   // kTileRows-row x 64-column CTA tiles
     Target row, col;
     const float* part_plain;
     const float* part_rht;       // the col-wise operand's partials (with or without RHT)
@@ -421,6 +424,40 @@ struct PairArgs {
 
 constexpr int kPairSlots = 2;
 constexpr uint32_t kSliceBytes = 16 * 128;   // 16 rows x 64 bf16
+// Each warp takes 64 rows (four 16-row slices) of a 512-row x 64-column CTA
+// tile, so that the col-wise codes of a column (32 bytes) and its four block
+// scales (4 bytes) leave in one store each, whole sectors, instead of 8-byte
+// pieces that four warps would each write at different times.
+constexpr uint32_t kWarpRows = 64;
+constexpr uint32_t kTileRows = (kThreads / 32) * kWarpRows;
+
+// Col-wise codes and scales of columns c, c + 1 over the warp's 64 rows from
+// row rb: q0[s], q1[s] the codes of 16-row slice s, sc0, sc1 the four scale
+// bytes (slice s in byte s).  Only the slices below `rows` are written.
+__device__ __forceinline__ void store_col64(const Target& t, uint32_t c, uint32_t rb, uint32_t rows,
+                                            const uint2* q0, const uint2* q1, uint32_t sc0, uint32_t sc1) {
+    uint8_t* d0 = t.codes + (int64_t)c * t.ld_codes + rb / 2;
+    uint8_t* d1 = d0 + t.ld_codes;
+    const uint32_t nv = (rows - rb) / 16u;
+    if (nv >= 4u) {
+        *reinterpret_cast<uint4*>(d0) = make_uint4(q0[0].x, q0[0].y, q0[1].x, q0[1].y);
+        *reinterpret_cast<uint4*>(d0 + 16) = make_uint4(q0[2].x, q0[2].y, q0[3].x, q0[3].y);
+        *reinterpret_cast<uint4*>(d1) = make_uint4(q1[0].x, q1[0].y, q1[1].x, q1[1].y);
+        *reinterpret_cast<uint4*>(d1 + 16) = make_uint4(q1[2].x, q1[2].y, q1[3].x, q1[3].y);
+        *reinterpret_cast<uint32_t*>(t.scales + scale_offset(c, rb / 16u, t.s4)) = sc0;
+        *reinterpret_cast<uint32_t*>(t.scales + scale_offset(c + 1, rb / 16u, t.s4)) = sc1;
+    } else {
+#pragma unroll
+        for (uint32_t s = 0; s < 3u; ++s) {
+            if (s < nv) {
+                *reinterpret_cast<uint2*>(d0 + 8 * s) = q0[s];
+                *reinterpret_cast<uint2*>(d1 + 8 * s) = q1[s];
+                t.scales[scale_offset(c, rb / 16u + s, t.s4)] = (uint8_t)(sc0 >> (8 * s));
+                t.scales[scale_offset(c + 1, rb / 16u + s, t.s4)] = (uint8_t)(sc1 >> (8 * s));
+            }
+        }
+    }
+}
 
 // kColRHT: the col-wise operand gets the RHT (else none); the row-wise
 // operand never does.  Either orientation may be left out (emit_*).
@@ -447,36 +484,43 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     __syncthreads();
     const PhiloxKeys& keys = a.keys;   // SR round keys, formed by the host
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
-    // this warp's slice of the CTA's k-th tile, if it holds rows
-    auto slice_of = [&](uint32_t k, uint32_t& r0, uint32_t& c0) -> bool {
-        const uint32_t tile = blockIdx.x + k * gridDim.x;
+    // this warp's 16-row slice j of the CTA's tiles: tile j / 4, slice j % 4
+    // of the warp's 64 rows, if it holds rows
+    auto slice_of = [&](uint32_t j, uint32_t& r0, uint32_t& c0) -> bool {
+        const uint32_t tile = blockIdx.x + (j >> 2) * gridDim.x;
         if (tile >= ntiles) return false;
-        r0 = (tile % a.tiles_r) * 128u + warp * 16u;
+        r0 = (tile % a.tiles_r) * kTileRows + warp * kWarpRows + (j & 3u) * 16u;
         c0 = (tile / a.tiles_r) * 64u;
         return r0 < a.rows;
     };
-    auto issue = [&](uint32_t k) {
+    auto issue = [&](uint32_t j) {
         uint32_t r0, c0;
-        if (lane == 0 && slice_of(k, r0, c0)) {
-            uint64_t* bar = &full[warp][k & 1u];
+        if (lane == 0 && slice_of(j, r0, c0)) {
+            uint64_t* bar = &full[warp][j & 1u];
             mbar_arrive_expect_tx(bar, kSliceBytes);
-            tma_load_2d(ring[warp][k & 1u], &tmap_x, bar, (int32_t)c0, (int32_t)r0);
+            tma_load_2d(ring[warp][j & 1u], &tmap_x, bar, (int32_t)c0, (int32_t)r0);
         }
     };
     const uint32_t kcount = (ntiles > blockIdx.x) ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
     uint32_t parity = 0;   // bit s: parity of the next wait on slot s
+    // the col-wise codes and scales of the warp's four slices of a tile, slice
+    // s in element / byte s, stored once the fourth slice is encoded
+    uint2 cq0[4], cq1[4];
+    uint32_t cs0 = 0, cs1 = 0;
     issue(0);
-    for (uint32_t k = 0; k < kcount; ++k) {
+    for (uint32_t j = 0; j < 4u * kcount; ++j) {
         __syncwarp();   // every lane is done with the slot the next copy fills
-        issue(k + 1);
+        issue(j + 1);
         uint32_t r0, c0;
-        if (!slice_of(k, r0, c0)) continue;
-        const uint32_t sl = k & 1u;
+        uint2 q0 = make_uint2(0u, 0u), q1 = make_uint2(0u, 0u);
+        uint32_t sc0 = 0, sc1 = 0;
+        if (slice_of(j, r0, c0)) {
+        const uint32_t sl = j & 1u;
         if (!mbar_wait(&full[warp][sl], (parity >> sl) & 1u, 2000000000ull)) {
             // a copy that never landed: let the next one (issued above) land
             // before this CTA can exit, then stop
             uint32_t r1, c1;
-            if (slice_of(k + 1, r1, c1))
+            if (slice_of(j + 1, r1, c1))
                 (void)mbar_wait(&full[warp][sl ^ 1u], (parity >> (sl ^ 1u)) & 1u, 2000000000ull);
             break;
         }
@@ -514,7 +558,6 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                     m1 = __fmul_rn(m1, 0.25f);
                 }
                 float rb0, rb1;
-                uint32_t sc0, sc1;
                 if constexpr (kS46) {
                     const float xs_mult = fold ? __fmul_rn(ts_col.s_enc, 0.25f) : ts_col.s_enc;
                     sc0 = block_scale_46(t0, m0, ts_col.s_enc, xs_mult, rb_col, &rb0);
@@ -523,12 +566,8 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                     sc0 = block_scale_tab(m0, ts_col.s_enc, rb_col, &rb0);
                     sc1 = block_scale_tab(m1, ts_col.s_enc, rb_col, &rb1);
                 }
-                const uint2 q0 = encode16<kSR>(t0, rb0, keys, a.stream_col, (uint64_t)c * a.rows + r0);
-                const uint2 q1 = encode16<kSR>(t1, rb1, keys, a.stream_col, (uint64_t)(c + 1) * a.rows + r0);
-                *reinterpret_cast<uint2*>(a.col.codes + (int64_t)c * a.col.ld_codes + r0 / 2) = q0;
-                *reinterpret_cast<uint2*>(a.col.codes + (int64_t)(c + 1) * a.col.ld_codes + r0 / 2) = q1;
-                a.col.scales[scale_offset(c, r0 / 16, a.col.s4)] = (uint8_t)sc0;
-                a.col.scales[scale_offset(c + 1, r0 / 16, a.col.s4)] = (uint8_t)sc1;
+                q0 = encode16<kSR>(t0, rb0, keys, a.stream_col, (uint64_t)c * a.rows + r0);
+                q1 = encode16<kSR>(t1, rb1, keys, a.stream_col, (uint64_t)(c + 1) * a.rows + r0);
             }
         }
         // ---- row-wise without RHT: lane = row r0 + lane / 2, 32 columns
@@ -576,6 +615,19 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                 }
             }
         }
+        }
+        // slice j % 4 joins the warp's col-wise codes; after the fourth, they
+        // go out as whole sectors
+        cq0[0] = cq0[1], cq0[1] = cq0[2], cq0[2] = cq0[3], cq0[3] = q0;
+        cq1[0] = cq1[1], cq1[1] = cq1[2], cq1[2] = cq1[3], cq1[3] = q1;
+        cs0 = (cs0 >> 8) | (sc0 << 24);
+        cs1 = (cs1 >> 8) | (sc1 << 24);
+        if ((j & 3u) == 3u && a.emit_col) {
+            const uint32_t tile = blockIdx.x + (j >> 2) * gridDim.x;
+            const uint32_t rb = (tile % a.tiles_r) * kTileRows + warp * kWarpRows;
+            const uint32_t c = (tile / a.tiles_r) * 64u + lane * 2u;
+            if (tile < ntiles && rb < a.rows && c < a.cols) store_col64(a.col, c, rb, a.rows, cq0, cq1, cs0, cs1);
+        }
     }
 }
 
@@ -587,7 +639,7 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
 // every element with the tile's r_b, so the two are exact transposes.
 struct Tile2dArgs {
     uint32_t rows, cols;
-    uint32_t tiles_r, tiles_c;   // 128-row x 64-column CTA tiles
+    uint32_t tiles_r, tiles_c;   // kTileRows-row x 64-column CTA tiles
     Target row, col;
     bool emit_row, emit_col;
     const float* partials;
@@ -610,33 +662,40 @@ __global__ void __launch_bounds__(kThreads) tile2d_rne_kernel(const __grid_const
     }
     __syncthreads();
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
-    auto slice_of = [&](uint32_t k, uint32_t& r0, uint32_t& c0) -> bool {
-        const uint32_t tile = blockIdx.x + k * gridDim.x;
+    // this warp's 16-row slice j of the CTA's tiles: tile j / 4, slice j % 4
+    // of the warp's 64 rows, if it holds rows
+    auto slice_of = [&](uint32_t j, uint32_t& r0, uint32_t& c0) -> bool {
+        const uint32_t tile = blockIdx.x + (j >> 2) * gridDim.x;
         if (tile >= ntiles) return false;
-        r0 = (tile % a.tiles_r) * 128u + warp * 16u;
+        r0 = (tile % a.tiles_r) * kTileRows + warp * kWarpRows + (j & 3u) * 16u;
         c0 = (tile / a.tiles_r) * 64u;
         return r0 < a.rows;
     };
-    auto issue = [&](uint32_t k) {
+    auto issue = [&](uint32_t j) {
         uint32_t r0, c0;
-        if (lane == 0 && slice_of(k, r0, c0)) {
-            uint64_t* bar = &full[warp][k & 1u];
+        if (lane == 0 && slice_of(j, r0, c0)) {
+            uint64_t* bar = &full[warp][j & 1u];
             mbar_arrive_expect_tx(bar, kSliceBytes);
-            tma_load_2d(ring[warp][k & 1u], &tmap_x, bar, (int32_t)c0, (int32_t)r0);
+            tma_load_2d(ring[warp][j & 1u], &tmap_x, bar, (int32_t)c0, (int32_t)r0);
         }
     };
     const uint32_t kcount = (ntiles > blockIdx.x) ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
     uint32_t parity = 0;
+    // the col-wise codes and scales of the warp's four slices of a tile
+    uint2 cq0[4], cq1[4];
+    uint32_t cs = 0;
     issue(0);
-    for (uint32_t k = 0; k < kcount; ++k) {
+    for (uint32_t j = 0; j < 4u * kcount; ++j) {
         __syncwarp();
-        issue(k + 1);
+        issue(j + 1);
         uint32_t r0, c0;
-        if (!slice_of(k, r0, c0)) continue;
-        const uint32_t sl = k & 1u;
+        uint2 q0 = make_uint2(0u, 0u), q1 = make_uint2(0u, 0u);
+        uint32_t sc = 0;
+        if (slice_of(j, r0, c0)) {
+        const uint32_t sl = j & 1u;
         if (!mbar_wait(&full[warp][sl], (parity >> sl) & 1u, 2000000000ull)) {
             uint32_t r1, c1;
-            if (slice_of(k + 1, r1, c1))
+            if (slice_of(j + 1, r1, c1))
                 (void)mbar_wait(&full[warp][sl ^ 1u], (parity >> (sl ^ 1u)) & 1u, 2000000000ull);
             break;
         }
@@ -659,7 +718,7 @@ __global__ void __launch_bounds__(kThreads) tile2d_rne_kernel(const __grid_const
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
         float rb;
-        const uint32_t sc = block_scale_tab(m, ts.s_enc, rb_tab, &rb);
+        sc = block_scale_tab(m, ts.s_enc, rb_tab, &rb);
         if (a.emit_col && c < a.cols) {
             float v0[16], v1[16];
 #pragma unroll
@@ -667,12 +726,8 @@ __global__ void __launch_bounds__(kThreads) tile2d_rne_kernel(const __grid_const
                 v0[i] = __fmul_rn(t0[i], rb);
                 v1[i] = __fmul_rn(t1[i], rb);
             }
-            const uint2 q0 = make_uint2(e2m1_rne_x8(v0), e2m1_rne_x8(v0 + 8));
-            const uint2 q1 = make_uint2(e2m1_rne_x8(v1), e2m1_rne_x8(v1 + 8));
-            *reinterpret_cast<uint2*>(a.col.codes + (int64_t)c * a.col.ld_codes + r0 / 2) = q0;
-            *reinterpret_cast<uint2*>(a.col.codes + (int64_t)(c + 1) * a.col.ld_codes + r0 / 2) = q1;
-            a.col.scales[scale_offset(c, r0 / 16, a.col.s4)] = (uint8_t)sc;
-            a.col.scales[scale_offset(c + 1, r0 / 16, a.col.s4)] = (uint8_t)sc;
+            q0 = make_uint2(e2m1_rne_x8(v0), e2m1_rne_x8(v0 + 8));
+            q1 = make_uint2(e2m1_rne_x8(v1), e2m1_rne_x8(v1 + 8));
         }
         if (a.emit_row) {
             // row layout: row r0 + lane / 2, columns c0 + 32 (lane & 1) .. + 31
@@ -711,6 +766,18 @@ __global__ void __launch_bounds__(kThreads) tile2d_rne_kernel(const __grid_const
                     a.row.scales[scale_offset(r, j0, a.row.s4)] = (uint8_t)sct0;
                 }
             }
+        }
+        }
+        // slice j % 4 joins the warp's col-wise codes; after the fourth, they
+        // go out as whole sectors (both columns share the tile's scale)
+        cq0[0] = cq0[1], cq0[1] = cq0[2], cq0[2] = cq0[3], cq0[3] = q0;
+        cq1[0] = cq1[1], cq1[1] = cq1[2], cq1[2] = cq1[3], cq1[3] = q1;
+        cs = (cs >> 8) | (sc << 24);
+        if ((j & 3u) == 3u && a.emit_col) {
+            const uint32_t tile = blockIdx.x + (j >> 2) * gridDim.x;
+            const uint32_t rb = (tile % a.tiles_r) * kTileRows + warp * kWarpRows;
+            const uint32_t c = (tile / a.tiles_r) * 64u + lane * 2u;
+            if (tile < ntiles && rb < a.rows && c < a.cols) store_col64(a.col, c, rb, a.rows, cq0, cq1, cs, cs);
         }
     }
 }
@@ -772,16 +839,19 @@ cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, in
     CUtensorMap tmap;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)ld_x * 2u};
+    // 16-row x 64-column slices; no L2 sector promotion (a 256-byte
+    // promotion fetched the neighbouring 128 bytes again later: 25 % more
+    // DRAM reads on a 16x16 encode)
     const cuuint32_t box[2] = {64, 16};
     const cuuint32_t elem[2] = {1, 1};
     if (fn(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, elem,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     PairArgs pa{};
     pa.rows = (uint32_t)rows;
     pa.cols = (uint32_t)cols;
-    pa.tiles_r = (uint32_t)((rows + 127) / 128);
+    pa.tiles_r = (uint32_t)((rows + kTileRows - 1) / kTileRows);
     pa.tiles_c = (uint32_t)((cols + 63) / 64);
     pa.row = make_target(row);
     pa.col = make_target(col);
@@ -864,13 +934,13 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
         const cuuint32_t box[2] = {64, 16};
         const cuuint32_t elem[2] = {1, 1};
         if (!fn || fn(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, elem,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
         Tile2dArgs ta{};
         ta.rows = (uint32_t)rows;
         ta.cols = (uint32_t)cols;
-        ta.tiles_r = ca.tiles_r;
+        ta.tiles_r = (uint32_t)((rows + kTileRows - 1) / kTileRows);
         ta.tiles_c = ca.tiles_c;
         ta.row = make_target(row);
         ta.col = make_target(col);
@@ -879,7 +949,7 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
         ta.partials = part_a;
         ta.n_partials = ca.n_partials;
         auto k = tile2d_rne_kernel;
-        k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(tmap, ta);
+        k<<<persistent_grid(k, (int64_t)ta.tiles_r * ta.tiles_c), kThreads, 0, st>>>(tmap, ta);
         return cudaGetLastError();
     }
 
@@ -971,13 +1041,13 @@ cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t
     const cuuint32_t box[2] = {64, 16};
     const cuuint32_t elem[2] = {1, 1};
     if (fn(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, elem,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     PairArgs pa{};
     pa.rows = (uint32_t)rows;
     pa.cols = (uint32_t)cols;
-    pa.tiles_r = ca.tiles_r;
+    pa.tiles_r = (uint32_t)((rows + kTileRows - 1) / kTileRows);
     pa.tiles_c = ca.tiles_c;
     pa.row = make_target(row);
     pa.col = make_target(col);
@@ -989,7 +1059,8 @@ cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t
     pa.keys = philox_keys(seed);
     pa.stream_row = stream_row;
     pa.stream_col = stream_col;
-    auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(tmap, pa); };
+    const int64_t pair_tiles = (int64_t)pa.tiles_r * pa.tiles_c;
+    auto launch = [&](auto k) { k<<<persistent_grid(k, pair_tiles), kThreads, 0, st>>>(tmap, pa); };
     if (sr) launch(pair_encode_kernel<true, true>);
     else launch(pair_encode_kernel<false, true>);
     return cudaGetLastError();
