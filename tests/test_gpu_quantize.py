@@ -56,7 +56,9 @@ MODES = [
 
 @pytest.mark.parametrize("scaling,rounding,rht", MODES)
 @pytest.mark.parametrize("orientation", [oracle.ROWWISE, oracle.COLWISE])
-@pytest.mark.parametrize("shape", [(16, 16), (272, 336), (128, 1024), (400, 192)])
+# rows 48, 96 and 560 leave a warp's group of 64 rows with 3, 2 and 3 of
+# its four 16-row slices (the col-wise stores of a partial group)
+@pytest.mark.parametrize("shape", [(16, 16), (272, 336), (128, 1024), (400, 192), (48, 64), (96, 128), (560, 96)])
 def test_quantize_parity_small(shape, orientation, scaling, rounding, rht):
     rows, cols = shape
     bits = inputs.normal(rows, cols, seed=rows * 7 + cols, outlier_channels=2)
@@ -171,7 +173,8 @@ def _check_against_oracle(g, ref):
 
 
 @pytest.mark.parametrize("rounding", [0, 1])
-@pytest.mark.parametrize("shape", [(16, 16), (272, 336), (128, 1024), (400, 192), (1040, 3072)])
+@pytest.mark.parametrize("shape", [(16, 16), (272, 336), (128, 1024), (400, 192), (1040, 3072), (48, 64),
+                                   (96, 128), (560, 96)])
 def test_row_col_rht_matches_oracle_and_separate_calls(shape, rounding):
     """nvfp4_quantize_row_col_rht: row-wise without RHT and col-wise with RHT
     from one shared amax pass, identical to the two separate calls."""
