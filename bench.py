@@ -6,9 +6,11 @@ tensor amaxes).
 
 Prints one JSON line.  `value` is the step's GEMM work (6 GEMMs x 2*M*N*K)
 divided by the device time of the whole step (all quantize and GEMM kernels),
-inputs resident in HBM.  `e2e` is the same metric with the bf16 inputs copied
-from pinned host memory and the six outputs copied back inside the timed
-region.  `roofline` reports the kernel that takes most of the step's time
+inputs resident in HBM.  `e2e` is the same metric with the bf16 inputs (X,
+W_up, W_down, dY_down) copied from pinned host memory and the step's results
+(Y, dX, dW_down, dW_up) copied back, every step, inside the timed region
+(copies on their own streams, two device buffer sets, so a step's copies
+overlap its neighbours' compute; H and dY_up never leave the device).  `roofline` reports the kernel that takes most of the step's time
 against its measured peak.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -451,25 +453,56 @@ def measure(args):
     flops = step.flops()
     value = whole_job_tflops(flops, world, ms_per_step)
 
-    # ---- end to end: pinned host inputs in and the six outputs out, every step
+    # ---- end to end: pinned host inputs in and the step's four results out, every step.
+    # Copies run on their own streams (one per direction) and two device
+    # buffer sets alternate, so step i's copy-in and copy-out overlap the
+    # compute of steps i + 1 and i - 1; the time runs from the first copy-in
+    # to the last copy-out.
     pinned_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
                  for k, v in host.items() if not produced(k)}
-    pinned_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in step.out.items()}
+    # the step's results: Y (fprop_down), dX (dgrad_up), dW_down and dW_up; H and
+    # dY_up are the layer's internal tensors and stay on the device
+    pinned_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in step.out.items()
+                  if k not in PRODUCED.values()}
     h2d = sum(t.numel() * 2 for t in pinned_in.values())
     d2h = sum(t.numel() * 2 for t in pinned_out.values())
-    e2e_steps = max(1, min(args.steps, 10))
-    barrier()
+    e2e_steps = max(2, min(args.steps, 10))
+    dev_b = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda() for k, v in host.items()}
+    step_b = Step(dev_b, mask, seed)
     with torch.cuda.stream(stream):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
+        step_b.run()
+    barrier()
+    g_step_b = capture(torch, step_b.run, stream)
+    sets = [(dev, step, g_step), (dev_b, step_b, g_step_b)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        b = i & 1
+        d, st, g = sets[b]
+        if i >= 2:
+            s_in.wait_event(comp_done[b])       # step i - 2 has read this set's inputs
+        with torch.cuda.stream(s_in):
             for k, t in pinned_in.items():
-                dev[k].copy_(t, non_blocking=True)
-            g_step.replay()
+                d[k].copy_(t, non_blocking=True)
+        in_done[b].record(s_in)
+        stream.wait_event(in_done[b])
+        if i >= 2:
+            stream.wait_event(out_done[b])      # step i - 2's outputs are out
+        with torch.cuda.stream(stream):
+            g.replay()
+        comp_done[b].record(stream)
+        s_out.wait_event(comp_done[b])
+        with torch.cuda.stream(s_out):
             for k, t in pinned_out.items():
-                t.copy_(step.out[k], non_blocking=True)
-        e1.record(stream)
+                t.copy_(st.out[k], non_blocking=True)
+        out_done[b].record(s_out)
+    s_in.wait_stream(s_out)
+    e1.record(s_in)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
