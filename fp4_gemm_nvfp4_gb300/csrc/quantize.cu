@@ -415,7 +415,8 @@ struct PairArgs {
     Target row, col;
     const float* part_plain;
     const float* part_rht;       // the col-wise operand's partials (with or without RHT)
-    int n_partials;
+    int n_partials;              // partials of part_plain
+    int n_partials_col;          // partials of part_rht
     bool emit_row, emit_col;
     uint32_t mask;
     PhiloxKeys keys;             // SR round keys of the seed
@@ -459,10 +460,11 @@ __device__ __forceinline__ void store_col64(const Target& t, uint32_t c, uint32_
     }
 }
 
-// kColRHT: the col-wise operand gets the RHT (else none); the row-wise
-// operand never does.  Either orientation may be left out (emit_*).
+// kColRHT: the col-wise operand gets the RHT (else none); kRowRHT: the
+// row-wise operand gets it too (along its rows; both orientations of an RHT
+// quantize call).  Either orientation may be left out (emit_*).
 // kS46: 4/6 adaptive block scales (block_scale_46) in both orientations.
-template <bool kSR, bool kColRHT, bool kS46 = false>
+template <bool kSR, bool kColRHT, bool kS46 = false, bool kRowRHT = false>
 __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                                const PairArgs a) {
     __shared__ float red[32];
@@ -471,10 +473,11 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     __shared__ uint64_t full[kThreads / 32][kPairSlots];
     TensorScale ts_row{1.0f, 1.0f}, ts_col{1.0f, 1.0f};
     if (a.emit_row) ts_row = load_tensor_scale(a.part_plain, a.n_partials, red, a.row, nullptr);
-    if (a.emit_col) ts_col = load_tensor_scale(a.part_rht, a.n_partials, red, a.col, nullptr);
+    if (a.emit_col) ts_col = load_tensor_scale(a.part_rht, a.n_partials_col, red, a.col, nullptr);
     // the col-wise RHT's 1/4 lives in its multipliers (rht_quarter_foldable)
     const bool fold = kColRHT && rht_quarter_foldable(ts_col.s_enc);
-    fill_rb_table_at(rb_row, ts_row.s_enc, 0);
+    const bool fold_row = kRowRHT && rht_quarter_foldable(ts_row.s_enc);
+    fill_rb_table_at(rb_row, ts_row.s_enc, 0, fold_row ? 0.25f : 1.0f);
     fill_rb_table_at(rb_col, ts_col.s_enc, 128, fold ? 0.25f : 1.0f);
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     if (lane == 0) {
@@ -589,6 +592,14 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                     v[8 * kk + 6] = bf16lo(u.w);
                     v[8 * kk + 7] = bf16hi(u.w);
                 }
+                if constexpr (kRowRHT) {
+                    rht16_unscaled(v, a.mask);   // the 1/4 comes below
+                    rht16_unscaled(v + 16, a.mask);
+                    if (!fold_row) {
+                        scale16(v, 0.25f);
+                        scale16(v + 16, 0.25f);
+                    }
+                }
                 const bool two = cb + 16u < a.cols;
                 uint2 q[2];
                 uint32_t sc[2];
@@ -597,8 +608,11 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                     float m = 0.0f;
 #pragma unroll
                     for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[16 * jj + e]));
+                    if (fold_row) m = __fmul_rn(m, 0.25f);
                     float rb;
-                    sc[jj] = kS46 ? block_scale_46(v + 16 * jj, m, ts_row.s_enc, ts_row.s_enc, rb_row, &rb)
+                    sc[jj] = kS46 ? block_scale_46(v + 16 * jj, m, ts_row.s_enc,
+                                                   fold_row ? __fmul_rn(ts_row.s_enc, 0.25f) : ts_row.s_enc, rb_row,
+                                                   &rb)
                                    : block_scale_tab(m, ts_row.s_enc, rb_row, &rb);
                     q[jj] = encode16<kSR>(v + 16 * jj, rb, keys, a.stream_row,
                                           (uint64_t)r * a.cols + cb + 16u * (uint32_t)jj);
@@ -833,7 +847,8 @@ int row_amax(const RowArgs& base, float* partials, cudaStream_t st) {
 cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool sr, bool col_rht,
                                uint32_t sign_mask, uint64_t seed, uint64_t stream_row, uint64_t stream_col,
                                const QuantTarget* row, const QuantTarget* col, const float* part_row,
-                               const float* part_col, int n_partials, bool s46, cudaStream_t st) {
+                               const float* part_col, int n_partials, bool s46, cudaStream_t st,
+                               bool row_rht = false, int n_partials_col = -1) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     CUtensorMap tmap;
@@ -860,12 +875,20 @@ cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, in
     pa.part_plain = part_row;
     pa.part_rht = part_col;
     pa.n_partials = n_partials;
+    pa.n_partials_col = n_partials_col < 0 ? n_partials : n_partials_col;
     pa.mask = sign_mask;
     pa.keys = philox_keys(seed);
     pa.stream_row = stream_row;
     pa.stream_col = stream_col;
     const int64_t ntiles = (int64_t)pa.tiles_r * pa.tiles_c;
     auto launch = [&](auto k) { k<<<persistent_grid(k, ntiles), kThreads, 0, st>>>(tmap, pa); };
+    if (row_rht) {   // both orientations with the RHT (col_rht is set too)
+        if (s46 && sr) launch(pair_encode_kernel<true, true, true, true>);
+        else if (s46) launch(pair_encode_kernel<false, true, true, true>);
+        else if (sr) launch(pair_encode_kernel<true, true, false, true>);
+        else launch(pair_encode_kernel<false, true, false, true>);
+        return cudaGetLastError();
+    }
     if (s46) {
         if (sr && col_rht) launch(pair_encode_kernel<true, true, true>);
         else if (col_rht) launch(pair_encode_kernel<false, true, true>);
@@ -970,9 +993,10 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
         }
     }
 
-    // row-wise: the thread-per-block kernel, unless a plain col-wise operand
-    // is emitted too (then one slice-staged pass emits both)
-    const bool joint = row && col && !rht;
+    // row-wise: the thread-per-block kernel, unless a col-wise operand is
+    // emitted too (then one slice-staged pass emits both, each orientation
+    // with its own tensor scale when the RHT is on)
+    const bool joint = row && col;
     if (row && !joint) {
         RowArgs r = ra;
         r.out = make_target(row);
@@ -995,7 +1019,8 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
     }
     if (col)
         return launch_pair_encode(x, rows, cols, ld_x, sr, rht, sign_mask, seed, stream_id, stream_id,
-                                  joint ? row : nullptr, col, part_a, part_b, joint ? n_row : n_col, scale_46, st);
+                                  joint ? row : nullptr, col, part_a, part_b, n_row, scale_46, st, joint && rht,
+                                  rht ? n_col : n_row);
     return cudaGetLastError();
 }
 
@@ -1054,6 +1079,7 @@ cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t
     pa.part_plain = part_plain;
     pa.part_rht = part_rht;
     pa.n_partials = n;
+    pa.n_partials_col = n;
     pa.emit_row = pa.emit_col = true;
     pa.mask = sign_mask;
     pa.keys = philox_keys(seed);

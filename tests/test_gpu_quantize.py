@@ -96,11 +96,13 @@ def test_quantize_ties_and_negative_zero():
     assert_parity(bits, oracle.ROWWISE, rounding=1, seed=1)
 
 
-def test_quantize_both_orientations_in_one_call():
-    bits = inputs.normal(256, 320, seed=44, outlier_channels=3)
+@pytest.mark.parametrize("shape", [(256, 320), (560, 96)])
+def test_quantize_both_orientations_in_one_call(shape):
+    bits = inputs.normal(*shape, seed=44, outlier_channels=3)
     x = helpers.to_device_bf16(bits)
-    for kw in (dict(), dict(sr=True, seed=4), dict(rht_mask=0x0F0F), dict(two_d=True), dict(scale46=True),
-               dict(scale46=True, sr=True, seed=6), dict(scale46=True, rht_mask=0x3C3C)):
+    for kw in (dict(), dict(sr=True, seed=4), dict(rht_mask=0x0F0F), dict(rht_mask=0x0F0F, sr=True, seed=5),
+               dict(two_d=True), dict(scale46=True), dict(scale46=True, sr=True, seed=6),
+               dict(scale46=True, rht_mask=0x3C3C), dict(scale46=True, rht_mask=0x3C3C, sr=True, seed=7)):
         row, col = ops.quantize(x, rowwise=True, colwise=True, stream_id=2, **kw)
         torch.cuda.synchronize()
         common = dict(scaling=1 if kw.get("two_d") else (2 if kw.get("scale46") else 0),
