@@ -163,6 +163,40 @@ __device__ __forceinline__ void rht16_unscaled(float* t, uint32_t sign_mask) {
     }
 }
 
+// rht16_unscaled on two blocks at once, as packed binary32 pairs (a[i], b[i]):
+// each lane of add.rn.f32x2 / sub.rn.f32x2 rounds like the scalar operation,
+// so the results are those of two rht16_unscaled calls, in half the
+// instructions.
+__device__ __forceinline__ void rht16_unscaled_x2(float* a, float* b, uint32_t sign_mask) {
+    uint64_t t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t sgn = ((sign_mask >> i) & 1u) << 31;
+        asm("mov.b64 %0, {%1, %2};"
+            : "=l"(t[i])
+            : "r"(__float_as_uint(a[i]) ^ sgn), "r"(__float_as_uint(b[i]) ^ sgn));
+    }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (i & (1 << s)) continue;
+            uint64_t sum, dif;
+            asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(t[i]), "l"(t[i | (1 << s)]));
+            asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dif) : "l"(t[i]), "l"(t[i | (1 << s)]));
+            t[i] = sum;
+            t[i | (1 << s)] = dif;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        uint32_t lo, hi;
+        asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(t[i]));
+        a[i] = __uint_as_float(lo);
+        b[i] = __uint_as_float(hi);
+    }
+}
+
 __device__ __forceinline__ void scale16(float* t, float f) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) t[i] = __fmul_rn(t[i], f);

@@ -183,8 +183,7 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
             for (int i = 0; i < 16; ++i) plain_max = fmaxf(plain_max, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
         }
         if constexpr (kRHT) {
-            rht16_unscaled(t0, a.mask);   // the 1/4 comes below
-            rht16_unscaled(t1, a.mask);
+            rht16_unscaled_x2(t0, t1, a.mask);   // the 1/4 comes below
             if (P == Pass::kEncode && !fold) {
                 scale16(t0, 0.25f);
                 scale16(t1, 0.25f);
@@ -287,8 +286,9 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const RequantArgs a) 
             t0[i] = __fmul_rn(__fmul_rn(g.x, sb), sg);
             t1[i] = __fmul_rn(__fmul_rn(g.y, sb), sg);
         }
-        rht16(t0, a.mask);
-        rht16(t1, a.mask);
+        rht16_unscaled_x2(t0, t1, a.mask);
+        scale16(t0, 0.25f);
+        scale16(t1, 0.25f);
         float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -543,8 +543,7 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
             }
             if (a.emit_col && c < a.cols) {
                 if constexpr (kColRHT) {
-                    rht16_unscaled(t0, a.mask);   // the 1/4 comes below
-                    rht16_unscaled(t1, a.mask);
+                    rht16_unscaled_x2(t0, t1, a.mask);   // the 1/4 comes below
                     if (!fold) {
                         scale16(t0, 0.25f);
                         scale16(t1, 0.25f);
@@ -593,8 +592,7 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                     v[8 * kk + 7] = bf16hi(u.w);
                 }
                 if constexpr (kRowRHT) {
-                    rht16_unscaled(v, a.mask);   // the 1/4 comes below
-                    rht16_unscaled(v + 16, a.mask);
+                    rht16_unscaled_x2(v, v + 16, a.mask);   // the 1/4 comes below
                     if (!fold_row) {
                         scale16(v, 0.25f);
                         scale16(v + 16, 0.25f);
