@@ -197,6 +197,38 @@ __device__ __forceinline__ void rht16_unscaled_x2(float* a, float* b, uint32_t s
     }
 }
 
+// rht16_unscaled of one block with stages 0-2 on packed pairs (t[i], t[i + 8])
+// (stage s < 3 pairs i with i ^ 2^s in both halves alike) and stage 3, which
+// pairs the two halves, in scalar: the same operations in the same order.
+__device__ __forceinline__ void rht16_unscaled_packed(float* t, uint32_t sign_mask) {
+    uint64_t p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = __float_as_uint(t[i]) ^ (((sign_mask >> i) & 1u) << 31);
+        const uint32_t hi = __float_as_uint(t[i + 8]) ^ (((sign_mask >> (i + 8)) & 1u) << 31);
+        asm("mov.b64 %0, {%1, %2};" : "=l"(p[i]) : "r"(lo), "r"(hi));
+    }
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i & (1 << s)) continue;
+            uint64_t sum, dif;
+            asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(p[i]), "l"(p[i | (1 << s)]));
+            asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dif) : "l"(p[i]), "l"(p[i | (1 << s)]));
+            p[i] = sum;
+            p[i | (1 << s)] = dif;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t lo, hi;
+        asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(p[i]));
+        t[i] = __fadd_rn(__uint_as_float(lo), __uint_as_float(hi));
+        t[i + 8] = __fsub_rn(__uint_as_float(lo), __uint_as_float(hi));
+    }
+}
+
 __device__ __forceinline__ void scale16(float* t, float f) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) t[i] = __fmul_rn(t[i], f);

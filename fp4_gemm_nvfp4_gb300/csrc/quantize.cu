@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
                        bf16lo(u0.w), bf16hi(u0.w), bf16lo(u1.x), bf16hi(u1.x), bf16lo(u1.y), bf16hi(u1.y),
                        bf16lo(u1.z), bf16hi(u1.z), bf16lo(u1.w), bf16hi(u1.w)};
         if constexpr (kRHT) {
-            rht16_unscaled(t, a.mask);   // the 1/4 comes below
+            rht16_unscaled_packed(t, a.mask);   // the 1/4 comes below
             if (P == Pass::kEncode && !fold) scale16(t, 0.25f);
         }
         float amax_b = 0.0f;
