@@ -256,7 +256,7 @@ NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_tensor *A, const nvfp4_tensor *B, 
 /*
  * nvfp4_gemm_amax -- nvfp4_gemm with BF16 output that also takes, in its
  * epilogue, the two tensor amaxes the quantization of D needs [FS App. 9:
- * quantization fused with the operation that produces its input; SURVEY f1]:
+ * quantization fused with the operation that produces its input]:
  *  amax_out[0]  max |D| over the BF16 outputs (the row-wise operand's amax);
  *  amax_out[1]  max |U d| over the 16-row blocks d of each column of D, with
  *               U = H16 * diag(rht_sign_mask) / 4 (the col-wise RHT operand's

@@ -1,7 +1,7 @@
 """The output amax fused into the producing GEMM (nvfp4_gemm_amax) and the
 quantization that takes it (nvfp4_quantize_row_col_rht_amax): the
-quantization's amax pass moves into the GEMM epilogue (the pages'
-Appendix 9 on fusing quantization with the producing operation).
+quantization's amax pass moves into the GEMM epilogue ("Full-Stack FP4",
+Appendix 9, on fusing quantization with the producing operation).
 
 The fused maxima are checked against their definition applied to the GEMM's
 own BF16 output (max |D|, and max |H16 D d| / 4 over 16-row blocks in the
