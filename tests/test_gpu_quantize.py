@@ -144,6 +144,9 @@ def _ranges(n, k=48):
     ("c4_dY_row", 16384, 3072, "grad", oracle.ROWWISE, 0, 1, False),
     ("c4_H_46_row", 16384, 9216, "normal", oracle.ROWWISE, 2, 0, False),
     ("c3_dY_46_col", 8192, 9216, "grad", oracle.COLWISE, 2, 1, True),
+    # the quantizer sweep's largest size, 2^29 elements (1 GiB of bf16)
+    ("c5_max_row", 65536, 8192, "grad", oracle.ROWWISE, 0, 0, False),
+    ("c5_max_2d_col", 65536, 8192, "grad", oracle.COLWISE, 1, 0, False),
 ])
 def test_quantize_parity_full_size(name, rows, cols, kind, orientation, scaling, rounding, rht):
     seed = zlib.crc32(name.encode()) % 1000
@@ -212,6 +215,45 @@ def test_row_col_rht_zero_tensor():
         codes, scales, amax, sg, _ = helpers.operand_to_host(g)
         assert amax == 0 and sg == 1 and not scales.any()
     assert not helpers.operand_to_host(row)[0].any()
+
+
+@pytest.mark.parametrize("name,rows,cols,rounding,amax_given", [
+    ("c4_X", 16384, 3072, 0, False),
+    ("c4_dY_down", 16384, 3072, 1, False),
+    ("c4_H", 16384, 9216, 0, True),
+    ("c4_dY_up", 16384, 9216, 1, True),
+])
+def test_row_col_rht_full_size_sampled(name, rows, cols, rounding, amax_given):
+    """The 3B FFN layer step's four activation/gradient quantizations at 16384
+    tokens, in the launch configuration the layer step uses (one pair pass;
+    H and dY_up with their two tensor amaxes given, as the producing GEMM
+    supplies them): sampled logical rows of both outputs against the oracle,
+    which takes each tensor amax over the whole tensor itself."""
+    seed = zlib.crc32(name.encode()) % 1000
+    bits = inputs.student_t(rows, cols, seed) if rounding else \
+        inputs.normal(rows, cols, seed, outlier_channels=inputs.outlier_count(cols))
+    mask = inputs.rht_sign_mask(seed)
+    x = helpers.to_device_bf16(bits)
+    ref_amax = {oracle.ROWWISE: oracle.amax(bits, oracle.ROWWISE), oracle.COLWISE: oracle.amax(bits, oracle.COLWISE,
+                                                                                               True, mask)}
+    if amax_given:
+        amax = torch.tensor([ref_amax[oracle.ROWWISE], ref_amax[oracle.COLWISE]], dtype=torch.float32, device="cuda")
+        row, col = ops.quantize_row_col_rht_amax(x, mask, amax, sr=rounding == 1, seed=seed,
+                                                 stream_row=1, stream_col=2)
+    else:
+        row, col = ops.quantize_row_col_rht(x, mask, sr=rounding == 1, seed=seed, stream_row=1, stream_col=2)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    del x
+    for op, orientation, rht, stream in ((row, oracle.ROWWISE, False, 1), (col, oracle.COLWISE, True, 2)):
+        codes, scales, amax_g, sg, _ = helpers.operand_to_host(op)
+        assert amax_g == ref_amax[orientation]
+        for lr0, lr1 in _ranges(op.rows):
+            ref = oracle.quantize(bits, orientation, rounding=rounding, use_rht=rht, sign_mask=mask, seed=seed,
+                                  stream_id=stream, rows_subset=(lr0, lr1), amax_value=ref_amax[orientation])
+            assert sg == ref["s_g"]
+            assert np.array_equal(codes[lr0:lr1], ref["codes"]), (name, orientation, lr0)
+            assert np.array_equal(scales[lr0:lr1], ref["scales"]), (name, orientation, lr0)
 
 
 # ---- Wgrad re-quantization from the forward's row-wise operand (Eq. (2)) ----
