@@ -96,6 +96,36 @@ def student_t(rows: int, cols: int, seed: int, df: int = 3, scale: float = 1e-3)
     return to_bf16_bits(_chunked(rows, cols, seed, draw))
 
 
+def extreme_range(rows: int, cols: int, seed: int, amax: float, span_log2: int = 40,
+                  zero_tile_frac: float = 1 / 16, zero_block_frac: float = 1 / 32) -> np.ndarray:
+    """Edge-case bf16 bits spanning about 2^-span_log2 of the tensor amax.
+
+    N(0, 1) values whose 16x16 tiles are each scaled by 2^-k, k uniform on
+    0..span_log2, with some tiles all zero, some 16-element row blocks all
+    zero and some zeros negative; everything is scaled so that the largest
+    magnitude is just below ``amax`` and element (0, 0) is set to ``amax``
+    itself (pass a bfloat16 value).  Values that fall below the smallest
+    bfloat16 subnormal become zeros.  rows and cols are multiples of 16.
+    """
+    assert rows % 16 == 0 and cols % 16 == 0
+    rng = np.random.default_rng([seed, 0xE7])
+    x = rng.standard_normal((rows, cols), dtype=np.float32).astype(np.float64)
+    tiles = x.reshape(rows // 16, 16, cols // 16, 16)
+    k = rng.integers(0, span_log2 + 1, (rows // 16, cols // 16))
+    tiles *= np.exp2(-k.astype(np.float64))[:, None, :, None]
+    tiles *= (rng.random((rows // 16, cols // 16)) >= zero_tile_frac)[:, None, :, None]
+    blocks = x.reshape(rows, cols // 16, 16)
+    blocks *= (rng.random((rows, cols // 16)) >= zero_block_frac)[:, :, None]
+    m = np.abs(x).max()
+    if m > 0:
+        x *= (float(amax) * 0.99) / m
+    x[x == 0] = 0.0
+    neg = rng.random((rows, cols)) < 0.5
+    x[(x == 0) & neg] = -0.0
+    x[0, 0] = amax
+    return to_bf16_bits(x.astype(np.float32))
+
+
 def rht_sign_mask(seed: int) -> int:
     """The 16 random signs of D for one backward pass, as a bit mask."""
     rng = np.random.default_rng([seed, 0xD])

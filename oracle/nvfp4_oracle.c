@@ -15,6 +15,9 @@
  *    amax_t = 0 and FLT_MAX when the quotient overflows;
  *  - block scale: s_b = E4M3_rne_satfinite((amax_b / 6) * S_enc);
  *  - encode multiplier r_b = S_enc / s_b (0 when s_b = 0), v = x * r_b;
+ *    when that quotient overflows (S_enc near FLT_MAX, s_b < 1: a tensor
+ *    amax below about 4e-33), v = (x * S_enc) / s_b, each operation rounded
+ *    once, so that zeros stay (signed) zeros and the rest keep their size;
  *  - RNE ties go to the even mantissa; the code's sign bit is v's sign bit;
  *  - SR: round up iff (float)u < frac * 2^16, frac = d / step, u a 16-bit
  *    random value;
@@ -293,6 +296,19 @@ int oracle_quantize_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t 
                         orientation, amax, lr0, lr1, codes, scales);
 }
 
+/* The value the E2M1 encoder rounds: x / (s_b * s_g) = x * S_enc / s_b,
+ * evaluated as v = x * r_b with r_b = S_enc / s_b ("Full-Stack FP4", Sec. 2:
+ * x^ = x_E2M1 * s * s_g, so the encode divides by s * s_g).  When r_b
+ * overflows to +inf (S_enc close to FLT_MAX and s_b < 1), x * r_b would be
+ * +-inf for every non-zero x and NaN for x = +-0; the quotient is then taken
+ * as (x * S_enc) / s_b, whose intermediate stays finite. */
+static float encode_value(float x, float r_b, float s_enc, float sb)
+{
+    if (isinf(r_b))
+        return (x * s_enc) / sb;
+    return x * r_b;
+}
+
 static int quantize_src(const struct source *x, int64_t rows, int64_t cols,
                         int scaling, int rounding, int use_rht, uint16_t sign_mask,
                         uint64_t seed, uint64_t stream_id, int orientation,
@@ -371,8 +387,8 @@ static int quantize_src(const struct source *x, int64_t rows, int64_t cols,
                 float err6 = 0.0f, err4 = 0.0f;
                 for (int t = 0; t < 16; ++t) {
                     float xs = blk[t] * s_enc;
-                    float g6 = (float)oracle_e2m1_value(oracle_e2m1_rne(blk[t] * r_b));
-                    float g4 = (float)oracle_e2m1_value(oracle_e2m1_rne(blk[t] * r4));
+                    float g6 = (float)oracle_e2m1_value(oracle_e2m1_rne(encode_value(blk[t], r_b, s_enc, sb)));
+                    float g4 = (float)oracle_e2m1_value(oracle_e2m1_rne(encode_value(blk[t], r4, s_enc, sb4)));
                     float d6 = xs - g6 * sb;
                     float d4 = xs - g4 * sb4;
                     err6 = fmaf(d6, d6, err6);
@@ -381,6 +397,7 @@ static int quantize_src(const struct source *x, int64_t rows, int64_t cols,
                 if (err4 < err6) {
                     sb_code = code4;
                     r_b = r4;
+                    sb = sb4;
                 }
             }
             srow[b] = sb_code;
@@ -389,7 +406,7 @@ static int quantize_src(const struct source *x, int64_t rows, int64_t cols,
                 uint8_t q[2];
                 for (int u = 0; u < 2; ++u) {
                     int64_t j = 16 * b + t + u;
-                    float v = blk[t + u] * r_b;
+                    float v = encode_value(blk[t + u], r_b, s_enc, sb);
                     if (rounding == 0) {
                         q[u] = oracle_e2m1_rne(v);
                     } else {

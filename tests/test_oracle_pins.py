@@ -453,6 +453,132 @@ def test_quantize_rejects_bad_shapes():
         oracle.quantize(np.zeros((24, 32), np.uint16), scaling=1)
 
 
+# --------------------------------------------------------- extreme range ----
+# Tensors whose block amaxes span 2^-40 of the tensor amax (subnormal and zero
+# block scales), with tensor amaxes from the smallest bfloat16 subnormal (the
+# tensor scale saturates at FLT_MAX and S_enc / s_b overflows) to 3e38.  The
+# encode is checked against the format's definition evaluated in float64:
+# the code of x is the E2M1 grid point nearest to |x| / (s_b * s_g) with
+# s_b decoded by torch, i.e. x^ = x_E2M1 * s * s_g ("Full-Stack FP4", Sec. 2).
+FLT_MAX = float(np.finfo(np.float32).max)
+EXTREME_AMAX = [2688.0, 2.0 ** -133, float(np.float32(1e-36)), 3.0e38]
+
+
+def _extreme(amax, span=40, seed=0):
+    return inputs.extreme_range(64, 256, seed + 7, amax, span_log2=span)
+
+
+def test_tensor_scale_saturates_for_a_subnormal_amax():
+    """amax = 2^-133 (smallest bfloat16 subnormal): 2688 / amax overflows, so
+    S_enc = FLT_MAX and s_g = RN(1 / FLT_MAX) = 2^-128 (1 / FLT_MAX is
+    2^-128 (1 + 2^-24 + ...), whose nearest binary32 value, a subnormal with
+    spacing 2^-149, is 2^-128)."""
+    s_enc, s_g = oracle.tensor_scale(2.0 ** -133)
+    assert s_enc == np.float32(FLT_MAX)
+    exact = Fraction(1) / Fraction(int(np.float32(FLT_MAX)))
+    assert Fraction(float(s_g)) == Fraction(1, 2 ** 128)
+    assert abs(exact - Fraction(1, 2 ** 128)) < Fraction(1, 2 ** 150)
+
+
+def _nearest_grid_f64(a):
+    """Index of the E2M1 grid point nearest to a >= 0 (saturating at 6), and
+    the distance of a to the nearest decision boundary (midpoint)."""
+    k = np.clip(np.searchsorted(GRID, a, side="right") - 1, 0, 7)
+    k1 = np.minimum(k + 1, 7)
+    mid = (GRID[k] + GRID[k1]) / 2
+    idx = np.where((k < 7) & (a > mid), k1, k)
+    margin = np.where(k < 7, np.abs(a - mid), np.inf)
+    return idx, margin
+
+
+@pytest.mark.parametrize("amax", EXTREME_AMAX)
+@pytest.mark.parametrize("orientation", [oracle.ROWWISE, oracle.COLWISE])
+@pytest.mark.parametrize("scaling", [0, 1])
+def test_rne_encode_is_the_nearest_grid_point_across_the_range(amax, orientation, scaling):
+    """Every RNE code (no RHT) is the grid point nearest to |x| S_enc / s_b
+    computed in float64, with x's sign bit (also for -0); blocks whose scale
+    rounded to 0 encode every element as a signed zero."""
+    x = _extreme(amax)
+    q = oracle.quantize(x, orientation, scaling=scaling)
+    xf = inputs.bf16_bits_to_f32(x)
+    if orientation == oracle.COLWISE:
+        xf = np.ascontiguousarray(xf.T)
+    assert q["amax"] == np.float32(np.abs(xf).max())
+    codes = _unpack(q["codes"])
+    sb = np.repeat(_torch_e4m3_values(q["scales"]), 16, axis=1)
+    s_enc = float(q["s_enc"])
+    a = np.abs(xf.astype(np.float64)) * s_enc / np.where(sb == 0, 1.0, sb)
+    idx, margin = _nearest_grid_f64(a)
+    decided = (sb > 0) & (margin > 1e-5 * np.maximum(a, 1.0))
+    assert decided.sum() >= 0.9 * (sb > 0).sum() > 0
+    assert np.array_equal(codes[decided] & 7, idx[decided])
+    assert np.all(codes[sb == 0] & 7 == 0)
+    assert np.array_equal((codes & 8) != 0, np.signbit(xf))
+
+
+@pytest.mark.parametrize("amax", EXTREME_AMAX)
+@pytest.mark.parametrize("use_rht", [False, True])
+def test_sr_codes_are_a_neighbouring_grid_point_across_the_range(amax, use_rht):
+    """SR codes are one of the two grid points around |x| S_enc / s_b (the
+    value itself when it is a grid point); with the RHT the rotated values
+    come from the pinned rht16."""
+    if use_rht and amax > 1e37:
+        amax = 1.0e37        # the butterfly of 16 such values stays finite
+    x = _extreme(float(inputs.bf16_bits_to_f32(inputs.to_bf16_bits(np.array([amax], np.float32)))[0]))
+    q = oracle.quantize(x, rounding=1, use_rht=use_rht, sign_mask=0x6A5C, seed=3)
+    xf = inputs.bf16_bits_to_f32(x)
+    if use_rht:
+        xf = np.stack([oracle.rht16(b, 0x6A5C) for b in xf.reshape(-1, 16)]).reshape(xf.shape)
+    codes = _unpack(q["codes"])
+    sb = np.repeat(_torch_e4m3_values(q["scales"]), 16, axis=1)
+    a = np.abs(xf.astype(np.float64)) * float(q["s_enc"]) / np.where(sb == 0, 1.0, sb)
+    lo = np.clip(np.searchsorted(GRID, a * (1 - 1e-6), side="right") - 1, 0, 7)
+    hi = np.minimum(np.clip(np.searchsorted(GRID, a * (1 + 1e-6), side="left"), 0, 7), 7)
+    mag = codes & 7
+    ok = (sb == 0) & (mag == 0) | (sb > 0) & (mag >= lo) & (mag <= hi)
+    assert ok.all(), np.argwhere(~ok)[:5]
+
+
+@pytest.mark.parametrize("amax", EXTREME_AMAX)
+def test_46_and_requantize_stay_finite_across_the_range(amax):
+    """4/6 scaling and the Wgrad re-quantization on extreme tensors decode to
+    values within the block's reach: every decoded |x^| <= 6 s_b s_g, zeros
+    of x give zeros (4/6, no RHT)."""
+    x = _extreme(amax)
+    q = oracle.quantize(x, scaling=2)
+    deq = oracle.dequantize(q["codes"], q["scales"], q["s_g"])
+    xf = inputs.bf16_bits_to_f32(x)
+    assert np.all(np.isfinite(deq))
+    assert np.all(deq[xf == 0] == 0)
+    unit = np.repeat(_torch_e4m3_values(q["scales"]), 16, axis=1) * float(q["s_g"])
+    assert np.all(np.abs(deq) <= 6 * unit * (1 + 2 ** -20))
+    if amax <= 1e37:
+        r = oracle.requantize_col_rht(oracle.quantize(x), 0x1234, rounding=1, seed=2)
+        assert np.all(np.isfinite(oracle.dequantize(r["codes"], r["scales"], r["s_g"])))
+
+
+def test_overflowing_multiplier_encodes_by_the_quotient():
+    """A tensor amax of about 1e-36 saturates S_enc at FLT_MAX; blocks whose
+    amax is below about 1.6e-38 get E4M3 scales below 1, where S_enc / s_b
+    overflows: their values are encoded as (x S_enc) / s_b, so a block of
+    [a, a/2, a/100, 0, -0] keeps the ratios (6, 3, 0, 0, -0) instead of
+    becoming all +-6 (and NaN for the zeros)."""
+    a = np.float32(2.0 ** -128)                 # 2.9e-39: its block scale is below 1
+    row = np.zeros(16, np.float32)
+    row[:5] = [a, a / 2, a / 100, 0.0, -0.0]
+    x = np.zeros((16, 32), np.float32)
+    x[0, 16:] = row
+    x[0, 0] = np.float32(1e-36)
+    bits = inputs.to_bf16_bits(x)
+    q = oracle.quantize(bits)
+    assert q["s_enc"] == np.float32(FLT_MAX)
+    sb = _torch_e4m3_values(q["scales"][:1, 1:2])[0, 0]
+    assert 0 < sb < 1
+    assert float(np.float32(FLT_MAX)) / sb > FLT_MAX      # r_b would overflow
+    codes = _unpack(q["codes"])[0, 16:21]
+    assert list(codes) == [7, 5, 0, 0, 8]
+
+
 # ------------------------------------------------- 4/6 adaptive scaling ----
 # "Full-Stack FP4" names 4/6 scaling (its related-work section: MSE-optimal
 # adaptive block scaling) without printing the rule; the oracle's reading is
