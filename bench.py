@@ -271,13 +271,50 @@ class Step:
 
 
 # ----------------------------------------------------------------- clocks --
+def smi_gpu_id(local):
+    """nvidia-smi's name for the GPU torch uses as device `local`: its UUID
+    (CUDA_VISIBLE_DEVICES may renumber devices, so the ordinal can name
+    another GPU), else the ordinal."""
+    import torch
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        if uuid:
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except (AttributeError, RuntimeError):
+        pass
+    return str(local)
+
+
+def host_cpu():
+    """The host CPU model and the cores the OS reports."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"cpu_model": model or "unknown", "nproc": os.cpu_count()}
+
+
 class ClockSampler:
     QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
-        self.index = index
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
         self.proc = None
         self.path = os.path.join(tempfile.gettempdir(), f"nvfp4_clocks_{os.getpid()}.csv")
 
@@ -285,7 +322,7 @@ class ClockSampler:
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.5)     # let the sampler start before the timed region
@@ -346,29 +383,48 @@ def _oracle_kw(kw, mask, seed, orient):
 def cpu_baseline(host, mask, seed, rows_a=8, rows_b=1024):
     """The oracle, as it stands, on a bounded sample of the step.  Each GEMM
     computes a rows_a x rows_b block of its output; the quantize calls encode
-    exactly the operand rows that block needs (each after the oracle's own
-    full-tensor amax pass).  Returns (GEMM FLOP of the sample / total seconds
-    in TFLOP/s, seconds, description, threads)."""
+    exactly the operand rows that block needs, after the oracle's own
+    full-tensor amax pass.  Returns a dict: the sample's GEMM FLOP rate over
+    its whole time (TFLOP/s), its seconds, a description, the threads used,
+    and the full step's time extrapolated from the sample (the amax passes as
+    timed, the encode scaled by elements, the GEMM by FLOPs)."""
     import oracle
     src_of = {n: s for n, s, _ in QUANTS}
     kw_of = {n: k for n, _, k in QUANTS}
-    t0 = time.perf_counter()
-    flops = 0
+    t_amax = t_enc = t_gemm = 0.0
+    enc_elems = full_elems = flops = full_flops = 0
     for gname, (an, ao), (bn, bo) in GEMMS:
-        ops_ = []
+        ops_, full_rows = [], []
         for qn, orient, nrows in ((an, ao, rows_a), (bn, bo, rows_b)):
             o = oracle.ROWWISE if orient == "row" else oracle.COLWISE
             bits = host[src_of[qn]]
-            lrows = bits.shape[0] if o == oracle.ROWWISE else bits.shape[1]
-            ops_.append(oracle.quantize(bits, o, rows_subset=(0, min(nrows, lrows)),
-                                        **_oracle_kw(kw_of[qn], mask, seed, orient)))
+            lrows, lcols = (bits.shape if o == oracle.ROWWISE else bits.shape[::-1])
+            kw = _oracle_kw(kw_of[qn], mask, seed, orient)
+            n = min(nrows, lrows)
+            t0 = time.perf_counter()
+            amax = oracle.amax(bits, o, kw["use_rht"], kw["sign_mask"])
+            t1 = time.perf_counter()
+            ops_.append(oracle.quantize(bits, o, rows_subset=(0, n), amax_value=amax, **kw))
+            t2 = time.perf_counter()
+            t_amax += t1 - t0
+            t_enc += t2 - t1
+            enc_elems += n * lcols
+            full_elems += lrows * lcols
+            full_rows.append(lrows)
         a, b = ops_
+        t0 = time.perf_counter()
         oracle.gemm_f64(a, b, with_abs=False)
-        flops += 2 * a["codes"].shape[0] * b["codes"].shape[0] * a["codes"].shape[1] * 2
-    dt = time.perf_counter() - t0
+        t_gemm += time.perf_counter() - t0
+        K = a["codes"].shape[1] * 2
+        flops += 2 * a["codes"].shape[0] * b["codes"].shape[0] * K
+        full_flops += 2 * full_rows[0] * full_rows[1] * K
+    dt = t_amax + t_enc + t_gemm
     desc = (f"oracle on the host cores: each of the 6 GEMMs on a {rows_a} x {rows_b} block of its "
             f"output, its operand rows quantized by the oracle (full-tensor amax pass included)")
-    return flops / dt / 1e12, dt, desc, oracle.num_threads()
+    extrapolated = t_amax + t_enc * full_elems / max(enc_elems, 1) + t_gemm * full_flops / max(flops, 1)
+    return {"value": flops / dt / 1e12, "seconds": dt, "sample": desc, "threads": oracle.num_threads(),
+            "extrapolated_full_step_s": extrapolated,
+            "sample_split_s": {"amax_passes": round(t_amax, 3), "encode": round(t_enc, 3), "gemm": round(t_gemm, 3)}}
 
 
 # --------------------------------------------------------------- measure --
@@ -432,7 +488,7 @@ def measure(args):
 
     # ---- the timed region: exactly K steps, inputs resident in HBM
     windows = []
-    with ClockSampler(local) as clocks:
+    with ClockSampler(smi_gpu_id(local)) as clocks:
         barrier()
         t0 = time.time()
         with torch.cuda.stream(stream):
@@ -537,6 +593,16 @@ def measure(args):
                 "algorithmic_bytes_per_step": round(qbytes),
                 "peak_source": f"{peak_src} hbm_gbs"}
 
+    quant_roof = {"kernel": "quantize (amax + encode passes of the step)", "bound": "hbm",
+                  "achieved": round(quant_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                  "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "traffic": measured_traffic("quantize"),
+                  "traffic_basis": "DRAM bytes per step over the class's launches (ncu)",
+                  "algorithmic_bytes_per_step": round(qbytes), "peak_source": f"{peak_src} hbm_gbs"}
+    gemm_roof = {"kernel": "gemm_nvf4_kernel (the step's 6 GEMMs)", "bound": "tensor",
+                 "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                 "frac": round(gemm_tflops / fp4_peak, 4), "traffic": measured_traffic("gemm"),
+                 "traffic_basis": "DRAM bytes per step over the class's launches (ncu)",
+                 "peak_source": f"{peak_src} bf16 burst x {FP4_OVER_BF16:g} (nominal fp4/bf16)"}
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -549,6 +615,7 @@ def measure(args):
                                 "those GEMMs' epilogue" if FUSE_AMAX else "all six bf16 tensors are inputs"),
                    "launch": "each step is one CUDA graph replay"},
         "roofline": roof,
+        "roofline_by_class": {"gemm": gemm_roof, "quantize": quant_roof},
         "gemm_tflops": round(gemm_tflops, 1),
         "gemm_frac_of_fp4_peak": round(gemm_tflops / fp4_peak, 4),
         "quantize_gbs": round(quant_gbs, 1),
@@ -560,9 +627,15 @@ def measure(args):
         "clocks": clocks.summary(windows),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        v, dt, desc, cores = cpu_baseline(host, mask, seed, rows_a=512, rows_b=4096)
-        result["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                                  "sample": desc, "seconds": round(dt, 2)}
+        cb = cpu_baseline(host, mask, seed, rows_a=512, rows_b=4096)
+        result["cpu_baseline"] = {"value": cb["value"], "unit": "TFLOP/s", "cores": cb["threads"], "kind": "oracle",
+                                  "sample": cb["sample"], "seconds": round(cb["seconds"], 2),
+                                  **host_cpu(),
+                                  "extrapolated_full_step_s": round(cb["extrapolated_full_step_s"], 1),
+                                  "extrapolated_note": ("extrapolated, not measured: the sample's amax passes as "
+                                                        "timed, its encode time scaled by the step's elements and "
+                                                        "its GEMM time by the step's FLOPs"),
+                                  "sample_split_s": cb["sample_split_s"]}
     if world > 1:
         torch.distributed.destroy_process_group()
     return result, rank
@@ -581,8 +654,9 @@ def reference_arm(args):
         cpu_baseline(host, mask, seed, **kw)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        v, dt, desc, cores = cpu_baseline(host, mask, seed, **kw)
-        vals.append(v)
+        cb = cpu_baseline(host, mask, seed, **kw)
+        vals.append(cb["value"])
+        desc, cores = cb["sample"], cb["threads"]
     total = time.perf_counter() - t0
     value = statistics.mean(vals)
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -591,7 +665,7 @@ def reference_arm(args):
             "data": "synthetic", "config": {"workload": workload_name(), "tokens": TOKENS, "hidden": HIDDEN,
                                             "ffn": FFN},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, **host_cpu()},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

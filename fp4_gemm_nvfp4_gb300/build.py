@@ -21,7 +21,7 @@ FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std
 
 def _newest_input():
     paths = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    paths.append(os.path.join(ROOT, "include", "nvfp4.h"))
+    paths += [os.path.join(ROOT, "include", h) for h in ("nvfp4.h", "nvfp4_testing.h")]
     paths.append(os.path.abspath(__file__))
     return max(os.path.getmtime(p) for p in paths)
 

@@ -37,7 +37,8 @@ EXPORTED = ("nvfp4_scale_bytes", "nvfp4_quantize_workspace_size", "nvfp4_quantiz
             "nvfp4_device_error", "nvfp4_quantize_noalloc", "nvfp4_quantize_row_col_rht",
             "nvfp4_requantize_col_rht", "nvfp4_gemm_lora", "nvfp4_gemm_lora_workspace_size",
             "nvfp4_gemm_amax", "nvfp4_quantize_row_col_rht_amax", "nvfp4_gemm_axpby",
-            "nvfp4_newton_schulz_workspace_size", "nvfp4_newton_schulz_step")
+            "nvfp4_newton_schulz_workspace_size", "nvfp4_newton_schulz_step",
+            "nvfp4_testing_arm_gemm_timeout")
 
 
 class nvfp4_tensor(ctypes.Structure):
@@ -103,6 +104,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_dequantize.restype = i32
     L.nvfp4_status_string.argtypes, L.nvfp4_status_string.restype = [i32], ctypes.c_char_p
     L.nvfp4_device_error.argtypes, L.nvfp4_device_error.restype = [vp], i32
+    L.nvfp4_testing_arm_gemm_timeout.argtypes = [ctypes.c_uint32]
+    L.nvfp4_testing_arm_gemm_timeout.restype = i32
     _lib = L
     return L
 
@@ -209,6 +212,12 @@ def nvfp4_status_string(status):
 
 def nvfp4_device_error(stream):
     return load().nvfp4_device_error(stream)
+
+
+def nvfp4_testing_arm_gemm_timeout(wait_limit_us):
+    """Test support (include/nvfp4_testing.h): the next GEMM launch withholds
+    one barrier arrival and gives up on its waits after wait_limit_us."""
+    return load().nvfp4_testing_arm_gemm_timeout(wait_limit_us)
 
 
 def status_string(status):

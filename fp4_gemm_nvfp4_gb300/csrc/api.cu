@@ -3,16 +3,28 @@
 // Every check runs on the host before anything is enqueued, so an error
 // status means no kernel was launched (except NVFP4_ERR_CUDA from a launch).
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cmath>
 #include <cstdint>
 
 #include "../../include/nvfp4.h"
+#include "../../include/nvfp4_testing.h"
 #include "kernels.h"
 
 namespace {
 
 using nvfp4::QuantTarget;
+
+// An NVTX range around one C-ABI call (host side only: a profiler's timeline
+// then attributes each kernel launch to the entry point that enqueued it; with
+// no tool attached a push/pop costs a null check).
+struct ApiRange {
+    explicit ApiRange(const char* name) { nvtxRangePushA(name); }
+    ~ApiRange() { nvtxRangePop(); }
+    ApiRange(const ApiRange&) = delete;
+    ApiRange& operator=(const ApiRange&) = delete;
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -198,6 +210,7 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
                             nvfp4_rounding rounding, uint64_t seed, uint64_t stream_id, int orientations,
                             const nvfp4_tensor* out_row, const nvfp4_tensor* out_col, void* workspace,
                             size_t workspace_bytes, nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_quantize");
     return quantize_impl(x, rows, cols, ld_x, scaling, rounding, seed, stream_id, orientations, out_row, out_col,
                          false, 0, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -206,6 +219,7 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64
                                 nvfp4_rounding rounding, uint64_t seed, uint64_t stream_id, int orientations,
                                 const nvfp4_tensor* out_row, const nvfp4_tensor* out_col, uint16_t rht_sign_mask,
                                 void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_rht_quantize");
     return quantize_impl(x, rows, cols, ld_x, scaling, rounding, seed, stream_id, orientations, out_row, out_col,
                          true, rht_sign_mask, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -215,6 +229,7 @@ nvfp4_status nvfp4_quantize_row_col_rht(const void* x, int64_t rows, int64_t col
                                         uint64_t stream_col, uint16_t rht_sign_mask, const nvfp4_tensor* out_row,
                                         const nvfp4_tensor* out_col, void* workspace, size_t workspace_bytes,
                                         nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_quantize_row_col_rht");
     if (rounding != NVFP4_ROUND_RNE && rounding != NVFP4_ROUND_SR) return NVFP4_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
     if (cols % 16 != 0 || rows % 16 != 0) return NVFP4_ERR_SHAPE;
@@ -234,6 +249,7 @@ nvfp4_status nvfp4_quantize_row_col_rht(const void* x, int64_t rows, int64_t col
 nvfp4_status nvfp4_requantize_col_rht(const nvfp4_tensor* in_row, nvfp4_rounding rounding, uint64_t seed,
                                       uint64_t stream_id, uint16_t rht_sign_mask, const nvfp4_tensor* out_col,
                                       void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_requantize_col_rht");
     if (rounding != NVFP4_ROUND_RNE && rounding != NVFP4_ROUND_SR) return NVFP4_ERR_INVALID_ARG;
     if (!in_row || !out_col) return NVFP4_ERR_INVALID_ARG;
     const int64_t rows = in_row->rows, cols = in_row->cols;
@@ -258,6 +274,7 @@ nvfp4_status nvfp4_requantize_col_rht(const nvfp4_tensor* in_row, nvfp4_rounding
 
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, int64_t ldd,
                         nvfp4_dtype out_dtype, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_gemm");
     (void)workspace;
     (void)workspace_bytes;
     if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
@@ -283,6 +300,7 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, i
 
 nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, int64_t ldd, float* amax_out,
                              uint16_t rht_sign_mask, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_gemm_amax");
     (void)workspace;
     (void)workspace_bytes;
     nvfp4_status s;
@@ -314,6 +332,7 @@ nvfp4_status nvfp4_quantize_row_col_rht_amax(const void* x, int64_t rows, int64_
                                              uint64_t stream_col, uint16_t rht_sign_mask, const float* amax_in,
                                              const nvfp4_tensor* out_row, const nvfp4_tensor* out_col,
                                              nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_quantize_row_col_rht_amax");
     if (rounding != NVFP4_ROUND_RNE && rounding != NVFP4_ROUND_SR) return NVFP4_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0) return NVFP4_ERR_SHAPE;
     if (cols % 16 != 0 || rows % 16 != 0) return NVFP4_ERR_SHAPE;
@@ -338,6 +357,7 @@ nvfp4_status nvfp4_gemm_lora(const nvfp4_tensor* A, const nvfp4_tensor* B, void*
                              nvfp4_dtype out_dtype, const void* U, int64_t ldu, const void* V, int64_t ldv,
                              int64_t r, float beta, void* workspace, size_t workspace_bytes,
                              nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_gemm_lora");
     if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
     nvfp4_status s;
     if ((s = check_operand(A)) != NVFP4_OK) return s;
@@ -367,6 +387,7 @@ nvfp4_status nvfp4_gemm_lora(const nvfp4_tensor* A, const nvfp4_tensor* B, void*
 nvfp4_status nvfp4_gemm_axpby(const nvfp4_tensor* A, const nvfp4_tensor* B, void* D, int64_t ldd,
                               nvfp4_dtype out_dtype, float alpha, const void* C, int64_t ldc, float beta,
                               void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_gemm_axpby");
     (void)workspace;
     (void)workspace_bytes;
     return gemm_axpby_impl(A, B, D, ldd, out_dtype, alpha, C, ldc, beta, reinterpret_cast<cudaStream_t>(stream));
@@ -380,6 +401,7 @@ size_t nvfp4_newton_schulz_workspace_size(int64_t m, int64_t n) {
 nvfp4_status nvfp4_newton_schulz_step(const void* X, int64_t m, int64_t n, int64_t ldx, float a, float b, float c,
                                       uint16_t rht_sign_mask, void* X_out, int64_t ld_out, void* workspace,
                                       size_t workspace_bytes, nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_newton_schulz_step");
     if (!std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c)) return NVFP4_ERR_INVALID_ARG;
     if (m <= 0 || n <= 0 || m % 16 != 0 || n % 16 != 0) return NVFP4_ERR_SHAPE;
     nvfp4_status s;
@@ -414,6 +436,7 @@ nvfp4_status nvfp4_newton_schulz_step(const void* X, int64_t m, int64_t n, int64
 
 nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, void* y, int64_t ldy, nvfp4_dtype out_dtype,
                               nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_dequantize");
     if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
     nvfp4_status s;
     if ((s = check_operand(q)) != NVFP4_OK) return s;
@@ -442,7 +465,14 @@ const char* nvfp4_status_string(nvfp4_status status) {
     return "NVFP4_ERR_UNKNOWN";
 }
 
+nvfp4_status nvfp4_testing_arm_gemm_timeout(uint32_t wait_limit_us) {
+    if (wait_limit_us < 1000u || wait_limit_us > 2000000u) return NVFP4_ERR_INVALID_ARG;
+    nvfp4::arm_gemm_fault((uint64_t)wait_limit_us * 1000u);
+    return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_device_error(nvfp4_stream_t stream) {
+    const ApiRange range("nvfp4_device_error");
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return NVFP4_ERR_CUDA;
     unsigned int status = 0;
     if (nvfp4::gemm_read_and_clear_status(&status) != cudaSuccess) return NVFP4_ERR_CUDA;

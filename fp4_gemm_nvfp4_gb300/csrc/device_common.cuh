@@ -347,6 +347,35 @@ __device__ __forceinline__ void e2m1_decode_byte(uint32_t b, float& lo, float& h
         : "r"(b));
 }
 
+// The values the E2M1 encoder rounds, v_i = RN(t_i * r_b) (x / (s_b s_g) with
+// x^ = x_E2M1 * s_b * s_g: "Full-Stack FP4", Sec. 2).  When r_b = S_enc / s_b
+// has overflowed to +inf (S_enc saturated near FLT_MAX and a block scale below
+// 1, i.e. tensor amaxes below about 4e-33), t_i * r_b would be +-inf for every
+// non-zero t_i and NaN for zeros; such blocks take v_i = RN(RN(t_i * s_mult) /
+// s_b) instead, with s_mult = S_enc (times 1/4 when t holds the RHT's values
+// before its 1/4, which the multipliers then carry).  The test costs one
+// comparison per block.
+// (v may be t itself.)  kGuard = false leaves the test out: kernels take
+// that form whenever multiplier_may_overflow(S_enc) is false, i.e. for every
+// tensor amax above about 4e-33.
+// Whether S_enc / s_b can overflow for some E4M3 code: the smallest positive
+// s_b is 2^-9, so not while S_enc < FLT_MAX * 2^-9 (about 6.6e35, a tensor
+// amax above about 4e-33).  Conservative: a true answer only selects the
+// checked form of encode_values.
+__device__ __forceinline__ bool multiplier_may_overflow(float s_enc) { return s_enc >= 6.0e35f; }
+
+template <int N, bool kGuard = true>
+__device__ __forceinline__ void encode_values(const float* t, float r_b, uint32_t code, float s_mult, float* v) {
+    if (kGuard && r_b > 3.402823466e38f) {
+        const float sb = e4m3_decode(code);
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] = __fdiv_rn(__fmul_rn(t[i], s_mult), sb);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] = __fmul_rn(t[i], r_b);
+    }
+}
+
 // 4/6 adaptive scaling of one 1x16 block (the oracle's reading of the 4/6
 // scaling "Full-Stack FP4" names): the block's amax mapped to 6 (the plain
 // scale) or to 4, each candidate encoded with RNE and measured by
@@ -355,6 +384,7 @@ __device__ __forceinline__ void e2m1_decode_byte(uint32_t b, float& lo, float& h
 // values the multipliers of `table` apply to and xs_mult * t_i = x_i S_enc
 // (both carry the RHT's 1/4 when it is folded into the multipliers).  Returns
 // the chosen scale code and its multiplier in *r_b.
+template <bool kGuard = true>
 __device__ __forceinline__ uint32_t block_scale_46(const float* t, float amax_b, float s_enc, float xs_mult,
                                                    const float* table, float* r_b) {
     float r6;
@@ -363,11 +393,8 @@ __device__ __forceinline__ uint32_t block_scale_46(const float* t, float amax_b,
     const float r4 = table[c4];
     const float sb6 = e4m3_decode(c6), sb4 = e4m3_decode(c4);
     float v6[16], v4[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        v6[i] = __fmul_rn(t[i], r6);
-        v4[i] = __fmul_rn(t[i], r4);
-    }
+    encode_values<16, kGuard>(t, r6, c6, xs_mult, v6);
+    encode_values<16, kGuard>(t, r4, c4, xs_mult, v4);
     float g6[16], g4[16];
     e2m1_decode_x8(e2m1_rne_x8(v6), g6);
     e2m1_decode_x8(e2m1_rne_x8(v6 + 8), g6 + 8);
@@ -390,15 +417,15 @@ __device__ __forceinline__ uint32_t block_scale_46(const float* t, float amax_b,
     return c6;
 }
 
-// Encode the 16 values t of one block with multiplier r_b: codes in a uint2
-// (element 0 in the low nibble of byte 0).  idx_base is the SR index of
-// element 0 (a multiple of 16 for 1x16 blocks).
-template <bool kSR>
-__device__ __forceinline__ uint2 encode16(const float* t, float r_b, const PhiloxKeys& keys, uint64_t stream_id,
-                                          uint64_t idx_base) {
+// Encode the 16 values t of one block with multiplier r_b (scale code `code`;
+// s_mult as for encode_values): codes in a uint2 (element 0 in the low nibble
+// of byte 0).  idx_base is the SR index of element 0 (a multiple of 16 for
+// 1x16 blocks).
+template <bool kSR, bool kGuard = true>
+__device__ __forceinline__ uint2 encode16(const float* t, float r_b, uint32_t code, float s_mult,
+                                          const PhiloxKeys& keys, uint64_t stream_id, uint64_t idx_base) {
     float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(t[i], r_b);
+    encode_values<16, kGuard>(t, r_b, code, s_mult, v);
     if constexpr (!kSR) {
         return make_uint2(e2m1_rne_x8(v), e2m1_rne_x8(v + 8));
     } else {

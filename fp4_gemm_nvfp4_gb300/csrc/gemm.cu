@@ -40,6 +40,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -48,6 +49,10 @@
 namespace nvfp4 {
 
 static __device__ unsigned int g_gemm_status = 0;
+
+// Wait limit of the next GEMM launch that withholds one arrival (0: none
+// armed); set by arm_gemm_fault, consumed by launch_gemm.
+static std::atomic<uint64_t> g_armed_fault_ns{0};
 
 namespace {
 
@@ -110,6 +115,8 @@ struct Params {
     int64_t ldc;
     float beta;
     int c_vec;                   // every row of C starts on a 16-byte boundary
+    uint64_t timeout_ns;         // limit of every mbarrier wait
+    uint32_t withhold;           // test support: the leader's first scale-warp arrival is left out
 };
 
 // 32 consecutive values of C's row `row` from column n0 (zeros past M or N):
@@ -365,7 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     uint32_t mt, nt;
                     tile_coords(tile, p, mt, nt);
                     for (uint32_t ks = 0; ks < p.kstages; ++ks) {
-                        if (!mbar_wait(&empty[stage], phase ^ 1u, kTimeoutNs)) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns)) {
                             record_timeout(abort_flag);
                             break;
                         }
@@ -399,7 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // the low-rank term: 64 BF16 columns of U' and V per stage in
                     // the A and B slots (the same 16 KiB boxes), no scales
                     for (uint32_t ls = 0; ls < p.lora_stages && !*abort_flag; ++ls) {
-                        if (!mbar_wait(&empty[stage], phase ^ 1u, kTimeoutNs)) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns)) {
                             record_timeout(abort_flag);
                             break;
                         }
@@ -429,8 +436,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int s = 0; s < kStages; ++s) {
                     if (!((armed >> s) & 1u)) continue;
                     const uint32_t par = (armed_parity >> s) & 1u;
-                    if (warp == kProdAWarp && leader) (void)mbar_wait_cluster(&full[s], par, kTimeoutNs);
-                    if (warp == kProdSfWarp) (void)mbar_wait(&sf_full[s], par, kTimeoutNs);
+                    if (warp == kProdAWarp && leader) (void)mbar_wait_cluster(&full[s], par, p.timeout_ns);
+                    if (warp == kProdSfWarp) (void)mbar_wait(&sf_full[s], par, p.timeout_ns);
                 }
             }
         } else {
@@ -454,14 +461,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 uint32_t stage = 0, phase = 0, tiles_done = 0;
                 uint32_t alo = lo0, sfc = sfc0, fa = full0, ea = empty0;
                 for (uint32_t tile = first_tile; tile < num_tiles && !*abort_flag; tile += tile_stride) {
-                    if (!mbar_wait_cluster(acc_empty, (tiles_done & 1u) ^ 1u, kTimeoutNs)) {
+                    if (!mbar_wait_cluster(acc_empty, (tiles_done & 1u) ^ 1u, p.timeout_ns)) {
                         record_timeout(abort_flag);
                         break;
                     }
                     tc_fence_after();
                     bool ok = true;
                     for (uint32_t ks = 0; ks < kst; ++ks) {
-                        if (!mbar_wait_addr(fa, phase, kTimeoutNs)) {
+                        if (!mbar_wait_addr(fa, phase, p.timeout_ns)) {
                             record_timeout(abort_flag);
                             ok = false;
                             break;
@@ -494,7 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
                     for (uint32_t ls = 0; ok && ls < p.lora_stages; ++ls) {
-                        if (!mbar_wait_addr(fa, phase, kTimeoutNs)) {
+                        if (!mbar_wait_addr(fa, phase, p.timeout_ns)) {
                             record_timeout(abort_flag);
                             ok = false;
                             break;
@@ -522,7 +529,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 // all MMAs complete before either CTA frees its tensor memory
                 tc_commit_pair_multicast(drain, 0x1);
-                (void)mbar_wait(drain, 0, kTimeoutNs);
+                (void)mbar_wait(drain, 0, p.timeout_ns);
             }
         }
     } else if (warp < (uint32_t)kFirstEpiWarp) {
@@ -540,7 +547,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // one thread waits, the other scale warps sleep in a named
                 // barrier; all leave together
                 if (warp == (uint32_t)kFirstSfWarp && lane == 0) {
-                    bool landed = !*abort_flag && mbar_wait(&sf_full[stage], phase, kTimeoutNs);
+                    bool landed = !*abort_flag && mbar_wait(&sf_full[stage], phase, p.timeout_ns);
                     if (!landed && !*abort_flag) record_timeout(abort_flag);
                     sf_ok[count & 1u] = landed ? 1u : 0u;
                 }
@@ -576,7 +583,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(leader_full0 + stage * 8u);
+                // (test support: with p.withhold the leader's first scale warp
+                // never arrives for the first stage, so the MMA issuer's wait
+                // on that full barrier runs out)
+                if (lane == 0 && !(p.withhold && count == 0 && leader && warp == (uint32_t)kFirstSfWarp))
+                    mbar_arrive_cluster(leader_full0 + stage * 8u);
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1u;
@@ -585,7 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // low-rank stages carry no scales: only the arrival on full
             for (uint32_t ls = 0; ok && ls < p.lora_stages; ++ls, ++count) {
                 if (warp == (uint32_t)kFirstSfWarp && lane == 0) {
-                    bool landed = !*abort_flag && mbar_wait(&sf_full[stage], phase, kTimeoutNs);
+                    bool landed = !*abort_flag && mbar_wait(&sf_full[stage], phase, p.timeout_ns);
                     if (!landed && !*abort_flag) record_timeout(abort_flag);
                     sf_ok[count & 1u] = landed ? 1u : 0u;
                 }
@@ -630,7 +641,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // cycles per tile).
             uint32_t ready = 0;
             if (lane == 0) {
-                ready = (!*abort_flag && mbar_wait_cluster(acc_full, tiles_done & 1u, kTimeoutNs)) ? 1u : 0u;
+                ready = (!*abort_flag && mbar_wait_cluster(acc_full, tiles_done & 1u, p.timeout_ns)) ? 1u : 0u;
                 if (!ready && !*abort_flag) record_timeout(abort_flag);
             }
             ready = __shfl_sync(0xffffffffu, ready, 0);
@@ -995,6 +1006,15 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     p.ldd = ldd;
     p.out_fp32 = out_fp32 ? 1 : 0;
     p.alpha = 1.0f;
+    p.timeout_ns = kTimeoutNs;
+    {
+        // a fault armed by the test support entry point applies to this launch only
+        const uint64_t armed = g_armed_fault_ns.exchange(0);
+        if (armed) {
+            p.timeout_ns = armed;
+            p.withhold = 1;
+        }
+    }
     const int64_t esz = out_fp32 ? 4 : 2;
     if (axpby) {
         // the C term goes with the plain product only
@@ -1039,6 +1059,8 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
         gemm_nvf4_kernel<kEpiPlain><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, msa, msb, md, mu, mv, p);
     return cudaGetLastError();
 }
+
+void arm_gemm_fault(uint64_t timeout_ns) { g_armed_fault_ns.store(timeout_ns); }
 
 cudaError_t gemm_read_and_clear_status(unsigned int* status) {
     unsigned int v = 0, zero = 0;

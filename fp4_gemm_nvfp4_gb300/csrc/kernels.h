@@ -91,6 +91,10 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
 // Read and clear the GEMM kernels' device status word (synchronous).
 cudaError_t gemm_read_and_clear_status(unsigned int* status);
 
+// Test support: the next GEMM launch waits at most timeout_ns per barrier and
+// its leader CTA leaves out one scale-warp arrival, so one wait runs out.
+void arm_gemm_fault(uint64_t timeout_ns);
+
 cudaError_t launch_dequantize(const uint8_t* codes, int64_t ld_codes, const uint8_t* scales, const float* sg,
                               int64_t rows, int64_t cols, void* y, int64_t ldy, bool out_fp32,
                               cudaStream_t stream);

@@ -14,6 +14,8 @@
 // (Q_16x1 of "Full-Stack FP4" Eq. (2)); 16x16 tiles share one scale (Q_16x16).
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "device_common.cuh"
 #include "kernels.h"
 
@@ -81,6 +83,8 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
         fill_rb_table(rb_table, ts.s_enc, fold ? 0.25f : 1.0f);
         __syncthreads();
     }
+    // the values' factor S_enc (with the RHT's 1/4 when it is folded)
+    const float s_mult = fold ? __fmul_rn(ts.s_enc, 0.25f) : ts.s_enc;
     float local_max = 0.0f;
     const PhiloxKeys& keys = a.keys;   // SR round keys, formed by the host
     // block b = r * bpr + j; (r, j) advance by the grid stride without a division
@@ -88,39 +92,48 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
     const uint32_t stride_r = stride / a.bpr, stride_j = stride - stride_r * a.bpr;
     uint32_t b = blockIdx.x * kThreads + threadIdx.x;
     uint32_t r = b / a.bpr, j = b - r * a.bpr;
-    for (; b < a.total; b += stride) {
-        const uint16_t* src = a.x + (int64_t)r * a.ld_x + (int64_t)j * 16;
-        const uint4 u0 = ld_nc_v4(src), u1 = ld_nc_v4(src + 8);
-        float t[16] = {bf16lo(u0.x), bf16hi(u0.x), bf16lo(u0.y), bf16hi(u0.y), bf16lo(u0.z), bf16hi(u0.z),
-                       bf16lo(u0.w), bf16hi(u0.w), bf16lo(u1.x), bf16hi(u1.x), bf16lo(u1.y), bf16hi(u1.y),
-                       bf16lo(u1.z), bf16hi(u1.z), bf16lo(u1.w), bf16hi(u1.w)};
-        if constexpr (kRHT) {
-            rht16_unscaled_packed(t, a.mask);   // the 1/4 comes below
-            if (P == Pass::kEncode && !fold) scale16(t, 0.25f);
+    // the main loop, instantiated with and without the multiplier-overflow
+    // test (encode_values); the tested form only when S_enc makes it possible
+    auto main_loop = [&](auto guard) {
+        constexpr bool G = decltype(guard)::value;
+        for (; b < a.total; b += stride) {
+            const uint16_t* src = a.x + (int64_t)r * a.ld_x + (int64_t)j * 16;
+            const uint4 u0 = ld_nc_v4(src), u1 = ld_nc_v4(src + 8);
+            float t[16] = {bf16lo(u0.x), bf16hi(u0.x), bf16lo(u0.y), bf16hi(u0.y), bf16lo(u0.z), bf16hi(u0.z),
+                           bf16lo(u0.w), bf16hi(u0.w), bf16lo(u1.x), bf16hi(u1.x), bf16lo(u1.y), bf16hi(u1.y),
+                           bf16lo(u1.z), bf16hi(u1.z), bf16lo(u1.w), bf16hi(u1.w)};
+            if constexpr (kRHT) {
+                rht16_unscaled_packed(t, a.mask);   // the 1/4 comes below
+                if (P == Pass::kEncode && !fold) scale16(t, 0.25f);
+            }
+            float amax_b = 0.0f;
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(t[i]));
+            if constexpr (P == Pass::kAmax) {
+                local_max = fmaxf(local_max, amax_b);
+            } else {
+                if (fold) amax_b = __fmul_rn(amax_b, 0.25f);
+                float r_b;
+                const uint32_t sc =
+                    kS46 ? block_scale_46<G>(t, amax_b, ts.s_enc, s_mult, rb_table, &r_b)
+                          : block_scale_tab(amax_b, ts.s_enc, rb_table, &r_b);
+                const uint64_t idx = (uint64_t)r * ((uint64_t)a.bpr * 16u) + (uint64_t)j * 16u;
+                const uint2 q = encode16<kSR, G>(t, r_b, sc, s_mult, keys, a.stream, idx);
+                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)r * a.out.ld_codes + (int64_t)j * 8) = q;
+                a.out.scales[scale_offset(r, j, a.out.s4)] = (uint8_t)sc;
+            }
+            j += stride_j;
+            r += stride_r;
+            if (j >= a.bpr) {
+                j -= a.bpr;
+                ++r;
+            }
         }
-        float amax_b = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(t[i]));
-        if constexpr (P == Pass::kAmax) {
-            local_max = fmaxf(local_max, amax_b);
-        } else {
-            if (fold) amax_b = __fmul_rn(amax_b, 0.25f);
-            float r_b;
-            const uint32_t sc =
-                kS46 ? block_scale_46(t, amax_b, ts.s_enc, fold ? __fmul_rn(ts.s_enc, 0.25f) : ts.s_enc, rb_table, &r_b)
-                      : block_scale_tab(amax_b, ts.s_enc, rb_table, &r_b);
-            const uint64_t idx = (uint64_t)r * ((uint64_t)a.bpr * 16u) + (uint64_t)j * 16u;
-            const uint2 q = encode16<kSR>(t, r_b, keys, a.stream, idx);
-            *reinterpret_cast<uint2*>(a.out.codes + (int64_t)r * a.out.ld_codes + (int64_t)j * 8) = q;
-            a.out.scales[scale_offset(r, j, a.out.s4)] = (uint8_t)sc;
-        }
-        j += stride_j;
-        r += stride_r;
-        if (j >= a.bpr) {
-            j -= a.bpr;
-            ++r;
-        }
-    }
+    };
+    if (P == Pass::kEncode && multiplier_may_overflow(ts.s_enc))
+        main_loop(std::true_type{});
+    else
+        main_loop(std::false_type{});
     if constexpr (P == Pass::kAmax) {
         if constexpr (kRHT) local_max = __fmul_rn(local_max, 0.25f);
         block_max_store(local_max, a.partials_out, red);
@@ -162,57 +175,67 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
         fill_rb_table(rb_table, ts.s_enc, fold ? 0.25f : 1.0f);
         __syncthreads();
     }
+    const float s_mult = fold ? __fmul_rn(ts.s_enc, 0.25f) : ts.s_enc;
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
     float local_max = 0.0f, plain_max = 0.0f;
     const PhiloxKeys& keys = a.keys;   // SR round keys, formed by the host
-    for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const uint32_t tr = tile % a.tiles_r, tc = tile / a.tiles_r;
-        const uint32_t r0 = tr * 128u + warp * 16u, c = tc * 64u + lane * 2u;
-        if (r0 >= a.rows || c >= a.cols) continue;
-        const uint16_t* src = a.x + (int64_t)r0 * a.ld_x + c;
-        float t0[16], t1[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t w = ld_nc_u32(src + (int64_t)i * a.ld_x);
-            t0[i] = bf16lo(w);
-            t1[i] = bf16hi(w);
-        }
-        if constexpr (kDual) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) plain_max = fmaxf(plain_max, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
-        }
-        if constexpr (kRHT) {
-            rht16_unscaled_x2(t0, t1, a.mask);   // the 1/4 comes below
-            if (P == Pass::kEncode && !fold) {
-                scale16(t0, 0.25f);
-                scale16(t1, 0.25f);
+    // the main loop, instantiated with and without the multiplier-overflow
+    // test (encode_values); the tested form only when S_enc makes it possible
+    auto main_loop = [&](auto guard) {
+        constexpr bool G = decltype(guard)::value;
+        for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            const uint32_t tr = tile % a.tiles_r, tc = tile / a.tiles_r;
+            const uint32_t r0 = tr * 128u + warp * 16u, c = tc * 64u + lane * 2u;
+            if (r0 >= a.rows || c >= a.cols) continue;
+            const uint16_t* src = a.x + (int64_t)r0 * a.ld_x + c;
+            float t0[16], t1[16];
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t w = ld_nc_u32(src + (int64_t)i * a.ld_x);
+                t0[i] = bf16lo(w);
+                t1[i] = bf16hi(w);
+            }
+            if constexpr (kDual) {
+    #pragma unroll
+                for (int i = 0; i < 16; ++i) plain_max = fmaxf(plain_max, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
+            }
+            if constexpr (kRHT) {
+                rht16_unscaled_x2(t0, t1, a.mask);   // the 1/4 comes below
+                if (P == Pass::kEncode && !fold) {
+                    scale16(t0, 0.25f);
+                    scale16(t1, 0.25f);
+                }
+            }
+            float m0 = 0.0f, m1 = 0.0f;
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                m0 = fmaxf(m0, fabsf(t0[i]));
+                m1 = fmaxf(m1, fabsf(t1[i]));
+            }
+            if constexpr (P == Pass::kAmax) {
+                local_max = fmaxf(local_max, fmaxf(m0, m1));
+            } else {
+                if (fold) {
+                    m0 = __fmul_rn(m0, 0.25f);
+                    m1 = __fmul_rn(m1, 0.25f);
+                }
+                float rb0, rb1;
+                const uint32_t sc0 = block_scale_tab(m0, ts.s_enc, rb_table, &rb0);
+                const uint32_t sc1 = block_scale_tab(m1, ts.s_enc, rb_table, &rb1);
+                const uint2 q0 = encode16<kSR, G>(t0, rb0, sc0, s_mult, keys, a.stream, (uint64_t)c * a.rows + r0);
+                const uint2 q1 = encode16<kSR, G>(t1, rb1, sc1, s_mult, keys, a.stream, (uint64_t)(c + 1) * a.rows + r0);
+                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
+                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)(c + 1) * a.out.ld_codes + r0 / 2) = q1;
+                a.out.scales[scale_offset(c, r0 / 16, a.out.s4)] = (uint8_t)sc0;
+                a.out.scales[scale_offset(c + 1, r0 / 16, a.out.s4)] = (uint8_t)sc1;
             }
         }
-        float m0 = 0.0f, m1 = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            m0 = fmaxf(m0, fabsf(t0[i]));
-            m1 = fmaxf(m1, fabsf(t1[i]));
-        }
-        if constexpr (P == Pass::kAmax) {
-            local_max = fmaxf(local_max, fmaxf(m0, m1));
-        } else {
-            if (fold) {
-                m0 = __fmul_rn(m0, 0.25f);
-                m1 = __fmul_rn(m1, 0.25f);
-            }
-            float rb0, rb1;
-            const uint32_t sc0 = block_scale_tab(m0, ts.s_enc, rb_table, &rb0);
-            const uint32_t sc1 = block_scale_tab(m1, ts.s_enc, rb_table, &rb1);
-            const uint2 q0 = encode16<kSR>(t0, rb0, keys, a.stream, (uint64_t)c * a.rows + r0);
-            const uint2 q1 = encode16<kSR>(t1, rb1, keys, a.stream, (uint64_t)(c + 1) * a.rows + r0);
-            *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
-            *reinterpret_cast<uint2*>(a.out.codes + (int64_t)(c + 1) * a.out.ld_codes + r0 / 2) = q1;
-            a.out.scales[scale_offset(c, r0 / 16, a.out.s4)] = (uint8_t)sc0;
-            a.out.scales[scale_offset(c + 1, r0 / 16, a.out.s4)] = (uint8_t)sc1;
-        }
-    }
+    };
+    if (P == Pass::kEncode && multiplier_may_overflow(ts.s_enc))
+        main_loop(std::true_type{});
+    else
+        main_loop(std::false_type{});
     if constexpr (P == Pass::kAmax) {
         if constexpr (kRHT) local_max = __fmul_rn(local_max, 0.25f);
         block_max_store(local_max, a.partials_out, red);
@@ -266,49 +289,59 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const RequantArgs a) 
         fill_rb_table(rb_table, ts.s_enc);
     }
     __syncthreads();
+    const float s_mult = ts.s_enc;     // the values carry their 1/4 already
     const float sg = *a.in_sg;
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
     float local_max = 0.0f;
     const PhiloxKeys& keys = a.keys;
-    for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const uint32_t tr = tile % a.tiles_r, tc = tile / a.tiles_r;
-        const uint32_t r0 = tr * 128u + warp * 16u, c = tc * 64u + lane * 2u;
-        if (r0 >= a.rows || c >= a.cols) continue;
-        // rows r0 .. r0+15 of one 32-row quadrant: their scales are 16 bytes apart
-        const uint8_t* srow = a.in_scales + scale_offset(r0, c / 16, a.in_s4);
-        const uint8_t* crow = a.in_codes + (int64_t)r0 * a.in_ld + c / 2;
-        float t0[16], t1[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float2 g = g_tab[__ldg(crow + (int64_t)i * a.in_ld)];
-            const float sb = sb_tab[__ldg(srow + 16 * i) & 0x7Fu];
-            t0[i] = __fmul_rn(__fmul_rn(g.x, sb), sg);
-            t1[i] = __fmul_rn(__fmul_rn(g.y, sb), sg);
+    // the main loop, instantiated with and without the multiplier-overflow
+    // test (encode_values); the tested form only when S_enc makes it possible
+    auto main_loop = [&](auto guard) {
+        constexpr bool G = decltype(guard)::value;
+        for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            const uint32_t tr = tile % a.tiles_r, tc = tile / a.tiles_r;
+            const uint32_t r0 = tr * 128u + warp * 16u, c = tc * 64u + lane * 2u;
+            if (r0 >= a.rows || c >= a.cols) continue;
+            // rows r0 .. r0+15 of one 32-row quadrant: their scales are 16 bytes apart
+            const uint8_t* srow = a.in_scales + scale_offset(r0, c / 16, a.in_s4);
+            const uint8_t* crow = a.in_codes + (int64_t)r0 * a.in_ld + c / 2;
+            float t0[16], t1[16];
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float2 g = g_tab[__ldg(crow + (int64_t)i * a.in_ld)];
+                const float sb = sb_tab[__ldg(srow + 16 * i) & 0x7Fu];
+                t0[i] = __fmul_rn(__fmul_rn(g.x, sb), sg);
+                t1[i] = __fmul_rn(__fmul_rn(g.y, sb), sg);
+            }
+            rht16_unscaled_x2(t0, t1, a.mask);
+            scale16(t0, 0.25f);
+            scale16(t1, 0.25f);
+            float m0 = 0.0f, m1 = 0.0f;
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                m0 = fmaxf(m0, fabsf(t0[i]));
+                m1 = fmaxf(m1, fabsf(t1[i]));
+            }
+            if constexpr (P == Pass::kAmax) {
+                local_max = fmaxf(local_max, fmaxf(m0, m1));
+            } else {
+                float rb0, rb1;
+                const uint32_t sc0 = block_scale_tab(m0, ts.s_enc, rb_table, &rb0);
+                const uint32_t sc1 = block_scale_tab(m1, ts.s_enc, rb_table, &rb1);
+                const uint2 q0 = encode16<kSR, G>(t0, rb0, sc0, s_mult, keys, a.stream, (uint64_t)c * a.rows + r0);
+                const uint2 q1 = encode16<kSR, G>(t1, rb1, sc1, s_mult, keys, a.stream, (uint64_t)(c + 1) * a.rows + r0);
+                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
+                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)(c + 1) * a.out.ld_codes + r0 / 2) = q1;
+                a.out.scales[scale_offset(c, r0 / 16, a.out.s4)] = (uint8_t)sc0;
+                a.out.scales[scale_offset(c + 1, r0 / 16, a.out.s4)] = (uint8_t)sc1;
+            }
         }
-        rht16_unscaled_x2(t0, t1, a.mask);
-        scale16(t0, 0.25f);
-        scale16(t1, 0.25f);
-        float m0 = 0.0f, m1 = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            m0 = fmaxf(m0, fabsf(t0[i]));
-            m1 = fmaxf(m1, fabsf(t1[i]));
-        }
-        if constexpr (P == Pass::kAmax) {
-            local_max = fmaxf(local_max, fmaxf(m0, m1));
-        } else {
-            float rb0, rb1;
-            const uint32_t sc0 = block_scale_tab(m0, ts.s_enc, rb_table, &rb0);
-            const uint32_t sc1 = block_scale_tab(m1, ts.s_enc, rb_table, &rb1);
-            const uint2 q0 = encode16<kSR>(t0, rb0, keys, a.stream, (uint64_t)c * a.rows + r0);
-            const uint2 q1 = encode16<kSR>(t1, rb1, keys, a.stream, (uint64_t)(c + 1) * a.rows + r0);
-            *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
-            *reinterpret_cast<uint2*>(a.out.codes + (int64_t)(c + 1) * a.out.ld_codes + r0 / 2) = q1;
-            a.out.scales[scale_offset(c, r0 / 16, a.out.s4)] = (uint8_t)sc0;
-            a.out.scales[scale_offset(c + 1, r0 / 16, a.out.s4)] = (uint8_t)sc1;
-        }
-    }
+    };
+    if (P == Pass::kEncode && multiplier_may_overflow(ts.s_enc))
+        main_loop(std::true_type{});
+    else
+        main_loop(std::false_type{});
     if constexpr (P == Pass::kAmax) block_max_store(local_max, a.partials_out, red);
 }
 
@@ -333,69 +366,74 @@ __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
     const PhiloxKeys& keys = a.keys;   // SR round keys, formed by the host
-    for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const uint32_t tr = tile % a.tiles_r, tc = tile / a.tiles_r;
-        const uint32_t r0 = tr * 128u + warp * 16u, c = tc * 64u + lane * 2u;
-        // rows % 16 == 0 and cols % 16 == 0: the 8 lanes of a tile agree on this
-        const bool valid = (r0 < a.rows) && (c < a.cols);
-        float t0[16], t1[16];
-        float m = 0.0f;
-        if (valid) {
-            const uint16_t* src = a.x + (int64_t)r0 * a.ld_x + c;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t w = ld_nc_u32(src + (int64_t)i * a.ld_x);
-                t0[i] = bf16lo(w);
-                t1[i] = bf16hi(w);
-                m = fmaxf(m, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
+    // the main loop, instantiated with and without the multiplier-overflow
+    // test (encode_values); the tested form only when S_enc makes it possible
+    auto main_loop = [&](auto guard) {
+        constexpr bool G = decltype(guard)::value;
+        for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            const uint32_t tr = tile % a.tiles_r, tc = tile / a.tiles_r;
+            const uint32_t r0 = tr * 128u + warp * 16u, c = tc * 64u + lane * 2u;
+            // rows % 16 == 0 and cols % 16 == 0: the 8 lanes of a tile agree on this
+            const bool valid = (r0 < a.rows) && (c < a.cols);
+            float t0[16], t1[16];
+            float m = 0.0f;
+            if (valid) {
+                const uint16_t* src = a.x + (int64_t)r0 * a.ld_x + c;
+    #pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const uint32_t w = ld_nc_u32(src + (int64_t)i * a.ld_x);
+                    t0[i] = bf16lo(w);
+                    t1[i] = bf16hi(w);
+                    m = fmaxf(m, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
+                }
+            }
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+            if (!valid) continue;
+            float r_b;
+            const uint32_t sc = block_scale_tab(m, ts.s_enc, rb_table, &r_b);
+            uint2 q0, q1;
+            encode_values<16, G>(t0, r_b, sc, ts.s_enc, t0);
+            encode_values<16, G>(t1, r_b, sc, ts.s_enc, t1);
+            if constexpr (!kSR) {
+                q0 = make_uint2(e2m1_rne_x8(t0), e2m1_rne_x8(t0 + 8));
+                q1 = make_uint2(e2m1_rne_x8(t1), e2m1_rne_x8(t1 + 8));
+            } else {
+                float g0[16], g1[16];
+    #pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    // SR index: the row-wise index of x, shared by both orientations
+                    const uint64_t idx = (uint64_t)(r0 + i) * a.cols + c;     // even: c and c+1 share a word
+                    const uint4 w = sr_words4(keys, a.stream, idx >> 3);
+                    const uint32_t sel = (uint32_t)(idx >> 1) & 3u;
+                    const uint32_t word = sel == 0 ? w.x : (sel == 1 ? w.y : (sel == 2 ? w.z : w.w));
+                    g0[i] = e2m1_sr_grid(t0[i], sr_addend_lo(word));
+                    g1[i] = e2m1_sr_grid(t1[i], sr_addend_hi(word));
+                }
+                q0 = make_uint2(e2m1_rne_x8(g0), e2m1_rne_x8(g0 + 8));
+                q1 = make_uint2(e2m1_rne_x8(g1), e2m1_rne_x8(g1 + 8));
+            }
+            if (a.emit_col) {
+                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
+                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)(c + 1) * a.out.ld_codes + r0 / 2) = q1;
+                a.out.scales[scale_offset(c, r0 / 16, a.out.s4)] = (uint8_t)sc;
+                a.out.scales[scale_offset(c + 1, r0 / 16, a.out.s4)] = (uint8_t)sc;
+            }
+            if (a.emit_row) {
+    #pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    a.out2.codes[(int64_t)(r0 + i) * a.out2.ld_codes + c / 2] =
+                        (uint8_t)(nibble(q0, i) | (nibble(q1, i) << 4));
+                    if ((lane & 7u) == 0) a.out2.scales[scale_offset(r0 + i, c / 16, a.out2.s4)] = (uint8_t)sc;
+                }
             }
         }
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-        if (!valid) continue;
-        float r_b;
-        const uint32_t sc = block_scale_tab(m, ts.s_enc, rb_table, &r_b);
-        uint2 q0, q1;
-        if constexpr (!kSR) {
-            float v0[16], v1[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                v0[i] = __fmul_rn(t0[i], r_b);
-                v1[i] = __fmul_rn(t1[i], r_b);
-            }
-            q0 = make_uint2(e2m1_rne_x8(v0), e2m1_rne_x8(v0 + 8));
-            q1 = make_uint2(e2m1_rne_x8(v1), e2m1_rne_x8(v1 + 8));
-        } else {
-            float g0[16], g1[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                // SR index: the row-wise index of x, shared by both orientations
-                const uint64_t idx = (uint64_t)(r0 + i) * a.cols + c;     // even: c and c+1 share a word
-                const uint4 w = sr_words4(keys, a.stream, idx >> 3);
-                const uint32_t sel = (uint32_t)(idx >> 1) & 3u;
-                const uint32_t word = sel == 0 ? w.x : (sel == 1 ? w.y : (sel == 2 ? w.z : w.w));
-                g0[i] = e2m1_sr_grid(__fmul_rn(t0[i], r_b), sr_addend_lo(word));
-                g1[i] = e2m1_sr_grid(__fmul_rn(t1[i], r_b), sr_addend_hi(word));
-            }
-            q0 = make_uint2(e2m1_rne_x8(g0), e2m1_rne_x8(g0 + 8));
-            q1 = make_uint2(e2m1_rne_x8(g1), e2m1_rne_x8(g1 + 8));
-        }
-        if (a.emit_col) {
-            *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
-            *reinterpret_cast<uint2*>(a.out.codes + (int64_t)(c + 1) * a.out.ld_codes + r0 / 2) = q1;
-            a.out.scales[scale_offset(c, r0 / 16, a.out.s4)] = (uint8_t)sc;
-            a.out.scales[scale_offset(c + 1, r0 / 16, a.out.s4)] = (uint8_t)sc;
-        }
-        if (a.emit_row) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                a.out2.codes[(int64_t)(r0 + i) * a.out2.ld_codes + c / 2] =
-                    (uint8_t)(nibble(q0, i) | (nibble(q1, i) << 4));
-                if ((lane & 7u) == 0) a.out2.scales[scale_offset(r0 + i, c / 16, a.out2.s4)] = (uint8_t)sc;
-            }
-        }
-    }
+    };
+    if (multiplier_may_overflow(ts.s_enc))
+        main_loop(std::true_type{});
+    else
+        main_loop(std::false_type{});
 }
 
 // ------------------------------------------- row + col-RHT pair encode -----
@@ -477,6 +515,9 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     // the col-wise RHT's 1/4 lives in its multipliers (rht_quarter_foldable)
     const bool fold = kColRHT && rht_quarter_foldable(ts_col.s_enc);
     const bool fold_row = kRowRHT && rht_quarter_foldable(ts_row.s_enc);
+    // the values' factor S_enc per orientation (with the RHT's 1/4 when folded)
+    const float s_mult_col = fold ? __fmul_rn(ts_col.s_enc, 0.25f) : ts_col.s_enc;
+    const float s_mult_row = fold_row ? __fmul_rn(ts_row.s_enc, 0.25f) : ts_row.s_enc;
     fill_rb_table_at(rb_row, ts_row.s_enc, 0, fold_row ? 0.25f : 1.0f);
     fill_rb_table_at(rb_col, ts_col.s_enc, 128, fold ? 0.25f : 1.0f);
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
@@ -511,136 +552,142 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     uint2 cq0[4], cq1[4];
     uint32_t cs0 = 0, cs1 = 0;
     issue(0);
-    for (uint32_t j = 0; j < 4u * kcount; ++j) {
-        __syncwarp();   // every lane is done with the slot the next copy fills
-        issue(j + 1);
-        uint32_t r0, c0;
-        uint2 q0 = make_uint2(0u, 0u), q1 = make_uint2(0u, 0u);
-        uint32_t sc0 = 0, sc1 = 0;
-        if (slice_of(j, r0, c0)) {
-        const uint32_t sl = j & 1u;
-        if (!mbar_wait(&full[warp][sl], (parity >> sl) & 1u, 2000000000ull)) {
-            // a copy that never landed: let the next one (issued above) land
-            // before this CTA can exit, then stop
-            uint32_t r1, c1;
-            if (slice_of(j + 1, r1, c1))
-                (void)mbar_wait(&full[warp][sl ^ 1u], (parity >> (sl ^ 1u)) & 1u, 2000000000ull);
-            break;
-        }
-        parity ^= 1u << sl;
-        const uint8_t* src = ring[warp][sl];
+    // the main loop, instantiated with and without the multiplier-overflow
+    // test (encode_values); the tested form only when S_enc makes it possible
+    auto main_loop = [&](auto guard) {
+        constexpr bool G = decltype(guard)::value;
+        for (uint32_t j = 0; j < 4u * kcount; ++j) {
+            __syncwarp();   // every lane is done with the slot the next copy fills
+            issue(j + 1);
+            uint32_t r0, c0;
+            uint2 q0 = make_uint2(0u, 0u), q1 = make_uint2(0u, 0u);
+            uint32_t sc0 = 0, sc1 = 0;
+            if (slice_of(j, r0, c0)) {
+            const uint32_t sl = j & 1u;
+            if (!mbar_wait(&full[warp][sl], (parity >> sl) & 1u, 2000000000ull)) {
+                // a copy that never landed: let the next one (issued above) land
+                // before this CTA can exit, then stop
+                uint32_t r1, c1;
+                if (slice_of(j + 1, r1, c1))
+                    (void)mbar_wait(&full[warp][sl ^ 1u], (parity >> (sl ^ 1u)) & 1u, 2000000000ull);
+                break;
+            }
+            parity ^= 1u << sl;
+            const uint8_t* src = ring[warp][sl];
 
-        // ---- col-wise with RHT: lane = columns c0 + 2 lane, c0 + 2 lane + 1
-        {
-            const uint32_t c = c0 + lane * 2u;
-            float t0[16], t1[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t off = (uint32_t)i * 128u + (((lane >> 2) ^ (uint32_t)(i & 7)) << 4) + (lane & 3u) * 4u;
-                const uint32_t w = *reinterpret_cast<const uint32_t*>(src + off);
-                t0[i] = bf16lo(w);
-                t1[i] = bf16hi(w);
-            }
-            if (a.emit_col && c < a.cols) {
-                if constexpr (kColRHT) {
-                    rht16_unscaled_x2(t0, t1, a.mask);   // the 1/4 comes below
-                    if (!fold) {
-                        scale16(t0, 0.25f);
-                        scale16(t1, 0.25f);
-                    }
-                }
-                float m0 = 0.0f, m1 = 0.0f;
-#pragma unroll
+            // ---- col-wise with RHT: lane = columns c0 + 2 lane, c0 + 2 lane + 1
+            {
+                const uint32_t c = c0 + lane * 2u;
+                float t0[16], t1[16];
+    #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    m0 = fmaxf(m0, fabsf(t0[i]));
-                    m1 = fmaxf(m1, fabsf(t1[i]));
+                    const uint32_t off = (uint32_t)i * 128u + (((lane >> 2) ^ (uint32_t)(i & 7)) << 4) + (lane & 3u) * 4u;
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(src + off);
+                    t0[i] = bf16lo(w);
+                    t1[i] = bf16hi(w);
                 }
-                if (fold) {
-                    m0 = __fmul_rn(m0, 0.25f);
-                    m1 = __fmul_rn(m1, 0.25f);
+                if (a.emit_col && c < a.cols) {
+                    if constexpr (kColRHT) {
+                        rht16_unscaled_x2(t0, t1, a.mask);   // the 1/4 comes below
+                        if (!fold) {
+                            scale16(t0, 0.25f);
+                            scale16(t1, 0.25f);
+                        }
+                    }
+                    float m0 = 0.0f, m1 = 0.0f;
+    #pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        m0 = fmaxf(m0, fabsf(t0[i]));
+                        m1 = fmaxf(m1, fabsf(t1[i]));
+                    }
+                    if (fold) {
+                        m0 = __fmul_rn(m0, 0.25f);
+                        m1 = __fmul_rn(m1, 0.25f);
+                    }
+                    float rb0, rb1;
+                    if constexpr (kS46) {
+                        sc0 = block_scale_46<G>(t0, m0, ts_col.s_enc, s_mult_col, rb_col, &rb0);
+                        sc1 = block_scale_46<G>(t1, m1, ts_col.s_enc, s_mult_col, rb_col, &rb1);
+                    } else {
+                        sc0 = block_scale_tab(m0, ts_col.s_enc, rb_col, &rb0);
+                        sc1 = block_scale_tab(m1, ts_col.s_enc, rb_col, &rb1);
+                    }
+                    q0 = encode16<kSR, G>(t0, rb0, sc0, s_mult_col, keys, a.stream_col, (uint64_t)c * a.rows + r0);
+                    q1 = encode16<kSR, G>(t1, rb1, sc1, s_mult_col, keys, a.stream_col, (uint64_t)(c + 1) * a.rows + r0);
                 }
-                float rb0, rb1;
-                if constexpr (kS46) {
-                    const float xs_mult = fold ? __fmul_rn(ts_col.s_enc, 0.25f) : ts_col.s_enc;
-                    sc0 = block_scale_46(t0, m0, ts_col.s_enc, xs_mult, rb_col, &rb0);
-                    sc1 = block_scale_46(t1, m1, ts_col.s_enc, xs_mult, rb_col, &rb1);
-                } else {
-                    sc0 = block_scale_tab(m0, ts_col.s_enc, rb_col, &rb0);
-                    sc1 = block_scale_tab(m1, ts_col.s_enc, rb_col, &rb1);
-                }
-                q0 = encode16<kSR>(t0, rb0, keys, a.stream_col, (uint64_t)c * a.rows + r0);
-                q1 = encode16<kSR>(t1, rb1, keys, a.stream_col, (uint64_t)(c + 1) * a.rows + r0);
             }
-        }
-        // ---- row-wise without RHT: lane = row r0 + lane / 2, 32 columns
-        {
-            const uint32_t i = lane >> 1, h = lane & 1u;
-            const uint32_t r = r0 + i, cb = c0 + 32u * h;
-            if (a.emit_row && cb < a.cols) {
-                float v[32];
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t off = i * 128u + (((4u * h + (uint32_t)kk) ^ (i & 7u)) << 4);
-                    const uint4 u = *reinterpret_cast<const uint4*>(src + off);
-                    v[8 * kk + 0] = bf16lo(u.x);
-                    v[8 * kk + 1] = bf16hi(u.x);
-                    v[8 * kk + 2] = bf16lo(u.y);
-                    v[8 * kk + 3] = bf16hi(u.y);
-                    v[8 * kk + 4] = bf16lo(u.z);
-                    v[8 * kk + 5] = bf16hi(u.z);
-                    v[8 * kk + 6] = bf16lo(u.w);
-                    v[8 * kk + 7] = bf16hi(u.w);
-                }
-                if constexpr (kRowRHT) {
-                    rht16_unscaled_x2(v, v + 16, a.mask);   // the 1/4 comes below
-                    if (!fold_row) {
-                        scale16(v, 0.25f);
-                        scale16(v + 16, 0.25f);
+            // ---- row-wise without RHT: lane = row r0 + lane / 2, 32 columns
+            {
+                const uint32_t i = lane >> 1, h = lane & 1u;
+                const uint32_t r = r0 + i, cb = c0 + 32u * h;
+                if (a.emit_row && cb < a.cols) {
+                    float v[32];
+    #pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t off = i * 128u + (((4u * h + (uint32_t)kk) ^ (i & 7u)) << 4);
+                        const uint4 u = *reinterpret_cast<const uint4*>(src + off);
+                        v[8 * kk + 0] = bf16lo(u.x);
+                        v[8 * kk + 1] = bf16hi(u.x);
+                        v[8 * kk + 2] = bf16lo(u.y);
+                        v[8 * kk + 3] = bf16hi(u.y);
+                        v[8 * kk + 4] = bf16lo(u.z);
+                        v[8 * kk + 5] = bf16hi(u.z);
+                        v[8 * kk + 6] = bf16lo(u.w);
+                        v[8 * kk + 7] = bf16hi(u.w);
+                    }
+                    if constexpr (kRowRHT) {
+                        rht16_unscaled_x2(v, v + 16, a.mask);   // the 1/4 comes below
+                        if (!fold_row) {
+                            scale16(v, 0.25f);
+                            scale16(v + 16, 0.25f);
+                        }
+                    }
+                    const bool two = cb + 16u < a.cols;
+                    uint2 q[2];
+                    uint32_t sc[2];
+    #pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        float m = 0.0f;
+    #pragma unroll
+                        for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[16 * jj + e]));
+                        if (fold_row) m = __fmul_rn(m, 0.25f);
+                        float rb;
+                        sc[jj] = kS46 ? block_scale_46<G>(v + 16 * jj, m, ts_row.s_enc, s_mult_row, rb_row, &rb)
+                                       : block_scale_tab(m, ts_row.s_enc, rb_row, &rb);
+                        q[jj] = encode16<kSR, G>(v + 16 * jj, rb, sc[jj], s_mult_row, keys, a.stream_row,
+                                              (uint64_t)r * a.cols + cb + 16u * (uint32_t)jj);
+                    }
+                    uint8_t* dst = a.row.codes + (int64_t)r * a.row.ld_codes + cb / 2;
+                    const uint32_t j0 = cb / 16u;
+                    if (two) {
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
+                        *reinterpret_cast<uint16_t*>(a.row.scales + scale_offset(r, j0, a.row.s4)) =
+                            (uint16_t)(sc[0] | (sc[1] << 8));
+                    } else {
+                        *reinterpret_cast<uint2*>(dst) = q[0];
+                        a.row.scales[scale_offset(r, j0, a.row.s4)] = (uint8_t)sc[0];
                     }
                 }
-                const bool two = cb + 16u < a.cols;
-                uint2 q[2];
-                uint32_t sc[2];
-#pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    float m = 0.0f;
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[16 * jj + e]));
-                    if (fold_row) m = __fmul_rn(m, 0.25f);
-                    float rb;
-                    sc[jj] = kS46 ? block_scale_46(v + 16 * jj, m, ts_row.s_enc,
-                                                   fold_row ? __fmul_rn(ts_row.s_enc, 0.25f) : ts_row.s_enc, rb_row,
-                                                   &rb)
-                                   : block_scale_tab(m, ts_row.s_enc, rb_row, &rb);
-                    q[jj] = encode16<kSR>(v + 16 * jj, rb, keys, a.stream_row,
-                                          (uint64_t)r * a.cols + cb + 16u * (uint32_t)jj);
-                }
-                uint8_t* dst = a.row.codes + (int64_t)r * a.row.ld_codes + cb / 2;
-                const uint32_t j0 = cb / 16u;
-                if (two) {
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
-                    *reinterpret_cast<uint16_t*>(a.row.scales + scale_offset(r, j0, a.row.s4)) =
-                        (uint16_t)(sc[0] | (sc[1] << 8));
-                } else {
-                    *reinterpret_cast<uint2*>(dst) = q[0];
-                    a.row.scales[scale_offset(r, j0, a.row.s4)] = (uint8_t)sc[0];
-                }
+            }
+            }
+            // slice j % 4 joins the warp's col-wise codes; after the fourth, they
+            // go out as whole sectors
+            cq0[0] = cq0[1], cq0[1] = cq0[2], cq0[2] = cq0[3], cq0[3] = q0;
+            cq1[0] = cq1[1], cq1[1] = cq1[2], cq1[2] = cq1[3], cq1[3] = q1;
+            cs0 = (cs0 >> 8) | (sc0 << 24);
+            cs1 = (cs1 >> 8) | (sc1 << 24);
+            if ((j & 3u) == 3u && a.emit_col) {
+                const uint32_t tile = blockIdx.x + (j >> 2) * gridDim.x;
+                const uint32_t rb = (tile % a.tiles_r) * kTileRows + warp * kWarpRows;
+                const uint32_t c = (tile / a.tiles_r) * 64u + lane * 2u;
+                if (tile < ntiles && rb < a.rows && c < a.cols) store_col64(a.col, c, rb, a.rows, cq0, cq1, cs0, cs1);
             }
         }
-        }
-        // slice j % 4 joins the warp's col-wise codes; after the fourth, they
-        // go out as whole sectors
-        cq0[0] = cq0[1], cq0[1] = cq0[2], cq0[2] = cq0[3], cq0[3] = q0;
-        cq1[0] = cq1[1], cq1[1] = cq1[2], cq1[2] = cq1[3], cq1[3] = q1;
-        cs0 = (cs0 >> 8) | (sc0 << 24);
-        cs1 = (cs1 >> 8) | (sc1 << 24);
-        if ((j & 3u) == 3u && a.emit_col) {
-            const uint32_t tile = blockIdx.x + (j >> 2) * gridDim.x;
-            const uint32_t rb = (tile % a.tiles_r) * kTileRows + warp * kWarpRows;
-            const uint32_t c = (tile / a.tiles_r) * 64u + lane * 2u;
-            if (tile < ntiles && rb < a.rows && c < a.cols) store_col64(a.col, c, rb, a.rows, cq0, cq1, cs0, cs1);
-        }
-    }
+    };
+    if (multiplier_may_overflow(ts_row.s_enc) || multiplier_may_overflow(ts_col.s_enc))
+        main_loop(std::true_type{});
+    else
+        main_loop(std::false_type{});
 }
 
 // ------------------------------------------------ 16x16, RNE, via TMA -----
@@ -697,101 +744,101 @@ __global__ void __launch_bounds__(kThreads) tile2d_rne_kernel(const __grid_const
     uint2 cq0[4], cq1[4];
     uint32_t cs = 0;
     issue(0);
-    for (uint32_t j = 0; j < 4u * kcount; ++j) {
-        __syncwarp();
-        issue(j + 1);
-        uint32_t r0, c0;
-        uint2 q0 = make_uint2(0u, 0u), q1 = make_uint2(0u, 0u);
-        uint32_t sc = 0;
-        if (slice_of(j, r0, c0)) {
-        const uint32_t sl = j & 1u;
-        if (!mbar_wait(&full[warp][sl], (parity >> sl) & 1u, 2000000000ull)) {
-            uint32_t r1, c1;
-            if (slice_of(j + 1, r1, c1))
-                (void)mbar_wait(&full[warp][sl ^ 1u], (parity >> (sl ^ 1u)) & 1u, 2000000000ull);
-            break;
-        }
-        parity ^= 1u << sl;
-        const uint8_t* src = ring[warp][sl];
-        // col layout: tile amax and scale; col-wise codes
-        const uint32_t c = c0 + lane * 2u;
-        float t0[16], t1[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(
-                src + (uint32_t)i * 128u + (((lane >> 2) ^ (uint32_t)(i & 7)) << 4) + (lane & 3u) * 4u);
-            t0[i] = bf16lo(w);
-            t1[i] = bf16hi(w);
-        }
-        float m = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-        float rb;
-        sc = block_scale_tab(m, ts.s_enc, rb_tab, &rb);
-        if (a.emit_col && c < a.cols) {
-            float v0[16], v1[16];
-#pragma unroll
+    // the main loop, instantiated with and without the multiplier-overflow
+    // test (encode_values); the tested form only when S_enc makes it possible
+    auto main_loop = [&](auto guard) {
+        constexpr bool G = decltype(guard)::value;
+        for (uint32_t j = 0; j < 4u * kcount; ++j) {
+            __syncwarp();
+            issue(j + 1);
+            uint32_t r0, c0;
+            uint2 q0 = make_uint2(0u, 0u), q1 = make_uint2(0u, 0u);
+            uint32_t sc = 0;
+            if (slice_of(j, r0, c0)) {
+            const uint32_t sl = j & 1u;
+            if (!mbar_wait(&full[warp][sl], (parity >> sl) & 1u, 2000000000ull)) {
+                uint32_t r1, c1;
+                if (slice_of(j + 1, r1, c1))
+                    (void)mbar_wait(&full[warp][sl ^ 1u], (parity >> (sl ^ 1u)) & 1u, 2000000000ull);
+                break;
+            }
+            parity ^= 1u << sl;
+            const uint8_t* src = ring[warp][sl];
+            // col layout: tile amax and scale; col-wise codes
+            const uint32_t c = c0 + lane * 2u;
+            float t0[16], t1[16];
+    #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                v0[i] = __fmul_rn(t0[i], rb);
-                v1[i] = __fmul_rn(t1[i], rb);
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(
+                    src + (uint32_t)i * 128u + (((lane >> 2) ^ (uint32_t)(i & 7)) << 4) + (lane & 3u) * 4u);
+                t0[i] = bf16lo(w);
+                t1[i] = bf16hi(w);
             }
-            q0 = make_uint2(e2m1_rne_x8(v0), e2m1_rne_x8(v0 + 8));
-            q1 = make_uint2(e2m1_rne_x8(v1), e2m1_rne_x8(v1 + 8));
-        }
-        if (a.emit_row) {
-            // row layout: row r0 + lane / 2, columns c0 + 32 (lane & 1) .. + 31
-            // = tiles 2h and 2h+1 of the slice, whose scales lanes 16h and
-            // 16h + 8 hold
-            const uint32_t i = lane >> 1, h = lane & 1u;
-            const uint32_t r = r0 + i, cb = c0 + 32u * h;
-            const float rbt0 = __shfl_sync(0xFFFFFFFFu, rb, 16 * h), rbt1 = __shfl_sync(0xFFFFFFFFu, rb, 16 * h + 8);
-            const uint32_t sct0 = __shfl_sync(0xFFFFFFFFu, sc, 16 * h),
-                           sct1 = __shfl_sync(0xFFFFFFFFu, sc, 16 * h + 8);
-            if (cb < a.cols) {
-                float v[32];
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t off = i * 128u + (((4u * h + (uint32_t)kk) ^ (i & 7u)) << 4);
-                    const uint4 u = *reinterpret_cast<const uint4*>(src + off);
-                    const float rbk = kk < 2 ? rbt0 : rbt1;
-                    v[8 * kk + 0] = __fmul_rn(bf16lo(u.x), rbk);
-                    v[8 * kk + 1] = __fmul_rn(bf16hi(u.x), rbk);
-                    v[8 * kk + 2] = __fmul_rn(bf16lo(u.y), rbk);
-                    v[8 * kk + 3] = __fmul_rn(bf16hi(u.y), rbk);
-                    v[8 * kk + 4] = __fmul_rn(bf16lo(u.z), rbk);
-                    v[8 * kk + 5] = __fmul_rn(bf16hi(u.z), rbk);
-                    v[8 * kk + 6] = __fmul_rn(bf16lo(u.w), rbk);
-                    v[8 * kk + 7] = __fmul_rn(bf16hi(u.w), rbk);
-                }
-                uint8_t* dst = a.row.codes + (int64_t)r * a.row.ld_codes + cb / 2;
-                const uint32_t j0 = cb / 16u;
-                if (cb + 16u < a.cols) {
-                    *reinterpret_cast<uint4*>(dst) =
-                        make_uint4(e2m1_rne_x8(v), e2m1_rne_x8(v + 8), e2m1_rne_x8(v + 16), e2m1_rne_x8(v + 24));
-                    *reinterpret_cast<uint16_t*>(a.row.scales + scale_offset(r, j0, a.row.s4)) =
-                        (uint16_t)(sct0 | (sct1 << 8));
-                } else {
-                    *reinterpret_cast<uint2*>(dst) = make_uint2(e2m1_rne_x8(v), e2m1_rne_x8(v + 8));
-                    a.row.scales[scale_offset(r, j0, a.row.s4)] = (uint8_t)sct0;
+            float m = 0.0f;
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+            float rb;
+            sc = block_scale_tab(m, ts.s_enc, rb_tab, &rb);
+            if (a.emit_col && c < a.cols) {
+                float v0[16], v1[16];
+                encode_values<16, G>(t0, rb, sc, ts.s_enc, v0);
+                encode_values<16, G>(t1, rb, sc, ts.s_enc, v1);
+                q0 = make_uint2(e2m1_rne_x8(v0), e2m1_rne_x8(v0 + 8));
+                q1 = make_uint2(e2m1_rne_x8(v1), e2m1_rne_x8(v1 + 8));
+            }
+            if (a.emit_row) {
+                // row layout: row r0 + lane / 2, columns c0 + 32 (lane & 1) .. + 31
+                // = tiles 2h and 2h+1 of the slice, whose scales lanes 16h and
+                // 16h + 8 hold
+                const uint32_t i = lane >> 1, h = lane & 1u;
+                const uint32_t r = r0 + i, cb = c0 + 32u * h;
+                const float rbt0 = __shfl_sync(0xFFFFFFFFu, rb, 16 * h), rbt1 = __shfl_sync(0xFFFFFFFFu, rb, 16 * h + 8);
+                const uint32_t sct0 = __shfl_sync(0xFFFFFFFFu, sc, 16 * h),
+                               sct1 = __shfl_sync(0xFFFFFFFFu, sc, 16 * h + 8);
+                if (cb < a.cols) {
+                    float v[32];
+    #pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t off = i * 128u + (((4u * h + (uint32_t)kk) ^ (i & 7u)) << 4);
+                        const uint4 u = *reinterpret_cast<const uint4*>(src + off);
+                        const float x8[8] = {bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y),
+                                             bf16lo(u.z), bf16hi(u.z), bf16lo(u.w), bf16hi(u.w)};
+                        encode_values<8, G>(x8, kk < 2 ? rbt0 : rbt1, kk < 2 ? sct0 : sct1, ts.s_enc, v + 8 * kk);
+                    }
+                    uint8_t* dst = a.row.codes + (int64_t)r * a.row.ld_codes + cb / 2;
+                    const uint32_t j0 = cb / 16u;
+                    if (cb + 16u < a.cols) {
+                        *reinterpret_cast<uint4*>(dst) =
+                            make_uint4(e2m1_rne_x8(v), e2m1_rne_x8(v + 8), e2m1_rne_x8(v + 16), e2m1_rne_x8(v + 24));
+                        *reinterpret_cast<uint16_t*>(a.row.scales + scale_offset(r, j0, a.row.s4)) =
+                            (uint16_t)(sct0 | (sct1 << 8));
+                    } else {
+                        *reinterpret_cast<uint2*>(dst) = make_uint2(e2m1_rne_x8(v), e2m1_rne_x8(v + 8));
+                        a.row.scales[scale_offset(r, j0, a.row.s4)] = (uint8_t)sct0;
+                    }
                 }
             }
+            }
+            // slice j % 4 joins the warp's col-wise codes; after the fourth, they
+            // go out as whole sectors (both columns share the tile's scale)
+            cq0[0] = cq0[1], cq0[1] = cq0[2], cq0[2] = cq0[3], cq0[3] = q0;
+            cq1[0] = cq1[1], cq1[1] = cq1[2], cq1[2] = cq1[3], cq1[3] = q1;
+            cs = (cs >> 8) | (sc << 24);
+            if ((j & 3u) == 3u && a.emit_col) {
+                const uint32_t tile = blockIdx.x + (j >> 2) * gridDim.x;
+                const uint32_t rb = (tile % a.tiles_r) * kTileRows + warp * kWarpRows;
+                const uint32_t c = (tile / a.tiles_r) * 64u + lane * 2u;
+                if (tile < ntiles && rb < a.rows && c < a.cols) store_col64(a.col, c, rb, a.rows, cq0, cq1, cs, cs);
+            }
         }
-        }
-        // slice j % 4 joins the warp's col-wise codes; after the fourth, they
-        // go out as whole sectors (both columns share the tile's scale)
-        cq0[0] = cq0[1], cq0[1] = cq0[2], cq0[2] = cq0[3], cq0[3] = q0;
-        cq1[0] = cq1[1], cq1[1] = cq1[2], cq1[2] = cq1[3], cq1[3] = q1;
-        cs = (cs >> 8) | (sc << 24);
-        if ((j & 3u) == 3u && a.emit_col) {
-            const uint32_t tile = blockIdx.x + (j >> 2) * gridDim.x;
-            const uint32_t rb = (tile % a.tiles_r) * kTileRows + warp * kWarpRows;
-            const uint32_t c = (tile / a.tiles_r) * 64u + lane * 2u;
-            if (tile < ntiles && rb < a.rows && c < a.cols) store_col64(a.col, c, rb, a.rows, cq0, cq1, cs, cs);
-        }
-    }
+    };
+    if (multiplier_may_overflow(ts.s_enc))
+        main_loop(std::true_type{});
+    else
+        main_loop(std::false_type{});
 }
 
 // ------------------------------------------------------------- launch -----

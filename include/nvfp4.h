@@ -62,7 +62,11 @@
  *  3. per block: s_b = E4M3_rne_satfinite((amax_b / 6) * S_enc) [NV Sec. 2:
  *     the block amax maps onto the FP4 maximum 6]; amax_b is over the 1x16
  *     block or the 16x16 tile of x.
- *  4. r_b = S_enc / s_b (0 if s_b = 0); v = t * r_b.
+ *  4. r_b = S_enc / s_b (0 if s_b = 0); v = t * r_b.  When r_b overflows to
+ *     +inf (S_enc saturated near FLT_MAX and s_b < 1: tensor amaxes below
+ *     about 4e-33), v = (t * S_enc) / s_b instead, each operation rounded
+ *     once, so that zeros stay signed zeros [FS Sec. 2: the encode divides
+ *     by s_b * s_g].
  *  5. RNE: nearest E2M1 value, ties to the even mantissa, |v| > 6 -> 6 [NV
  *     Sec. 4].  SR [FS App. 7]: round |v| up from grid point c_k to c_k+1 iff
  *     (float)r < ((|v| - c_k) / step_k) * 2^16, r 16 random bits (so
@@ -378,7 +382,10 @@ NVFP4_API nvfp4_status nvfp4_dequantize(const nvfp4_tensor *q, void *y, int64_t 
  * with the same arguments, workspace aside.
  *  - The first call on a device looks up the scratch's device address (one
  *    cudaGetSymbolAddress with that device current); make that first call
- *    before any stream capture on the device.
+ *    before any stream capture on the device.  The address is cached per
+ *    device and CUDA context: after a device reset (or a primary context
+ *    released and created again) the next call looks it up again, so make
+ *    that call outside a capture as well.
  *  - Every call shares the one scratch array and it keeps the previous call's
  *    contents (each call writes the amax partials it reads, so nothing needs
  *    clearing).  Calls that overlap on the GPU -- on different streams, or

@@ -13,7 +13,8 @@ from fp4_gemm_nvfp4_gb300 import capi
 from tests import helpers
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -23,8 +24,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"NVFP4_API\s+[\w\s\*]+?\b(nvfp4_\w+)\s*\(", text)))
+    """Every entry point the headers in include/ declare."""
+    names = set()
+    for h in HEADERS:
+        names |= set(re.findall(r"NVFP4_API\s+[\w\s\*]+?\b(nvfp4_\w+)\s*\(", open(h).read()))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
@@ -38,6 +42,20 @@ def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_testing_arm_rejects_limits_out_of_range(lib):
+    # valid limits arm a fault for the next GEMM launch; only the rejections
+    # are exercised here (no GEMM runs on the CPU)
+    for us in (0, 999, 2000001, 2 ** 32 - 1):
+        assert capi.nvfp4_testing_arm_gemm_timeout(us) == capi.NVFP4_ERR_INVALID_ARG
+
+
+def test_quantize_workspace_is_the_documented_32_kib(lib):
+    # the no-allocation quantizer's library-held scratch is 32 KiB: the
+    # workspace every shape asks for must not outgrow it
+    for rows, cols, orient in ((16, 16, 1), (8192, 3072, 3), (65536, 8192, 2)):
+        assert capi.nvfp4_quantize_workspace_size(rows, cols, orient) == 32 * 1024
 
 
 def test_status_strings(lib):

@@ -119,15 +119,35 @@ def test_gemm_c1_single_linear_forward():
         _check(y.float().cpu().numpy(), y_ref, abs_sum, dt == torch.bfloat16)
 
 
+# Full-size GEMMs: (A rows, A cols, A kind, A quantizer kw, B rows, B cols, B
+# kind, B quantizer kw, fused amax).  A and B are the bf16 tensors the
+# operands are quantized from (a col-wise operand is the transpose of its
+# tensor); kinds as in the 3B workloads (activations with outlier channels,
+# weights N(0, 0.02^2), gradients t(3) * 1e-3), gradients with SR and the
+# Wgrad operands with the RHT as in the layer step.
+_GRAD_SR_ROW = dict(orientation=oracle.ROWWISE, rounding=1, seed=21, stream_id=1)
+_GRAD_SR_COL = dict(orientation=oracle.COLWISE, rounding=1, use_rht=True, sign_mask=0x6B2D, seed=21, stream_id=2)
+_ACT_COL = dict(orientation=oracle.COLWISE, use_rht=True, sign_mask=0x6B2D)
+_ROW = dict(orientation=oracle.ROWWISE)
+_W_ROW = dict(orientation=oracle.ROWWISE, scaling=1)
+_W_COL = dict(orientation=oracle.COLWISE, scaling=1)
+T4, T2 = 16384, 8192
 FULL = {
-    # name: (A rows, A cols, A kind, A quantizer kw, B rows, B cols, B kind, B quantizer kw)
-    "c2_fprop_qkv": (8192, 3072, "normal", dict(orientation=oracle.ROWWISE),
-                     6144, 3072, "weight", dict(orientation=oracle.ROWWISE, scaling=1)),
-    "c2_dgrad_o": (8192, 3072, "grad", dict(orientation=oracle.ROWWISE),
-                   3072, 3072, "weight", dict(orientation=oracle.COLWISE, scaling=1)),
-    "c3_wgrad": (8192, 9216, "grad", dict(orientation=oracle.COLWISE, rounding=1, use_rht=True,
-                                          sign_mask=0x6B2D, seed=3, stream_id=2),
-                 8192, 3072, "normal", dict(orientation=oracle.COLWISE, use_rht=True, sign_mask=0x6B2D)),
+    # attention projections at 8192 tokens (3072 -> 6144 QKV, 3072 -> 3072 O)
+    "c2_fprop_qkv": (T2, 3072, "normal", _ROW, 6144, 3072, "weight", _W_ROW, False),
+    "c2_fprop_o": (T2, 3072, "normal", _ROW, 3072, 3072, "weight", _W_ROW, False),
+    "c2_dgrad_qkv": (T2, 6144, "grad", _ROW, 6144, 3072, "weight", _W_COL, False),
+    "c2_dgrad_o": (T2, 3072, "grad", _ROW, 3072, 3072, "weight", _W_COL, False),
+    # FFN Wgrad at 8192 tokens
+    "c3_wgrad": (T2, 9216, "grad", _GRAD_SR_COL, T2, 3072, "normal", _ACT_COL, False),
+    # the FFN layer step at 16384 tokens: up 3072 -> 9216, down 9216 -> 3072;
+    # fprop_up and dgrad_down take their output's two amaxes in the epilogue
+    "c4_fprop_up": (T4, 3072, "normal", _ROW, 9216, 3072, "weight", _W_ROW, True),
+    "c4_fprop_down": (T4, 9216, "normal", _ROW, 3072, 9216, "weight", _W_ROW, False),
+    "c4_dgrad_down": (T4, 3072, "grad", _GRAD_SR_ROW, 3072, 9216, "weight", _W_COL, True),
+    "c4_dgrad_up": (T4, 9216, "grad", _GRAD_SR_ROW, 9216, 3072, "weight", _W_COL, False),
+    "c4_wgrad_down": (T4, 3072, "grad", _GRAD_SR_COL, T4, 9216, "normal", _ACT_COL, False),
+    "c4_wgrad_up": (T4, 9216, "grad", _GRAD_SR_COL, T4, 3072, "normal", _ACT_COL, False),
 }
 
 
@@ -139,22 +159,62 @@ def _make(kind, rows, cols, seed):
     return inputs.student_t(rows, cols, seed)
 
 
+def _gpu_operand(bits, orientation, scaling=0, rounding=0, use_rht=False, sign_mask=0, seed=0, stream_id=0):
+    row, col = ops.quantize(helpers.to_device_bf16(bits), two_d=scaling == 1, sr=rounding == 1,
+                            rht_mask=sign_mask if use_rht else None, seed=seed, stream_id=stream_id,
+                            rowwise=orientation == oracle.ROWWISE, colwise=orientation == oracle.COLWISE)
+    return row if orientation == oracle.ROWWISE else col
+
+
+def oracle_rows(bits, kw, rows):
+    """The oracle's quantization of the listed logical rows of one
+    orientation, with the tensor amax taken over the whole tensor."""
+    kw = dict(kw)
+    orientation = kw.pop("orientation", oracle.ROWWISE)
+    amax = oracle.amax(bits, orientation, kw.get("use_rht", False), kw.get("sign_mask", 0))
+    parts = [oracle.quantize(bits, orientation, rows_subset=(int(r), int(r) + 1), amax_value=amax, **kw)
+             for r in rows]
+    return dict(codes=np.concatenate([q["codes"] for q in parts]),
+                scales=np.concatenate([q["scales"] for q in parts]), s_g=parts[0]["s_g"])
+
+
+def sample_rows(M, n=24, seed=7):
+    rows = np.sort(np.random.default_rng(seed).choice(M, n, replace=False))
+    rows[0], rows[-1] = 0, M - 1
+    return rows
+
+
 @pytest.mark.parametrize("name", sorted(FULL))
 def test_gemm_full_size_sampled_rows(name):
-    ar, ac, ak, akw, br, bc, bk, bkw = FULL[name]
+    """Sampled rows (each with all N columns) of the full-size GEMM against the
+    oracle's FP64 GEMM of the oracle's own quantization of the same inputs;
+    the fused-amax GEMMs also write their two tensor amaxes, checked against
+    the oracle's amax of the tensor the GEMM wrote."""
+    ar, ac, ak, akw, br, bc, bk, bkw, fused = FULL[name]
     a_bits, b_bits = _make(ak, ar, ac, 11), _make(bk, br, bc, 12)
-    ga, gb = _quantized_pair(a_bits, b_bits, akw, bkw)
-    y = ops.gemm(ga, gb, out_dtype=torch.bfloat16)
+    ga, gb = _gpu_operand(a_bits, **akw), _gpu_operand(b_bits, **bkw)
+    mask = 0x39C6
+    if fused:
+        y, amax = ops.gemm_amax(ga, gb, mask)
+    else:
+        y = ops.gemm(ga, gb, out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     assert ops.device_error() == capi.NVFP4_OK
     M, N = ga.rows, gb.rows
-    rng = np.random.default_rng(7)
-    rows = np.sort(rng.choice(M, 24, replace=False))
-    rows[0], rows[-1] = 0, M - 1
-    qa = oracle.quantize(a_bits, **akw)
-    qb = oracle.quantize(b_bits, **bkw)
-    y_ref, abs_sum = oracle.gemm_f64(qa, qb, row_ids=rows)
+    del ga, gb
+    rows = sample_rows(M)
+    qa = oracle_rows(a_bits, akw, rows)
+    bkw_ = dict(bkw)
+    qb = oracle.quantize(b_bits, bkw_.pop("orientation"), **bkw_)
+    y_ref, abs_sum = oracle.gemm_f64(qa, qb)
     _check(y[torch.from_numpy(rows).cuda()].float().cpu().numpy(), y_ref, abs_sum, True)
+    if fused:
+        # the two tensor amaxes the pair quantization of D takes: max |D| and
+        # the col-wise RHT amax (16-row blocks of D's columns)
+        d_bits = y.view(torch.int16).cpu().numpy().view(np.uint16)
+        got = amax.cpu().numpy()
+        assert got[0] == oracle.amax(d_bits, oracle.ROWWISE)
+        assert got[1] == oracle.amax(d_bits, oracle.COLWISE, True, mask)
 
 
 def test_wgrad_rht_cancels_in_the_product():

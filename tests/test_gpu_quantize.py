@@ -285,3 +285,36 @@ def test_requantize_col_rht_full_size_sampled():
         assert amax == ref["amax"] and sg == ref["s_g"]
         assert np.array_equal(codes[lr0:lr1], ref["codes"])
         assert np.array_equal(scales[lr0:lr1], ref["scales"])
+
+
+# ---- whole tensors at the layer step's size (every code and scale) -------
+def test_whole_tensor_c4_dy_up_pair():
+    """The layer step's dY_up pair quantization (16384 x 9216, SR in both
+    orientations, RHT on the col-wise operand, both tensor amaxes given as
+    the producing GEMM supplies them), compared with the oracle over the
+    whole tensor: every code byte and every scale of both outputs."""
+    rows, cols, seed = 16384, 9216, 17
+    bits = inputs.student_t(rows, cols, seed)
+    mask = inputs.rht_sign_mask(seed)
+    ref_row = oracle.quantize(bits, oracle.ROWWISE, rounding=1, seed=seed, stream_id=3)
+    ref_col = oracle.quantize(bits, oracle.COLWISE, rounding=1, use_rht=True, sign_mask=mask, seed=seed,
+                              stream_id=4)
+    amax = torch.tensor([ref_row["amax"], ref_col["amax"]], dtype=torch.float32, device="cuda")
+    row, col = ops.quantize_row_col_rht_amax(helpers.to_device_bf16(bits), mask, amax, sr=True, seed=seed,
+                                             stream_row=3, stream_col=4)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    _check_against_oracle(row, ref_row)
+    _check_against_oracle(col, ref_col)
+
+
+def test_whole_tensor_c4_weight_16x16():
+    """W_up (9216 x 3072) with 16x16 scaling, both orientations from one
+    call, compared with the oracle over the whole tensor."""
+    rows, cols, seed = 9216, 3072, 18
+    bits = inputs.normal(rows, cols, seed, std=0.02)
+    row, col = ops.quantize(helpers.to_device_bf16(bits), two_d=True, rowwise=True, colwise=True)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    _check_against_oracle(row, oracle.quantize(bits, oracle.ROWWISE, scaling=1))
+    _check_against_oracle(col, oracle.quantize(bits, oracle.COLWISE, scaling=1))
