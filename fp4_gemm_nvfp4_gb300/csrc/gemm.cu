@@ -115,6 +115,7 @@ struct Params {
     int64_t ldc;
     float beta;
     int c_vec;                   // every row of C starts on a 16-byte boundary
+    int c_tma;                   // C read through the epilogue's slices by TMA (map in tma_u)
     uint64_t timeout_ns;         // limit of every mbarrier wait
     uint32_t withhold;           // test support: the leader's first scale-warp arrival is left out
 };
@@ -156,6 +157,19 @@ __device__ __forceinline__ void load_c_f32x32(const Params& p, uint32_t row, uin
 #pragma unroll
         for (int i = 0; i < 32; ++i) f[i] = (row < p.M && n0 + i < p.N) ? src[i] : 0.0f;
     }
+}
+
+// L2 prefetch of the C values one epilogue lane combines for a tile: its
+// row's 128 columns from n0 (BF16: 256 bytes, FP32: 512 bytes), in 128-byte
+// lines, only inside C.  Issued before the lane waits for the tile's
+// accumulator, so that C's reads after it hit L2 instead of waiting on DRAM.
+__device__ __forceinline__ void prefetch_c_row(const Params& p, uint32_t row, uint32_t n0) {
+    if (row >= p.M || n0 >= p.N) return;
+    const int64_t esz = p.out_fp32 ? 4 : 2;
+    const char* base = static_cast<const char*>(p.c) + ((int64_t)row * p.ldc + n0) * esz;
+    const uint32_t cols = (p.N - n0) < 128u ? (p.N - n0) : 128u;
+    const int64_t bytes = (int64_t)cols * esz;
+    for (int64_t off = 0; off < bytes; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
 }
 
 // One output value: RN(acc * alpha) + RN(beta * c) in binary32 (the C term
@@ -309,7 +323,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t* acc_full = empty + kStages;        // local: released by the leader's commit
     uint64_t* acc_empty = acc_full + 1;          // leader: 2 x kNumEpiWarps arrivals
     uint64_t* drain = acc_empty + 1;             // leader
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* c_full = drain + 1;                // local, per epilogue warp: C slice landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c_full + kNumEpiWarps);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     volatile uint32_t* sf_ok = tmem_slot + 4;    // [2]: scales-landed verdicts, by stage-count parity
 
@@ -325,6 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 2 * kNumEpiWarps);
         mbar_init(drain, 1);
+        for (int w = 0; w < kNumEpiWarps; ++w) mbar_init(&c_full[w], 1);
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -341,6 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tma_sfb);
     }
     if (warp == kFirstEpiWarp && lane == 0 && p.tma_store) prefetch_tmap(&tma_d);
+    if (warp == kFirstEpiWarp && lane == 0 && p.c_tma) prefetch_tmap(&tma_u);
     if (warp == kMmaWarp) {
         tmem_alloc_pair(tmem_slot, kTmemCols);
         tmem_relinquish_pair();
@@ -629,11 +646,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // then butterfly stages by shuffles; stage s: lanes with bit s set
         // take partner - t, the others t + partner)
         float amax_plain = 0.0f, amax_rht = 0.0f;
+        uint32_t c_parity = 0;   // phase of this warp's C barrier
         const uint32_t row_local = q * 32 + lane;
         uint32_t tiles_done = 0;
         for (uint32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
             uint32_t mt, nt;
             tile_coords(tile, p, mt, nt);
+            if constexpr (has_c)
+                prefetch_c_row(p, mt * kPairM + rank * kCtaM + row_local, nt * kBN + half * 128);
             // One thread per warp waits for the accumulator, suspended in the
             // barrier's try_wait (no issue slots taken from the MMA issuer);
             // each warp wakes on the barrier itself, not behind a named
@@ -651,7 +671,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t row = row0 + row_local;
             const uint32_t nbase = nt * kBN + half * 128;
             const uint32_t taddr = tmem + ((q * 32u) << 16) + kAccCol + half * 128;
-            if (p.tma_store && !p.out_fp32) {
+            if (has_c && p.c_tma) {
+                // C through this warp's 4 KiB slice: each round a TMA load puts
+                // the round's 32 rows of C into the slice (the output map's box
+                // and swizzle), every lane replaces its row's values by the
+                // outputs in place, and the slice goes out with a TMA store.
+                // BF16: two rounds of 64 columns; FP32: four of 32.
+                uint8_t* slice = staging + (half * 4 + q) * 4096u;
+                uint64_t* cbar = &c_full[warp - kFirstEpiWarp];
+                uint32_t v[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, v[c]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
+                const uint32_t y = row0 + q * 32;
+                const int rounds = p.out_fp32 ? 4 : 2;
+                bool landed = true;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    if (r >= rounds) break;
+                    const uint32_t x = nbase + (uint32_t)r * (p.out_fp32 ? 32u : 64u);
+                    // the slice's previous store must have read it before C lands in it
+                    if (lane == 0) {
+                        bulk_wait_read_all();
+                        mbar_arrive_expect_tx(cbar, 4096u);
+                        tma_load_2d(slice, &tma_u, cbar, (int32_t)x, (int32_t)y);
+                    }
+                    // every lane waits (the TMA writes become visible to the lanes
+                    // that observe the phase); a wait that ran out in any lane
+                    // stops the whole warp
+                    landed = __all_sync(0xFFFFFFFFu, mbar_wait(cbar, c_parity, p.timeout_ns) ? 1 : 0) != 0;
+                    c_parity ^= 1u;
+                    if (!landed) break;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        uint4* cell = reinterpret_cast<uint4*>(slice + lane * 128u + ((uint32_t)i ^ (lane & 7u)) * 16u);
+                        const uint4 cw = *cell;
+                        uint4 o;
+                        if (p.out_fp32) {
+                            // columns 4i .. 4i+3 of round r = chunk r
+                            o.x = __float_as_uint(epi_value(v[r][4 * i], alpha, true, p.beta, __uint_as_float(cw.x)));
+                            o.y = __float_as_uint(epi_value(v[r][4 * i + 1], alpha, true, p.beta, __uint_as_float(cw.y)));
+                            o.z = __float_as_uint(epi_value(v[r][4 * i + 2], alpha, true, p.beta, __uint_as_float(cw.z)));
+                            o.w = __float_as_uint(epi_value(v[r][4 * i + 3], alpha, true, p.beta, __uint_as_float(cw.w)));
+                        } else {
+                            // columns 8i .. 8i+7 of round r = chunk 2r + i/4, from 8 (i % 4)
+                            const uint32_t* a = &v[2 * r + (i >> 2)][8 * (i & 3)];
+                            o.x = pack_bf16x2(epi_value(a[0], alpha, true, p.beta, bf16lo(cw.x)),
+                                              epi_value(a[1], alpha, true, p.beta, bf16hi(cw.x)));
+                            o.y = pack_bf16x2(epi_value(a[2], alpha, true, p.beta, bf16lo(cw.y)),
+                                              epi_value(a[3], alpha, true, p.beta, bf16hi(cw.y)));
+                            o.z = pack_bf16x2(epi_value(a[4], alpha, true, p.beta, bf16lo(cw.z)),
+                                              epi_value(a[5], alpha, true, p.beta, bf16hi(cw.z)));
+                            o.w = pack_bf16x2(epi_value(a[6], alpha, true, p.beta, bf16lo(cw.w)),
+                                              epi_value(a[7], alpha, true, p.beta, bf16hi(cw.w)));
+                        }
+                        *cell = o;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
+                        bulk_commit_group();
+                    }
+                }
+                if (!landed) {
+                    if (lane == 0 && !*abort_flag) record_timeout(abort_flag);
+                    break;
+                }
+            } else if (p.tma_store && !p.out_fp32) {
                 // All 128 columns are loaded under one wait and the
                 // accumulator goes back to the MMAs at once; then two rounds
                 // of 64 columns through this warp's 4 KiB slice of the staging
@@ -1036,7 +1126,9 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
         p.amax_out = amax_out;
         p.rht_mask = rht_mask;
     }
-    CUtensorMap mu = ma, mv = ma;  // unused without a low-rank term
+    CUtensorMap mu = ma, mv = ma;  // low-rank operands, or C's map for the staged C term
+    if (p.c && p.c_vec && p.tma_store)
+        p.c_tma = make_output_map(&mu, const_cast<void*>(p.c), a.rows, b.rows, p.ldc, out_fp32) ? 1 : 0;
     if (lora) {
         if (!make_bf16_rows_map(&mu, lora->u_scaled, a.rows, lora->r, lora->r) ||
             !make_bf16_rows_map(&mv, lora->v, b.rows, lora->r, lora->ldv))
