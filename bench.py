@@ -46,8 +46,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_write.sum, one pass per launch); the figure holds while the
 # kernel sources hash to the recorded value, and is reported as null otherwise.
 TRAFFIC = {
-    "quantize": ("27ccb5229bdb2783", ("quantize.cu", "device_common.cuh"), 1538036480),
-    "gemm": ("b793fad5c8c65a5d", ("gemm.cu", "device_common.cuh"), 1235648000),
+    "quantize": ("e346080b933dd33d", ("quantize.cu", "device_common.cuh"), 1539275776),
+    "gemm": ("e9d6c88c7ecaebb7", ("gemm.cu", "device_common.cuh"), 1239611904),
 }
 
 
@@ -285,6 +285,50 @@ def smi_gpu_id(local):
     return str(local)
 
 
+def gpu_local_cpus(local):
+    """The CPUs the OS lists as local to the GPU torch uses as device `local`
+    (sysfs of its PCI function), or None."""
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(local)
+        bus = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bus}/local_cpulist") as f:
+            spec = f.read().strip()
+    except (AttributeError, OSError, RuntimeError):
+        return None
+    cpus = set()
+    for part in spec.split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus or None
+
+
+class LocalPinning:
+    """Within the block the calling thread runs on the GPU-local CPUs, so the
+    pinned host buffers it allocates land on the memory next to the GPU (a
+    copy from the far socket's memory crosses one more link)."""
+
+    def __init__(self, local):
+        self.cpus = gpu_local_cpus(local)
+        self.saved = None
+
+    def __enter__(self):
+        if self.cpus:
+            try:
+                self.saved = os.sched_getaffinity(0)
+                os.sched_setaffinity(0, self.cpus & self.saved or self.cpus)
+            except OSError:
+                self.saved = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.saved is not None:
+            os.sched_setaffinity(0, self.saved)
+
+
 def host_cpu():
     """The host CPU model and the cores the OS reports."""
     model = None
@@ -515,12 +559,13 @@ def measure(args):
     # buffer sets alternate, so step i's copy-in and copy-out overlap the
     # compute of steps i + 1 and i - 1; the time runs from the first copy-in
     # to the last copy-out.
-    pinned_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
-                 for k, v in host.items() if not produced(k)}
-    # the step's results: Y (fprop_down), dX (dgrad_up), dW_down and dW_up; H and
-    # dY_up are the layer's internal tensors and stay on the device
-    pinned_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in step.out.items()
-                  if k not in PRODUCED.values()}
+    with LocalPinning(local):
+        pinned_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+                     for k, v in host.items() if not produced(k)}
+        # the step's results: Y (fprop_down), dX (dgrad_up), dW_down and dW_up; H and
+        # dY_up are the layer's internal tensors and stay on the device
+        pinned_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in step.out.items()
+                      if k not in PRODUCED.values()}
     h2d = sum(t.numel() * 2 for t in pinned_in.values())
     d2h = sum(t.numel() * 2 for t in pinned_out.values())
     e2e_steps = max(2, min(args.steps, 10))
@@ -622,7 +667,9 @@ def measure(args):
         "quantize_frac_of_hbm": round(quant_gbs / peaks["hbm_gbs"], 4),
         "per_launch_ms": {k: round(v, 4) for k, v in sorted(launch_ms.items())},
         "e2e": {"value": round(whole_job_tflops(flops, world, e2e_ms), 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                "host_buffers": ("pinned, allocated on the GPU-local CPUs" if gpu_local_cpus(local)
+                                 else "pinned (no GPU-local CPU list found)")},
         "gpu_launches": step.launches() * args.steps,
         "clocks": clocks.summary(windows),
     }

@@ -540,9 +540,9 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     auto issue = [&](uint32_t j) {
         uint32_t r0, c0;
         if (lane == 0 && slice_of(j, r0, c0)) {
-            uint64_t* bar = &full[warp][j & 1u];
+            uint64_t* bar = &full[warp][j % kPairSlots];
             mbar_arrive_expect_tx(bar, kSliceBytes);
-            tma_load_2d(ring[warp][j & 1u], &tmap_x, bar, (int32_t)c0, (int32_t)r0);
+            tma_load_2d(ring[warp][j % kPairSlots], &tmap_x, bar, (int32_t)c0, (int32_t)r0);
         }
     };
     const uint32_t kcount = (ntiles > blockIdx.x) ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
@@ -551,25 +551,28 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     // s in element / byte s, stored once the fourth slice is encoded
     uint2 cq0[4], cq1[4];
     uint32_t cs0 = 0, cs1 = 0;
-    issue(0);
+    for (uint32_t k = 0; k + 1 < (uint32_t)kPairSlots; ++k) issue(k);   // kPairSlots - 1 slices ahead
     // the main loop, instantiated with and without the multiplier-overflow
     // test (encode_values); the tested form only when S_enc makes it possible
     auto main_loop = [&](auto guard) {
         constexpr bool G = decltype(guard)::value;
         for (uint32_t j = 0; j < 4u * kcount; ++j) {
             __syncwarp();   // every lane is done with the slot the next copy fills
-            issue(j + 1);
+            issue(j + kPairSlots - 1);
             uint32_t r0, c0;
             uint2 q0 = make_uint2(0u, 0u), q1 = make_uint2(0u, 0u);
             uint32_t sc0 = 0, sc1 = 0;
             if (slice_of(j, r0, c0)) {
-            const uint32_t sl = j & 1u;
+            const uint32_t sl = j % kPairSlots;
             if (!mbar_wait(&full[warp][sl], (parity >> sl) & 1u, 2000000000ull)) {
-                // a copy that never landed: let the next one (issued above) land
+                // a copy that never landed: let the ones issued after it land
                 // before this CTA can exit, then stop
-                uint32_t r1, c1;
-                if (slice_of(j + 1, r1, c1))
-                    (void)mbar_wait(&full[warp][sl ^ 1u], (parity >> (sl ^ 1u)) & 1u, 2000000000ull);
+                for (uint32_t k = 1; k < (uint32_t)kPairSlots; ++k) {
+                    uint32_t r1, c1;
+                    const uint32_t s2 = (j + k) % kPairSlots;
+                    if (slice_of(j + k, r1, c1))
+                        (void)mbar_wait(&full[warp][s2], (parity >> s2) & 1u, 2000000000ull);
+                }
                 break;
             }
             parity ^= 1u << sl;
@@ -733,9 +736,9 @@ __global__ void __launch_bounds__(kThreads) tile2d_rne_kernel(const __grid_const
     auto issue = [&](uint32_t j) {
         uint32_t r0, c0;
         if (lane == 0 && slice_of(j, r0, c0)) {
-            uint64_t* bar = &full[warp][j & 1u];
+            uint64_t* bar = &full[warp][j % kPairSlots];
             mbar_arrive_expect_tx(bar, kSliceBytes);
-            tma_load_2d(ring[warp][j & 1u], &tmap_x, bar, (int32_t)c0, (int32_t)r0);
+            tma_load_2d(ring[warp][j % kPairSlots], &tmap_x, bar, (int32_t)c0, (int32_t)r0);
         }
     };
     const uint32_t kcount = (ntiles > blockIdx.x) ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u;
@@ -743,23 +746,26 @@ __global__ void __launch_bounds__(kThreads) tile2d_rne_kernel(const __grid_const
     // the col-wise codes and scales of the warp's four slices of a tile
     uint2 cq0[4], cq1[4];
     uint32_t cs = 0;
-    issue(0);
+    for (uint32_t k = 0; k + 1 < (uint32_t)kPairSlots; ++k) issue(k);   // kPairSlots - 1 slices ahead
     // the main loop, instantiated with and without the multiplier-overflow
     // test (encode_values); the tested form only when S_enc makes it possible
     auto main_loop = [&](auto guard) {
         constexpr bool G = decltype(guard)::value;
         for (uint32_t j = 0; j < 4u * kcount; ++j) {
             __syncwarp();
-            issue(j + 1);
+            issue(j + kPairSlots - 1);
             uint32_t r0, c0;
             uint2 q0 = make_uint2(0u, 0u), q1 = make_uint2(0u, 0u);
             uint32_t sc = 0;
             if (slice_of(j, r0, c0)) {
-            const uint32_t sl = j & 1u;
+            const uint32_t sl = j % kPairSlots;
             if (!mbar_wait(&full[warp][sl], (parity >> sl) & 1u, 2000000000ull)) {
-                uint32_t r1, c1;
-                if (slice_of(j + 1, r1, c1))
-                    (void)mbar_wait(&full[warp][sl ^ 1u], (parity >> (sl ^ 1u)) & 1u, 2000000000ull);
+                for (uint32_t k = 1; k < (uint32_t)kPairSlots; ++k) {
+                    uint32_t r1, c1;
+                    const uint32_t s2 = (j + k) % kPairSlots;
+                    if (slice_of(j + k, r1, c1))
+                        (void)mbar_wait(&full[warp][s2], (parity >> s2) & 1u, 2000000000ull);
+                }
                 break;
             }
             parity ^= 1u << sl;
