@@ -73,8 +73,10 @@ __device__ __forceinline__ uint32_t e2m1_rne_x8(const float* v) {
 // rounded upward (which keeps ceil(frac * 2^16): float spacing there, 2^-24,
 // is finer than 2^-18), lies in [0.5, 1) where the same addition applies,
 // and 2 z - 1 maps the rounded z back.  max(|v|, (|v| + 1) / 2) selects z
-// exactly when |v| < 1, and min(q, 2 q - 1) selects 2 q - 1 exactly when
-// q < 1.  The result is |v|'s rounded value with v's sign: a grid value, or
+// exactly when |v| < 1; the rounded value q maps back as q - sat(1 - q),
+// which is 2 q - 1 for q in [0.5, 1) and q from 1 up (every step exact),
+// on the FMA pipe (the kernels that round stochastically are bound by the
+// integer/logic pipe, where a min would run).  The result is |v|'s rounded value with v's sign: a grid value, or
 // a value >= 6 (|v| > 6 can round to 8 or 12), which the saturating RNE
 // conversion e2m1_rne_x8 then turns into the code without rounding, so no
 // clamp to 6 is needed.  With finite v, |v| here stays below 9 (the block
@@ -98,7 +100,7 @@ __device__ __forceinline__ float e2m1_sr_grid(float v, uint32_t addend) {
     const float a = fabsf(v);
     const float z = fmaxf(a, __fmaf_ru(a, 0.5f, 0.5f));
     const float zt = __uint_as_float((__float_as_uint(z) + addend) & 0xFFC00000u);
-    const float q = fminf(zt, __fmaf_rn(zt, 2.0f, -1.0f));
+    const float q = __fsub_rn(zt, __saturatef(__fmaf_rn(zt, -1.0f, 1.0f)));
     return __uint_as_float(__float_as_uint(q) | (__float_as_uint(v) & 0x80000000u));
 }
 
