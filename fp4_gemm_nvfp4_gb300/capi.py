@@ -38,7 +38,8 @@ EXPORTED = ("nvfp4_scale_bytes", "nvfp4_quantize_workspace_size", "nvfp4_quantiz
             "nvfp4_requantize_col_rht", "nvfp4_gemm_lora", "nvfp4_gemm_lora_workspace_size",
             "nvfp4_gemm_amax", "nvfp4_quantize_row_col_rht_amax", "nvfp4_gemm_axpby",
             "nvfp4_newton_schulz_workspace_size", "nvfp4_newton_schulz_step",
-            "nvfp4_testing_arm_gemm_timeout")
+            "nvfp4_testing_arm_gemm_timeout", "nvfp4_testing_bounds_violations",
+            "nvfp4_testing_bounds_shrink")
 
 
 class nvfp4_tensor(ctypes.Structure):
@@ -106,6 +107,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_device_error.argtypes, L.nvfp4_device_error.restype = [vp], i32
     L.nvfp4_testing_arm_gemm_timeout.argtypes = [ctypes.c_uint32]
     L.nvfp4_testing_arm_gemm_timeout.restype = i32
+    L.nvfp4_testing_bounds_violations.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+    L.nvfp4_testing_bounds_violations.restype = i32
+    L.nvfp4_testing_bounds_shrink.argtypes, L.nvfp4_testing_bounds_shrink.restype = [i64], i32
     _lib = L
     return L
 
@@ -218,6 +222,20 @@ def nvfp4_testing_arm_gemm_timeout(wait_limit_us):
     """Test support (include/nvfp4_testing.h): the next GEMM launch withholds
     one barrier arrival and gives up on its waits after wait_limit_us."""
     return load().nvfp4_testing_arm_gemm_timeout(wait_limit_us)
+
+
+def nvfp4_testing_bounds_violations():
+    """Test support (include/nvfp4_testing.h): (status, count of the stores the
+    debug build's bounds check skipped since the last call)."""
+    n = ctypes.c_uint64(0)
+    st = load().nvfp4_testing_bounds_violations(ctypes.byref(n))
+    return st, n.value
+
+
+def nvfp4_testing_bounds_shrink(nbytes):
+    """Test support (debug build): later calls declare each output buffer
+    nbytes bytes shorter than it is."""
+    return load().nvfp4_testing_bounds_shrink(nbytes)
 
 
 def status_string(status):

@@ -5,12 +5,29 @@
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
 #include "../../include/nvfp4.h"
 #include "../../include/nvfp4_testing.h"
+#include "bounds.cuh"
 #include "kernels.h"
+
+namespace nvfp4 {
+namespace {
+// Bytes taken off the end of every declared output range (test support of
+// the debug build; always 0 in the regular build).
+std::atomic<int64_t> g_extent_shrink{0};
+}  // namespace
+
+Extent extent_of(const void* p, int64_t bytes) {
+    const int64_t shrink = g_extent_shrink.load(std::memory_order_relaxed);
+    const int64_t n = bytes > shrink ? bytes - shrink : 0;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Extent{lo, lo + (uintptr_t)n};
+}
+}  // namespace nvfp4
 
 namespace {
 
@@ -469,6 +486,34 @@ nvfp4_status nvfp4_testing_arm_gemm_timeout(uint32_t wait_limit_us) {
     if (wait_limit_us < 1000u || wait_limit_us > 2000000u) return NVFP4_ERR_INVALID_ARG;
     nvfp4::arm_gemm_fault((uint64_t)wait_limit_us * 1000u);
     return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_testing_bounds_violations(uint64_t* count) {
+#ifdef NVFP4_BOUNDS_CHECK
+    if (!count) return NVFP4_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return NVFP4_ERR_CUDA;
+    uint64_t n = 0;
+    if (nvfp4::quantize_bounds_read_and_clear(&n) != cudaSuccess ||
+        nvfp4::gemm_bounds_read_and_clear(&n) != cudaSuccess ||
+        nvfp4::dequantize_bounds_read_and_clear(&n) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    *count = n;
+    return NVFP4_OK;
+#else
+    (void)count;
+    return NVFP4_ERR_UNSUPPORTED;
+#endif
+}
+
+nvfp4_status nvfp4_testing_bounds_shrink(int64_t bytes) {
+#ifdef NVFP4_BOUNDS_CHECK
+    if (bytes < 0 || bytes > 4096) return NVFP4_ERR_INVALID_ARG;
+    nvfp4::g_extent_shrink.store(bytes, std::memory_order_relaxed);
+    return NVFP4_OK;
+#else
+    (void)bytes;
+    return NVFP4_ERR_UNSUPPORTED;
+#endif
 }
 
 nvfp4_status nvfp4_device_error(nvfp4_stream_t stream) {

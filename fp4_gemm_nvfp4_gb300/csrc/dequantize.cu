@@ -3,6 +3,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "bounds.cuh"
 #include "device_common.cuh"
 #include "kernels.h"
 
@@ -27,6 +28,7 @@ struct DeqArgs {
     uint32_t bpr, total;
     void* y;
     int64_t ldy;
+    Extent xy;   // the bytes of y the call may write
 };
 
 // One thread = one block of 16 elements.  e2m1 * s_b is exact in binary32; the
@@ -46,8 +48,10 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const DeqArgs a) {
             float* dst = reinterpret_cast<float*>(a.y) + (int64_t)r * a.ldy + (int64_t)j * 16;
 #pragma unroll
             for (int i = 0; i < 16; i += 4)
-                *reinterpret_cast<float4*>(dst + i) = make_float4(__fmul_rn(p[i], s_g), __fmul_rn(p[i + 1], s_g),
-                                                                  __fmul_rn(p[i + 2], s_g), __fmul_rn(p[i + 3], s_g));
+                store_out(reinterpret_cast<float4*>(dst + i),
+                          make_float4(__fmul_rn(p[i], s_g), __fmul_rn(p[i + 1], s_g), __fmul_rn(p[i + 2], s_g),
+                                      __fmul_rn(p[i + 3], s_g)),
+                          a.xy);
         } else {
             uint32_t w[8];
 #pragma unroll
@@ -57,8 +61,8 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const DeqArgs a) {
                 w[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
             }
             uint16_t* dst = reinterpret_cast<uint16_t*>(a.y) + (int64_t)r * a.ldy + (int64_t)j * 16;
-            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4*>(dst + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+            store_out(reinterpret_cast<uint4*>(dst), make_uint4(w[0], w[1], w[2], w[3]), a.xy);
+            store_out(reinterpret_cast<uint4*>(dst + 8), make_uint4(w[4], w[5], w[6], w[7]), a.xy);
         }
     }
 }
@@ -67,8 +71,9 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const DeqArgs a) {
 
 cudaError_t launch_dequantize(const uint8_t* codes, int64_t ld_codes, const uint8_t* scales, const float* sg,
                               int64_t rows, int64_t cols, void* y, int64_t ldy, bool out_fp32, cudaStream_t st) {
+    const int64_t esz = out_fp32 ? 4 : 2;
     DeqArgs a{codes, ld_codes, scales, (uint32_t)((cols + 63) / 64), sg, (uint32_t)(cols / 16),
-              (uint32_t)(rows * (cols / 16)), y, ldy};
+              (uint32_t)(rows * (cols / 16)), y, ldy, extent_rows(y, rows, ldy * esz, cols * esz)};
     if (a.total == 0) return cudaSuccess;
     int64_t grid = ((int64_t)a.total + kThreads - 1) / kThreads;
     const int64_t cap = (int64_t)device_sm_count() * 8;
@@ -77,5 +82,7 @@ cudaError_t launch_dequantize(const uint8_t* codes, int64_t ld_codes, const uint
     else dequantize_kernel<false><<<(int)grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
+
+cudaError_t dequantize_bounds_read_and_clear(uint64_t* n) { return bounds_read_and_clear_local(n); }
 
 }  // namespace nvfp4

@@ -43,6 +43,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "bounds.cuh"
 #include "device_common.cuh"
 #include "kernels.h"
 
@@ -118,6 +119,7 @@ struct Params {
     int c_tma;                   // C read through the epilogue's slices by TMA (map in tma_u)
     uint64_t timeout_ns;         // limit of every mbarrier wait
     uint32_t withhold;           // test support: the leader's first scale-warp arrival is left out
+    Extent xd;                   // the bytes of D the epilogue's direct stores may write
 };
 
 // 32 consecutive values of C's row `row` from column n0 (zeros past M or N):
@@ -842,15 +844,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (p.vec_store && n0 + 32 <= p.N) {
 #pragma unroll
                             for (int i = 0; i < 32; i += 4)
-                                *reinterpret_cast<float4*>(dst + i) =
-                                    make_float4(epi_value(v[i], alpha, has_c, p.beta, cf[i]),
-                                                epi_value(v[i + 1], alpha, has_c, p.beta, cf[i + 1]),
-                                                epi_value(v[i + 2], alpha, has_c, p.beta, cf[i + 2]),
-                                                epi_value(v[i + 3], alpha, has_c, p.beta, cf[i + 3]));
+                                store_out(reinterpret_cast<float4*>(dst + i),
+                                          make_float4(epi_value(v[i], alpha, has_c, p.beta, cf[i]),
+                                                      epi_value(v[i + 1], alpha, has_c, p.beta, cf[i + 1]),
+                                                      epi_value(v[i + 2], alpha, has_c, p.beta, cf[i + 2]),
+                                                      epi_value(v[i + 3], alpha, has_c, p.beta, cf[i + 3])),
+                                          p.xd);
                         } else {
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
-                                if (n0 + i < p.N) dst[i] = epi_value(v[i], alpha, has_c, p.beta, cf[i]);
+                                if (n0 + i < p.N) store_out(dst + i, epi_value(v[i], alpha, has_c, p.beta, cf[i]), p.xd);
                         }
                     } else {
                         uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + (int64_t)row * p.ldd + n0;
@@ -863,12 +866,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (p.vec_store && n0 + 32 <= p.N) {
 #pragma unroll
                             for (int i = 0; i < 16; i += 4)
-                                *reinterpret_cast<uint4*>(dst + 2 * i) =
-                                    make_uint4(packed[i], packed[i + 1], packed[i + 2], packed[i + 3]);
+                                store_out(reinterpret_cast<uint4*>(dst + 2 * i),
+                                          make_uint4(packed[i], packed[i + 1], packed[i + 2], packed[i + 3]), p.xd);
                         } else {
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
-                                if (n0 + i < p.N) dst[i] = (uint16_t)((packed[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
+                                if (n0 + i < p.N)
+                                    store_out(dst + i, (uint16_t)((packed[i / 2] >> (16 * (i & 1))) & 0xFFFFu), p.xd);
                         }
                     }
                 }
@@ -1095,6 +1099,7 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
     p.d = d;
     p.ldd = ldd;
     p.out_fp32 = out_fp32 ? 1 : 0;
+    p.xd = extent_rows(d, a.rows, ldd * (out_fp32 ? 4 : 2), b.rows * (out_fp32 ? 4 : 2));
     p.alpha = 1.0f;
     p.timeout_ns = kTimeoutNs;
     {
@@ -1162,5 +1167,7 @@ cudaError_t gemm_read_and_clear_status(unsigned int* status) {
     *status = v;
     return e;
 }
+
+cudaError_t gemm_bounds_read_and_clear(uint64_t* n) { return bounds_read_and_clear_local(n); }
 
 }  // namespace nvfp4

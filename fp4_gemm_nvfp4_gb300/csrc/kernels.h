@@ -91,6 +91,13 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
 // Read and clear the GEMM kernels' device status word (synchronous).
 cudaError_t gemm_read_and_clear_status(unsigned int* status);
 
+// Add the stores that the debug build's bounds check skipped in one source
+// file's kernels to *n and clear that count (synchronous; in the regular
+// build they add nothing).
+cudaError_t quantize_bounds_read_and_clear(uint64_t* n);
+cudaError_t gemm_bounds_read_and_clear(uint64_t* n);
+cudaError_t dequantize_bounds_read_and_clear(uint64_t* n);
+
 // Test support: the next GEMM launch waits at most timeout_ns per barrier and
 // its leader CTA leaves out one scale-warp arrival, so one wait runs out.
 void arm_gemm_fault(uint64_t timeout_ns);

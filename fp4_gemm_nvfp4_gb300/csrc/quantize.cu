@@ -17,6 +17,7 @@
 #include <type_traits>
 
 #include "device_common.cuh"
+#include "bounds.cuh"
 #include "kernels.h"
 
 namespace nvfp4 {
@@ -33,7 +34,19 @@ struct Target {
     uint32_t s4;        // 4-scale groups per logical row
     float* amax;
     float* sg;
+    Extent xc, xs;      // the bytes of codes and scales the call may write
 };
+
+// Stores into an orientation's codes (logical row r, byte offset off) and
+// scales (byte index idx), through the bounds check of the debug build.
+template <typename T>
+__device__ __forceinline__ void put_codes(const Target& t, int64_t r, int64_t off, const T& v) {
+    store_out(reinterpret_cast<T*>(t.codes + r * t.ld_codes + off), v, t.xc);
+}
+template <typename T>
+__device__ __forceinline__ void put_scales(const Target& t, uint32_t idx, const T& v) {
+    store_out(reinterpret_cast<T*>(t.scales + idx), v, t.xs);
+}
 
 // Tensor scale from the amax partials; CTA 0 publishes amax and s_g.
 __device__ __forceinline__ TensorScale load_tensor_scale(const float* partials, int n, float* red,
@@ -119,8 +132,8 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
                           : block_scale_tab(amax_b, ts.s_enc, rb_table, &r_b);
                 const uint64_t idx = (uint64_t)r * ((uint64_t)a.bpr * 16u) + (uint64_t)j * 16u;
                 const uint2 q = encode16<kSR, G>(t, r_b, sc, s_mult, keys, a.stream, idx);
-                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)r * a.out.ld_codes + (int64_t)j * 8) = q;
-                a.out.scales[scale_offset(r, j, a.out.s4)] = (uint8_t)sc;
+                put_codes(a.out, (int64_t)r, (int64_t)j * 8, q);
+                put_scales(a.out, scale_offset(r, j, a.out.s4), (uint8_t)sc);
             }
             j += stride_j;
             r += stride_r;
@@ -225,10 +238,10 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
                 const uint32_t sc1 = block_scale_tab(m1, ts.s_enc, rb_table, &rb1);
                 const uint2 q0 = encode16<kSR, G>(t0, rb0, sc0, s_mult, keys, a.stream, (uint64_t)c * a.rows + r0);
                 const uint2 q1 = encode16<kSR, G>(t1, rb1, sc1, s_mult, keys, a.stream, (uint64_t)(c + 1) * a.rows + r0);
-                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
-                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)(c + 1) * a.out.ld_codes + r0 / 2) = q1;
-                a.out.scales[scale_offset(c, r0 / 16, a.out.s4)] = (uint8_t)sc0;
-                a.out.scales[scale_offset(c + 1, r0 / 16, a.out.s4)] = (uint8_t)sc1;
+                put_codes(a.out, (int64_t)c, (int64_t)(r0 / 2), q0);
+                put_codes(a.out, (int64_t)(c + 1), (int64_t)(r0 / 2), q1);
+                put_scales(a.out, scale_offset(c, r0 / 16, a.out.s4), (uint8_t)sc0);
+                put_scales(a.out, scale_offset(c + 1, r0 / 16, a.out.s4), (uint8_t)sc1);
             }
         }
     };
@@ -331,10 +344,10 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const RequantArgs a) 
                 const uint32_t sc1 = block_scale_tab(m1, ts.s_enc, rb_table, &rb1);
                 const uint2 q0 = encode16<kSR, G>(t0, rb0, sc0, s_mult, keys, a.stream, (uint64_t)c * a.rows + r0);
                 const uint2 q1 = encode16<kSR, G>(t1, rb1, sc1, s_mult, keys, a.stream, (uint64_t)(c + 1) * a.rows + r0);
-                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
-                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)(c + 1) * a.out.ld_codes + r0 / 2) = q1;
-                a.out.scales[scale_offset(c, r0 / 16, a.out.s4)] = (uint8_t)sc0;
-                a.out.scales[scale_offset(c + 1, r0 / 16, a.out.s4)] = (uint8_t)sc1;
+                put_codes(a.out, (int64_t)c, (int64_t)(r0 / 2), q0);
+                put_codes(a.out, (int64_t)(c + 1), (int64_t)(r0 / 2), q1);
+                put_scales(a.out, scale_offset(c, r0 / 16, a.out.s4), (uint8_t)sc0);
+                put_scales(a.out, scale_offset(c + 1, r0 / 16, a.out.s4), (uint8_t)sc1);
             }
         }
     };
@@ -415,17 +428,17 @@ __global__ void __launch_bounds__(kThreads) tile2d_kernel(const ColArgs a) {
                 q1 = make_uint2(e2m1_rne_x8(g1), e2m1_rne_x8(g1 + 8));
             }
             if (a.emit_col) {
-                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)c * a.out.ld_codes + r0 / 2) = q0;
-                *reinterpret_cast<uint2*>(a.out.codes + (int64_t)(c + 1) * a.out.ld_codes + r0 / 2) = q1;
-                a.out.scales[scale_offset(c, r0 / 16, a.out.s4)] = (uint8_t)sc;
-                a.out.scales[scale_offset(c + 1, r0 / 16, a.out.s4)] = (uint8_t)sc;
+                put_codes(a.out, (int64_t)c, (int64_t)(r0 / 2), q0);
+                put_codes(a.out, (int64_t)(c + 1), (int64_t)(r0 / 2), q1);
+                put_scales(a.out, scale_offset(c, r0 / 16, a.out.s4), (uint8_t)sc);
+                put_scales(a.out, scale_offset(c + 1, r0 / 16, a.out.s4), (uint8_t)sc);
             }
             if (a.emit_row) {
     #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    a.out2.codes[(int64_t)(r0 + i) * a.out2.ld_codes + c / 2] =
-                        (uint8_t)(nibble(q0, i) | (nibble(q1, i) << 4));
-                    if ((lane & 7u) == 0) a.out2.scales[scale_offset(r0 + i, c / 16, a.out2.s4)] = (uint8_t)sc;
+                    put_codes(a.out2, (int64_t)(r0 + i), (int64_t)(c / 2),
+                              (uint8_t)(nibble(q0, i) | (nibble(q1, i) << 4)));
+                    if ((lane & 7u) == 0) put_scales(a.out2, scale_offset(r0 + i, c / 16, a.out2.s4), (uint8_t)sc);
                 }
             }
         }
@@ -475,24 +488,23 @@ constexpr uint32_t kTileRows = (kThreads / 32) * kWarpRows;
 // bytes (slice s in byte s).  Only the slices below `rows` are written.
 __device__ __forceinline__ void store_col64(const Target& t, uint32_t c, uint32_t rb, uint32_t rows,
                                             const uint2* q0, const uint2* q1, uint32_t sc0, uint32_t sc1) {
-    uint8_t* d0 = t.codes + (int64_t)c * t.ld_codes + rb / 2;
-    uint8_t* d1 = d0 + t.ld_codes;
+    const int64_t off = rb / 2;
     const uint32_t nv = (rows - rb) / 16u;
     if (nv >= 4u) {
-        *reinterpret_cast<uint4*>(d0) = make_uint4(q0[0].x, q0[0].y, q0[1].x, q0[1].y);
-        *reinterpret_cast<uint4*>(d0 + 16) = make_uint4(q0[2].x, q0[2].y, q0[3].x, q0[3].y);
-        *reinterpret_cast<uint4*>(d1) = make_uint4(q1[0].x, q1[0].y, q1[1].x, q1[1].y);
-        *reinterpret_cast<uint4*>(d1 + 16) = make_uint4(q1[2].x, q1[2].y, q1[3].x, q1[3].y);
-        *reinterpret_cast<uint32_t*>(t.scales + scale_offset(c, rb / 16u, t.s4)) = sc0;
-        *reinterpret_cast<uint32_t*>(t.scales + scale_offset(c + 1, rb / 16u, t.s4)) = sc1;
+        put_codes(t, (int64_t)c, off, make_uint4(q0[0].x, q0[0].y, q0[1].x, q0[1].y));
+        put_codes(t, (int64_t)c, off + 16, make_uint4(q0[2].x, q0[2].y, q0[3].x, q0[3].y));
+        put_codes(t, (int64_t)(c + 1), off, make_uint4(q1[0].x, q1[0].y, q1[1].x, q1[1].y));
+        put_codes(t, (int64_t)(c + 1), off + 16, make_uint4(q1[2].x, q1[2].y, q1[3].x, q1[3].y));
+        put_scales(t, scale_offset(c, rb / 16u, t.s4), sc0);
+        put_scales(t, scale_offset(c + 1, rb / 16u, t.s4), sc1);
     } else {
 #pragma unroll
         for (uint32_t s = 0; s < 3u; ++s) {
             if (s < nv) {
-                *reinterpret_cast<uint2*>(d0 + 8 * s) = q0[s];
-                *reinterpret_cast<uint2*>(d1 + 8 * s) = q1[s];
-                t.scales[scale_offset(c, rb / 16u + s, t.s4)] = (uint8_t)(sc0 >> (8 * s));
-                t.scales[scale_offset(c + 1, rb / 16u + s, t.s4)] = (uint8_t)(sc1 >> (8 * s));
+                put_codes(t, (int64_t)c, off + 8 * s, q0[s]);
+                put_codes(t, (int64_t)(c + 1), off + 8 * s, q1[s]);
+                put_scales(t, scale_offset(c, rb / 16u + s, t.s4), (uint8_t)(sc0 >> (8 * s)));
+                put_scales(t, scale_offset(c + 1, rb / 16u + s, t.s4), (uint8_t)(sc1 >> (8 * s)));
             }
         }
     }
@@ -660,15 +672,13 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                         q[jj] = encode16<kSR, G>(v + 16 * jj, rb, sc[jj], s_mult_row, keys, a.stream_row,
                                               (uint64_t)r * a.cols + cb + 16u * (uint32_t)jj);
                     }
-                    uint8_t* dst = a.row.codes + (int64_t)r * a.row.ld_codes + cb / 2;
                     const uint32_t j0 = cb / 16u;
                     if (two) {
-                        *reinterpret_cast<uint4*>(dst) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
-                        *reinterpret_cast<uint16_t*>(a.row.scales + scale_offset(r, j0, a.row.s4)) =
-                            (uint16_t)(sc[0] | (sc[1] << 8));
+                        put_codes(a.row, (int64_t)r, (int64_t)(cb / 2), make_uint4(q[0].x, q[0].y, q[1].x, q[1].y));
+                        put_scales(a.row, scale_offset(r, j0, a.row.s4), (uint16_t)(sc[0] | (sc[1] << 8)));
                     } else {
-                        *reinterpret_cast<uint2*>(dst) = q[0];
-                        a.row.scales[scale_offset(r, j0, a.row.s4)] = (uint8_t)sc[0];
+                        put_codes(a.row, (int64_t)r, (int64_t)(cb / 2), q[0]);
+                        put_scales(a.row, scale_offset(r, j0, a.row.s4), (uint8_t)sc[0]);
                     }
                 }
             }
@@ -814,16 +824,15 @@ __global__ void __launch_bounds__(kThreads) tile2d_rne_kernel(const __grid_const
                                              bf16lo(u.z), bf16hi(u.z), bf16lo(u.w), bf16hi(u.w)};
                         encode_values<8, G>(x8, kk < 2 ? rbt0 : rbt1, kk < 2 ? sct0 : sct1, ts.s_enc, v + 8 * kk);
                     }
-                    uint8_t* dst = a.row.codes + (int64_t)r * a.row.ld_codes + cb / 2;
                     const uint32_t j0 = cb / 16u;
                     if (cb + 16u < a.cols) {
-                        *reinterpret_cast<uint4*>(dst) =
-                            make_uint4(e2m1_rne_x8(v), e2m1_rne_x8(v + 8), e2m1_rne_x8(v + 16), e2m1_rne_x8(v + 24));
-                        *reinterpret_cast<uint16_t*>(a.row.scales + scale_offset(r, j0, a.row.s4)) =
-                            (uint16_t)(sct0 | (sct1 << 8));
+                        put_codes(a.row, (int64_t)r, (int64_t)(cb / 2),
+                                  make_uint4(e2m1_rne_x8(v), e2m1_rne_x8(v + 8), e2m1_rne_x8(v + 16),
+                                             e2m1_rne_x8(v + 24)));
+                        put_scales(a.row, scale_offset(r, j0, a.row.s4), (uint16_t)(sct0 | (sct1 << 8)));
                     } else {
-                        *reinterpret_cast<uint2*>(dst) = make_uint2(e2m1_rne_x8(v), e2m1_rne_x8(v + 8));
-                        a.row.scales[scale_offset(r, j0, a.row.s4)] = (uint8_t)sct0;
+                        put_codes(a.row, (int64_t)r, (int64_t)(cb / 2), make_uint2(e2m1_rne_x8(v), e2m1_rne_x8(v + 8)));
+                        put_scales(a.row, scale_offset(r, j0, a.row.s4), (uint8_t)sct0);
                     }
                 }
             }
@@ -867,6 +876,8 @@ Target make_target(const QuantTarget* q) {
     t.s4 = (uint32_t)((q->lcols + 63) / 64);
     t.amax = q->amax;
     t.sg = q->sg;
+    t.xc = extent_rows(q->codes, q->lrows, q->ld_codes, (q->lcols + 1) / 2);
+    t.xs = extent_of(q->scales, ((q->lrows + 127) / 128) * (int64_t)t.s4 * 512);
     return t;
 }
 
@@ -1189,5 +1200,7 @@ cudaError_t launch_requantize_col_rht(const QuantTarget* in, bool sr, uint32_t s
     else launch(requant_kernel<Pass::kEncode, false>);
     return cudaGetLastError();
 }
+
+cudaError_t quantize_bounds_read_and_clear(uint64_t* n) { return bounds_read_and_clear_local(n); }
 
 }  // namespace nvfp4

@@ -51,6 +51,14 @@ def test_testing_arm_rejects_limits_out_of_range(lib):
         assert capi.nvfp4_testing_arm_gemm_timeout(us) == capi.NVFP4_ERR_INVALID_ARG
 
 
+def test_bounds_check_entry_points_are_debug_only(lib):
+    """The regular build has no bounds check: both test-support calls say so
+    without touching the GPU."""
+    st, _ = capi.nvfp4_testing_bounds_violations()
+    assert st == capi.NVFP4_ERR_UNSUPPORTED
+    assert capi.nvfp4_testing_bounds_shrink(16) == capi.NVFP4_ERR_UNSUPPORTED
+
+
 def test_quantize_workspace_is_the_documented_32_kib(lib):
     # the no-allocation quantizer's library-held scratch is 32 KiB: the
     # workspace every shape asks for must not outgrow it
