@@ -6,8 +6,8 @@ the tile layout; it is test code, independent of the CUDA sources.
 """
 import numpy as np
 
-NORTH_STAR_REL = 1e-4      # |y - y_ref| <= 1e-4 * sum_k |a_k b_k| + 1e-6
-NORTH_STAR_ABS = 1e-6
+GEMM_TOL_REL = 1e-4      # |y - y_ref| <= 1e-4 * sum_k |a_k b_k| + 1e-6
+GEMM_TOL_ABS = 1e-6
 
 
 def scale_index_map(rows: int, cols: int) -> np.ndarray:
@@ -67,7 +67,7 @@ def bf16_half_ulp(y: np.ndarray) -> np.ndarray:
 
 
 def gemm_bound(abs_sum: np.ndarray, y_ref: np.ndarray, bf16: bool) -> np.ndarray:
-    b = NORTH_STAR_REL * abs_sum + NORTH_STAR_ABS
+    b = GEMM_TOL_REL * abs_sum + GEMM_TOL_ABS
     if bf16:
         b = b + bf16_half_ulp(y_ref)
     return b
