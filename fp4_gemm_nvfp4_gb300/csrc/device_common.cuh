@@ -385,10 +385,12 @@ __device__ __forceinline__ void encode_values(const float* t, float r_b, uint32_
 // fused multiply-adds; the 4 candidate only when strictly closer.  t holds the
 // values the multipliers of `table` apply to and xs_mult * t_i = x_i S_enc
 // (both carry the RHT's 1/4 when it is folded into the multipliers).  Returns
-// the chosen scale code and its multiplier in *r_b.
+// the chosen scale code and its multiplier in *r_b; with rne_codes, also the
+// chosen candidate's RNE codes (as encode16<false> packs them: the same
+// values, so an RNE caller need not encode the block again).
 template <bool kGuard = true>
 __device__ __forceinline__ uint32_t block_scale_46(const float* t, float amax_b, float s_enc, float xs_mult,
-                                                   const float* table, float* r_b) {
+                                                   const float* table, float* r_b, uint2* rne_codes = nullptr) {
     float r6;
     const uint32_t c6 = block_scale_tab(amax_b, s_enc, table, &r6);
     const uint32_t c4 = e4m3_encode_satfinite(__fmul_rn(__fmul_rn(amax_b, 0.25f), s_enc));
@@ -398,10 +400,12 @@ __device__ __forceinline__ uint32_t block_scale_46(const float* t, float amax_b,
     encode_values<16, kGuard>(t, r6, c6, xs_mult, v6);
     encode_values<16, kGuard>(t, r4, c4, xs_mult, v4);
     float g6[16], g4[16];
-    e2m1_decode_x8(e2m1_rne_x8(v6), g6);
-    e2m1_decode_x8(e2m1_rne_x8(v6 + 8), g6 + 8);
-    e2m1_decode_x8(e2m1_rne_x8(v4), g4);
-    e2m1_decode_x8(e2m1_rne_x8(v4 + 8), g4 + 8);
+    const uint2 q6 = make_uint2(e2m1_rne_x8(v6), e2m1_rne_x8(v6 + 8));
+    const uint2 q4 = make_uint2(e2m1_rne_x8(v4), e2m1_rne_x8(v4 + 8));
+    e2m1_decode_x8(q6.x, g6);
+    e2m1_decode_x8(q6.y, g6 + 8);
+    e2m1_decode_x8(q4.x, g4);
+    e2m1_decode_x8(q4.y, g4 + 8);
     float e6 = 0.0f, e4 = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -413,9 +417,11 @@ __device__ __forceinline__ uint32_t block_scale_46(const float* t, float amax_b,
     }
     if (e4 < e6) {
         *r_b = r4;
+        if (rne_codes) *rne_codes = q4;
         return c4;
     }
     *r_b = r6;
+    if (rne_codes) *rne_codes = q6;
     return c6;
 }
 

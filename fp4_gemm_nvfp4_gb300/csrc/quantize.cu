@@ -127,11 +127,12 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
             } else {
                 if (fold) amax_b = __fmul_rn(amax_b, 0.25f);
                 float r_b;
+                uint2 q;   // with 4/6 scales and RNE, the chosen candidate's codes
                 const uint32_t sc =
-                    kS46 ? block_scale_46<G>(t, amax_b, ts.s_enc, s_mult, rb_table, &r_b)
+                    kS46 ? block_scale_46<G>(t, amax_b, ts.s_enc, s_mult, rb_table, &r_b, kSR ? nullptr : &q)
                           : block_scale_tab(amax_b, ts.s_enc, rb_table, &r_b);
                 const uint64_t idx = (uint64_t)r * ((uint64_t)a.bpr * 16u) + (uint64_t)j * 16u;
-                const uint2 q = encode16<kSR, G>(t, r_b, sc, s_mult, keys, a.stream, idx);
+                if (kSR || !kS46) q = encode16<kSR, G>(t, r_b, sc, s_mult, keys, a.stream, idx);
                 put_codes(a.out, (int64_t)r, (int64_t)j * 8, q);
                 put_scales(a.out, scale_offset(r, j, a.out.s4), (uint8_t)sc);
             }
@@ -621,14 +622,18 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                     }
                     float rb0, rb1;
                     if constexpr (kS46) {
-                        sc0 = block_scale_46<G>(t0, m0, ts_col.s_enc, s_mult_col, rb_col, &rb0);
-                        sc1 = block_scale_46<G>(t1, m1, ts_col.s_enc, s_mult_col, rb_col, &rb1);
+                        // with RNE the chosen candidates' codes are the block's codes
+                        sc0 = block_scale_46<G>(t0, m0, ts_col.s_enc, s_mult_col, rb_col, &rb0, kSR ? nullptr : &q0);
+                        sc1 = block_scale_46<G>(t1, m1, ts_col.s_enc, s_mult_col, rb_col, &rb1, kSR ? nullptr : &q1);
                     } else {
                         sc0 = block_scale_tab(m0, ts_col.s_enc, rb_col, &rb0);
                         sc1 = block_scale_tab(m1, ts_col.s_enc, rb_col, &rb1);
                     }
-                    q0 = encode16<kSR, G>(t0, rb0, sc0, s_mult_col, keys, a.stream_col, (uint64_t)c * a.rows + r0);
-                    q1 = encode16<kSR, G>(t1, rb1, sc1, s_mult_col, keys, a.stream_col, (uint64_t)(c + 1) * a.rows + r0);
+                    if (kSR || !kS46) {
+                        q0 = encode16<kSR, G>(t0, rb0, sc0, s_mult_col, keys, a.stream_col, (uint64_t)c * a.rows + r0);
+                        q1 = encode16<kSR, G>(t1, rb1, sc1, s_mult_col, keys, a.stream_col,
+                                              (uint64_t)(c + 1) * a.rows + r0);
+                    }
                 }
             }
             // ---- row-wise without RHT: lane = row r0 + lane / 2, 32 columns
@@ -667,10 +672,12 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                         for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[16 * jj + e]));
                         if (fold_row) m = __fmul_rn(m, 0.25f);
                         float rb;
-                        sc[jj] = kS46 ? block_scale_46<G>(v + 16 * jj, m, ts_row.s_enc, s_mult_row, rb_row, &rb)
+                        sc[jj] = kS46 ? block_scale_46<G>(v + 16 * jj, m, ts_row.s_enc, s_mult_row, rb_row, &rb,
+                                                          kSR ? nullptr : &q[jj])
                                        : block_scale_tab(m, ts_row.s_enc, rb_row, &rb);
-                        q[jj] = encode16<kSR, G>(v + 16 * jj, rb, sc[jj], s_mult_row, keys, a.stream_row,
-                                              (uint64_t)r * a.cols + cb + 16u * (uint32_t)jj);
+                        if (kSR || !kS46)
+                            q[jj] = encode16<kSR, G>(v + 16 * jj, rb, sc[jj], s_mult_row, keys, a.stream_row,
+                                                  (uint64_t)r * a.cols + cb + 16u * (uint32_t)jj);
                     }
                     const uint32_t j0 = cb / 16u;
                     if (two) {
