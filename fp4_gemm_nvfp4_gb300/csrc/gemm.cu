@@ -107,6 +107,7 @@ struct Params {
     int out_fp32;
     int vec_store;               // every output row starts on a 16-byte boundary
     int tma_store;               // output written through the D tensor map (BF16 or FP32)
+    uint32_t n_tma;              // columns the D map covers: N cut to whole 16-byte pieces
     int n_fast;                  // tile order: N tiles vary fastest (else M tiles)
     uint32_t lora_stages;        // 64-deep BF16 stages of the low-rank term per tile (0: none)
     float* amax_out;             // [2]: max |D| and max |RHT along D's rows| (BF16 TMA path), or null
@@ -303,6 +304,29 @@ __device__ __forceinline__ void slice_amax(const uint8_t* slice, uint32_t lane, 
             f32x2_unpack(t[i], lo, hi);
             amax_rht = fmax3(amax_rht, fabsf(lo), fabsf(hi));
         }
+    }
+}
+
+// The columns [max(x, n_tma), min(x + cols, N)) of this lane's row of a
+// staged round (x: the round's first column, cols its width; the slice holds
+// the round's 32 rows, row = lane, 128-byte swizzled).  A TMA store writes
+// whole 16-byte pieces of a row even past the tensor map's last column, so
+// the D map ends at n_tma, the last 16-byte boundary at or below N, and the
+// lanes store the at most 7 (BF16) or 3 (FP32) columns after it themselves.
+__device__ __forceinline__ void store_round_tail(const Params& p, const uint8_t* slice, uint32_t lane,
+                                                 uint32_t row, uint32_t x, uint32_t cols) {
+    const uint32_t lo = x > p.n_tma ? x : p.n_tma, hi = x + cols < p.N ? x + cols : p.N;
+    if (row >= p.M || lo >= hi) return;
+    const uint32_t esz = p.out_fp32 ? 4u : 2u;
+    for (uint32_t c = lo; c < hi; ++c) {
+        const uint32_t b = (c - x) * esz;
+        const uint8_t* src = slice + lane * 128u + (((b >> 4) ^ (lane & 7u)) << 4) + (b & 15u);
+        if (p.out_fp32)
+            store_out(reinterpret_cast<float*>(p.d) + (int64_t)row * p.ldd + c, *reinterpret_cast<const float*>(src),
+                      p.xd);
+        else
+            store_out(reinterpret_cast<uint16_t*>(p.d) + (int64_t)row * p.ldd + c,
+                      *reinterpret_cast<const uint16_t*>(src), p.xd);
     }
 }
 
@@ -735,9 +759,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
+                        if (y < p.M && x < p.n_tma) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
                         bulk_commit_group();
                     }
+                    store_round_tail(p, slice, lane, row, x, p.out_fp32 ? 32u : 64u);
                 }
                 if (!landed) {
                     if (lane == 0 && !*abort_flag) record_timeout(abort_flag);
@@ -787,9 +812,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         const uint32_t y = row0 + q * 32, x = nbase + r * 64;
-                        if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
+                        if (y < p.M && x < p.n_tma) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
                         bulk_commit_group();
                     }
+                    store_round_tail(p, slice, lane, row, nbase + r * 64, 64u);
                     // the slice now holds this warp's 32 rows x 64 columns: read
                     // it back by columns for the output's amax
                     if constexpr (kAmax) slice_amax(slice, lane, p.rht_mask, amax_plain, amax_rht);
@@ -824,9 +850,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         const uint32_t y = row0 + q * 32, x = nbase + (uint32_t)c * 32u;
-                        if (y < p.M && x < p.N) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
+                        if (y < p.M && x < p.n_tma) tma_store_2d(&tma_d, slice, (int32_t)x, (int32_t)y);
                         bulk_commit_group();
                     }
+                    store_round_tail(p, slice, lane, row, nbase + (uint32_t)c * 32u, 32u);
                 }
             } else {
 #pragma unroll 1
@@ -1121,7 +1148,12 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
         p.c_vec = ((reinterpret_cast<uintptr_t>(axpby->c) & 15u) == 0 && (axpby->ldc * esz) % 16 == 0) ? 1 : 0;
     }
     p.vec_store = ((reinterpret_cast<uintptr_t>(d) & 15u) == 0 && (ldd * esz) % 16 == 0) ? 1 : 0;
-    p.tma_store = (p.vec_store && make_output_map(&md, d, a.rows, b.rows, ldd, out_fp32)) ? 1 : 0;
+    // the D map stops at the last whole 16-byte piece of a row (a TMA store
+    // writes whole pieces); the columns after it go out by the lanes' stores
+    p.n_tma = (uint32_t)(out_fp32 ? (b.rows & ~int64_t(3)) : (b.rows & ~int64_t(7)));
+    p.tma_store = (p.vec_store && make_output_map(&md, d, a.rows, p.n_tma > 0 ? p.n_tma : b.rows, ldd, out_fp32))
+                      ? 1
+                      : 0;
     if (!p.tma_store) md = ma;   // unused by the kernel; any valid map
     if (amax_out) {
         // the amax is taken in the BF16 TMA-store epilogue

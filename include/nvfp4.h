@@ -249,7 +249,9 @@ NVFP4_API nvfp4_status nvfp4_quantize_row_col_rht(const void *x, int64_t rows, i
  * Requirements: K % 16 == 0 [SHAPE]; ldd >= N [SHAPE]; codes and scales
  * 16-byte aligned, ld_codes % 16 == 0, D aligned to its element size
  * [ALIGNMENT].  Rows of D that start on a 16-byte boundary are written with
- * vector stores.  M = 0 or N = 0 enqueues nothing; K = 0 writes D = 0.
+ * vector stores.  Only the N columns of each row are written: the padding
+ * after them (up to ldd) keeps its contents.  M = 0 or N = 0 enqueues
+ * nothing; K = 0 writes D = 0.
  * The kernel's pipeline waits are bounded; a wait that runs out records a
  * timeout which nvfp4_device_error() reports.
  */

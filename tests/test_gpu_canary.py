@@ -145,3 +145,46 @@ def test_dequantize_writes_only_its_output():
     torch.cuda.synchronize()
     assert buf.guards_intact()
     assert (buf.body.cpu().numpy().reshape(rows, ldy * 4)[:, cols * 4:] == CANARY).all()
+
+
+@pytest.mark.parametrize("N", [257, 263, 271, 300, 8, 3])
+@pytest.mark.parametrize("mode", ["bf16", "fp32", "amax", "axpby"])
+def test_gemm_tma_rows_write_only_their_columns(N, mode):
+    """Rows of D on 16-byte boundaries go out by TMA stores, which write whole
+    16-byte pieces: with N not a multiple of 8 (BF16) or 4 (FP32) the last
+    piece of a row reaches past column N, so it must not be stored by TMA.
+    The padding after column N keeps the canary."""
+    M, K = 96, 64
+    rng = np.random.default_rng(N)
+    a = ops.alloc_operand(M, K)
+    b = ops.alloc_operand(N, K)
+    for op in (a, b):
+        op.codes.copy_(torch.from_numpy(rng.integers(0, 256, op.codes.shape, dtype=np.uint8)))
+        op.scales.copy_(torch.from_numpy(rng.integers(0x20, 0x48, op.scales.shape, dtype=np.uint8)))
+        op.global_scale.fill_(1.0)
+    fp32 = mode == "fp32"
+    esz = 4 if fp32 else 2
+    ldd = (N + 7) // 8 * 8 + 8                     # rows on 16 bytes: the TMA-store path
+    buf = Guarded(M * ldd * esz)
+    d = buf.body.view(torch.float32 if fp32 else torch.bfloat16).view(M, ldd)[:, :N]
+    amax_buf = Guarded(16)
+    if mode == "amax":
+        ops.gemm_amax(a, b, 0x1234, out=d, amax=amax_buf.body[:8].view(torch.float32))
+    elif mode == "axpby":
+        # C with rows on 16 bytes too: the epilogue reads it through the staging slices
+        c = torch.randn((M, ldd), device="cuda").to(torch.bfloat16)[:, :N]
+        ops.gemm_axpby(a, b, 0.5, c, 2.0, out=d)
+    else:
+        ops.gemm(a, b, out=d)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    assert buf.guards_intact(), "write outside the output buffer"
+    pad = buf.body.cpu().numpy().reshape(M, ldd * esz)[:, N * esz:]
+    assert (pad == CANARY).all(), "write into the output's row padding"
+    if mode == "axpby":
+        ref_c = (0.5 * ops.gemm(a, b, out_dtype=torch.float32) + 2.0 * c.float())
+        assert torch.allclose(d.float(), ref_c, rtol=2 ** -7, atol=1e-6)
+    # and the columns themselves are the product
+    ref = ops.gemm(a, b, out_dtype=torch.float32) if not fp32 else None
+    if mode in ("bf16", "amax"):
+        assert torch.equal(d.float(), ref.to(torch.bfloat16).float())
