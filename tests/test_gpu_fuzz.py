@@ -14,7 +14,7 @@ from tests import helpers
 
 pytestmark = pytest.mark.gpu
 
-N_QUANT, N_PAIR, N_GEMM = 48, 16, 24
+N_QUANT, N_PAIR, N_GEMM, N_OTHER = 64, 24, 32, 16
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -132,3 +132,119 @@ def test_fuzz_gemm(case):
     bound = helpers.gemm_bound(abs_sum, ref, out_dtype == torch.bfloat16)
     err = np.abs(y.float().cpu().numpy().astype(np.float64) - ref)
     assert np.all(err <= bound), f"{int((err > bound).sum())} of {err.size} outside the bound"
+
+
+def _gemm_operands(rng, case, M, N, K):
+    a_bits = _bits(rng, M, K, 8_000 + case, max_log2=20)
+    b_bits = _bits(rng, N, K, 9_000 + case, max_log2=20)
+    a, _ = ops.quantize(helpers.to_device_bf16(a_bits))
+    b, _ = ops.quantize(helpers.to_device_bf16(b_bits))
+    return a, b
+
+
+@pytest.mark.parametrize("case", range(N_OTHER))
+def test_fuzz_requantize(case):
+    """The Wgrad re-quantization of a row-wise operand on random shapes."""
+    rng = np.random.default_rng(11_000 + case)
+    rows, cols = 16 * int(rng.integers(1, 50)), 16 * int(rng.integers(1, 50))
+    sr = bool(rng.integers(0, 2))
+    mask = int(rng.integers(0, 1 << 16))
+    seed, sid = (int(v) for v in rng.integers(0, 2 ** 62, 2))
+    bits = _bits(rng, rows, cols, 12_000 + case)
+    row, _ = ops.quantize(helpers.to_device_bf16(bits))
+    col = ops.requantize_col_rht(row, mask, sr=sr, seed=seed, stream_id=sid)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    _check(col, oracle.requantize_col_rht(oracle.quantize(bits), mask, rounding=int(sr), seed=seed,
+                                          stream_id=sid))
+
+
+@pytest.mark.parametrize("case", range(N_OTHER))
+def test_fuzz_dequantize(case):
+    """x^ = e2m1 s_b s_g of a random operand, into a padded BF16 or FP32 output."""
+    rng = np.random.default_rng(13_000 + case)
+    rows, cols = int(rng.integers(1, 500)), 16 * int(rng.integers(1, 60))
+    bits = _bits(rng, rows, cols, 14_000 + case)
+    q, _ = ops.quantize(helpers.to_device_bf16(bits), sr=bool(rng.integers(0, 2)), seed=case)
+    fp32 = bool(rng.integers(0, 2))
+    esz = 4 if fp32 else 2
+    ldy = cols + (16 // esz) * int(rng.integers(0, 3))
+    buf = torch.full((rows, ldy), 7.0, dtype=torch.float32 if fp32 else torch.bfloat16, device="cuda")
+    st = capi.nvfp4_dequantize(q.struct(), buf.data_ptr(), ldy, capi.NVFP4_OUT_FP32 if fp32 else capi.NVFP4_OUT_BF16,
+                               ops.stream_handle())
+    assert st == capi.NVFP4_OK
+    torch.cuda.synchronize()
+    codes, scales, _, sg, _ = helpers.operand_to_host(q)
+    ref = oracle.dequantize(codes, scales, sg)
+    y = buf[:, :cols].float().cpu().numpy().astype(np.float64)
+    want = ref.astype(np.float32).astype(np.float64) if fp32 else oracle.bf16_to_f64(oracle.round_bf16_array(ref))
+    assert np.array_equal(y, want), "dequantized values differ"
+    assert bool((buf[:, cols:] == 7.0).all()), "write into the output's row padding"
+
+
+@pytest.mark.parametrize("case", range(N_OTHER))
+def test_fuzz_gemm_amax(case):
+    """The fused-amax GEMM writes the plain GEMM's output and its two amaxes."""
+    rng = np.random.default_rng(15_000 + case)
+    M, N, K = 16 * int(rng.integers(1, 40)), int(rng.integers(1, 600)), 16 * int(rng.integers(1, 60))
+    a, b = _gemm_operands(rng, case, M, N, K)
+    mask = int(rng.integers(0, 1 << 16))
+    ldd = (N + 7) // 8 * 8 + 8 * int(rng.integers(0, 3))
+    out = torch.full((M, ldd), 7.0, dtype=torch.bfloat16, device="cuda")
+    d, amax = ops.gemm_amax(a, b, mask, out=out[:, :N])
+    d_plain = ops.gemm(a, b)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    assert torch.equal(d, d_plain)
+    assert bool((out[:, N:] == 7.0).all()), "write into the output's row padding"
+    d_bits = d.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    got = amax.cpu().numpy()
+    assert got[0] == oracle.amax(d_bits, oracle.ROWWISE)
+    assert got[1] == oracle.amax(d_bits, oracle.COLWISE, True, mask)
+
+
+@pytest.mark.parametrize("case", range(N_OTHER))
+def test_fuzz_gemm_axpby(case):
+    """D = alpha A B^T + beta C with random scalars, dtypes and strides."""
+    rng = np.random.default_rng(17_000 + case)
+    M, N, K = int(rng.integers(1, 400)), int(rng.integers(1, 400)), 16 * int(rng.integers(1, 60))
+    a, b = _gemm_operands(rng, case, M, N, K)
+    fp32 = bool(rng.integers(0, 2))
+    dtype = torch.float32 if fp32 else torch.bfloat16
+    alpha, beta = float(rng.uniform(-2, 2)), float(rng.uniform(-2, 2))
+    c_bits = inputs.normal(M, N, 18_000 + case)
+    c = helpers.to_device_bf16(c_bits).to(dtype)
+    ldd = N + int(rng.integers(0, 9))
+    out = torch.full((M, ldd), 7.0, dtype=dtype, device="cuda")
+    y = ops.gemm_axpby(a, b, alpha, c, beta, out=out[:, :N])
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    assert bool((out[:, N:] == 7.0).all()), "write into the output's row padding"
+    ref, abs_sum = oracle.gemm_axpby_f64(helpers.as_oracle_operand(a), helpers.as_oracle_operand(b), alpha, c_bits,
+                                         beta)
+    bound = helpers.gemm_bound(abs_sum, ref, not fp32)
+    err = np.abs(y.float().cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), f"{int((err > bound).sum())} of {err.size} outside the bound"
+
+
+@pytest.mark.parametrize("case", range(N_OTHER))
+def test_fuzz_noalloc_equals_quantize(case):
+    """nvfp4_quantize_noalloc gives the regular call's result."""
+    rng = np.random.default_rng(19_000 + case)
+    rows, cols = 16 * int(rng.integers(1, 40)), 16 * int(rng.integers(1, 40))
+    bits = _bits(rng, rows, cols, 20_000 + case)
+    x = helpers.to_device_bf16(bits)
+    scaling = int(rng.integers(0, 3))
+    sr = bool(rng.integers(0, 2))
+    seed = int(rng.integers(0, 2 ** 62))
+    r1, c1 = ops.quantize(x, two_d=scaling == 1, scale46=scaling == 2, sr=sr, seed=seed, colwise=True)
+    r2, c2 = ops.alloc_operand(rows, cols), ops.alloc_operand(cols, rows)
+    st = capi.nvfp4_quantize_noalloc(x.data_ptr(), rows, cols, x.stride(0), scaling, int(sr), seed, 0,
+                                     capi.NVFP4_ROWWISE | capi.NVFP4_COLWISE, r2.struct(), c2.struct(),
+                                     ops.stream_handle())
+    assert st == capi.NVFP4_OK
+    torch.cuda.synchronize()
+    for g, h in ((r1, r2), (c1, c2)):
+        hg, hh = helpers.operand_to_host(g), helpers.operand_to_host(h)
+        assert hg[2] == hh[2] and hg[3] == hh[3]
+        assert np.array_equal(hg[0], hh[0]) and np.array_equal(hg[1], hh[1])
