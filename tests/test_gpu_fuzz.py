@@ -248,3 +248,31 @@ def test_fuzz_noalloc_equals_quantize(case):
         hg, hh = helpers.operand_to_host(g), helpers.operand_to_host(h)
         assert hg[2] == hh[2] and hg[3] == hh[3]
         assert np.array_equal(hg[0], hh[0]) and np.array_equal(hg[1], hh[1])
+
+
+@pytest.mark.parametrize("case", range(N_OTHER))
+def test_fuzz_gemm_lora(case):
+    """D = A B^T + beta U V^T with a random rank (a multiple of 64), shapes,
+    beta and output dtype and leading dimension; tolerance as in the fixed
+    cases (the GEMM bound plus 2^-8 of sum |beta u v|, U being rounded to
+    BF16 once more on its way into the tensor cores)."""
+    rng = np.random.default_rng(21_000 + case)
+    M, N, K = int(rng.integers(1, 400)), int(rng.integers(1, 400)), 16 * int(rng.integers(1, 60))
+    r = 64 * int(rng.integers(1, 4))
+    a, b = _gemm_operands(rng, case, M, N, K)
+    beta = float(rng.uniform(-2, 2))
+    u_bits = inputs.to_bf16_bits(rng.standard_normal((M, r)).astype(np.float32) * float(rng.uniform(0.1, 4)))
+    v_bits = inputs.to_bf16_bits(rng.standard_normal((N, r)).astype(np.float32) * float(rng.uniform(0.1, 4)))
+    fp32 = bool(rng.integers(0, 2))
+    dtype = torch.float32 if fp32 else torch.bfloat16
+    ldd = N + int(rng.integers(0, 9))
+    out = torch.full((M, ldd), 7.0, dtype=dtype, device="cuda")
+    y = ops.gemm_lora(a, b, helpers.to_device_bf16(u_bits), helpers.to_device_bf16(v_bits), beta, out=out[:, :N])
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    assert bool((out[:, N:] == 7.0).all()), "write into the output's row padding"
+    ref, abs_sum, lora_abs = oracle.gemm_lora_f64(helpers.as_oracle_operand(a), helpers.as_oracle_operand(b), u_bits,
+                                                  v_bits, beta)
+    bound = helpers.gemm_bound(abs_sum, ref, not fp32) + 2.0 ** -8 * lora_abs
+    err = np.abs(y.float().cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), f"{int((err > bound).sum())} of {err.size} outside the bound"
