@@ -276,3 +276,44 @@ def test_fuzz_gemm_lora(case):
     bound = helpers.gemm_bound(abs_sum, ref, not fp32) + 2.0 ** -8 * lora_abs
     err = np.abs(y.float().cpu().numpy().astype(np.float64) - ref)
     assert np.all(err <= bound), f"{int((err > bound).sum())} of {err.size} outside the bound"
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_fuzz_quantize_large(case):
+    """Shapes of several persistent-grid rounds (up to 4096 x 4096), every
+    code and scale compared."""
+    rng = np.random.default_rng(23_000 + case)
+    rows, cols = 16 * int(rng.integers(64, 257)), 16 * int(rng.integers(64, 257))
+    scaling = int(rng.integers(0, 3))
+    rounding = int(rng.integers(0, 2))
+    rht = scaling != 1 and bool(rng.integers(0, 2))
+    mask = int(rng.integers(0, 1 << 16))
+    seed, sid = (int(v) for v in rng.integers(0, 2 ** 62, 2))
+    bits = _bits(rng, rows, cols, 24_000 + case)
+    row, col = ops.quantize(helpers.to_device_bf16(bits), two_d=scaling == 1, scale46=scaling == 2,
+                            sr=rounding == 1, rht_mask=mask if rht else None, seed=seed, stream_id=sid,
+                            rowwise=True, colwise=True)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    kw = dict(scaling=scaling, rounding=rounding, use_rht=rht, sign_mask=mask, seed=seed, stream_id=sid)
+    _check(row, oracle.quantize(bits, oracle.ROWWISE, **kw))
+    _check(col, oracle.quantize(bits, oracle.COLWISE, **kw))
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_fuzz_gemm_large_sampled_rows(case):
+    """GEMMs of several tile waves (M, N up to 3000, K up to 4096), compared
+    on 32 sampled rows with every column."""
+    rng = np.random.default_rng(25_000 + case)
+    M, N = int(rng.integers(600, 3000)), int(rng.integers(600, 3000))
+    K = 16 * int(rng.integers(16, 257))
+    a, b = _gemm_operands(rng, case, M, N, K)
+    fp32 = bool(rng.integers(0, 2))
+    y = ops.gemm(a, b, out_dtype=torch.float32 if fp32 else torch.bfloat16)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    ids = np.sort(rng.choice(M, 32, replace=False))
+    ref, abs_sum = oracle.gemm_f64(helpers.as_oracle_operand(a, ids), helpers.as_oracle_operand(b))
+    bound = helpers.gemm_bound(abs_sum, ref, not fp32)
+    err = np.abs(y[torch.from_numpy(ids).cuda()].float().cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), f"{int((err > bound).sum())} of {err.size} outside the bound"
