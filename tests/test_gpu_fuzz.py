@@ -317,3 +317,29 @@ def test_fuzz_gemm_large_sampled_rows(case):
     bound = helpers.gemm_bound(abs_sum, ref, not fp32)
     err = np.abs(y[torch.from_numpy(ids).cuda()].float().cpu().numpy().astype(np.float64) - ref)
     assert np.all(err <= bound), f"{int((err > bound).sum())} of {err.size} outside the bound"
+
+
+@pytest.mark.parametrize("case", range(N_OTHER))
+def test_fuzz_gemm_axpby_in_place(case):
+    """D = alpha A B^T + beta D with C and D the same buffer (each element is
+    read before it is written), random ragged N and leading dimension."""
+    rng = np.random.default_rng(27_000 + case)
+    M, N, K = int(rng.integers(1, 400)), int(rng.integers(1, 400)), 16 * int(rng.integers(1, 60))
+    a, b = _gemm_operands(rng, case, M, N, K)
+    fp32 = bool(rng.integers(0, 2))
+    dtype = torch.float32 if fp32 else torch.bfloat16
+    alpha, beta = float(rng.uniform(-2, 2)), float(rng.uniform(-2, 2))
+    c_bits = inputs.normal(M, N, 28_000 + case)
+    ldd = N + int(rng.integers(0, 9))
+    buf = torch.full((M, ldd), 7.0, dtype=dtype, device="cuda")
+    d = buf[:, :N]
+    d.copy_(helpers.to_device_bf16(c_bits).to(dtype))
+    y = ops.gemm_axpby(a, b, alpha, d, beta, out=d)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    assert bool((buf[:, N:] == 7.0).all()), "write into the output's row padding"
+    ref, abs_sum = oracle.gemm_axpby_f64(helpers.as_oracle_operand(a), helpers.as_oracle_operand(b), alpha, c_bits,
+                                         beta)
+    bound = helpers.gemm_bound(abs_sum, ref, not fp32)
+    err = np.abs(y.float().cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), f"{int((err > bound).sum())} of {err.size} outside the bound"
