@@ -70,7 +70,7 @@ def check_modes():
             ops.dequantize(row, dtype)
         torch.cuda.synchronize()
         expect_clean(f"dequantize {rows}x{cols}")
-    for M, N, K in ((200, 300, 320), (256, 512, 1024), (130, 260, 80)):
+    for M, N, K in ((200, 300, 320), (256, 512, 1024), (130, 260, 80), (96, 271, 64)):
         a = ops.alloc_operand(M, K)
         b = ops.alloc_operand(N, K)
         g = torch.Generator(device="cuda")
@@ -87,8 +87,16 @@ def check_modes():
                 ops.gemm(a, b, out_dtype=dtype, out=d)
                 c = torch.randn((M, N), device="cuda").to(dtype)
                 ops.gemm_axpby(a, b, 0.5, c, 2.0, out=d)
-        if M % 16 == 0:
+        if M % 16 == 0 and N % 8 == 0:
             ops.gemm_amax(a, b, 0x1234)
+        # rows on 16 bytes with N off a 16-byte multiple: TMA stores up to the
+        # last whole piece, the lanes' stores after it
+        ldt = (N + 7) // 8 * 8 + 8
+        for dtype in (torch.bfloat16, torch.float32):
+            d = torch.empty((M, ldt), dtype=dtype, device="cuda")[:, :N]
+            ops.gemm(a, b, out_dtype=dtype, out=d)
+        if M % 16 == 0:
+            ops.gemm_amax(a, b, 0x1234, out=torch.empty((M, ldt), dtype=torch.bfloat16, device="cuda")[:, :N])
         torch.cuda.synchronize()
         assert ops.device_error() == capi.NVFP4_OK
         expect_clean(f"gemm {M}x{N}x{K}")
