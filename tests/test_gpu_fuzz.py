@@ -38,6 +38,11 @@ def _bits(rng, rows, cols, seed, max_log2=60):
     return inputs.extreme_range(rows, cols, seed, amax=amax, span_log2=24)
 
 
+def _u64(rng):
+    """A seed or stream id over the whole 64-bit range."""
+    return int(rng.integers(0, 2 ** 64, dtype=np.uint64))
+
+
 def _padded(bits, pad):
     """bf16 device matrix whose rows are `pad` elements longer than the data."""
     rows, cols = bits.shape
@@ -70,7 +75,7 @@ def test_fuzz_quantize(case):
         rows = 16 * max(1, rows // 16)
     pad = 8 * int(rng.integers(0, 4))
     mask = int(rng.integers(0, 1 << 16))
-    seed, sid = int(rng.integers(0, 2 ** 62)), int(rng.integers(0, 2 ** 62))
+    seed, sid = _u64(rng), _u64(rng)
     bits = _bits(rng, rows, cols, 2_000 + case)
     row, col = ops.quantize(_padded(bits, pad), two_d=scaling == 1, scale46=scaling == 2, sr=rounding == 1,
                             rht_mask=mask if rht else None, seed=seed, stream_id=sid, rowwise=rowwise,
@@ -91,7 +96,7 @@ def test_fuzz_pair(case):
     rows, cols = 16 * int(rng.integers(1, 60)), 16 * int(rng.integers(1, 60))
     sr = bool(rng.integers(0, 2))
     mask = int(rng.integers(0, 1 << 16))
-    seed, s_row, s_col = (int(v) for v in rng.integers(0, 2 ** 62, 3))
+    seed, s_row, s_col = _u64(rng), _u64(rng), _u64(rng)
     bits = _bits(rng, rows, cols, 4_000 + case)
     ref_row = oracle.quantize(bits, oracle.ROWWISE, rounding=int(sr), seed=seed, stream_id=s_row)
     ref_col = oracle.quantize(bits, oracle.COLWISE, rounding=int(sr), use_rht=True, sign_mask=mask, seed=seed,
@@ -149,7 +154,7 @@ def test_fuzz_requantize(case):
     rows, cols = 16 * int(rng.integers(1, 50)), 16 * int(rng.integers(1, 50))
     sr = bool(rng.integers(0, 2))
     mask = int(rng.integers(0, 1 << 16))
-    seed, sid = (int(v) for v in rng.integers(0, 2 ** 62, 2))
+    seed, sid = _u64(rng), _u64(rng)
     bits = _bits(rng, rows, cols, 12_000 + case)
     row, _ = ops.quantize(helpers.to_device_bf16(bits))
     col = ops.requantize_col_rht(row, mask, sr=sr, seed=seed, stream_id=sid)
@@ -236,7 +241,7 @@ def test_fuzz_noalloc_equals_quantize(case):
     x = helpers.to_device_bf16(bits)
     scaling = int(rng.integers(0, 3))
     sr = bool(rng.integers(0, 2))
-    seed = int(rng.integers(0, 2 ** 62))
+    seed = _u64(rng)
     r1, c1 = ops.quantize(x, two_d=scaling == 1, scale46=scaling == 2, sr=sr, seed=seed, colwise=True)
     r2, c2 = ops.alloc_operand(rows, cols), ops.alloc_operand(cols, rows)
     st = capi.nvfp4_quantize_noalloc(x.data_ptr(), rows, cols, x.stride(0), scaling, int(sr), seed, 0,
@@ -288,7 +293,7 @@ def test_fuzz_quantize_large(case):
     rounding = int(rng.integers(0, 2))
     rht = scaling != 1 and bool(rng.integers(0, 2))
     mask = int(rng.integers(0, 1 << 16))
-    seed, sid = (int(v) for v in rng.integers(0, 2 ** 62, 2))
+    seed, sid = _u64(rng), _u64(rng)
     bits = _bits(rng, rows, cols, 24_000 + case)
     row, col = ops.quantize(helpers.to_device_bf16(bits), two_d=scaling == 1, scale46=scaling == 2,
                             sr=rounding == 1, rht_mask=mask if rht else None, seed=seed, stream_id=sid,
