@@ -117,7 +117,7 @@ struct Params {
     int64_t ldc;
     float beta;
     int c_vec;                   // every row of C starts on a 16-byte boundary
-    int c_tma;                   // C read through the epilogue's slices by TMA (map in tma_u)
+    int c_staged;                // C copied into the epilogue's slices by the lanes (cp.async)
     uint64_t timeout_ns;         // limit of every mbarrier wait
     uint32_t withhold;           // test support: the leader's first scale-warp arrival is left out
     Extent xd;                   // the bytes of D the epilogue's direct stores may write
@@ -174,6 +174,33 @@ __device__ __forceinline__ void prefetch_c_row(const Params& p, uint32_t row, ui
     const int64_t bytes = (int64_t)cols * esz;
     for (int64_t off = 0; off < bytes; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
 }
+
+// One round's 32 rows x 128 bytes of C at column x, row y into an epilogue
+// warp's slice (128-byte swizzle, as the output's TMA store reads it), by
+// the lanes' own asynchronous copies: instruction i moves rows 4i .. 4i+3,
+// eight 16-byte pieces each; pieces past N and rows past M read as zero.
+// The copies go through the load/store path, not through the TMA unit that
+// carries the operand ring.  Completed by cp_async_wait_all.
+__device__ __forceinline__ void load_c_slice_async(const Params& p, uint8_t* slice, uint32_t lane, uint32_t x,
+                                                   uint32_t y) {
+    const uint32_t esz = p.out_fp32 ? 4u : 2u;
+    const uint32_t per = 16u / esz;   // columns per piece
+    const uint32_t ch = lane & 7u;
+    const uint32_t c0 = x + ch * per;
+    const uint32_t nbytes = c0 >= p.N ? 0u : ((p.N - c0) >= per ? 16u : (p.N - c0) * esz);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t rr = 4u * (uint32_t)i + (lane >> 3);
+        const uint32_t grow = y + rr;
+        const uint32_t n = grow < p.M ? nbytes : 0u;
+        const char* src = static_cast<const char*>(p.c) + (n ? ((int64_t)grow * p.ldc + c0) * esz : 0);
+        const uint32_t dst = smem_u32(slice + rr * 128u + ((ch ^ (rr & 7u)) * 16u));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // One output value: RN(acc * alpha) + RN(beta * c) in binary32 (the C term
 // only when the call has one).
@@ -349,8 +376,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t* acc_full = empty + kStages;        // local: released by the leader's commit
     uint64_t* acc_empty = acc_full + 1;          // leader: 2 x kNumEpiWarps arrivals
     uint64_t* drain = acc_empty + 1;             // leader
-    uint64_t* c_full = drain + 1;                // local, per epilogue warp: C slice landed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c_full + kNumEpiWarps);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     volatile uint32_t* sf_ok = tmem_slot + 4;    // [2]: scales-landed verdicts, by stage-count parity
 
@@ -366,7 +392,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 2 * kNumEpiWarps);
         mbar_init(drain, 1);
-        for (int w = 0; w < kNumEpiWarps; ++w) mbar_init(&c_full[w], 1);
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -383,7 +408,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tma_sfb);
     }
     if (warp == kFirstEpiWarp && lane == 0 && p.tma_store) prefetch_tmap(&tma_d);
-    if (warp == kFirstEpiWarp && lane == 0 && p.c_tma) prefetch_tmap(&tma_u);
     if (warp == kMmaWarp) {
         tmem_alloc_pair(tmem_slot, kTmemCols);
         tmem_relinquish_pair();
@@ -672,7 +696,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // then butterfly stages by shuffles; stage s: lanes with bit s set
         // take partner - t, the others t + partner)
         float amax_plain = 0.0f, amax_rht = 0.0f;
-        uint32_t c_parity = 0;   // phase of this warp's C barrier
         const uint32_t row_local = q * 32 + lane;
         uint32_t tiles_done = 0;
         for (uint32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
@@ -697,14 +720,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t row = row0 + row_local;
             const uint32_t nbase = nt * kBN + half * 128;
             const uint32_t taddr = tmem + ((q * 32u) << 16) + kAccCol + half * 128;
-            if (has_c && p.c_tma) {
-                // C through this warp's 4 KiB slice: each round a TMA load puts
-                // the round's 32 rows of C into the slice (the output map's box
-                // and swizzle), every lane replaces its row's values by the
-                // outputs in place, and the slice goes out with a TMA store.
-                // BF16: two rounds of 64 columns; FP32: four of 32.
+            if (has_c && p.c_staged) {
+                // C through this warp's 4 KiB slice: each round the lanes copy
+                // the round's 32 rows of C into the slice (the output map's
+                // box and swizzle), every lane replaces its row's values by
+                // the outputs in place, and the slice goes out with a TMA
+                // store.  BF16: two rounds of 64 columns; FP32: four of 32.
                 uint8_t* slice = staging + (half * 4 + q) * 4096u;
-                uint64_t* cbar = &c_full[warp - kFirstEpiWarp];
                 uint32_t v[4][32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, v[c]);
@@ -714,23 +736,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
                 const uint32_t y = row0 + q * 32;
                 const int rounds = p.out_fp32 ? 4 : 2;
-                bool landed = true;
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     if (r >= rounds) break;
                     const uint32_t x = nbase + (uint32_t)r * (p.out_fp32 ? 32u : 64u);
                     // the slice's previous store must have read it before C lands in it
-                    if (lane == 0) {
-                        bulk_wait_read_all();
-                        mbar_arrive_expect_tx(cbar, 4096u);
-                        tma_load_2d(slice, &tma_u, cbar, (int32_t)x, (int32_t)y);
-                    }
-                    // every lane waits (the TMA writes become visible to the lanes
-                    // that observe the phase); a wait that ran out in any lane
-                    // stops the whole warp
-                    landed = __all_sync(0xFFFFFFFFu, mbar_wait(cbar, c_parity, p.timeout_ns) ? 1 : 0) != 0;
-                    c_parity ^= 1u;
-                    if (!landed) break;
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                    load_c_slice_async(p, slice, lane, x, y);
+                    // each lane waits for its own copies; the warp barrier then
+                    // makes every lane's pieces visible to the others
+                    cp_async_wait_all();
+                    __syncwarp();
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         uint4* cell = reinterpret_cast<uint4*>(slice + lane * 128u + ((uint32_t)i ^ (lane & 7u)) * 16u);
@@ -763,10 +780,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         bulk_commit_group();
                     }
                     store_round_tail(p, slice, lane, row, x, p.out_fp32 ? 32u : 64u);
-                }
-                if (!landed) {
-                    if (lane == 0 && !*abort_flag) record_timeout(abort_flag);
-                    break;
                 }
             } else if (p.tma_store && !p.out_fp32) {
                 // All 128 columns are loaded under one wait and the
@@ -1163,9 +1176,8 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
         p.amax_out = amax_out;
         p.rht_mask = rht_mask;
     }
-    CUtensorMap mu = ma, mv = ma;  // low-rank operands, or C's map for the staged C term
-    if (p.c && p.c_vec && p.tma_store)
-        p.c_tma = make_output_map(&mu, const_cast<void*>(p.c), a.rows, b.rows, p.ldc, out_fp32) ? 1 : 0;
+    CUtensorMap mu = ma, mv = ma;  // low-rank operands (unused by the kernel otherwise; any valid map)
+    p.c_staged = (p.c && p.c_vec && p.tma_store) ? 1 : 0;
     if (lora) {
         if (!make_bf16_rows_map(&mu, lora->u_scaled, a.rows, lora->r, lora->r) ||
             !make_bf16_rows_map(&mv, lora->v, b.rows, lora->r, lora->ldv))
