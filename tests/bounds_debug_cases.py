@@ -95,6 +95,9 @@ def check_modes():
         for dtype in (torch.bfloat16, torch.float32):
             d = torch.empty((M, ldt), dtype=dtype, device="cuda")[:, :N]
             ops.gemm(a, b, out_dtype=dtype, out=d)
+            # C on 16-byte rows as well: copied into the epilogue's slices
+            c = torch.randn((M, ldt), device="cuda").to(dtype)[:, :N]
+            ops.gemm_axpby(a, b, 0.5, c, 2.0, out=d)
         if M % 16 == 0:
             ops.gemm_amax(a, b, 0x1234, out=torch.empty((M, ldt), dtype=torch.bfloat16, device="cuda")[:, :N])
         torch.cuda.synchronize()

@@ -233,6 +233,40 @@ def test_fuzz_gemm_axpby(case):
 
 
 @pytest.mark.parametrize("case", range(N_OTHER))
+def test_fuzz_gemm_axpby_staged_c(case):
+    """The C term read through the epilogue's staging slices: C and D rows on
+    16-byte boundaries while N is ragged (a row's last 16-byte piece of C
+    partly past column N), M off the 32-row rounds, BF16 or FP32, half the
+    cases with C and D the same buffer."""
+    rng = np.random.default_rng(29_000 + case)
+    M, K = int(rng.integers(1, 400)), 16 * int(rng.integers(1, 60))
+    N = 8 * int(rng.integers(0, 50)) + int(rng.integers(1, 8))
+    a, b = _gemm_operands(rng, case, M, N, K)
+    fp32 = bool(rng.integers(0, 2))
+    dtype, per = (torch.float32, 4) if fp32 else (torch.bfloat16, 8)
+    alpha, beta = float(rng.uniform(-2, 2)), float(rng.uniform(-2, 2))
+    c_bits = inputs.normal(M, N, 30_000 + case)
+    ld = (N + per - 1) // per * per + per * int(rng.integers(0, 3))
+    buf = torch.full((M, ld), 7.0, dtype=dtype, device="cuda")
+    d = buf[:, :N]
+    if rng.integers(0, 2):
+        d.copy_(helpers.to_device_bf16(c_bits).to(dtype))
+        c = d
+    else:
+        c = torch.full((M, ld), -3.0, dtype=dtype, device="cuda")[:, :N]
+        c.copy_(helpers.to_device_bf16(c_bits).to(dtype))
+    y = ops.gemm_axpby(a, b, alpha, c, beta, out=d)
+    torch.cuda.synchronize()
+    assert ops.device_error() == capi.NVFP4_OK
+    assert bool((buf[:, N:] == 7.0).all()), "write into the output's row padding"
+    ref, abs_sum = oracle.gemm_axpby_f64(helpers.as_oracle_operand(a), helpers.as_oracle_operand(b), alpha, c_bits,
+                                         beta)
+    bound = helpers.gemm_bound(abs_sum, ref, not fp32)
+    err = np.abs(y.float().cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), f"{int((err > bound).sum())} of {err.size} outside the bound"
+
+
+@pytest.mark.parametrize("case", range(N_OTHER))
 def test_fuzz_noalloc_equals_quantize(case):
     """nvfp4_quantize_noalloc gives the regular call's result."""
     rng = np.random.default_rng(19_000 + case)
