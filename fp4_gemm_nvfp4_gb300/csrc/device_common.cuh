@@ -406,15 +406,24 @@ __device__ __forceinline__ uint32_t block_scale_46(const float* t, float amax_b,
     e2m1_decode_x8(q6.y, g6 + 8);
     e2m1_decode_x8(q4.x, g4);
     e2m1_decode_x8(q4.y, g4 + 8);
-    float e6 = 0.0f, e4 = 0.0f;
+    // d = RN(x S_enc - g s) in one fused multiply-add: g s is exact (at most
+    // 2 + 4 significant bits, between 2^-10 and 2688), so this is the
+    // rounded difference of the exact product.  The two candidates' sums
+    // advance together as one packed pair (e6, e4): each lane of
+    // fma.rn.f32x2 rounds like the scalar fused multiply-add, in index order.
+    uint64_t e;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(e) : "r"(0u));
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const float xs = __fmul_rn(t[i], xs_mult);
-        const float d6 = __fsub_rn(xs, __fmul_rn(g6[i], sb6));
-        const float d4 = __fsub_rn(xs, __fmul_rn(g4[i], sb4));
-        e6 = __fmaf_rn(d6, d6, e6);
-        e4 = __fmaf_rn(d4, d4, e4);
+        const float d6 = __fmaf_rn(-g6[i], sb6, xs);
+        const float d4 = __fmaf_rn(-g4[i], sb4, xs);
+        uint64_t d;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(d6), "f"(d4));
+        asm("fma.rn.f32x2 %0, %1, %1, %2;" : "=l"(e) : "l"(d), "l"(e));
     }
+    float e6, e4;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(e6), "=f"(e4) : "l"(e));
     if (e4 < e6) {
         *r_b = r4;
         if (rne_codes) *rne_codes = q4;
