@@ -146,6 +146,25 @@ __device__ __forceinline__ uint4 sr_words4(const PhiloxKeys& keys, uint64_t stre
 }
 
 // ------------------------------------------------------------------ RHT ----
+// The sign flips D of the RHT as XOR words on packed bf16 pairs, formed on
+// the host and read from the kernel parameters, so that each flip is one XOR
+// of a loaded word: col[i] flips both values of a word when bit i of the
+// mask is set (two columns of row i, the transform running down the
+// columns); row[k] flips the low value by bit 2k and the high value by bit
+// 2k + 1 (columns 2k and 2k + 1 of one row, the transform along the row).
+struct RhtSigns {
+    uint32_t col[16];
+    uint32_t row[8];
+};
+
+__host__ __device__ inline RhtSigns rht_signs(uint32_t mask) {
+    RhtSigns s;
+    for (int i = 0; i < 16; ++i) s.col[i] = ((mask >> i) & 1u) ? 0x80008000u : 0u;
+    for (int k = 0; k < 8; ++k)
+        s.row[k] = (((mask >> (2 * k)) & 1u) ? 0x00008000u : 0u) | (((mask >> (2 * k + 1)) & 1u) ? 0x80000000u : 0u);
+    return s;
+}
+
 // t <- H16 * D * t (without the 1/4): negate per mask, butterfly stages 0..3.
 // With bf16 inputs every value here is a multiple of 2^-133, so t / 4 is
 // exact even when subnormal: max|t| / 4 is the amax of the scaled transform,

@@ -112,6 +112,7 @@ struct Params {
     uint32_t lora_stages;        // 64-deep BF16 stages of the low-rank term per tile (0: none)
     float* amax_out;             // [2]: max |D| and max |RHT along D's rows| (BF16 TMA path), or null
     uint32_t rht_mask;
+    uint32_t rht_sgn[16];        // the mask's sign flips as XOR words on packed bf16 pairs (row i: bit i)
     float alpha;                 // extra factor on the product (1 for a plain GEMM)
     const void* c;               // D = alpha s_gA s_gB A B^T + beta C: C [M][ldc] of D's dtype, or null
     int64_t ldc;
@@ -304,7 +305,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // max |x| and max |H16 D x| of each block, the transform in the quantizer's
 // order (signs, then butterfly stages 0..3 as (a + b, a - b)), both columns
 // at once in packed pairs; the 1/4 is applied to the final maximum, exactly.
-__device__ __forceinline__ void slice_amax(const uint8_t* slice, uint32_t lane, uint32_t rht_mask,
+__device__ __forceinline__ void slice_amax(const uint8_t* slice, uint32_t lane, const Params& p,
                                            float& amax_plain, float& amax_rht) {
     const uint32_t chunk = lane >> 2, word = (lane & 3u) * 4u;
 #pragma unroll
@@ -314,7 +315,7 @@ __device__ __forceinline__ void slice_amax(const uint8_t* slice, uint32_t lane, 
         for (int i = 0; i < 16; ++i) {
             const uint32_t j = 16u * blk + i;
             uint32_t w = *reinterpret_cast<const uint32_t*>(slice + j * 128u + ((chunk ^ (j & 7u)) << 4) + word);
-            w ^= ((rht_mask >> i) & 1u) * 0x80008000u;     // D: both columns' sign bits
+            w ^= p.rht_sgn[i];     // D: both columns' sign bits
             const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
             amax_plain = fmax3(amax_plain, fabsf(lo), fabsf(hi));
             t[i] = f32x2_pack(lo, hi);
@@ -831,7 +832,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     store_round_tail(p, slice, lane, row, nbase + r * 64, 64u);
                     // the slice now holds this warp's 32 rows x 64 columns: read
                     // it back by columns for the output's amax
-                    if constexpr (kAmax) slice_amax(slice, lane, p.rht_mask, amax_plain, amax_rht);
+                    if constexpr (kAmax) slice_amax(slice, lane, p, amax_plain, amax_rht);
                 }
             } else if (p.tma_store && p.out_fp32) {
                 // FP32: all 128 columns loaded under one wait, the
@@ -1175,6 +1176,7 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
         if (e != cudaSuccess) return e;
         p.amax_out = amax_out;
         p.rht_mask = rht_mask;
+        for (int i = 0; i < 16; ++i) p.rht_sgn[i] = ((rht_mask >> i) & 1u) ? 0x80008000u : 0u;
     }
     CUtensorMap mu = ma, mv = ma;  // low-rank operands (unused by the kernel otherwise; any valid map)
     p.c_staged = (p.c && p.c_vec && p.tma_store) ? 1 : 0;

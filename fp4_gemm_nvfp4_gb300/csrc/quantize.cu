@@ -77,6 +77,7 @@ struct RowArgs {
     int n_partials;
     float* partials_out;
     uint32_t mask;
+    RhtSigns sg;                 // the mask's sign flips as XOR words
     PhiloxKeys keys;             // SR round keys of the seed
     uint64_t stream;
 };
@@ -111,12 +112,16 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const RowArgs a) {
         constexpr bool G = decltype(guard)::value;
         for (; b < a.total; b += stride) {
             const uint16_t* src = a.x + (int64_t)r * a.ld_x + (int64_t)j * 16;
-            const uint4 u0 = ld_nc_v4(src), u1 = ld_nc_v4(src + 8);
+            uint4 u0 = ld_nc_v4(src), u1 = ld_nc_v4(src + 8);
+            if constexpr (kRHT) {
+                u0.x ^= a.sg.row[0], u0.y ^= a.sg.row[1], u0.z ^= a.sg.row[2], u0.w ^= a.sg.row[3];
+                u1.x ^= a.sg.row[4], u1.y ^= a.sg.row[5], u1.z ^= a.sg.row[6], u1.w ^= a.sg.row[7];
+            }
             float t[16] = {bf16lo(u0.x), bf16hi(u0.x), bf16lo(u0.y), bf16hi(u0.y), bf16lo(u0.z), bf16hi(u0.z),
                            bf16lo(u0.w), bf16hi(u0.w), bf16lo(u1.x), bf16hi(u1.x), bf16lo(u1.y), bf16hi(u1.y),
                            bf16lo(u1.z), bf16hi(u1.z), bf16lo(u1.w), bf16hi(u1.w)};
             if constexpr (kRHT) {
-                rht16_unscaled_packed(t, a.mask);   // the 1/4 comes below
+                rht16_unscaled_packed(t, 0u);   // signs flipped above; the 1/4 comes below
                 if (P == Pass::kEncode && !fold) scale16(t, 0.25f);
             }
             float amax_b = 0.0f;
@@ -168,6 +173,7 @@ struct ColArgs {
     float* partials_out;
     float* partials_out_plain;   // kAmax with kDual: max |x| before the RHT
     uint32_t mask;
+    RhtSigns sg;                 // the mask's sign flips as XOR words
     PhiloxKeys keys;             // SR round keys of the seed
     uint64_t stream;
 };
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
             float t0[16], t1[16];
     #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const uint32_t w = ld_nc_u32(src + (int64_t)i * a.ld_x);
+                const uint32_t w = ld_nc_u32(src + (int64_t)i * a.ld_x) ^ (kRHT ? a.sg.col[i] : 0u);
                 t0[i] = bf16lo(w);
                 t1[i] = bf16hi(w);
             }
@@ -215,7 +221,7 @@ __global__ void __launch_bounds__(kThreads) colwise_kernel(const ColArgs a) {
                 for (int i = 0; i < 16; ++i) plain_max = fmaxf(plain_max, fmaxf(fabsf(t0[i]), fabsf(t1[i])));
             }
             if constexpr (kRHT) {
-                rht16_unscaled_x2(t0, t1, a.mask);   // the 1/4 comes below
+                rht16_unscaled_x2(t0, t1, 0u);   // signs flipped at the load; the 1/4 comes below
                 if (P == Pass::kEncode && !fold) {
                     scale16(t0, 0.25f);
                     scale16(t1, 0.25f);
@@ -471,6 +477,7 @@ struct PairArgs {
     int n_partials_col;          // partials of part_rht
     bool emit_row, emit_col;
     uint32_t mask;
+    RhtSigns sg;                 // the mask's sign flips as XOR words
     PhiloxKeys keys;             // SR round keys of the seed
     uint64_t stream_row, stream_col;
 };
@@ -598,13 +605,13 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const uint32_t off = (uint32_t)i * 128u + (((lane >> 2) ^ (uint32_t)(i & 7)) << 4) + (lane & 3u) * 4u;
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(src + off);
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(src + off) ^ (kColRHT ? a.sg.col[i] : 0u);
                     t0[i] = bf16lo(w);
                     t1[i] = bf16hi(w);
                 }
                 if (a.emit_col && c < a.cols) {
                     if constexpr (kColRHT) {
-                        rht16_unscaled_x2(t0, t1, a.mask);   // the 1/4 comes below
+                        rht16_unscaled_x2(t0, t1, 0u);   // signs flipped at the load; the 1/4 comes below
                         if (!fold) {
                             scale16(t0, 0.25f);
                             scale16(t1, 0.25f);
@@ -645,7 +652,11 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t off = i * 128u + (((4u * h + (uint32_t)kk) ^ (i & 7u)) << 4);
-                        const uint4 u = *reinterpret_cast<const uint4*>(src + off);
+                        uint4 u = *reinterpret_cast<const uint4*>(src + off);
+                        if constexpr (kRowRHT) {
+                            const uint32_t s0 = 4u * ((uint32_t)kk & 1u);
+                            u.x ^= a.sg.row[s0], u.y ^= a.sg.row[s0 + 1], u.z ^= a.sg.row[s0 + 2], u.w ^= a.sg.row[s0 + 3];
+                        }
                         v[8 * kk + 0] = bf16lo(u.x);
                         v[8 * kk + 1] = bf16hi(u.x);
                         v[8 * kk + 2] = bf16lo(u.y);
@@ -656,7 +667,7 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                         v[8 * kk + 7] = bf16hi(u.w);
                     }
                     if constexpr (kRowRHT) {
-                        rht16_unscaled_x2(v, v + 16, a.mask);   // the 1/4 comes below
+                        rht16_unscaled_x2(v, v + 16, 0u);   // signs flipped at the load; the 1/4 comes below
                         if (!fold_row) {
                             scale16(v, 0.25f);
                             scale16(v + 16, 0.25f);
@@ -946,6 +957,7 @@ cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, in
     pa.n_partials = n_partials;
     pa.n_partials_col = n_partials_col < 0 ? n_partials : n_partials_col;
     pa.mask = sign_mask;
+    pa.sg = rht_signs(sign_mask);
     pa.keys = philox_keys(seed);
     pa.stream_row = stream_row;
     pa.stream_col = stream_col;
@@ -989,6 +1001,7 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
     ra.bpr = (uint32_t)(cols / 16);
     ra.total = (uint32_t)(rows * (cols / 16));
     ra.mask = sign_mask;
+    ra.sg = rht_signs(sign_mask);
     ra.keys = philox_keys(seed);
     ra.stream = stream_id;
 
@@ -1000,6 +1013,7 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
     ca.tiles_r = (uint32_t)((rows + 127) / 128);
     ca.tiles_c = (uint32_t)((cols + 63) / 64);
     ca.mask = sign_mask;
+    ca.sg = rht_signs(sign_mask);
     ca.keys = philox_keys(seed);
     ca.stream = stream_id;
     const int64_t ntiles = (int64_t)ca.tiles_r * ca.tiles_c;
@@ -1111,6 +1125,7 @@ cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t
     ca.tiles_r = (uint32_t)((rows + 127) / 128);
     ca.tiles_c = (uint32_t)((cols + 63) / 64);
     ca.mask = sign_mask;
+    ca.sg = rht_signs(sign_mask);
     ca.keys = philox_keys(seed);
     const int64_t ntiles = (int64_t)ca.tiles_r * ca.tiles_c;
 
@@ -1151,6 +1166,7 @@ cudaError_t launch_quantize_row_col_rht(const uint16_t* x, int64_t rows, int64_t
     pa.n_partials_col = n;
     pa.emit_row = pa.emit_col = true;
     pa.mask = sign_mask;
+    pa.sg = rht_signs(sign_mask);
     pa.keys = philox_keys(seed);
     pa.stream_row = stream_row;
     pa.stream_col = stream_col;
