@@ -286,6 +286,7 @@ struct RequantArgs {
     int n_partials;
     float* partials_out;
     uint32_t mask;
+    uint32_t sgf[16];            // row i's sign flip of D as an XOR word on a binary32 (bit i of the mask)
     PhiloxKeys keys;             // SR round keys of the seed
     uint64_t stream;
 };
@@ -303,14 +304,24 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const RequantArgs a) 
         g_tab[threadIdx.x] = make_float2(lo, hi);
         if (threadIdx.x < 128) sb_tab[threadIdx.x] = e4m3_decode(threadIdx.x);
     }
+    const float sg = *a.in_sg;
+    // The RHT's 1/4 may go into the multipliers (as in the bf16 quantizers)
+    // when every value t / 4 is exact: with s_g >= 2^-114 every nonzero input
+    // RN(RN(e2m1 s_b) s_g) is at least 2^-10 s_g >= 2^-124, so the inputs and
+    // every butterfly value are multiples of 2^-147.
+    const bool fold_in = sg >= 0x1p-114f;
     TensorScale ts{1.0f, 1.0f};
+    bool fold = false;
     if constexpr (P == Pass::kEncode) {
         ts = load_tensor_scale(a.partials_in, a.n_partials, red, a.out, nullptr);
-        fill_rb_table(rb_table, ts.s_enc);
+        fold = fold_in && rht_quarter_foldable(ts.s_enc);
+        fill_rb_table(rb_table, ts.s_enc, fold ? 0.25f : 1.0f);
+    } else {
+        fold = fold_in;
     }
     __syncthreads();
-    const float s_mult = ts.s_enc;     // the values carry their 1/4 already
-    const float sg = *a.in_sg;
+    // the values' factor S_enc (with the RHT's 1/4 when it is folded)
+    const float s_mult = fold ? __fmul_rn(ts.s_enc, 0.25f) : ts.s_enc;
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t ntiles = a.tiles_r * a.tiles_c;
     float local_max = 0.0f;
@@ -330,18 +341,25 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const RequantArgs a) 
     #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const float2 g = g_tab[__ldg(crow + (int64_t)i * a.in_ld)];
-                const float sb = sb_tab[__ldg(srow + 16 * i) & 0x7Fu];
+                // D's sign flip of row i on its scale: RN(RN(g (-s_b)) s_g) = -RN(RN(g s_b) s_g)
+                const float sb = __uint_as_float(__float_as_uint(sb_tab[__ldg(srow + 16 * i) & 0x7Fu]) ^ a.sgf[i]);
                 t0[i] = __fmul_rn(__fmul_rn(g.x, sb), sg);
                 t1[i] = __fmul_rn(__fmul_rn(g.y, sb), sg);
             }
-            rht16_unscaled_x2(t0, t1, a.mask);
-            scale16(t0, 0.25f);
-            scale16(t1, 0.25f);
+            rht16_unscaled_x2(t0, t1, 0u);   // signs flipped above
+            if (!fold) {
+                scale16(t0, 0.25f);
+                scale16(t1, 0.25f);
+            }
             float m0 = 0.0f, m1 = 0.0f;
     #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 m0 = fmaxf(m0, fabsf(t0[i]));
                 m1 = fmaxf(m1, fabsf(t1[i]));
+            }
+            if (P == Pass::kEncode && fold) {
+                m0 = __fmul_rn(m0, 0.25f);
+                m1 = __fmul_rn(m1, 0.25f);
             }
             if constexpr (P == Pass::kAmax) {
                 local_max = fmaxf(local_max, fmaxf(m0, m1));
@@ -362,7 +380,10 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const RequantArgs a) 
         main_loop(std::true_type{});
     else
         main_loop(std::false_type{});
-    if constexpr (P == Pass::kAmax) block_max_store(local_max, a.partials_out, red);
+    if constexpr (P == Pass::kAmax) {
+        if (fold) local_max = __fmul_rn(local_max, 0.25f);
+        block_max_store(local_max, a.partials_out, red);
+    }
 }
 
 // -------------------------------------------------------------- 16x16 -----
@@ -1205,6 +1226,7 @@ cudaError_t launch_requantize_col_rht(const QuantTarget* in, bool sr, uint32_t s
     ra.tiles_c = (uint32_t)((in->lcols + 63) / 64);
     ra.out = make_target(out);
     ra.mask = sign_mask;
+    for (int i = 0; i < 16; ++i) ra.sgf[i] = ((sign_mask >> i) & 1u) ? 0x80000000u : 0u;
     ra.keys = philox_keys(seed);
     ra.stream = stream_id;
     const int64_t ntiles = (int64_t)ra.tiles_r * ra.tiles_c;
