@@ -111,8 +111,7 @@ struct Params {
     int n_fast;                  // tile order: N tiles vary fastest (else M tiles)
     uint32_t lora_stages;        // 64-deep BF16 stages of the low-rank term per tile (0: none)
     float* amax_out;             // [2]: max |D| and max |RHT along D's rows| (BF16 TMA path), or null
-    uint32_t rht_mask;
-    uint32_t rht_sgn[16];        // the mask's sign flips as XOR words on packed bf16 pairs (row i: bit i)
+    uint32_t rht_sgn[16];        // the RHT mask's sign flips as XOR words on packed bf16 pairs (row i: bit i)
     float alpha;                 // extra factor on the product (1 for a plain GEMM)
     const void* c;               // D = alpha s_gA s_gB A B^T + beta C: C [M][ldc] of D's dtype, or null
     int64_t ldc;
@@ -1175,7 +1174,6 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, void* d, int
         const cudaError_t e = cudaMemsetAsync(amax_out, 0, 2 * sizeof(float), stream);
         if (e != cudaSuccess) return e;
         p.amax_out = amax_out;
-        p.rht_mask = rht_mask;
         for (int i = 0; i < 16; ++i) p.rht_sgn[i] = ((rht_mask >> i) & 1u) ? 0x80008000u : 0u;
     }
     CUtensorMap mu = ma, mv = ma;  // low-rank operands (unused by the kernel otherwise; any valid map)
