@@ -14,7 +14,7 @@ from tests import helpers
 
 pytestmark = pytest.mark.gpu
 
-N_QUANT, N_PAIR, N_GEMM, N_OTHER = 64, 24, 32, 16
+N_QUANT, N_PAIR, N_GEMM, N_OTHER = 256, 96, 96, 48
 
 
 @pytest.fixture(scope="module", autouse=True)
