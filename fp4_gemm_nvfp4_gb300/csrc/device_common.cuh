@@ -255,12 +255,6 @@ __device__ __forceinline__ void scale16(float* t, float f) {
     for (int i = 0; i < 16; ++i) t[i] = __fmul_rn(t[i], f);
 }
 
-// t <- H16 * D * t / 4: negate per mask, butterfly stages 0..3, times 0.25.
-__device__ __forceinline__ void rht16(float* t, uint32_t sign_mask) {
-    rht16_unscaled(t, sign_mask);
-    scale16(t, 0.25f);
-}
-
 // ------------------------------------------------------------ tensor scale -
 struct TensorScale {
     float s_enc, s_g;
@@ -615,15 +609,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
         : "memory");
 }
 
-// Plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -776,27 +761,6 @@ __device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
-// Four pair MMAs over consecutive K = 64 steps of one stage: A and B
-// descriptors advance by 32 bytes (2 in the encoded address field) per step,
-// the scale columns by 4 (A) and 8 (B).  accumulate_first selects whether the
-// first step adds to D.
-__device__ __forceinline__ void mma_nvf4_pair_x4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate_first) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %7, %8, %3, [%9], [%10], 1;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %11, %12, %3, [%13], [%14], 1;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %15, %16, %3, [%17], [%18], 1;\n\t"
-        "}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate_first), "r"(sfa_tmem), "r"(sfb_tmem),
-        "l"(a_desc + 2), "l"(b_desc + 2), "r"(sfa_tmem + 4), "r"(sfb_tmem + 8),
-        "l"(a_desc + 4), "l"(b_desc + 4), "r"(sfa_tmem + 8), "r"(sfb_tmem + 16),
-        "l"(a_desc + 6), "l"(b_desc + 6), "r"(sfa_tmem + 12), "r"(sfb_tmem + 24)
-        : "memory");
-}
-
 // The four K = 64 MMAs of one 256-deep stage.  Descriptors are built from
 // their 32-bit low words (start address >> 4 in the low 14 bits, which never
 // carry: shared memory is below 256 KiB) and the common high word, so the
@@ -848,20 +812,6 @@ __device__ __forceinline__ void tc_commit_pair_multicast_addr(uint32_t bar, uint
 }
 
 // --------------------------------------------------------------- tcgen05 ---
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -870,38 +820,11 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Arrive on `bar` once every tcgen05 operation this thread issued so far has
-// completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
-}
-
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (>> 4), version 1 at bit 46, swizzle mode at 61.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
     return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swizzle << 61);
-}
-
-// D(tmem) (+)= A(smem) * B(smem)^T with E2M1 operands and per-16 E4M3 scales
-// taken from tensor memory (kind::mxf4nvf4, 4 scales per row per K = 64).
-__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
-        "}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-        : "memory");
-}
-
-// Copy 32 rows x 16 bytes from shared memory into tensor-memory lanes 0-31
-// (4 columns), replicated into all four 32-lane groups.
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns -> 32 registers per thread.
