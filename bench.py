@@ -151,32 +151,28 @@ def host_inputs(seed_base=4):
 
 
 def quant_launches(kw):
-    """Kernels one quantize call launches: an amax pass and an encode pass per
-    RHT orientation, else one amax pass plus one encode pass (row-wise plus
-    col-wise RHT of one input: one shared amax pass and one encode pass; with
-    the amax taken by the producing GEMM, the encode pass only)."""
+    """Kernels one quantize call launches: an amax pass (one per emitted
+    orientation when the RHT is on, each orientation's transform having its
+    own amax) and one encode pass emitting every requested orientation; a
+    row-wise plus col-wise RHT pair of one input shares one amax pass, and
+    with the amax taken by the producing GEMM only the encode pass runs."""
     if kw.get("pair"):
         return 1 if kw.get("amax_given") else 2
-    if kw.get("rht_mask") is not None:
-        return 2 * (int(kw.get("rowwise", True)) + int(kw.get("colwise", False)))
-    if kw.get("two_d"):
-        return 2
-    return 1 + int(kw.get("rowwise", True)) + int(kw.get("colwise", False))
+    outs = int(kw.get("rowwise", True)) + int(kw.get("colwise", False))
+    amax_passes = outs if (kw.get("rht_mask") is not None and not kw.get("two_d")) else 1
+    return amax_passes + 1
 
 
 def quant_bytes(rows, cols, kw):
     """Algorithmic HBM bytes of one quantize call: each amax pass reads the
-    input once, each encode pass reads it again and writes 0.5 B of codes and
-    1/16 B of scales per element per emitted orientation."""
+    input once; the encode pass reads it once more and writes 0.5 B of codes
+    and 1/16 B of scales per element per emitted orientation."""
     n = rows * cols
     if kw.get("pair"):                      # one amax pass, one encode pass emitting both orientations
         return n * 2 * (1 if kw.get("amax_given") else 2) + n * 2 * (0.5 + 1 / 16)
     outs = int(kw.get("rowwise", True)) + int(kw.get("colwise", False))
-    if kw.get("rht_mask") is not None:      # one amax and one encode pass per orientation
-        amax_passes, encode_reads = outs, outs
-    else:                                   # one encode pass emits both orientations (16x16, or 1x16
-        amax_passes, encode_reads = 1, 1    # row + col through the slice-staged pair kernel)
-    return n * 2 * (amax_passes + encode_reads) + n * outs * (0.5 + 1 / 16)
+    amax_passes = outs if (kw.get("rht_mask") is not None and not kw.get("two_d")) else 1
+    return n * 2 * (amax_passes + 1) + n * outs * (0.5 + 1 / 16)
 
 
 class Step:
