@@ -872,6 +872,70 @@ def sweep_ns(args):
         torch.cuda.empty_cache()
 
 
+def sweep_lora(args):
+    """The GEMM with the BF16 low-rank (LoRA-SVD) branch, D = A B^T + beta U V^T
+    ("Full-Stack FP4", the LoRA-SVD correction of a linear layer), against the
+    plain GEMM on the C4 layer's Fprop shapes at ranks 64 and 128.  Random
+    FP4 operands (codes and in-range E4M3 scales), U and V N(0, 0.02^2) BF16;
+    one JSON line per case; L2 flushed before every timed call."""
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from fp4_gemm_nvfp4_gb300 import capi, ops
+    peaks, peak_src = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(8)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        times = []
+        for _ in range(max(args.steps, 10)):
+            flush.fill_(1.0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    for name, M, N, K in [("fprop_up", 16384, 9216, 3072), ("fprop_down", 16384, 3072, 9216)]:
+        a, b = ops.alloc_operand(M, K), ops.alloc_operand(N, K)
+        for op in (a, b):
+            op.codes.copy_(torch.randint(0, 256, op.codes.shape, generator=gen, device="cuda",
+                                         dtype=torch.int32).to(torch.uint8))
+            op.scales.copy_(torch.randint(0x20, 0x48, op.scales.shape, generator=gen, device="cuda",
+                                          dtype=torch.int32).to(torch.uint8))
+            op.global_scale.fill_(1.0)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        plain_ms = timed(lambda: ops.gemm(a, b, out=out))
+        for r in (64, 128):
+            u = (torch.randn((M, r), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+            v = (torch.randn((N, r), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+            scratch = torch.empty(capi.nvfp4_gemm_lora_workspace_size(M, r), dtype=torch.uint8,
+                                  device="cuda")
+            lora_ms = timed(lambda: ops.gemm_lora(a, b, u, v, 0.5, out=out, scratch=scratch))
+            fp4_flop = 2 * M * N * K
+            print(json.dumps({"sweep": "lora", "gemm": name, "m": M, "n": N, "k": K, "rank": r,
+                              "plain_us": round(plain_ms * 1e3, 1), "lora_us": round(lora_ms * 1e3, 1),
+                              "overhead_pct": round(100 * (lora_ms / plain_ms - 1), 1),
+                              "low_rank_flop_pct": round(100 * 2 * M * N * r / fp4_flop, 2),
+                              "fp4_tflops": round(fp4_flop / (lora_ms * 1e-3) / 1e12, 1),
+                              "fp4_frac_of_peak": round(fp4_flop / (lora_ms * 1e-3) / 1e12 / fp4_peak, 4),
+                              "peak_source": f"{peak_src} bf16 burst x 6", "l2_flush": True,
+                              "status": ops.device_error()}), flush=True)
+            del u, v, scratch
+        del a, b, out
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -881,9 +945,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fuse-amax", action="store_true",
                     help="quantize H and dY_up as inputs with their own amax pass (no fused GEMM amax)")
-    ap.add_argument("--sweep", choices=["c5", "ns"], default=None,
-                    help="instead of the layer step, run the quantizer bandwidth sweep (c5) or the NVFP4 "
-                         "Newton-Schulz step on the 3B weight shapes (ns); one JSON line per case")
+    ap.add_argument("--sweep", choices=["c5", "ns", "lora"], default=None,
+                    help="instead of the layer step, run the quantizer bandwidth sweep (c5), the NVFP4 "
+                         "Newton-Schulz step on the 3B weight shapes (ns) or the GEMM with the low-rank "
+                         "branch against the plain GEMM (lora); one JSON line per case")
     ap.add_argument("--tokens", type=int, default=TOKENS,
                     help="tokens of the layer step (16384 is the benchmarked workload)")
     args = ap.parse_args()
@@ -897,6 +962,9 @@ def main():
         return
     if args.sweep == "ns":
         sweep_ns(args)
+        return
+    if args.sweep == "lora":
+        sweep_lora(args)
         return
     if args.impl == "reference":
         r = reference_arm(args)
