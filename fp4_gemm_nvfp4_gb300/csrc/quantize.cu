@@ -501,6 +501,8 @@ struct PairArgs {
     RhtSigns sg;                 // the mask's sign flips as XOR words
     PhiloxKeys keys;             // SR round keys of the seed
     uint64_t stream_row, stream_col;
+    float* part_out_row;         // amax only: one partial per CTA of each orientation
+    float* part_out_col;
 };
 
 constexpr int kPairSlots = 2;
@@ -543,7 +545,11 @@ __device__ __forceinline__ void store_col64(const Target& t, uint32_t c, uint32_
 // row-wise operand gets it too (along its rows; both orientations of an RHT
 // quantize call).  Either orientation may be left out (emit_*).
 // kS46: 4/6 adaptive block scales (block_scale_46) in both orientations.
-template <bool kSR, bool kColRHT, bool kS46 = false, bool kRowRHT = false>
+// kAmaxOnly: the amax pass of an RHT call emitting both orientations: no
+// encode; each CTA writes the max |value| of each orientation (after its
+// transform, the 1/4 included) to part_out_row and part_out_col, from one
+// read of x instead of one per orientation.
+template <bool kSR, bool kColRHT, bool kS46 = false, bool kRowRHT = false, bool kAmaxOnly = false>
 __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                                const PairArgs a) {
     __shared__ float red[32];
@@ -551,8 +557,11 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     __shared__ __align__(1024) uint8_t ring[kThreads / 32][kPairSlots][kSliceBytes];
     __shared__ uint64_t full[kThreads / 32][kPairSlots];
     TensorScale ts_row{1.0f, 1.0f}, ts_col{1.0f, 1.0f};
-    if (a.emit_row) ts_row = load_tensor_scale(a.part_plain, a.n_partials, red, a.row, nullptr);
-    if (a.emit_col) ts_col = load_tensor_scale(a.part_rht, a.n_partials_col, red, a.col, nullptr);
+    if (!kAmaxOnly && a.emit_row) ts_row = load_tensor_scale(a.part_plain, a.n_partials, red, a.row, nullptr);
+    if (!kAmaxOnly && a.emit_col) ts_col = load_tensor_scale(a.part_rht, a.n_partials_col, red, a.col, nullptr);
+    // with S_enc = 1 (amax only) both quarters count as folded: the block
+    // maxima below are those of the scaled transform, exactly
+    float row_max = 0.0f, col_max = 0.0f;
     // the col-wise RHT's 1/4 lives in its multipliers (rht_quarter_foldable)
     const bool fold = kColRHT && rht_quarter_foldable(ts_col.s_enc);
     const bool fold_row = kRowRHT && rht_quarter_foldable(ts_row.s_enc);
@@ -648,6 +657,9 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                         m0 = __fmul_rn(m0, 0.25f);
                         m1 = __fmul_rn(m1, 0.25f);
                     }
+                    if constexpr (kAmaxOnly) {
+                        col_max = fmaxf(col_max, fmaxf(m0, m1));
+                    } else {
                     float rb0, rb1;
                     if constexpr (kS46) {
                         // with RNE the chosen candidates' codes are the block's codes
@@ -661,6 +673,7 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                         q0 = encode16<kSR, G>(t0, rb0, sc0, s_mult_col, keys, a.stream_col, (uint64_t)c * a.rows + r0);
                         q1 = encode16<kSR, G>(t1, rb1, sc1, s_mult_col, keys, a.stream_col,
                                               (uint64_t)(c + 1) * a.rows + r0);
+                    }
                     }
                 }
             }
@@ -703,6 +716,10 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
     #pragma unroll
                         for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[16 * jj + e]));
                         if (fold_row) m = __fmul_rn(m, 0.25f);
+                        if constexpr (kAmaxOnly) {
+                            row_max = fmaxf(row_max, m);
+                            continue;
+                        }
                         float rb;
                         sc[jj] = kS46 ? block_scale_46<G>(v + 16 * jj, m, ts_row.s_enc, s_mult_row, rb_row, &rb,
                                                           kSR ? nullptr : &q[jj])
@@ -712,7 +729,8 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                                                   (uint64_t)r * a.cols + cb + 16u * (uint32_t)jj);
                     }
                     const uint32_t j0 = cb / 16u;
-                    if (two) {
+                    if (kAmaxOnly) {
+                    } else if (two) {
                         put_codes(a.row, (int64_t)r, (int64_t)(cb / 2), make_uint4(q[0].x, q[0].y, q[1].x, q[1].y));
                         put_scales(a.row, scale_offset(r, j0, a.row.s4), (uint16_t)(sc[0] | (sc[1] << 8)));
                     } else {
@@ -722,6 +740,7 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
                 }
             }
             }
+            if constexpr (kAmaxOnly) continue;
             // slice j % 4 joins the warp's col-wise codes; after the fourth, they
             // go out as whole sectors
             cq0[0] = cq0[1], cq0[1] = cq0[2], cq0[2] = cq0[3], cq0[3] = q0;
@@ -740,6 +759,11 @@ __global__ void __launch_bounds__(kThreads) pair_encode_kernel(const __grid_cons
         main_loop(std::true_type{});
     else
         main_loop(std::false_type{});
+    if constexpr (kAmaxOnly) {
+        block_max_store(row_max, a.part_out_row, red);
+        __syncthreads();
+        block_max_store(col_max, a.part_out_col, red);
+    }
 }
 
 // ------------------------------------------------ 16x16, RNE, via TMA -----
@@ -943,6 +967,48 @@ int row_amax(const RowArgs& base, float* partials, cudaStream_t st) {
     return g;
 }
 
+// Tensor map of x's 16-row x 64-column slices (128-byte swizzle) for the
+// slice-staged kernels; no L2 sector promotion (a 256-byte promotion fetched
+// the neighbouring 128 bytes again later: 25 % more DRAM reads on a 16x16
+// encode).
+bool make_slice_map(CUtensorMap* tmap, const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld_x * 2u};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t elem[2] = {1, 1};
+    return fn(tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The amax pass of an RHT call emitting both orientations, from one read of
+// x (pair_encode_kernel<..., kAmaxOnly>): partials of the row-wise operand's
+// transform in part_row, of the col-wise one's in part_col.  Returns the
+// number of partials of each (the grid), or -1 when the tensor map cannot be
+// made.
+int launch_pair_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, uint32_t sign_mask,
+                     float* part_row, float* part_col, cudaStream_t st) {
+    CUtensorMap tmap;
+    if (!make_slice_map(&tmap, x, rows, cols, ld_x)) return -1;
+    PairArgs pa{};
+    pa.rows = (uint32_t)rows;
+    pa.cols = (uint32_t)cols;
+    pa.tiles_r = (uint32_t)((rows + kTileRows - 1) / kTileRows);
+    pa.tiles_c = (uint32_t)((cols + 63) / 64);
+    pa.emit_row = pa.emit_col = true;
+    pa.mask = sign_mask;
+    pa.sg = rht_signs(sign_mask);
+    pa.part_out_row = part_row;
+    pa.part_out_col = part_col;
+    auto k = pair_encode_kernel<false, true, false, true, true>;
+    int g = persistent_grid(k, (int64_t)pa.tiles_r * pa.tiles_c);
+    if (g > kMaxAmaxPartials) g = kMaxAmaxPartials;
+    k<<<g, kThreads, 0, st>>>(tmap, pa);
+    return g;
+}
+
 // The slice-staged encode (pair_encode_kernel): optional row-wise operand
 // without RHT and optional col-wise operand with or without RHT.
 cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, bool sr, bool col_rht,
@@ -950,20 +1016,8 @@ cudaError_t launch_pair_encode(const uint16_t* x, int64_t rows, int64_t cols, in
                                const QuantTarget* row, const QuantTarget* col, const float* part_row,
                                const float* part_col, int n_partials, bool s46, cudaStream_t st,
                                bool row_rht = false, int n_partials_col = -1) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
     CUtensorMap tmap;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)ld_x * 2u};
-    // 16-row x 64-column slices; no L2 sector promotion (a 256-byte
-    // promotion fetched the neighbouring 128 bytes again later: 25 % more
-    // DRAM reads on a 16x16 encode)
-    const cuuint32_t box[2] = {64, 16};
-    const cuuint32_t elem[2] = {1, 1};
-    if (fn(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, elem,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    if (!make_slice_map(&tmap, x, rows, cols, ld_x)) return cudaErrorInvalidValue;
     PairArgs pa{};
     pa.rows = (uint32_t)rows;
     pa.cols = (uint32_t)cols;
@@ -1084,6 +1138,10 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
     if (!rht) {
         n_row = n_col = row_amax<false>(ra, part_a, st);
         part_b = part_a;
+    } else if (row && col) {
+        // both orientations' transforms from one read
+        n_row = n_col = launch_pair_amax(x, rows, cols, ld_x, sign_mask, part_a, part_b, st);
+        if (n_row < 0) return cudaErrorInvalidValue;
     } else {
         if (row) n_row = row_amax<true>(ra, part_a, st);
         if (col) {
